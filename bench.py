@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""DSA layer benchmark on GB300: tokens/s of one layer step (indexer + top-k,
+sparse attention forward and backward) at S = 131072, with the indexer's
+TFLOP/s and the attention kernels' GB/s against the measured peaks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one synthetic sequence:
+dsa_index_topk (32 indexer heads x 64, top 512 pools, query chunk 256),
+dsa_sparse_attn_fwd and dsa_sparse_attn_bwd (16 query heads sharing one KV
+head of dim 128).  Inputs are seeded bf16 N(0,1) (indexer queries x 1/8,
+head weights U(0,1)), resident in HBM before timing.  L2 is flushed (512 MiB
+write) between timed steps, outside the timed events.  Under torchrun each
+rank runs its own sequence (weak scaling, no collective on the data path).
+
+`--impl reference` times the CPU oracle on the host cores on bounded samples
+of the same workload (there is no other reference implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA layer fwd+bwd tokens/s at S=128k; indexer TFLOP/s & attn GB/s vs peak"
+UNIT = "tokens/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="s128k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time for the CPU baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- workload accounting
+
+def workload_counts(wl):
+    """Exact per-step unit counts: indexer (query, pool) pairs and attended (query, key) pairs."""
+    i = np.arange(wl.S, dtype=np.int64)
+    n = i // 4
+    pairs = int(n.sum())
+    keys = int((4 * np.minimum(n, wl.topk) + (i % 4) + 1).sum())
+    return pairs, keys
+
+
+def algorithmic_work(wl):
+    """Algorithmic flops / bytes per step of each kernel (see the design notes)."""
+    pairs, keys = workload_counts(wl)
+    S, Hq, D, k = wl.S, wl.Hq, wl.D, wl.topk
+    row_kv = 2 * D * 2                     # one K row + one V row, bf16
+    q_bytes = Hq * D * 2                   # one query's q (or o, dO, dq)
+    return {
+        "indexer": {"flops": 2 * wl.Hi * wl.Di * pairs},
+        "topk": {"bytes": 4 * pairs + 4 * S * k},
+        "attn_fwd": {"bytes": keys * row_kv + S * (2 * q_bytes + 4 * Hq + 4 * k)},
+        # gather K,V + read q, dO, lse, Delta, idx + write dq + fp32 dK/dV reductions (2 x 512 B per key)
+        "attn_bwd": {"bytes": keys * row_kv + S * (3 * q_bytes + 8 * Hq + 4 * k) + keys * 2 * D * 4},
+        "pairs": pairs, "keys": keys,
+    }
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, dev_index):
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[dev_index]
+        return str(dev_index)
+
+
+# ----------------------------------------------------------------------------- CPU baseline (oracle)
+
+def oracle_sample_step(wl, host, rows):
+    """Oracle work for a sample of query rows: indexer + top-k, forward, backward."""
+    import oracle
+    q_idx, k_idx, w, q, k, v, dO = host
+    sel, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk, rows=rows)
+    full = np.full((wl.S, wl.topk), -1, np.int32)
+    full[rows] = sel
+    oracle.attn_fwd(q, k, v, full, scale=wl.scale, rows=rows)
+    oracle.attn_bwd_rows(dO, q, k, v, full, scale=wl.scale, rows=rows)
+
+
+def cpu_baseline(wl, host, seconds, seed=12345):
+    import oracle
+    rs = np.random.RandomState(seed)
+    probe = np.sort(rs.randint(0, wl.S, 16))
+    t0 = time.perf_counter()
+    oracle_sample_step(wl, host, probe)
+    per_row = (time.perf_counter() - t0) / probe.size
+    n = int(max(16, min(4096, seconds / max(per_row, 1e-6))))
+    rows = np.sort(rs.randint(0, wl.S, n))
+    t0 = time.perf_counter()
+    oracle_sample_step(wl, host, rows)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} query rows drawn uniformly from the S={wl.S} sequence (seed {seed}); each row: indexer "
+                      f"scores over its floor(i/4) pools + top-{wl.topk} by full sort, forward and backward over its "
+                      f"key set; tokens/s = rows / oracle seconds ({dt:.1f} s)"}
+
+
+def host_inputs(wl):
+    import synth
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    q, k, v = synth.attention_inputs(wl)
+    dO = synth.grad_output(wl)
+    return q_idx, k_idx, w, q, k, v, dO
+
+
+def workload_config(wl, l2_note):
+    return {"workload": f"dsa_layer_fwd_bwd_S{wl.S}", "S": wl.S, "batch": 1, "indexer_heads": wl.Hi,
+            "indexer_dim": wl.Di, "pool_size": 4, "topk_pools": wl.topk, "query_chunk": wl.chunk,
+            "q_heads": wl.Hq, "kv_heads": 1, "head_dim": wl.D, "max_keys_per_query": 4 * wl.topk + 4,
+            "inputs": "seeded bf16 N(0,1); indexer queries x %g; head weights U(0,1) fp32" % wl.q_idx_scale,
+            "l2": l2_note}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    host = host_inputs(wl)
+    rs = np.random.RandomState(777)
+    rows_per_step = 24
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, host, np.sort(rs.randint(0, wl.S, rows_per_step)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(wl, host, np.sort(rs.randint(0, wl.S, rows_per_step)))
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    sample = (f"{rows_per_step} query rows per step drawn uniformly from the S={wl.S} sequence; each row: indexer + "
+              f"top-{wl.topk}, forward and backward over its key set; tokens/s = rows / oracle seconds")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl, "n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import long_context_sparse_index_gb300 as dsa
+    from long_context_sparse_index_gb300 import build as libbuild
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    libbuild.build()
+    wl = synth.WORKLOADS[args.workload]
+    peaks = load_peaks()
+
+    host = host_inputs(wl)
+    q_idx_h, k_idx_h, w_h, q_h, k_h, v_h, dO_h = host
+
+    def pinned_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    pin = {"q_idx": pinned_bf16(q_idx_h), "k_idx": pinned_bf16(k_idx_h), "w": torch.from_numpy(w_h).pin_memory(),
+           "q": pinned_bf16(q_h), "k": pinned_bf16(k_h), "v": pinned_bf16(v_h), "dO": pinned_bf16(dO_h)}
+    d = {name: t.to(dev) for name, t in pin.items()}
+    S, topk = wl.S, wl.topk
+    pool_idx = torch.empty((S, topk), dtype=torch.int32, device=dev)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((S, wl.Hq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    ws_idx = torch.empty(dsa.index_topk_workspace_size(S, wl.Hi, wl.Di, wl.chunk, topk), dtype=torch.uint8,
+                         device=dev)
+    ws_bwd = torch.empty(dsa.sparse_attn_bwd_workspace_size(S, wl.Hq, wl.D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        dsa.dsa_index_topk(t["q_idx"], t["k_idx"], t["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
+                           workspace=ws_idx)
+        dsa.dsa_sparse_attn_fwd(t["q"], t["k"], t["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
+        dsa.dsa_sparse_attn_bwd(t["dO"], t["q"], t["k"], t["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk,
+                                dv=dv, workspace=ws_bwd)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d)
+    dsa.dsa_sync_status()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device events per step, L2 flush outside the events
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    dsa.launch_count_reset()
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        evs[s][0].record(stream)
+        step(d)
+        evs[s][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    gpu_launches = dsa.launch_count()
+    dsa.dsa_sync_status()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = world * S * args.steps / total_s
+
+    # ---- per-kernel device time, live, with events around every launch (one more step)
+    flush.zero_()
+    torch.cuda.synchronize()
+    dsa.profile_enable(True)
+    step(d)
+    dsa.profile_enable(False)
+    prof = dsa.profile_read()
+    work = algorithmic_work(wl)
+    kernels = {}
+    for name, (ms, launches) in prof.items():
+        entry = {"ms": ms, "launches": launches}
+        if name == "indexer":
+            tf = work["indexer"]["flops"] / (ms * 1e-3) / 1e12
+            entry.update({"algorithmic_tflops": tf, "frac_of_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
+                          "executed_tensor_flops_factor": 2.0})
+        elif name in ("topk", "attn_fwd", "attn_bwd"):
+            gbs = work[name]["bytes"] / (ms * 1e-3) / 1e9
+            entry.update({"algorithmic_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]})
+        kernels[name] = entry
+    dom = max(prof.items(), key=lambda kv: kv[1][0])[0]
+    dms, dl = prof[dom]
+    if dom == "indexer":
+        ach = work["indexer"]["flops"] / (dms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None}
+    else:
+        ach = work.get(dom, {"bytes": 0})["bytes"] / (dms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None}
+    roof.update({"kernel": dom, "launches_per_step": dl, "avg_launch_ms": dms / max(dl, 1),
+                 "peak_source": peaks["source"] + (" (sustained bf16)" if dom == "indexer" else " (copy bandwidth)")})
+
+    # ---- end to end through the public API: pinned host -> device, the three calls, device -> host
+    e2e = None
+    if not args.no_e2e:
+        out_host = {"pool_idx": torch.empty(pool_idx.shape, dtype=pool_idx.dtype).pin_memory(),
+                    "o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                    "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+                    "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
+                    "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
+                    "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
+        bi = sum(t.numel() * t.element_size() for t in pin.values())
+        bo = sum(t.numel() * t.element_size() for t in out_host.values())
+        e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+        barrier()
+        for s in range(args.steps):
+            flush.zero_()
+            e2e_evs[s][0].record(stream)
+            for name, t in pin.items():
+                d[name].copy_(t, non_blocking=True)
+            step(d)
+            for name, src in (("pool_idx", pool_idx), ("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                out_host[name].copy_(src, non_blocking=True)
+            e2e_evs[s][1].record(stream)
+        barrier()
+        e2e_s = sum(a.elapsed_time(b) for a, b in e2e_evs) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * S * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo}
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(wl, host, args.cpu_seconds)
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
+                "parallelism": f"replicas x{world} (one independent sequence per GPU)",
+                "clocks": clocks, "gpu_launches": gpu_launches, "e2e": e2e, "roofline": roof,
+                "kernels": kernels, "cpu_baseline": cpu, "wall_s_timed_region": wall,
+                "step_ms": step_ms}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * dsa.h -- C ABI of libdsa, the DeepSeek-Sparse-Attention (DSA) layer hot
+ * path for one GB300 GPU (sm_103a): causal pooled indexer -> per-query top-k
+ * of key pools -> sparse attention forward and backward.
+ *
+ * Sources (page title and section; the pages print no formulas or code):
+ *  [SkyRL-1M]  "SkyRL 将 GLM-5.3-Flash 训练上下文扩至 100 万 token",
+ *              §模型与瓶颈: DSA attends to ~2048 keys per query, while its
+ *              indexer scores every query against every 4-token key pool,
+ *              which moves the quadratic cost into the indexer;
+ *              §1 DSA 真稀疏: the Flash variant has no positional encoding
+ *              and keeps 2051 keys; the indexer is scored query chunk by
+ *              query chunk (peak scoring memory ~64 GiB -> ~2.3 GiB at 32k)
+ *              and sharded by query, exchanging int32 selected-pool indices.
+ *  [Anyscale]  "How Lila Sciences and Anyscale Scaled GLM-5.3-Flash
+ *              Training", lessons "检查每一层是否运行您认为的内核" (a sparse
+ *              kernel that silently fell back to dense attention) and
+ *              "稀疏注意力会导致二次成本" (a few hundred queries scored at a
+ *              time keeps the score matrix under 2 GiB).
+ *  [CP-lesson] "128K 的序列,激活放在哪?" (context-parallel lesson),
+ *              §改进二 and evidence row ②: blockwise online softmax equals
+ *              the one-shot softmax.
+ *
+ * The pages give no indexer formula.  This library computes
+ *   Khat_p     = fp32 mean of k_idx rows 4p..4p+3, summed ((k0+k1)+(k2+k3))/4
+ *   score(i,p) = sum_h w[i,h] * ReLU(q_idx[i,h,:] . Khat_p)     for 4p+3 < i
+ * and selects, for every query i, the min(topk, floor(i/4)) eligible pools
+ * with the largest scores (ties to the lower pool index).  Query i then
+ * attends to the 4 keys of each selected pool plus its own partial pool
+ * {4*floor(i/4), ..., i} (1 to 4 tokens, i itself included): up to
+ * 4*topk + 4 keys.  With topk >= floor(i/4) this is dense causal attention.
+ *
+ * Conventions shared by every call:
+ *  - Batch 1, row-major, no padding.  bf16 tensors are passed as void*.
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library allocates no device memory; scratch comes from the caller's
+ *    `workspace` (sized by the *_workspace() queries).  Pointers must be
+ *    16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work and return; results are ready in stream order.
+ *  - Arguments are checked before anything is launched; on error nothing is
+ *    written and no kernel runs.  Unsupported shapes return
+ *    DSA_ERR_UNSUPPORTED: there is no fallback path of any kind.
+ *  - Device-side waits are bounded.  A wait that runs out sets a device
+ *    status word and the kernel returns early; dsa_sync_status() reports it.
+ *  - A failing call stores a message for dsa_last_error() (per host thread).
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or range  */
+  DSA_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels implement     */
+  DSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required   */
+  DSA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+  DSA_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out           */
+  DSA_ERR_INTERNAL = 6      /* a device-side consistency check failed       */
+} dsa_status_t;
+
+/* Bytes of workspace dsa_index_topk needs for sequence length S, Hi indexer
+ * heads of dim Di, query chunk `chunk` and `topk`: the pooled keys (as a bf16
+ * hi/lo pair, 256 B per pool) plus one chunk of fp32 scores
+ * (chunk x ceil(S/4 to 256) x 4 B; 32 MiB at S = 131072, chunk = 256).
+ * Returns 0 for invalid arguments. */
+size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
+
+/*
+ * Indexer + top-k  [SkyRL-1M §模型与瓶颈, §1 DSA 真稀疏; Anyscale lesson
+ * "稀疏注意力会导致二次成本"].
+ *
+ *  q_idx     bf16 [S, Hi, Di]  indexer queries (rows q_begin..q_end-1 read)
+ *  k_idx     bf16 [S, Di]      indexer keys
+ *  w         fp32 [S, Hi]      per-query head weights (any sign)
+ *  S         sequence length, 1 <= S <= 2^31 - 1
+ *  Hi, Di    indexer heads (1..64) and head dim (must be 64)
+ *  chunk     queries scored per pass (>= 1): bounds the score scratch
+ *  topk      pools kept per query (1..2048)
+ *  q_begin, q_end   query range to process, 0 <= q_begin < q_end <= S; a
+ *            shard of a sequence passes its own range (rows are independent)
+ *  pool_idx  int32 [q_end - q_begin, topk] output: for query i the selected
+ *            pools in ascending order, then -1 padding (row i holds
+ *            min(topk, floor(i/4)) pools)
+ *  workspace, ws_bytes  device scratch of at least
+ *            dsa_index_topk_workspace(S, Hi, Di, chunk, topk) bytes
+ *
+ * Selection is exact with respect to the fp32 scores the kernels compute
+ * (bf16 inputs, fp32 accumulation, pooled keys carried as a bf16 hi/lo pair
+ * so the product keeps ~16 more bits than a single bf16 rounding).
+ */
+dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
+                            int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Sparse attention forward  [SkyRL-1M §模型与瓶颈; CP-lesson §改进二].
+ *
+ *  q         bf16 [S, Hq, D]  queries (Hq heads share one KV head)
+ *  k, v      bf16 [S, D]      keys and values
+ *  pool_idx  int32 [S, topk]  selection as written by dsa_index_topk
+ *            (ascending, -1 padded, every entry < floor(i/4) for row i)
+ *  Hq = 16, D = 128 (other shapes: DSA_ERR_UNSUPPORTED)
+ *  scale     softmax scale; <= 0 means 1/sqrt(D)
+ *  o         bf16 [S, Hq, D]  output
+ *  lse       fp32 [S, Hq]     natural-log softmax normaliser of the scaled
+ *                             logits (kept for the backward)
+ * Online softmax in fp32 over blocks of gathered keys.
+ */
+dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                                 int Hq, int D, int topk, float scale, void* o, float* lse, void* stream);
+
+/* Bytes of workspace dsa_sparse_attn_bwd needs: fp32 dK and dV accumulators
+ * (2 x S x D x 4 B) plus the per-row softmax-gradient term (S x Hq x 4 B). */
+size_t dsa_sparse_attn_bwd_workspace(int64_t S, int Hq, int D);
+
+/*
+ * Sparse attention backward  [SkyRL-1M §模型与瓶颈: attention over the
+ * selected keys, trained end to end].
+ *
+ *  dO        bf16 [S, Hq, D]  upstream gradient of o
+ *  q, k, v, pool_idx, S, Hq, D, topk, scale   as in the forward
+ *  o, lse    the forward's outputs
+ *  dq        bf16 [S, Hq, D]  output
+ *  dk, dv    bf16 [S, D]      outputs
+ *  workspace, ws_bytes  at least dsa_sparse_attn_bwd_workspace(S, Hq, D)
+ * dK/dV contributions of every query are added into fp32 accumulators with
+ * atomic reductions, so their bits may vary from run to run (within fp32
+ * rounding); dq is deterministic.
+ */
+dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const int32_t* pool_idx, int64_t S, int Hq, int D, int topk,
+                                 float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/* Synchronises `stream` and returns DSA_ERR_TIMEOUT / DSA_ERR_INTERNAL if a
+ * kernel has recorded a failed bounded wait or check since the last
+ * dsa_clear_status(), DSA_ERR_CUDA if the stream reports an error, else
+ * DSA_OK. */
+dsa_status_t dsa_sync_status(void* stream);
+
+/* Clears the device status word (synchronous). */
+dsa_status_t dsa_clear_status(void);
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char* dsa_last_error(void);
+
+/* Library version string. */
+const char* dsa_version(void);
+
+/*
+ * Measurement helpers (no part of the layer's arithmetic).
+ *
+ * dsa_profile_enable(1) makes every subsequent launch record a pair of CUDA
+ * events on its stream; dsa_profile_enable(0) stops recording.
+ * dsa_profile_read() synchronises those events and writes, for up to
+ * `max_kernels` kernels, the kernel name into names[k*name_len ...] (NUL
+ * terminated), the summed device time in ms into ms[k] and the number of
+ * launches into launches[k]; it returns the number of kernels (or -1 on a
+ * CUDA error) and clears the recorded events.
+ * dsa_launch_count() returns the number of kernels launched by this library
+ * in this process since dsa_launch_count_reset(), whether or not profiling
+ * is enabled.
+ */
+void dsa_profile_enable(int on);
+int dsa_profile_read(char* names, int name_len, double* ms, int64_t* launches, int max_kernels);
+int64_t dsa_launch_count(void);
+void dsa_launch_count_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,213 @@
+"""ctypes binding of libdsa (argument marshalling only).
+
+Every function here checks tensor dtypes, shapes and devices, allocates
+outputs and workspace with torch when the caller does not pass them, and
+calls the C entry point of the same name on the current CUDA stream.  All
+arithmetic runs in libdsa's CUDA kernels; there is no other code path, and a
+missing library raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE = 0, 1, 2, 3
+DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_INTERNAL = 4, 5, 6
+STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
+                4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_INTERNAL"}
+
+# every symbol the C header declares
+EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd_workspace",
+            "dsa_sparse_attn_bwd", "dsa_sync_status", "dsa_clear_status", "dsa_last_error", "dsa_version",
+            "dsa_profile_enable", "dsa_profile_read", "dsa_launch_count", "dsa_launch_count_reset")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load():
+    """Loads libdsa.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise DsaError(DSA_ERR_CUDA, f"{LIB_PATH} is not built; run __graft_entry__.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            i64, i32, vp, sz, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+            lib.dsa_index_topk_workspace.argtypes = [i64, i32, i32, i32, i32]
+            lib.dsa_index_topk_workspace.restype = sz
+            lib.dsa_index_topk.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp, sz, vp]
+            lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
+            lib.dsa_sparse_attn_bwd_workspace.argtypes = [i64, i32, i32]
+            lib.dsa_sparse_attn_bwd_workspace.restype = sz
+            lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp,
+                                                sz, vp]
+            lib.dsa_sync_status.argtypes = [vp]
+            lib.dsa_clear_status.argtypes = []
+            for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_bwd, lib.dsa_sync_status,
+                      lib.dsa_clear_status):
+                f.restype = ctypes.c_int
+            lib.dsa_last_error.argtypes = []
+            lib.dsa_last_error.restype = ctypes.c_char_p
+            lib.dsa_version.argtypes = []
+            lib.dsa_version.restype = ctypes.c_char_p
+            lib.dsa_profile_enable.argtypes = [ctypes.c_int]
+            lib.dsa_profile_enable.restype = None
+            lib.dsa_profile_read.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
+            lib.dsa_profile_read.restype = ctypes.c_int
+            lib.dsa_launch_count.argtypes = []
+            lib.dsa_launch_count.restype = ctypes.c_int64
+            lib.dsa_launch_count_reset.argtypes = []
+            lib.dsa_launch_count_reset.restype = None
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int):
+    if rc != DSA_OK:
+        raise DsaError(rc, load().dsa_last_error().decode())
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor (got shape {tuple(t.shape)})")
+
+
+def index_topk_workspace_size(S: int, Hi: int, Di: int, chunk: int, topk: int) -> int:
+    return int(load().dsa_index_topk_workspace(S, Hi, Di, chunk, topk))
+
+
+def sparse_attn_bwd_workspace_size(S: int, Hq: int, D: int) -> int:
+    return int(load().dsa_sparse_attn_bwd_workspace(S, Hq, D))
+
+
+def _workspace(nbytes: int, device, given):
+    if given is not None:
+        return given
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def dsa_index_topk(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int = 0, q_end: int | None = None,
+                   pool_idx=None, workspace=None, stream=None):
+    """pool_idx [q_end - q_begin, topk] int32 of the selected pools (ascending, -1 padded)."""
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    _need(k_idx, "k_idx", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    S, Hi, Di = q_idx.shape
+    if k_idx.shape != (S, Di) or w.shape != (S, Hi):
+        raise ValueError("k_idx must be [S, Di] and w [S, Hi]")
+    q_end = S if q_end is None else q_end
+    if pool_idx is None:
+        pool_idx = torch.empty((max(q_end - q_begin, 0), topk), dtype=torch.int32, device=q_idx.device)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    lib = load()
+    ws = _workspace(lib.dsa_index_topk_workspace(S, Hi, Di, chunk, topk), q_idx.device, workspace)
+    _check(lib.dsa_index_topk(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), S, Hi, Di, chunk, topk, q_begin,
+                              q_end, pool_idx.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+                              _stream_handle(stream)))
+    return pool_idx
+
+
+def dsa_sparse_attn_fwd(q, k, v, pool_idx, scale: float = 0.0, o=None, lse=None, stream=None):
+    """(o [S, Hq, D] bf16, lse [S, Hq] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 2)
+    _need(v, "v", torch.bfloat16, 2)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    S, Hq, D = q.shape
+    if k.shape != (S, D) or v.shape != (S, D) or pool_idx.shape[0] != S:
+        raise ValueError("k, v must be [S, D] and pool_idx [S, topk]")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(load().dsa_sparse_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S, Hq, D,
+                                      pool_idx.shape[1], float(scale), o.data_ptr(), lse.data_ptr(),
+                                      _stream_handle(stream)))
+    return o, lse
+
+
+def dsa_sparse_attn_bwd(dO, q, k, v, o, lse, pool_idx, scale: float = 0.0, dq=None, dk=None, dv=None,
+                        workspace=None, stream=None):
+    """(dq [S, Hq, D], dk [S, D], dv [S, D]) in bf16."""
+    for t, n, nd in ((dO, "dO", 3), (q, "q", 3), (o, "o", 3), (k, "k", 2), (v, "v", 2)):
+        _need(t, n, torch.bfloat16, nd)
+    _need(lse, "lse", torch.float32, 2)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    S, Hq, D = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = load()
+    ws = _workspace(lib.dsa_sparse_attn_bwd_workspace(S, Hq, D), q.device, workspace)
+    _check(lib.dsa_sparse_attn_bwd(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), pool_idx.data_ptr(), S, Hq, D, pool_idx.shape[1], float(scale),
+                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                                   ws.numel() * ws.element_size(), _stream_handle(stream)))
+    return dq, dk, dv
+
+
+def dsa_sync_status(stream=None):
+    """Synchronises the stream; raises DsaError if a kernel recorded a failed bounded wait or check."""
+    _check(load().dsa_sync_status(_stream_handle(stream)))
+
+
+def dsa_clear_status():
+    _check(load().dsa_clear_status())
+
+
+def profile_enable(on: bool = True):
+    """Record a CUDA event pair around every kernel launch (measurement only)."""
+    load().dsa_profile_enable(1 if on else 0)
+
+
+def profile_read() -> dict:
+    """{kernel name: (total device ms, launches)} since the last read; synchronises."""
+    lib = load()
+    n, name_len = 64, 64
+    names = ctypes.create_string_buffer(n * name_len)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    k = lib.dsa_profile_read(names, name_len, ms, cnt, n)
+    if k < 0:
+        raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
+    raw = names.raw
+    out = {}
+    for j in range(k):
+        nm = raw[j * name_len:(j + 1) * name_len].split(b"\0", 1)[0].decode()
+        out[nm] = (float(ms[j]), int(cnt[j]))
+    return out
+
+
+def launch_count() -> int:
+    return int(load().dsa_launch_count())
+
+
+def launch_count_reset():
+    load().dsa_launch_count_reset()
+
+
+def version() -> str:
+    return load().dsa_version().decode()

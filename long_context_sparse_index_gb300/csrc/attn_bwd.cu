@@ -1,0 +1,417 @@
+// attn_bwd.cu -- sparse attention backward over the selected key pools.
+//
+// [SkyRL-1M §模型与瓶颈] the selected-key attention is trained, so its
+// gradient flows to q, k and v.  For query i, head h and key j of its key set
+// (selected pools plus its own partial pool):
+//   P_hj  = exp(s_hj - lse_h)              s_hj = scale * q_h . k_j
+//   dS_hj = P_hj (dO_h . v_j - Delta_h)    Delta_h = dO_h . O_h
+//   dq_h  = scale * sum_j dS_hj k_j
+//   dk_j += scale * sum_h dS_hj q_h ;  dv_j += sum_h P_hj dO_h
+// The forward's lse lets P be recomputed instead of stored.
+//
+// One CTA (4 warps) per query gathers K and V blocks exactly as the forward
+// does.  Per warp and 16-key slice: S and dP on mma.sync, dQ accumulated in
+// registers, and the slice's dK/dV rows (16 keys x 128 dims, already summed
+// over the 16 heads by the MMA) added into fp32 accumulators with 16-byte
+// vector reductions.  A final kernel rounds the accumulators to bf16.
+#include "dsa_device.cuh"
+#include "dsa_kernels.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kHq = 16;
+constexpr int kD = 128;
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kBlkPools = 16;
+constexpr int kBlkKeys = 4 * kBlkPools;
+constexpr int kStages = 3;
+constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;
+constexpr uint32_t kStageBytes = 2 * kTileBytes;
+constexpr uint32_t kQBytes = kHq * kD * 2;
+constexpr uint32_t kTBytes = kHq * 16 * 2;  // per-warp [16 heads][16 keys] bf16 tile
+constexpr int kMaxTopk = 2048;
+constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 2 * kWarps * kTBytes;
+constexpr size_t smem_bytes(int topk) { return kSmemFixed + (topk + 8) * sizeof(int32_t); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>(r * 256 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* __restrict__ k,
+                                             const __nv_bfloat16* __restrict__ v, const int32_t* slots, int nsel,
+                                             int64_t i, int blk) {
+  const int64_t m = i >> 2;
+#pragma unroll
+  for (int u = 0; u < (kBlkKeys * 16) / kThreads; ++u) {
+    const int c = threadIdx.x + u * kThreads;
+    const int kr = c >> 4, cc = c & 15;
+    const int slot = blk * kBlkPools + (kr >> 2);
+    int64_t row = 0;
+    bool ok = false;
+    if (slot < nsel) {
+      const int32_t p = slots[slot];
+      row = 4 * static_cast<int64_t>(p) + (kr & 3);
+      ok = p >= 0;
+    } else if (slot == nsel) {
+      row = 4 * m + (kr & 3);
+      ok = row <= i;
+    }
+    const int64_t src = (ok ? row : 0) * kD + cc * 8;
+    cp_async16(st + swz(kr, cc), k + src, ok);
+    cp_async16(st + kTileBytes + swz(kr, cc), v + src, ok);
+  }
+}
+
+// Adds one 16-key x 8-dim C fragment (rows = keys) into acc[row, :] with
+// v4 reductions: the two lanes of a pair swap halves so each lane owns four
+// consecutive columns of one key.
+__device__ __forceinline__ void red_tile(float* __restrict__ acc, const float (&c)[4], int64_t row_g, bool ok_g,
+                                         int64_t row_g8, bool ok_g8, int col0, int t4, float mul) {
+  const bool odd = t4 & 1;
+  const float s0 = odd ? c[0] : c[2];
+  const float s1 = odd ? c[1] : c[3];
+  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+  const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+  if (!odd) {
+    if (ok_g) red_add_v4(acc + row_g * kD + col0 + 2 * t4, mul * c[0], mul * c[1], mul * r0, mul * r1);
+  } else {
+    if (ok_g8) red_add_v4(acc + row_g8 * kD + col0 + 2 * t4 - 2, mul * r0, mul * r1, mul * c[2], mul * c[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ q,
+                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                    const float* __restrict__ lse, const float* __restrict__ delta,
+                    const int32_t* __restrict__ pool_idx, int64_t S, int topk, float scale, float scale_log2,
+                    __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
+                    unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base;
+  const uint32_t sdO = base + kQBytes;
+  const uint32_t sKV = base + 2 * kQBytes;
+  const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P tile, then dS tile
+  int32_t* slots = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 2 * kWarps * kTBytes);
+  __shared__ int s_nsel;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int64_t i = blockIdx.x;
+  const int64_t n_elig = i >> 2;
+
+  if (tid == 0) s_nsel = topk;
+  __syncthreads();
+  const int32_t* prow = pool_idx + i * topk;
+  for (int j = tid; j < topk; j += kThreads) {
+    const int32_t p = prow[j];
+    if (p < 0) atomicMin(&s_nsel, j);
+    slots[j] = p;
+  }
+  __syncthreads();
+  const int nsel = s_nsel;
+  bool bad = false;
+  for (int j = tid; j < nsel; j += kThreads) {
+    const int32_t p = prow[j];
+    if (p >= n_elig) {
+      slots[j] = -1;
+      bad = true;
+    } else if (j > 0 && p <= prow[j - 1]) {
+      bad = true;
+    }
+  }
+  if (bad) record_status(status, kStatusInternal);
+  const int nblk = (nsel + 1 + kBlkPools - 1) / kBlkPools;
+
+  {
+    const __nv_bfloat16* qrow = q + i * (kHq * kD);
+    const __nv_bfloat16* drow = dO + i * (kHq * kD);
+#pragma unroll
+    for (int u = 0; u < (kHq * 16) / kThreads; ++u) {
+      const int c = tid + u * kThreads;
+      cp_async16(sQ + swz(c >> 4, c & 15), qrow + c * 8, true);
+      cp_async16(sdO + swz(c >> 4, c & 15), drow + c * 8, true);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, slots, nsel, i, s);
+    cp_async_commit();
+  }
+
+  // per-row constants (rows g and g+8 of this thread's fragments = heads)
+  const float lse2_0 = lse[i * kHq + g] * kLog2e, lse2_1 = lse[i * kHq + g + 8] * kLog2e;
+  const float dl0 = delta[i * kHq + g], dl1 = delta[i * kHq + g + 8];
+
+  float dq_acc[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) dq_acc[j][0] = dq_acc[j][1] = dq_acc[j][2] = dq_acc[j][3] = 0.f;
+  uint32_t qa[8][4], da[8][4];
+  const uint32_t sPt = sT + warp * 2 * kTBytes;
+  const uint32_t sDt = sPt + kTBytes;
+  uint8_t* gPt = gbase + (sPt - base);
+  uint8_t* gDt = gbase + (sDt - base);
+
+  for (int b = 0; b < nblk; ++b) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    if (b == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int mat = lane >> 3;
+        const int r = (lane & 7) + ((mat & 1) << 3);
+        const int c = 2 * kk + (mat >> 1);
+        ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        ldsm_x4(sdO + swz(r, c), da[kk][0], da[kk][1], da[kk][2], da[kk][3]);
+      }
+    }
+    {
+      const int nb = b + kStages - 1;
+      if (nb < nblk) gather_block(sKV + (nb % kStages) * kStageBytes, k, v, slots, nsel, i, nb);
+      cp_async_commit();
+    }
+    const uint32_t sK = sKV + (b % kStages) * kStageBytes;
+    const uint32_t sV = sK + kTileBytes;
+    const int key0 = warp * 16;
+
+    // S = Q K^T and dP = dO V^T for this warp's 16 keys
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int mat = lane >> 3;
+      const int r = key0 + ((mat >> 1) << 3) + (lane & 7);
+      const int c = 2 * kk + (mat & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sK + swz(r, c), b0, b1, b2, b3);
+      mma_bf16_16816(s0, qa[kk], b0, b1);
+      mma_bf16_16816(s1, qa[kk], b2, b3);
+      ldsm_x4(sV + swz(r, c), b0, b1, b2, b3);
+      mma_bf16_16816(p0, da[kk], b0, b1);
+      mma_bf16_16816(p1, da[kk], b2, b3);
+    }
+
+    // key validity and global rows of this thread's columns (2t, 2t+1, 8+2t, 9+2t)
+    // and of its dK/dV rows (keys g and g+8 of the slice)
+    bool valid[4];
+    {
+      const int kc[4] = {key0 + 2 * t4, key0 + 2 * t4 + 1, key0 + 8 + 2 * t4, key0 + 9 + 2 * t4};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int slot = b * kBlkPools + (kc[e] >> 2);
+        valid[e] = slot < nsel ? (slots[slot] >= 0) : (slot == nsel && 4 * n_elig + (kc[e] & 3) <= i);
+      }
+    }
+    int64_t krow[2];
+    bool kok[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int kb = key0 + g + 8 * e;
+      const int slot = b * kBlkPools + (kb >> 2);
+      if (slot < nsel) {
+        const int32_t p = slots[slot];
+        krow[e] = 4 * static_cast<int64_t>(p) + (kb & 3);
+        kok[e] = p >= 0;
+      } else {
+        krow[e] = 4 * n_elig + (kb & 3);
+        kok[e] = slot == nsel && krow[e] <= i;
+      }
+    }
+
+    // P and dS (fragment order: e=0..3 row g / g+8 for n-tile 0, then n-tile 1)
+    float P[8], dS[8];
+    {
+      const float sc[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
+      const float dp[8] = {p0[0], p0[1], p0[2], p0[3], p1[0], p1[1], p1[2], p1[3]};
+      const bool vm[8] = {valid[0], valid[1], valid[0], valid[1], valid[2], valid[3], valid[2], valid[3]};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool hi = (e & 2) != 0;  // row g+8
+        P[e] = vm[e] ? exp2f(sc[e] * scale_log2 - (hi ? lse2_1 : lse2_0)) : 0.f;
+        dS[e] = P[e] * (dp[e] - (hi ? dl1 : dl0));
+      }
+    }
+    uint32_t dsa[4];
+    dsa[0] = pack_bf16(dS[0], dS[1]);
+    dsa[1] = pack_bf16(dS[2], dS[3]);
+    dsa[2] = pack_bf16(dS[4], dS[5]);
+    dsa[3] = pack_bf16(dS[6], dS[7]);
+    // dQ += dS K (K rows are the k dimension: ldmatrix .trans)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int mat = lane >> 3;
+      const int r = key0 + ((mat & 1) << 3) + (lane & 7);
+      const int c = 2 * j + (mat >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sK + swz(r, c), b0, b1, b2, b3);
+      mma_bf16_16816(dq_acc[2 * j], dsa, b0, b1);
+      mma_bf16_16816(dq_acc[2 * j + 1], dsa, b2, b3);
+    }
+
+    // P and dS as [16 heads][16 keys] bf16 tiles -> A fragments of P^T and dS^T
+    {
+      uint32_t* pt = reinterpret_cast<uint32_t*>(gPt);
+      uint32_t* dt = reinterpret_cast<uint32_t*>(gDt);
+      // word index of (head, key pair) in a 32-B row: head * 8 + key / 2
+      pt[g * 8 + t4] = pack_bf16(P[0], P[1]);
+      pt[(g + 8) * 8 + t4] = pack_bf16(P[2], P[3]);
+      pt[g * 8 + 4 + t4] = pack_bf16(P[4], P[5]);
+      pt[(g + 8) * 8 + 4 + t4] = pack_bf16(P[6], P[7]);
+      dt[g * 8 + t4] = dsa[0];
+      dt[(g + 8) * 8 + t4] = dsa[1];
+      dt[g * 8 + 4 + t4] = dsa[2];
+      dt[(g + 8) * 8 + 4 + t4] = dsa[3];
+    }
+    __syncwarp();
+    uint32_t pta[4], dta[4];
+    {
+      const int mat = lane >> 3;
+      const int h = (lane & 7) + ((mat >> 1) << 3);
+      const uint32_t off = static_cast<uint32_t>(h * 32 + (mat & 1) * 16);
+      ldsm_x4_t(sPt + off, pta[0], pta[1], pta[2], pta[3]);
+      ldsm_x4_t(sDt + off, dta[0], dta[1], dta[2], dta[3]);
+    }
+    // dV rows += P^T dO ; dK rows += scale * dS^T Q   (16 keys x 128 dims)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int mat = lane >> 3;
+      const int r = (lane & 7) + ((mat & 1) << 3);
+      const int c = 2 * j + (mat >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sdO + swz(r, c), b0, b1, b2, b3);
+      float cv0[4] = {0.f, 0.f, 0.f, 0.f}, cv1[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16_16816(cv0, pta, b0, b1);
+      mma_bf16_16816(cv1, pta, b2, b3);
+      red_tile(dv_acc, cv0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4, 1.f);
+      red_tile(dv_acc, cv1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4, 1.f);
+      ldsm_x4_t(sQ + swz(r, c), b0, b1, b2, b3);
+      float ck0[4] = {0.f, 0.f, 0.f, 0.f}, ck1[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16_16816(ck0, dta, b0, b1);
+      mma_bf16_16816(ck1, dta, b2, b3);
+      red_tile(dk_acc, ck0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4, scale);
+      red_tile(dk_acc, ck1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4, scale);
+    }
+    __syncwarp();  // tiles are rewritten by the next slice
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- dq = scale * sum over the four warps' partial dq
+  float* red = reinterpret_cast<float*>(gbase + 2 * kQBytes);  // reuses the gather ring
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int col = 8 * j + 2 * t4;
+    *reinterpret_cast<float2*>(red + (warp * kHq + g) * kD + col) = make_float2(dq_acc[j][0], dq_acc[j][1]);
+    *reinterpret_cast<float2*>(red + (warp * kHq + g + 8) * kD + col) = make_float2(dq_acc[j][2], dq_acc[j][3]);
+  }
+  __syncthreads();
+  {
+    const int e0 = tid * 16;
+    uint32_t packed[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        a0 += red[w * kHq * kD + e0 + e];
+        a1 += red[w * kHq * kD + e0 + e + 1];
+      }
+      packed[e >> 1] = pack_bf16(scale * a0, scale * a1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(dq + i * (kHq * kD) + e0);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  }
+}
+
+// Delta[r] = dO[r,:] . O[r,:] for every (query, head) row r; zeroes the dK/dV
+// accumulators.  Half a warp per row, 8 dims per lane.
+__global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ o,
+                               int64_t rows, float* __restrict__ delta, float4* __restrict__ zero, int64_t nzero4) {
+  const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gt >> 4;
+  const int part = threadIdx.x & 15;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = reinterpret_cast<const uint4*>(dO + row * kD)[part];
+    const uint4 b = reinterpret_cast<const uint4*>(o + row * kD)[part];
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) delta[row] = acc;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t z = gt; z < nzero4; z += nthreads) zero[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void cast_kernel(const float* __restrict__ a, const float* __restrict__ b, int64_t n8,
+                            __nv_bfloat16* __restrict__ ao, __nv_bfloat16* __restrict__ bo) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= 2 * n8) return;
+  const bool second = t >= n8;
+  const int64_t e = second ? t - n8 : t;
+  const float4* src = reinterpret_cast<const float4*>(second ? b : a) + 2 * e;
+  const float4 x = src[0], y = src[1];
+  uint4 out = make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y), pack_bf16(y.z, y.w));
+  reinterpret_cast<uint4*>(second ? bo : ao)[e] = out;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t S, float* delta, float* dk_acc,
+                                float* dv_acc, const LaunchCtx& ctx) {
+  // dk_acc and dv_acc are adjacent in the workspace: zero 2 * S * D floats from dk_acc
+  (void)dv_acc;
+  const int64_t rows = S * kHq;
+  const int block = 256;
+  const int64_t grid = (rows * 16 + block - 1) / block;
+  bwd_pre_kernel<<<static_cast<unsigned>(grid), block, 0, ctx.stream>>>(
+      static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(o), rows, delta,
+      reinterpret_cast<float4*>(dk_acc), 2 * S * kD / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
+                            const float* delta, const int32_t* pool_idx, int64_t S, int topk, float scale, void* dq,
+                            float* dk_acc, float* dv_acc, const LaunchCtx& ctx) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes(kMaxTopk)));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
+  }
+  attn_bwd_kernel<<<static_cast<unsigned>(S), kThreads, smem_bytes(topk), ctx.stream>>>(
+      static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(q),
+      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), lse, delta, pool_idx, S, topk,
+      scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc, ctx.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_dkdv(const float* dk_acc, const float* dv_acc, int64_t n, void* dk, void* dv,
+                             const LaunchCtx& ctx) {
+  const int64_t n8 = n / 8;  // n = S * D, a multiple of 8
+  const int block = 256;
+  const int64_t grid = (2 * n8 + block - 1) / block;
+  if (grid == 0) return cudaSuccess;
+  cast_kernel<<<static_cast<unsigned>(grid), block, 0, ctx.stream>>>(dk_acc, dv_acc, n8,
+                                                                        static_cast<__nv_bfloat16*>(dk),
+                                                                        static_cast<__nv_bfloat16*>(dv));
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,325 @@
+// attn_fwd.cu -- sparse attention forward over the selected key pools.
+//
+// [SkyRL-1M §模型与瓶颈] each query attends to ~2048 selected keys (the 4
+// tokens of each selected pool) rather than to the whole prefix; here query i
+// also attends to its own partial pool {4*floor(i/4), ..., i}.  The 16 query
+// heads share one KV head, so one gathered K/V row serves all 16 heads.
+// [CP-lesson §改进二, evidence ②] the softmax is computed online over blocks
+// of keys, which reproduces the one-shot softmax exactly in real arithmetic.
+//
+// Layout of the work: one CTA (4 warps) per query.  The key list is walked in
+// blocks of 16 pool slots (64 keys); 128 threads gather the K and V rows of a
+// block with 16-byte cp.async copies into a 3-stage ring in shared memory
+// (rows XOR-swizzled in 16-B chunks so ldmatrix reads are conflict-free).
+// Warp w owns keys 16w..16w+15 of every block: S = Q K^T and O += P V run on
+// bf16 mma.sync (m16n8k16, M = the 16 heads), with the running max, the
+// normaliser and O in fp32 registers.  The four warps' partial softmax
+// states are merged through shared memory at the end.
+#include "dsa_device.cuh"
+#include "dsa_kernels.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kHq = 16;
+constexpr int kD = 128;
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kBlkPools = 16;
+constexpr int kBlkKeys = 4 * kBlkPools;       // 64
+constexpr int kStages = 3;
+constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;   // 16 KB (K or V of one block)
+constexpr uint32_t kStageBytes = 2 * kTileBytes;     // 32 KB
+constexpr uint32_t kQBytes = kHq * kD * 2;           // 4 KB
+constexpr int kMaxTopk = 2048;
+constexpr size_t kSmemFixed = 128 + kQBytes + kStages * kStageBytes;
+constexpr size_t smem_bytes(int topk) { return kSmemFixed + (topk + 8) * sizeof(int32_t); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// byte offset of 16-B chunk c (0..15) of row r in a swizzled [rows][256 B] tile
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>(r * 256 + ((c ^ (r & 7)) << 4));
+}
+
+// Gathers the K and V rows of block `blk` into stage buffer `st`.
+// Slot s < nsel holds pool slots[s]; slot nsel is the query's own pool m
+// (rows 4m .. i); slots beyond are empty.  Empty or out-of-range rows are
+// zero-filled (and masked by the caller).
+__device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* __restrict__ k,
+                                             const __nv_bfloat16* __restrict__ v, const int32_t* slots, int nsel,
+                                             int64_t i, int blk) {
+  const int64_t m = i >> 2;
+#pragma unroll
+  for (int u = 0; u < (kBlkKeys * 16) / kThreads; ++u) {
+    const int c = threadIdx.x + u * kThreads;  // 0 .. 1023: (key row, 16-B chunk)
+    const int kr = c >> 4, cc = c & 15;
+    const int slot = blk * kBlkPools + (kr >> 2);
+    int64_t row = 0;
+    bool ok = false;
+    if (slot < nsel) {
+      const int32_t p = slots[slot];
+      row = 4 * static_cast<int64_t>(p) + (kr & 3);
+      ok = p >= 0;
+    } else if (slot == nsel) {
+      row = 4 * m + (kr & 3);
+      ok = row <= i;
+    }
+    const int64_t src = (ok ? row : 0) * kD + cc * 8;
+    cp_async16(st + swz(kr, cc), k + src, ok);
+    cp_async16(st + kTileBytes + swz(kr, cc), v + src, ok);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                    const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t S, int topk,
+                    float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base;
+  const uint32_t sKV = base + kQBytes;
+  int32_t* slots = reinterpret_cast<int32_t*>(gbase + kQBytes + kStages * kStageBytes);
+  __shared__ int s_nsel;
+  __shared__ float s_m[kWarps][kHq], s_l[kWarps][kHq];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int64_t i = blockIdx.x;
+  const int64_t n_elig = i >> 2;
+
+  // ---- selected pools of this query (leading non-negative entries)
+  if (tid == 0) s_nsel = topk;
+  __syncthreads();
+  const int32_t* prow = pool_idx + i * topk;
+  for (int j = tid; j < topk; j += kThreads) {
+    const int32_t p = prow[j];
+    if (p < 0) atomicMin(&s_nsel, j);
+    slots[j] = p;
+  }
+  __syncthreads();
+  const int nsel = s_nsel;
+  // An entry that is not an eligible pool, or breaks ascending order, is
+  // recorded as a device-side check failure; ineligible entries become holes
+  // (-1: never read, always masked) so no access leaves the K/V rows.
+  bool bad = false;
+  for (int j = tid; j < nsel; j += kThreads) {
+    const int32_t p = prow[j];
+    if (p >= n_elig) {
+      slots[j] = -1;
+      bad = true;
+    } else if (j > 0 && p <= prow[j - 1]) {
+      bad = true;
+    }
+  }
+  if (bad) record_status(status, kStatusInternal);
+  const int nblk = (nsel + 1 + kBlkPools - 1) / kBlkPools;
+
+  // ---- Q tile (swizzled) and the gather pipeline prologue
+  {
+    const __nv_bfloat16* qrow = q + i * (kHq * kD);
+#pragma unroll
+    for (int u = 0; u < (kHq * 16) / kThreads; ++u) {
+      const int c = tid + u * kThreads;
+      cp_async16(sQ + swz(c >> 4, c & 15), qrow + c * 8, true);
+    }
+  }
+  __syncthreads();  // slots rewritten above are visible to the gather
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, slots, nsel, i, s);
+    cp_async_commit();
+  }
+
+  float o_acc[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o_acc[j][0] = o_acc[j][1] = o_acc[j][2] = o_acc[j][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  uint32_t qa[8][4];
+
+  for (int b = 0; b < nblk; ++b) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    if (b == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int mat = lane >> 3;
+        const int r = (lane & 7) + ((mat & 1) << 3);
+        const int c = 2 * kk + (mat >> 1);
+        ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
+    }
+    {
+      const int nb = b + kStages - 1;
+      if (nb < nblk) gather_block(sKV + (nb % kStages) * kStageBytes, k, v, slots, nsel, i, nb);
+      cp_async_commit();
+    }
+    const uint32_t sK = sKV + (b % kStages) * kStageBytes;
+    const uint32_t sV = sK + kTileBytes;
+    const int key0 = warp * 16;
+
+    // S = Q K^T for this warp's 16 keys (two n-tiles of 8)
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int mat = lane >> 3;
+      const int r = key0 + ((mat >> 1) << 3) + (lane & 7);
+      const int c = 2 * kk + (mat & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sK + swz(r, c), b0, b1, b2, b3);
+      mma_bf16_16816(s0, qa[kk], b0, b1);
+      mma_bf16_16816(s1, qa[kk], b2, b3);
+    }
+
+    // mask: slot of each of this thread's 4 key columns
+    float x[8];
+    {
+      const int kc[4] = {key0 + 2 * t4, key0 + 2 * t4 + 1, key0 + 8 + 2 * t4, key0 + 9 + 2 * t4};
+      bool valid[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int slot = b * kBlkPools + (kc[e] >> 2);
+        valid[e] = slot < nsel ? (slots[slot] >= 0) : (slot == nsel && 4 * n_elig + (kc[e] & 3) <= i);
+      }
+      x[0] = valid[0] ? s0[0] * scale_log2 : -INFINITY;
+      x[1] = valid[1] ? s0[1] * scale_log2 : -INFINITY;
+      x[2] = valid[0] ? s0[2] * scale_log2 : -INFINITY;
+      x[3] = valid[1] ? s0[3] * scale_log2 : -INFINITY;
+      x[4] = valid[2] ? s1[0] * scale_log2 : -INFINITY;
+      x[5] = valid[3] ? s1[1] * scale_log2 : -INFINITY;
+      x[6] = valid[2] ? s1[2] * scale_log2 : -INFINITY;
+      x[7] = valid[3] ? s1[3] * scale_log2 : -INFINITY;
+    }
+    // online softmax: row g holds x[0,1,4,5]; row g+8 holds x[2,3,6,7]
+    float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[4], x[5]));
+    float mx1 = fmaxf(fmaxf(x[2], x[3]), fmaxf(x[6], x[7]));
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m_run[0] - mu0), al1 = exp2f(m_run[1] - mu1);
+    float p[8];
+    p[0] = exp2f(x[0] - mu0);
+    p[1] = exp2f(x[1] - mu0);
+    p[4] = exp2f(x[4] - mu0);
+    p[5] = exp2f(x[5] - mu0);
+    p[2] = exp2f(x[2] - mu1);
+    p[3] = exp2f(x[3] - mu1);
+    p[6] = exp2f(x[6] - mu1);
+    p[7] = exp2f(x[7] - mu1);
+    l_run[0] = l_run[0] * al0 + (p[0] + p[1] + p[4] + p[5]);
+    l_run[1] = l_run[1] * al1 + (p[2] + p[3] + p[6] + p[7]);
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      o_acc[j][0] *= al0;
+      o_acc[j][1] *= al0;
+      o_acc[j][2] *= al1;
+      o_acc[j][3] *= al1;
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(p[0], p[1]);
+    pa[1] = pack_bf16(p[2], p[3]);
+    pa[2] = pack_bf16(p[4], p[5]);
+    pa[3] = pack_bf16(p[6], p[7]);
+    // O += P V: V rows are the k dimension (ldmatrix .trans)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int mat = lane >> 3;
+      const int r = key0 + ((mat & 1) << 3) + (lane & 7);
+      const int c = 2 * j + (mat >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sV + swz(r, c), b0, b1, b2, b3);
+      mma_bf16_16816(o_acc[2 * j], pa, b0, b1);
+      mma_bf16_16816(o_acc[2 * j + 1], pa, b2, b3);
+    }
+  }
+  cp_async_wait<0>();
+
+  // ---- merge the four warps' partial states
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {
+    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+  }
+  if (t4 == 0) {
+    s_m[warp][g] = m_run[0];
+    s_m[warp][g + 8] = m_run[1];
+    s_l[warp][g] = l_run[0];
+    s_l[warp][g + 8] = l_run[1];
+  }
+  __syncthreads();
+  float fac[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = g + 8 * hh;
+    float M = s_m[0][h];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_m[w][h]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) L += s_l[w][h] * exp2f(s_m[w][h] - M);
+    const float mine = m_run[hh] == -INFINITY ? 0.f : exp2f(m_run[hh] - M);
+    fac[hh] = mine / L;
+    if (warp == 0 && t4 == 0) lse[i * kHq + h] = (M + log2f(L)) * kLn2;
+  }
+  // partial O (already normalised) into shared memory, one [16][128] fp32 slab per warp
+  float* red = reinterpret_cast<float*>(gbase + kQBytes);  // reuses the gather ring
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int col = 8 * j + 2 * t4;
+    *reinterpret_cast<float2*>(red + (warp * kHq + g) * kD + col) =
+        make_float2(o_acc[j][0] * fac[0], o_acc[j][1] * fac[0]);
+    *reinterpret_cast<float2*>(red + (warp * kHq + g + 8) * kD + col) =
+        make_float2(o_acc[j][2] * fac[1], o_acc[j][3] * fac[1]);
+  }
+  __syncthreads();
+  // 16 x 128 outputs, 16 per thread, written as bf16x8 vectors
+  {
+    const int e0 = tid * 16;  // flat index into [16][128]
+    uint32_t packed[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        a0 += red[w * kHq * kD + e0 + e];
+        a1 += red[w * kHq * kD + e0 + e + 1];
+      }
+      packed[e >> 1] = pack_bf16(a0, a1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(o + i * (kHq * kD) + e0);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                            int topk, float scale, void* o, float* lse, const LaunchCtx& ctx) {
+  if (S <= 0) return cudaSuccess;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes(kMaxTopk)));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
+  }
+  attn_fwd_kernel<<<static_cast<unsigned>(S), kThreads, smem_bytes(topk), ctx.stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), pool_idx, S, topk, scale * kLog2e, static_cast<__nv_bfloat16*>(o), lse,
+      ctx.status);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,385 @@
+// dsa_api.cu -- the C ABI of libdsa (declared in include/dsa.h): argument
+// checks, workspace carving, TMA descriptors and the query-chunk loop.
+//
+// [SkyRL-1M §1 DSA 真稀疏; Anyscale "稀疏注意力会导致二次成本"] the indexer
+// scores one chunk of queries at a time, so its scratch is one chunk of
+// scores (chunk x pools x 4 B) rather than the whole S x S/4 matrix.
+// [Anyscale "检查每一层是否运行您认为的内核"] a shape the kernels do not
+// implement is an error, never a silent fallback.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dsa.h"
+#include "dsa_device.cuh"
+#include "dsa_kernels.h"
+
+namespace {
+
+__device__ unsigned int g_dsa_status;
+
+thread_local std::string g_last_error;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDi = 64;
+constexpr int kHq = 16;
+constexpr int kD = 128;
+constexpr int kMaxTopk = 2048;
+constexpr int kMaxHi = 64;
+constexpr int64_t kPoolTile = 256;
+
+dsa_status_t fail(dsa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+dsa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DeviceInfo {
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+dsa_status_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.num_sms == 0) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(DSA_ERR_UNSUPPORTED, "libdsa is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dsa_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<unsigned*>(p);
+    d.num_sms = sms;
+  }
+  *out = d;
+  return DSA_OK;
+}
+
+dsa_status_t make_ctx(void* stream, dsa::LaunchCtx* ctx) {
+  DeviceInfo d;
+  dsa_status_t st = device_info(&d);
+  if (st != DSA_OK) return st;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  ctx->status = d.status;
+  ctx->num_sms = d.num_sms;
+  // every device-side spin-wait gives up after this long (default 2 s)
+  double ms = 2000.0;
+  if (const char* s = getenv("DSA_WAIT_LIMIT_MS")) ms = atof(s);
+  ctx->inject_timeout = 0;
+  if (const char* s = getenv("DSA_FAULT_INJECT")) {
+    if (strcmp(s, "timeout") == 0) {
+      ctx->inject_timeout = 1;
+      ms = 1.0;
+    }
+  }
+  ctx->wait_limit_ns = static_cast<uint64_t>(ms * 1e6);
+  return DSA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// ---------------------------------------------------------------- launch accounting
+std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_profiling{0};
+std::mutex g_prof_mu;
+struct ProfRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::vector<ProfRec> g_prof;
+
+// Runs one launcher (each launches exactly one kernel), counting it and, when
+// profiling is on, bracketing it with events on the launch stream.
+template <typename F>
+cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
+  const bool prof = g_profiling.load(std::memory_order_relaxed) != 0;
+  ProfRec rec{name, nullptr, nullptr};
+  if (prof) {
+    cudaEventCreate(&rec.start);
+    cudaEventCreate(&rec.stop);
+    cudaEventRecord(rec.start, stream);
+  }
+  cudaError_t e = launch();
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (prof) {
+    cudaEventRecord(rec.stop, stream);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back(rec);
+  }
+  return e;
+}
+
+size_t index_ws_khat(int64_t S) { return round_up(static_cast<size_t>(S / 4 > 0 ? S / 4 : 1) * 2 * kDi * 2, 256); }
+int64_t pools_padded(int64_t S) { return ((S / 4 + kPoolTile - 1) / kPoolTile) * kPoolTile + (S / 4 == 0 ? kPoolTile : 0); }
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+const char* dsa_version(void) { return "libdsa 0.1.0 (sm_103a)"; }
+
+size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk) {
+  if (S < 1 || Hi < 1 || Di < 1 || chunk < 1 || topk < 1) return 0;
+  const int64_t rows = chunk < S ? chunk : S;
+  return index_ws_khat(S) + round_up(static_cast<size_t>(rows) * pools_padded(S) * sizeof(float), 256);
+}
+
+dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
+                            int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  if (!q_idx || !k_idx || !w || !pool_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: null tensor pointer");
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(pool_idx))
+    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: tensor pointers must be 16-byte aligned");
+  if (S < 1 || S > 0x7FFFFFFFLL) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: S=%lld out of range", (long long)S);
+  if (chunk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: chunk=%d must be >= 1", chunk);
+  if (topk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: topk=%d must be >= 1", topk);
+  if (Hi < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: Hi=%d must be >= 1", Hi);
+  if (q_begin < 0 || q_end > S || q_begin >= q_end)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: query range [%lld, %lld) not inside [0, %lld)",
+                (long long)q_begin, (long long)q_end, (long long)S);
+  if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Di=%d unsupported (kernels implement Di=64)", Di);
+  if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Hi=%d unsupported (max %d)", Hi, kMaxHi);
+  if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: topk=%d unsupported (max %d)", topk, kMaxTopk);
+  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk);
+  if (!workspace || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk: workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: workspace must be 256-byte aligned");
+
+  dsa::LaunchCtx ctx;
+  dsa_status_t st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+
+  const int64_t P = S / 4;
+  const int64_t ld = pools_padded(S);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* khat2 = ws;
+  float* scores = reinterpret_cast<float*>(ws + index_ws_khat(S));
+
+  CUtensorMap q_map, k_map;
+  const bool need_indexer = (q_end - 1) / 4 > topk;  // some row has more eligible pools than topk
+  if (need_indexer) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return fail(DSA_ERR_CUDA, "dsa_index_topk: cuTensorMapEncodeTiled unavailable from the driver");
+    {
+      cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDi), static_cast<cuuint64_t>(Hi), static_cast<cuuint64_t>(S)};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDi) * 2, static_cast<cuuint64_t>(Hi) * kDi * 2};
+      cuuint32_t box[3] = {static_cast<cuuint32_t>(kDi), 1u, 128u};
+      cuuint32_t estr[3] = {1u, 1u, 1u};
+      CUresult r = enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_idx), dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "dsa_index_topk: q_idx tensor map (CUresult %d)", (int)r);
+    }
+    {
+      cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * kDi), static_cast<cuuint64_t>(P)};
+      cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * kDi) * 2};
+      cuuint32_t box[2] = {static_cast<cuuint32_t>(kDi), static_cast<cuuint32_t>(kPoolTile)};
+      cuuint32_t estr[2] = {1u, 1u};
+      CUresult r = enc(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, khat2, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "dsa_index_topk: pooled-key tensor map (CUresult %d)", (int)r);
+    }
+    cudaError_t e = timed_launch("pool_keys", ctx.stream, [&] { return dsa::launch_pool_keys(k_idx, P, khat2, ctx); });
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: pool_keys launch");
+  }
+  for (int64_t c0 = q_begin; c0 < q_end; c0 += chunk) {
+    const int64_t c1 = c0 + chunk < q_end ? c0 + chunk : q_end;
+    const int nrows = static_cast<int>(c1 - c0);
+    if ((c1 - 1) / 4 > topk) {
+      cudaError_t e = timed_launch("indexer", ctx.stream,
+                                   [&] { return dsa::launch_indexer(q_map, k_map, w, scores, ld, c0, nrows, Hi, ctx); });
+      if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: indexer launch");
+    }
+    cudaError_t e = timed_launch("topk", ctx.stream, [&] {
+      return dsa::launch_topk(scores, ld, c0, nrows, topk, pool_idx + (c0 - q_begin) * topk, ctx);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: top-k launch");
+  }
+  return DSA_OK;
+}
+
+static dsa_status_t check_attn_args(const char* fn, int64_t S, int Hq, int D, int topk) {
+  if (S < 1 || S > 0x7FFFFFFFLL) return fail(DSA_ERR_INVALID_ARG, "%s: S=%lld out of range", fn, (long long)S);
+  if (topk < 1) return fail(DSA_ERR_INVALID_ARG, "%s: topk=%d must be >= 1", fn, topk);
+  if (Hq != kHq || D != kD)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: Hq=%d, D=%d unsupported (kernels implement Hq=16, D=128)", fn, Hq, D);
+  if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "%s: topk=%d unsupported (max %d)", fn, topk, kMaxTopk);
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                                 int Hq, int D, int topk, float scale, void* o, float* lse, void* stream) {
+  if (!q || !k || !v || !pool_idx || !o || !lse)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(pool_idx) || !aligned16(o) || !aligned16(lse))
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: tensor pointers must be 16-byte aligned");
+  dsa_status_t st = check_attn_args("dsa_sparse_attn_fwd", S, Hq, D, topk);
+  if (st != DSA_OK) return st;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  cudaError_t e = timed_launch("attn_fwd", ctx.stream,
+                               [&] { return dsa::launch_attn_fwd(q, k, v, pool_idx, S, topk, scale, o, lse, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_fwd: launch");
+  return DSA_OK;
+}
+
+size_t dsa_sparse_attn_bwd_workspace(int64_t S, int Hq, int D) {
+  if (S < 1 || Hq < 1 || D < 1) return 0;
+  return round_up(static_cast<size_t>(S) * D * sizeof(float), 256) * 2 +
+         round_up(static_cast<size_t>(S) * Hq * sizeof(float), 256);
+}
+
+dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const int32_t* pool_idx, int64_t S, int Hq, int D, int topk,
+                                 float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: null tensor pointer");
+  if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(pool_idx) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: tensor pointers must be 16-byte aligned");
+  dsa_status_t st = check_attn_args("dsa_sparse_attn_bwd", S, Hq, D, topk);
+  if (st != DSA_OK) return st;
+  const size_t need = dsa_sparse_attn_bwd_workspace(S, Hq, D);
+  if (!workspace || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "dsa_sparse_attn_bwd: workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: workspace must be 256-byte aligned");
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t acc_bytes = round_up(static_cast<size_t>(S) * D * sizeof(float), 256);
+  float* dk_acc = reinterpret_cast<float*>(ws);
+  float* dv_acc = reinterpret_cast<float*>(ws + acc_bytes);
+  float* delta = reinterpret_cast<float*>(ws + 2 * acc_bytes);
+  // S * D floats is a multiple of 64, so acc_bytes == S * D * 4 and the accumulators are adjacent
+  cudaError_t e = timed_launch("attn_bwd_pre", ctx.stream,
+                               [&] { return dsa::launch_attn_bwd_pre(dO, o, S, delta, dk_acc, dv_acc, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd: preprocess launch");
+  e = timed_launch("attn_bwd", ctx.stream, [&] {
+    return dsa::launch_attn_bwd(dO, q, k, v, lse, delta, pool_idx, S, topk, scale, dq, dk_acc, dv_acc, ctx);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd: launch");
+  e = timed_launch("attn_bwd_cast", ctx.stream,
+                   [&] { return dsa::launch_cast_dkdv(dk_acc, dv_acc, S * D, dk, dv, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd: cast launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sync_status: stream");
+  unsigned s = 0;
+  e = cudaMemcpyFromSymbol(&s, g_dsa_status, sizeof(s));
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sync_status: read status");
+  if (s & dsa::kStatusTimeout) return fail(DSA_ERR_TIMEOUT, "a bounded device-side wait ran out");
+  if (s & dsa::kStatusInternal) return fail(DSA_ERR_INTERNAL, "a device-side check failed (malformed pool_idx?)");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_clear_status(void) {
+  const unsigned z = 0;
+  cudaError_t e = cudaMemcpyToSymbol(g_dsa_status, &z, sizeof(z));
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_clear_status");
+  return DSA_OK;
+}
+
+void dsa_profile_enable(int on) { g_profiling.store(on ? 1 : 0); }
+
+int dsa_profile_read(char* names, int name_len, double* ms, int64_t* launches, int max_kernels) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  std::map<std::string, std::pair<double, int64_t>> agg;
+  std::vector<std::string> order;
+  bool ok = true;
+  for (ProfRec& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      ok = false;
+    if (!agg.count(r.name)) order.push_back(r.name);
+    agg[r.name].first += t;
+    agg[r.name].second += 1;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  if (!ok) {
+    fail(DSA_ERR_CUDA, "dsa_profile_read: event timing failed");
+    return -1;
+  }
+  int k = 0;
+  for (const std::string& n : order) {
+    if (k >= max_kernels) break;
+    if (names && name_len > 0) {
+      snprintf(names + static_cast<size_t>(k) * name_len, name_len, "%s", n.c_str());
+    }
+    if (ms) ms[k] = agg[n].first;
+    if (launches) launches[k] = agg[n].second;
+    ++k;
+  }
+  return k;
+}
+
+int64_t dsa_launch_count(void) { return g_launches.load(); }
+
+void dsa_launch_count_reset(void) { g_launches.store(0); }
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// dsa_kernels.h -- host-side launchers of the libdsa kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace dsa {
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  unsigned* status;        // device status word (kStatus* bits)
+  uint64_t wait_limit_ns;  // bound on every device-side spin-wait
+  int inject_timeout;      // fault injection: producers issue no copies, so waits run out
+  int num_sms;
+};
+
+// Pooled indexer keys: khat2 [P, 128] bf16, hi in columns 0..63, lo in 64..127.
+cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, const LaunchCtx& ctx);
+
+// Scores of query rows [row0, row0 + nrows) against pools [0, floor((row0+nrows-1)/4)):
+// scores[(i - row0) * ld + p]; entries p >= floor(i/4) are not meaningful.
+cudaError_t launch_indexer(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
+                           int64_t ld, int64_t row0, int nrows, int Hi, const LaunchCtx& ctx);
+size_t indexer_smem_bytes();
+
+// Per-row top-k of the scores written by launch_indexer; out rows are
+// pool_idx rows for queries row0 .. row0 + nrows - 1.
+cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows, int topk, int32_t* out,
+                        const LaunchCtx& ctx);
+
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                            int topk, float scale, void* o, float* lse, const LaunchCtx& ctx);
+
+cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t S, float* delta, float* dk_acc,
+                                float* dv_acc, const LaunchCtx& ctx);
+cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
+                            const float* delta, const int32_t* pool_idx, int64_t S, int topk, float scale, void* dq,
+                            float* dk_acc, float* dv_acc, const LaunchCtx& ctx);
+cudaError_t launch_cast_dkdv(const float* dk_acc, const float* dv_acc, int64_t n, void* dk, void* dv,
+                             const LaunchCtx& ctx);
+
+}  // namespace dsa

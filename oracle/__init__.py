@@ -58,7 +58,8 @@ def _load():
             lib.oracle_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, dbl, vp, i64, vp, vp]
             lib.oracle_attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, dbl, vp, i64, vp]
             lib.oracle_attn_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, dbl, vp, i64, vp, vp]
-            for name in ("oracle_num_threads", "oracle_pool_keys", "oracle_index_scores", "oracle_topk",
+            lib.oracle_attn_bwd_rows.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, dbl, vp, i64, vp, vp, vp]
+            for name in ("oracle_attn_bwd_rows", "oracle_num_threads", "oracle_pool_keys", "oracle_index_scores", "oracle_topk",
                          "oracle_index_topk", "oracle_attn_fwd", "oracle_attn_bwd_dq", "oracle_attn_bwd_dkdv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -163,3 +164,19 @@ def attn_bwd_dkdv(dO, q, k, v, pool_idx, scale=0.0, key_rows=None):
                                         pool_idx.ctypes.data, S, Hq, D, pool_idx.shape[1], float(scale),
                                         key_rows.ctypes.data, key_rows.size, dk.ctypes.data, dv.ctypes.data))
     return dk, dv
+
+
+def attn_bwd_rows(dO, q, k, v, pool_idx, scale=0.0, rows=None):
+    """Backward of the listed query rows -> (dq [n, Hq, D], dk [S, D], dv [S, D]) in double;
+    dk/dv hold only those rows' contributions (all rows: the whole backward)."""
+    dO, q, k, v = _c(dO, np.uint16), _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    pool_idx = _c(pool_idx, np.int32)
+    S, Hq, D = q.shape
+    rows = _rows(rows, S)
+    dq = np.empty((rows.size, Hq, D), np.float64)
+    dk = np.zeros((S, D), np.float64)
+    dv = np.zeros((S, D), np.float64)
+    _check(_load().oracle_attn_bwd_rows(dO.ctypes.data, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                        pool_idx.ctypes.data, S, Hq, D, pool_idx.shape[1], float(scale),
+                                        rows.ctypes.data, rows.size, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data))
+    return dq, dk, dv

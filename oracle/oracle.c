@@ -497,3 +497,59 @@ int oracle_attn_bwd_dkdv(const uint16_t* dO, const uint16_t* q, const uint16_t* 
   free(slot);
   return status;
 }
+
+/* Backward contributions of the listed query rows: dq [nrows, Hq, D] for
+ * those rows, and their dk/dv contributions added into dk, dv [S, D] (which
+ * the caller zeroes).  With every row listed this is the whole backward.
+ * Concurrent rows add into shared keys with atomic double additions. */
+int oracle_attn_bwd_rows(const uint16_t* dO, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const int32_t* pool_idx, int64_t S, int64_t Hq, int64_t D, int64_t topk, double scale,
+                         const int64_t* rows, int64_t nrows, double* dq, double* dk, double* dv) {
+  if (S < 0 || Hq <= 0 || D <= 0 || topk <= 0 || nrows < 0) return -1;
+  if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= S) return -1;
+  int status = 0;
+#pragma omp parallel
+  {
+    row_scratch w;
+    const int ok = row_scratch_init(&w, Hq, D, topk);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+      if (ok != 0) {
+#pragma omp atomic write
+        status = -3;
+        continue;
+      }
+      const int64_t i = rows[r];
+      const int64_t nk = backward_row(dO, q, k, v, pool_idx, Hq, D, topk, scale, i, &w);
+      if (nk < 0) {
+#pragma omp atomic write
+        status = -2;
+        continue;
+      }
+      for (int64_t h = 0; h < Hq; ++h)
+        for (int64_t d = 0; d < D; ++d) {
+          double acc = 0.0;
+          for (int64_t j = 0; j < nk; ++j) acc += w.dS[h * nk + j] * bf16(k[w.keys[j] * D + d]);
+          dq[(r * Hq + h) * D + d] = scale * acc;
+        }
+      for (int64_t j = 0; j < nk; ++j) {
+        const int64_t key = w.keys[j];
+        for (int64_t d = 0; d < D; ++d) {
+          double ak = 0.0, av = 0.0;
+          for (int64_t h = 0; h < Hq; ++h) {
+            ak += w.dS[h * nk + j] * bf16(q[(i * Hq + h) * D + d]);
+            av += w.P[h * nk + j] * bf16(dO[(i * Hq + h) * D + d]);
+          }
+#pragma omp atomic
+          dk[key * D + d] += scale * ak;
+#pragma omp atomic
+          dv[key * D + d] += av;
+        }
+      }
+    }
+    row_scratch_free(&w);
+  }
+  return status;
+}

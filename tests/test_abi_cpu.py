@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/dsa.h declares, and rejects bad arguments with the
+documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from long_context_sparse_index_gb300 import build as b
+    b.build()
+    import long_context_sparse_index_gb300 as dsa
+    return dsa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls_and_helpers():
+    names = declared_functions()
+    for n in ("dsa_index_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_index_topk_workspace",
+              "dsa_sparse_attn_bwd_workspace", "dsa_sync_status", "dsa_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import long_context_sparse_index_gb300 as dsa
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in dsa.EXPORTED or name in ("dsa_index_topk_workspace",)
+
+
+def test_version(lib):
+    assert lib.dsa_version().startswith(b"libdsa")
+
+
+def test_workspace_sizes(lib):
+    # pooled keys (256 B per pool) + one chunk of fp32 scores (pools padded to 256)
+    S, chunk = 131072, 256
+    P = S // 4
+    assert lib.dsa_index_topk_workspace(S, 32, 64, chunk, 512) == P * 256 + chunk * P * 4
+    assert lib.dsa_index_topk_workspace(0, 32, 64, chunk, 512) == 0
+    # chunk larger than S is clamped to S rows
+    assert lib.dsa_index_topk_workspace(1000, 8, 64, 4096, 64) == lib.dsa_index_topk_workspace(1000, 8, 64, 1000, 64)
+    assert lib.dsa_sparse_attn_bwd_workspace(S, 16, 128) == 2 * S * 128 * 4 + S * 16 * 4
+
+
+FAKE = 0x10000  # 16-byte aligned dummy address; calls below fail validation before any device access
+
+
+def _idx(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, w=FAKE, S=1024, Hi=8, Di=64, chunk=128, topk=64, b=0, e=1024, out=FAKE, ws=FAKE,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.dsa_index_topk(a["q"], a["k"], a["w"], a["S"], a["Hi"], a["Di"], a["chunk"], a["topk"], a["b"], a["e"],
+                              a["out"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_index_topk_rejects_bad_arguments(lib):
+    import long_context_sparse_index_gb300 as dsa
+    assert _idx(lib, q=None) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, w=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, S=0) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, chunk=0) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, topk=0) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, b=10, e=10) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, e=1025) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, Di=128) == dsa.DSA_ERR_UNSUPPORTED
+    assert _idx(lib, Hi=65) == dsa.DSA_ERR_UNSUPPORTED
+    assert _idx(lib, topk=4096) == dsa.DSA_ERR_UNSUPPORTED
+    assert _idx(lib, wsb=100) == dsa.DSA_ERR_WORKSPACE
+    assert _idx(lib, ws=None) == dsa.DSA_ERR_WORKSPACE
+    assert _idx(lib, ws=FAKE + 16) == dsa.DSA_ERR_INVALID_ARG
+    assert b"workspace" in lib.dsa_last_error()
+
+
+def test_attention_rejects_bad_arguments(lib):
+    import long_context_sparse_index_gb300 as dsa
+    f = lib.dsa_sparse_attn_fwd
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 16, 128, 8, 0.0, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 8, 128, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 16, 64, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 16, 128, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_INVALID_ARG
+    b = lib.dsa_sparse_attn_bwd
+    args = [FAKE] * 7 + [64, 16, 128, 8, 0.0] + [FAKE] * 3
+    assert b(*args, FAKE, 16, None) == dsa.DSA_ERR_WORKSPACE
+    assert b(*args, None, 1 << 30, None) == dsa.DSA_ERR_WORKSPACE
+    assert b(*args[:7], 64, 16, 128, 4096, 0.0, *args[12:], FAKE, 1 << 30, None) == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_no_device_reports_cuda_error_not_crash(lib):
+    """With valid arguments but no usable GPU the call fails with DSA_ERR_CUDA
+    (or runs, on a GPU host) -- it never falls back to another path."""
+    import long_context_sparse_index_gb300 as dsa
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    assert _idx(lib) == dsa.DSA_ERR_CUDA
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import long_context_sparse_index_gb300 as dsa
+    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        dsa.dsa_index_topk(q, torch.zeros(8, 64, dtype=torch.bfloat16), torch.zeros(8, 2), chunk=4, topk=1)

@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests._util import (assert_close, bits_to_torch, check_selection_scores, check_selection_valid,
+                         torch_bf16_to_f64)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import long_context_sparse_index_gb300 as dsa
+DEV = "cuda"
+
+
+def _indexer_to_gpu(q_idx, k_idx, w):
+    return bits_to_torch(q_idx, DEV), bits_to_torch(k_idx, DEV), torch.from_numpy(w).to(DEV)
+
+
+def _attn_to_gpu(*arrs):
+    return [bits_to_torch(a, DEV) for a in arrs]
+
+
+# --------------------------------------------------------------------------- indexer + top-k
+
+@pytest.mark.parametrize("chunk", [1, 7, 64, 256, 2048])
+def test_index_topk_tiny_int_bit_exact_every_chunk(chunk):
+    """Integer inputs: all arithmetic exact, so pool indices are bit-exact,
+    and the result is the same for every query chunk."""
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=chunk, topk=wl.topk)
+    dsa.dsa_sync_status()
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_index_topk_query_range_shards_concatenate():
+    """Query-range shards computed separately equal the unsharded call (the
+    query-sharded indexer: each shard scores only its own queries)."""
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q, k, w = _indexer_to_gpu(*synth.indexer_inputs(wl))
+    full = dsa.dsa_index_topk(q, k, w, chunk=256, topk=wl.topk)
+    parts = [dsa.dsa_index_topk(q, k, w, chunk=100, topk=wl.topk, q_begin=a, q_end=b)
+             for a, b in ((0, 333), (333, 1024), (1024, 1999), (1999, 2048))]
+    dsa.dsa_sync_status()
+    assert torch.equal(torch.cat(parts), full)
+
+
+@pytest.mark.parametrize("S,Hi,topk,chunk", [(1, 1, 1, 1), (2, 3, 1, 5), (3, 1, 4, 2), (4, 2, 1, 4), (5, 1, 1, 3),
+                                             (9, 4, 1, 4), (37, 5, 3, 10), (255, 1, 2, 300), (257, 8, 16, 64),
+                                             (1023, 2, 64, 129), (1030, 8, 255, 500), (3001, 16, 100, 1000)])
+def test_index_topk_edge_shapes_int(S, Hi, topk, chunk):
+    """Ragged S (not a multiple of 4, smaller than a tile), topk larger than
+    the available pools, chunk not dividing S, a single head."""
+    q_idx = synth.int_bf16(S, 1, (S, Hi, 64), -3, 3)
+    k_idx = synth.int_bf16(S, 2, (S, 64), -3, 3)
+    w = synth.int_f32(S, 3, (S, Hi), -1, 3)
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, topk)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=chunk, topk=topk)
+    dsa.dsa_sync_status()
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_index_topk_all_ties_take_lowest_pools():
+    """All scores equal (zero queries): every row keeps pools 0..topk-1."""
+    S, Hi, topk = 1500, 4, 17
+    q_idx = np.zeros((S, Hi, 64), np.uint16)
+    k_idx = synth.int_bf16(5, 2, (S, 64), -3, 3)
+    w = np.ones((S, Hi), np.float32)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=256, topk=topk).cpu().numpy()
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, topk)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(got[-1], np.arange(topk))
+
+
+def test_index_topk_s16k_float_selection_within_tolerance():
+    """bf16 N(0,1) inputs at S=16384, 32 heads, top 512, chunk 256: every GPU
+    row is a valid selection and every selected pool scores within 1e-3 of
+    the oracle's k-th score."""
+    wl = synth.WORKLOADS["s16k"]
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=wl.chunk, topk=wl.topk).cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(0, 4100, 7), np.arange(wl.S - 64, wl.S),
+                                     np.random.RandomState(0).randint(2052, wl.S, 400)]))
+    check_selection_valid(got[rows], rows, wl.topk)
+    scores = oracle.index_scores(q_idx, k_idx, w, rows=rows)
+    ref, kth = oracle.index_topk(q_idx, k_idx, w, wl.topk, rows=rows)
+    check_selection_scores(got[rows], rows, scores, kth, wl.topk)
+    agree = np.mean([len(np.intersect1d(a[a >= 0], b[b >= 0])) / max(1, (b >= 0).sum()) for a, b in zip(got[rows], ref)])
+    assert agree > 0.99, agree
+
+
+# --------------------------------------------------------------------------- attention forward
+
+def _fwd_check(q, k, v, sel, rows=None, scale=0.0):
+    qt, kt, vt = _attn_to_gpu(q, k, v)
+    o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, torch.from_numpy(sel).to(DEV), scale=scale)
+    dsa.dsa_sync_status()
+    ro, rl = oracle.attn_fwd(q, k, v, sel, scale=scale, rows=rows)
+    go = torch_bf16_to_f64(o)
+    gl = lse.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        go, gl = go[rows], gl[rows]
+    assert_close(go, ro, "o")
+    assert_close(gl, rl, "lse", bf16_out=False)
+
+
+def test_attn_fwd_tiny_int_with_oracle_selection():
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    sel, _ = oracle.index_topk(*synth.indexer_inputs(wl), wl.topk)
+    _fwd_check(*synth.attention_inputs(wl), sel)
+
+
+@pytest.mark.parametrize("S,topk", [(1, 1), (2, 4), (5, 1), (7, 3), (64, 16), (301, 8), (4096, 512), (4099, 100)])
+def test_attn_fwd_normal_edge_shapes(S, topk):
+    wl = synth.Workload("t", S, topk=topk, seed=S)
+    q, k, v = synth.attention_inputs(wl)
+    sel = synth.stand_in_selection(wl)
+    _fwd_check(q, k, v, sel, scale=0.0 if S % 2 else 0.07)
+
+
+# --------------------------------------------------------------------------- attention backward
+
+def _bwd_check(q, k, v, dO, sel, q_rows=None, key_rows=None, scale=0.0):
+    qt, kt, vt, dOt = _attn_to_gpu(q, k, v, dO)
+    st = torch.from_numpy(sel).to(DEV)
+    o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, st, scale=scale)
+    dq, dk, dv = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st, scale=scale)
+    dsa.dsa_sync_status()
+    rdq = oracle.attn_bwd_dq(dO, q, k, v, sel, scale=scale, rows=q_rows)
+    rdk, rdv = oracle.attn_bwd_dkdv(dO, q, k, v, sel, scale=scale, key_rows=key_rows)
+    gdq, gdk, gdv = torch_bf16_to_f64(dq), torch_bf16_to_f64(dk), torch_bf16_to_f64(dv)
+    if q_rows is not None:
+        gdq = gdq[q_rows]
+    if key_rows is not None:
+        gdk, gdv = gdk[key_rows], gdv[key_rows]
+    assert_close(gdq, rdq, "dq")
+    assert_close(gdk, rdk, "dk")
+    assert_close(gdv, rdv, "dv")
+
+
+def test_attn_bwd_tiny_int():
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    sel, _ = oracle.index_topk(*synth.indexer_inputs(wl), wl.topk)
+    q, k, v = synth.attention_inputs(wl)
+    # integer values in [-2, 2] give large logits; a small scale keeps the softmax soft
+    _bwd_check(q, k, v, synth.grad_output(wl), sel, scale=0.02)
+
+
+@pytest.mark.parametrize("S,topk", [(1, 1), (6, 2), (67, 4), (4096, 256), (2051, 512)])
+def test_attn_bwd_normal_edge_shapes(S, topk):
+    wl = synth.Workload("t", S, topk=topk, seed=100 + S)
+    q, k, v = synth.attention_inputs(wl)
+    _bwd_check(q, k, v, synth.grad_output(wl), synth.stand_in_selection(wl))
+
+
+def test_attn_bwd_repeatable_within_rounding():
+    """dK/dV use atomic reductions: two runs agree to fp32 rounding."""
+    wl = synth.Workload("t", 4096, topk=256, seed=7, values="zipf")
+    q, k, v = synth.attention_inputs(wl)
+    qt, kt, vt, dOt = _attn_to_gpu(q, k, v, synth.grad_output(wl))
+    st = torch.from_numpy(synth.stand_in_selection(wl)).to(DEV)
+    o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, st)
+    a = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st)
+    b = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st)
+    assert torch.equal(a[0], b[0])
+    for x, y in zip(a[1:], b[1:]):
+        assert (x.float() - y.float()).abs().max().item() <= 2 ** -6 * max(1.0, x.float().abs().max().item())
+
+
+# --------------------------------------------------------------------------- device status / bounded waits
+
+def test_bounded_wait_timeout_reports_status():
+    """With fault injection the indexer's producer issues no copies, so every
+    bounded wait runs out; the kernels return, the host reads DSA_ERR_TIMEOUT,
+    and the context stays usable."""
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q, k, w = _indexer_to_gpu(*synth.indexer_inputs(wl))
+    dsa.dsa_clear_status()
+    os.environ["DSA_FAULT_INJECT"] = "timeout"
+    try:
+        dsa.dsa_index_topk(q, k, w, chunk=2048, topk=wl.topk)
+        with pytest.raises(dsa.DsaError) as ei:
+            dsa.dsa_sync_status()
+        assert ei.value.status == dsa.DSA_ERR_TIMEOUT
+    finally:
+        del os.environ["DSA_FAULT_INJECT"]
+    dsa.dsa_clear_status()
+    got = dsa.dsa_index_topk(q, k, w, chunk=2048, topk=wl.topk)
+    dsa.dsa_sync_status()
+    ref, _ = oracle.index_topk(*synth.indexer_inputs(wl), wl.topk)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_malformed_selection_is_reported_not_read():
+    """An ineligible pool index is never dereferenced and is reported as DSA_ERR_INTERNAL."""
+    S, topk = 256, 8
+    wl = synth.Workload("t", S, topk=topk, seed=3)
+    q, k, v = _attn_to_gpu(*synth.attention_inputs(wl))
+    sel = synth.stand_in_selection(wl)
+    sel[200, 0] = 10 ** 6
+    dsa.dsa_clear_status()
+    dsa.dsa_sparse_attn_fwd(q, k, v, torch.from_numpy(sel).to(DEV))
+    with pytest.raises(dsa.DsaError) as ei:
+        dsa.dsa_sync_status()
+    assert ei.value.status == dsa.DSA_ERR_INTERNAL
+    dsa.dsa_clear_status()

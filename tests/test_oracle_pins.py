@@ -375,3 +375,16 @@ def test_attn_backward_finite_differences():
             lm = loss(q, shifted(kk, (j, d2), -h) if name == "k" else kk, shifted(vv, (j, d2), -h) if name == "v" else vv)
             fd = (lp - lm) / (2 * h)
             assert abs(fd - gg[j, d2]) < 2e-3 * max(1.0, abs(fd)), (name, fd, gg[j, d2])
+
+
+def test_attn_backward_rows_whole_equals_per_key():
+    """The row-set backward over every row equals the per-key form (pinned to autograd above)."""
+    S, Hq, D, topk = 80, 2, 8, 3
+    q, k, v, dO = _attn_inputs(S, Hq, D, 29)
+    sel = synth.pool_selection(9, 8, S, topk, hot=np.array([2]))
+    dq, dk, dv = oracle.attn_bwd_rows(dO, q, k, v, sel)
+    dq2 = oracle.attn_bwd_dq(dO, q, k, v, sel)
+    dk2, dv2 = oracle.attn_bwd_dkdv(dO, q, k, v, sel)
+    np.testing.assert_allclose(dq, dq2, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dk, dk2, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dv, dv2, rtol=1e-12, atol=1e-14)
