@@ -32,7 +32,7 @@ constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kQBytes = kHq * kD * 2;
 constexpr uint32_t kTBytes = kHq * 16 * 2;  // per-warp [16 heads][16 keys] bf16 tile
 constexpr int kMaxTopk = 2048;
-constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 2 * kWarps * kTBytes;
+constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes;
 constexpr size_t smem_bytes(int topk) { return kSmemFixed + (topk + 8) * sizeof(int32_t); }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -66,23 +66,6 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
   }
 }
 
-// Adds one 16-key x 8-dim C fragment (rows = keys) into acc[row, :] with
-// v4 reductions: the two lanes of a pair swap halves so each lane owns four
-// consecutive columns of one key.
-__device__ __forceinline__ void red_tile(float* __restrict__ acc, const float (&c)[4], int64_t row_g, bool ok_g,
-                                         int64_t row_g8, bool ok_g8, int col0, int t4, float mul) {
-  const bool odd = t4 & 1;
-  const float s0 = odd ? c[0] : c[2];
-  const float s1 = odd ? c[1] : c[3];
-  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
-  const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
-  if (!odd) {
-    if (ok_g) red_add_v4(acc + row_g * kD + col0 + 2 * t4, mul * c[0], mul * c[1], mul * r0, mul * r1);
-  } else {
-    if (ok_g8) red_add_v4(acc + row_g8 * kD + col0 + 2 * t4 - 2, mul * r0, mul * r1, mul * c[2], mul * c[3]);
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 2)
     attn_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ q,
                     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
@@ -97,8 +80,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sQ = base;
   const uint32_t sdO = base + kQBytes;
   const uint32_t sKV = base + 2 * kQBytes;
-  const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P tile, then dS tile
-  int32_t* slots = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 2 * kWarps * kTBytes);
+  const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P hi, P lo, dS hi, dS lo tiles
+  int32_t* slots = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes);
   __shared__ int s_nsel;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -153,11 +136,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   float dq_acc[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j) dq_acc[j][0] = dq_acc[j][1] = dq_acc[j][2] = dq_acc[j][3] = 0.f;
-  uint32_t qa[8][4], da[8][4];
-  const uint32_t sPt = sT + warp * 2 * kTBytes;
-  const uint32_t sDt = sPt + kTBytes;
-  uint8_t* gPt = gbase + (sPt - base);
-  uint8_t* gDt = gbase + (sDt - base);
+  uint32_t qa[8][4];
+  const uint32_t sTw = sT + warp * 4 * kTBytes;
+  uint8_t* gT = gbase + (sTw - base);
 
   for (int b = 0; b < nblk; ++b) {
     cp_async_wait<kStages - 2>();
@@ -169,7 +150,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int r = (lane & 7) + ((mat & 1) << 3);
         const int c = 2 * kk + (mat >> 1);
         ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-        ldsm_x4(sdO + swz(r, c), da[kk][0], da[kk][1], da[kk][2], da[kk][3]);
       }
     }
     {
@@ -193,9 +173,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       ldsm_x4(sK + swz(r, c), b0, b1, b2, b3);
       mma_bf16_16816(s0, qa[kk], b0, b1);
       mma_bf16_16816(s1, qa[kk], b2, b3);
+      uint32_t da[4];
+      {
+        const int ra = (lane & 7) + ((mat & 1) << 3);
+        const int ca = 2 * kk + (mat >> 1);
+        ldsm_x4(sdO + swz(ra, ca), da[0], da[1], da[2], da[3]);
+      }
       ldsm_x4(sV + swz(r, c), b0, b1, b2, b3);
-      mma_bf16_16816(p0, da[kk], b0, b1);
-      mma_bf16_16816(p1, da[kk], b2, b3);
+      mma_bf16_16816(p0, da, b0, b1);
+      mma_bf16_16816(p1, da, b2, b3);
     }
 
     // key validity and global rows of this thread's columns (2t, 2t+1, 8+2t, 9+2t)
@@ -209,22 +195,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         valid[e] = slot < nsel ? (slots[slot] >= 0) : (slot == nsel && 4 * n_elig + (kc[e] & 3) <= i);
       }
     }
-    int64_t krow[2];
-    bool kok[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int kb = key0 + g + 8 * e;
-      const int slot = b * kBlkPools + (kb >> 2);
-      if (slot < nsel) {
-        const int32_t p = slots[slot];
-        krow[e] = 4 * static_cast<int64_t>(p) + (kb & 3);
-        kok[e] = p >= 0;
-      } else {
-        krow[e] = 4 * n_elig + (kb & 3);
-        kok[e] = slot == nsel && krow[e] <= i;
-      }
-    }
-
     // P and dS (fragment order: e=0..3 row g / g+8 for n-tile 0, then n-tile 1)
     float P[8], dS[8];
     {
@@ -255,48 +225,94 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_bf16_16816(dq_acc[2 * j + 1], dsa, b2, b3);
     }
 
-    // P and dS as [16 heads][16 keys] bf16 tiles -> A fragments of P^T and dS^T
+    // P and dS as [16 heads][16 keys] bf16 tiles, each split into hi + lo
+    // (x = hi + lo to ~2^-17): the dK/dV sums run over thousands of queries
+    // for popular keys, where a single bf16 rounding of P or dS accumulates
+    // beyond the gradient tolerance.  Tiles: P hi, P lo, dS hi, dS lo.
     {
-      uint32_t* pt = reinterpret_cast<uint32_t*>(gPt);
-      uint32_t* dt = reinterpret_cast<uint32_t*>(gDt);
-      // word index of (head, key pair) in a 32-B row: head * 8 + key / 2
-      pt[g * 8 + t4] = pack_bf16(P[0], P[1]);
-      pt[(g + 8) * 8 + t4] = pack_bf16(P[2], P[3]);
-      pt[g * 8 + 4 + t4] = pack_bf16(P[4], P[5]);
-      pt[(g + 8) * 8 + 4 + t4] = pack_bf16(P[6], P[7]);
-      dt[g * 8 + t4] = dsa[0];
-      dt[(g + 8) * 8 + t4] = dsa[1];
-      dt[g * 8 + 4 + t4] = dsa[2];
-      dt[(g + 8) * 8 + 4 + t4] = dsa[3];
+      uint32_t* tw = reinterpret_cast<uint32_t*>(gT);
+      const int widx[4] = {g * 8 + t4, (g + 8) * 8 + t4, g * 8 + 4 + t4, (g + 8) * 8 + 4 + t4};
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const float* x = m == 0 ? P : dS;
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          const uint32_t hi = pack_bf16(x[2 * qd], x[2 * qd + 1]);
+          const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+          tw[(2 * m) * 128 + widx[qd]] = hi;
+          tw[(2 * m + 1) * 128 + widx[qd]] = pack_bf16(x[2 * qd] - h0, x[2 * qd + 1] - h1);
+        }
+      }
     }
     __syncwarp();
-    uint32_t pta[4], dta[4];
+    uint32_t pth[4], ptl[4], dth[4], dtl[4];
     {
       const int mat = lane >> 3;
       const int h = (lane & 7) + ((mat >> 1) << 3);
       const uint32_t off = static_cast<uint32_t>(h * 32 + (mat & 1) * 16);
-      ldsm_x4_t(sPt + off, pta[0], pta[1], pta[2], pta[3]);
-      ldsm_x4_t(sDt + off, dta[0], dta[1], dta[2], dta[3]);
+      ldsm_x4_t(sTw + 0 * kTBytes + off, pth[0], pth[1], pth[2], pth[3]);
+      ldsm_x4_t(sTw + 1 * kTBytes + off, ptl[0], ptl[1], ptl[2], ptl[3]);
+      ldsm_x4_t(sTw + 2 * kTBytes + off, dth[0], dth[1], dth[2], dth[3]);
+      ldsm_x4_t(sTw + 3 * kTBytes + off, dtl[0], dtl[1], dtl[2], dtl[3]);
     }
-    // dV rows += P^T dO ; dK rows += scale * dS^T Q   (16 keys x 128 dims)
+    // This warp's K and V rows are no longer read: they become the fp32
+    // staging tile [16 keys][128 dims] (rows 0-7 in the K slice, 8-15 in the
+    // V slice, 16-B chunks XOR-swizzled by row) so each reduction below covers
+    // one whole 512-B key row.
+    uint8_t* stage_k = gbase + (sK - base) + key0 * 256;
+    uint8_t* stage_v = gbase + (sV - base) + key0 * 256;
+    // dV rows = P^T dO, then dK rows = scale * dS^T Q   (16 keys x 128 dims)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int mat = lane >> 3;
-      const int r = (lane & 7) + ((mat & 1) << 3);
-      const int c = 2 * j + (mat >> 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sdO + swz(r, c), b0, b1, b2, b3);
-      float cv0[4] = {0.f, 0.f, 0.f, 0.f}, cv1[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16_16816(cv0, pta, b0, b1);
-      mma_bf16_16816(cv1, pta, b2, b3);
-      red_tile(dv_acc, cv0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4, 1.f);
-      red_tile(dv_acc, cv1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4, 1.f);
-      ldsm_x4_t(sQ + swz(r, c), b0, b1, b2, b3);
-      float ck0[4] = {0.f, 0.f, 0.f, 0.f}, ck1[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16_16816(ck0, dta, b0, b1);
-      mma_bf16_16816(ck1, dta, b2, b3);
-      red_tile(dk_acc, ck0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4, scale);
-      red_tile(dk_acc, ck1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4, scale);
+    for (int pass = 0; pass < 2; ++pass) {
+      const uint32_t (&ah)[4] = pass == 0 ? pth : dth;
+      const uint32_t (&al)[4] = pass == 0 ? ptl : dtl;
+      const uint32_t sB = pass == 0 ? sdO : sQ;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int mat = lane >> 3;
+        const int r = (lane & 7) + ((mat & 1) << 3);
+        const int c = 2 * j + (mat >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sB + swz(r, c), b0, b1, b2, b3);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(c0, ah, b0, b1);
+        mma_bf16_16816(c0, al, b0, b1);
+        mma_bf16_16816(c1, ah, b2, b3);
+        mma_bf16_16816(c1, al, b2, b3);
+        // n-tile 2j covers dims 16j..16j+7, n-tile 2j+1 dims 16j+8..16j+15
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float* cc = half == 0 ? c0 : c1;
+          const int chunk = 4 * j + 2 * half + (t4 >> 1);
+          const int sub = (t4 & 1) * 8;
+          *reinterpret_cast<float2*>(stage_k + g * 512 + ((chunk ^ g) << 4) + sub) = make_float2(cc[0], cc[1]);
+          *reinterpret_cast<float2*>(stage_v + g * 512 + ((chunk ^ g) << 4) + sub) = make_float2(cc[2], cc[3]);
+        }
+      }
+      __syncwarp();
+      float* acc = pass == 0 ? dv_acc : dk_acc;
+      const float mul = pass == 0 ? 1.f : scale;
+#pragma unroll 4
+      for (int r = 0; r < 16; ++r) {
+        const int kb = key0 + r;
+        const int slot = b * kBlkPools + (kb >> 2);
+        int64_t row;
+        bool ok;
+        if (slot < nsel) {
+          const int32_t p = slots[slot];
+          row = 4 * static_cast<int64_t>(p) + (kb & 3);
+          ok = p >= 0;
+        } else {
+          row = 4 * n_elig + (kb & 3);
+          ok = slot == nsel && row <= i;
+        }
+        if (ok) {
+          const float4 x = *reinterpret_cast<const float4*>((r < 8 ? stage_k : stage_v) + (r & 7) * 512 +
+                                                             ((lane ^ (r & 7)) << 4));
+          red_add_v4(acc + row * kD + 4 * lane, mul * x.x, mul * x.y, mul * x.z, mul * x.w);
+        }
+      }
+      __syncwarp();
     }
     __syncwarp();  // tiles are rewritten by the next slice
   }

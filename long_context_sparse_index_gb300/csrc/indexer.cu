@@ -53,7 +53,7 @@ __device__ __forceinline__ int pool_tiles_of(const IndexerArgs& a, int qb) {
   return static_cast<int>((n + kBN - 1) / kBN);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     indexer_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const IndexerArgs a) {
   extern __shared__ uint8_t smem_raw[];

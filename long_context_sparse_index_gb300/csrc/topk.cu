@@ -3,16 +3,23 @@
 // [SkyRL-1M §1 DSA 真稀疏] each query keeps its highest-scoring pools and the
 // selection travels as int32 pool indices.  For query i with n = floor(i/4)
 // eligible pools the kernel keeps min(topk, n) of them: every pool whose
-// score is larger than the k-th largest, plus the lowest-indexed pools tied
-// with it.  The kept pools are written in ascending pool order, then -1.
+// score is larger than the k-th largest score T, plus the lowest-indexed
+// pools whose score equals T.  Kept pools are written in ascending order,
+// then -1.
 //
-// Method: radix select on order-preserving 32-bit keys of the fp32 scores.
-// A min/max pass skips the bits all keys share; each further pass builds an
-// 8-bit digit histogram of the keys that still match the selected prefix
-// (per-warp histograms fed by warp-aggregated increments), and picks the
-// digit bin holding the k-th largest key.  A final pass compacts the kept
-// indices in index order with two block-wide scans.  One CTA per query row;
-// rows of up to kCacheMax scores are staged in shared memory once.
+// Method (one CTA per query row).  Scores map to order-preserving 32-bit
+// keys.  The search keeps a key interval [lo, hi] known to contain T and the
+// number `need` of keys still to take inside it:
+//   1. lo, hi = min, max key of the row.
+//   2. A 2048-bin histogram of the keys in [lo, hi], bins linear in key
+//      value, locates the bin holding the need-th largest key; keys in higher
+//      bins are kept, the interval shrinks to that bin.  Repeat until the bin
+//      holds at most kCap keys (or the interval is a single key).
+//   3. The bin's keys are compacted into shared memory and an exact radix
+//      select on them yields T and the number of ties at T to keep.
+//   4. A stable compaction pass writes the kept indices in index order.
+// Rows of up to kThreads * kEpt scores keep their keys in registers (one
+// read of the row); longer rows re-read the scores (L2) in each pass.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -21,17 +28,27 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCacheMax = 49152;
-constexpr size_t kHistBytes = kWarps * 256 * sizeof(uint32_t);
+constexpr int kEpt = 64;                       // keys per thread in the register-resident variant
+constexpr int kRegMax = kThreads * kEpt;       // 32768
+constexpr int kBins = 2048;
+constexpr int kCap = 4096;                     // candidate buffer (keys + indices)
 
-// Larger float -> larger key; -0 and +0 map to the same key.
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
-  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;
+  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;  // -0 == +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one value per thread; returns the block total in *total.
+struct Smem {
+  uint32_t hist[kBins];
+  uint32_t cand_key[kCap];
+  uint32_t warp_tmp[kWarps + 1];
+  uint32_t red[2 * kWarps];
+  uint32_t sel[4];
+  uint32_t ncand;
+};
+
+// Exclusive scan of one value per thread over the block; *total gets the sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -43,7 +60,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp
   if (lane == 31) s_warp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = lane < kWarps ? s_warp[lane] : 0u;
+    const uint32_t w = lane < kWarps ? s_warp[lane] : 0u;
     uint32_t incl = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -60,17 +77,97 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp
   return r;
 }
 
-template <bool kCached>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict__ scores, int64_t ld, int64_t row0,
-                                                        int topk, int32_t* __restrict__ out) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* hist = smem;                         // [kWarps][256]
-  uint32_t* keys = smem + kWarps * 256;          // [n] (kCached)
-  __shared__ uint32_t s_warp[kWarps + 1];
-  __shared__ uint32_t s_minmax[2 * kWarps];
-  __shared__ uint32_t s_sel[2];
+__device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, Smem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    sm.red[warp] = mn;
+    sm.red[kWarps + warp] = mx;
+  }
+  __syncthreads();
+  mn = sm.red[0];
+  mx = sm.red[kWarps];
+  for (int w = 1; w < kWarps; ++w) {
+    mn = min(mn, sm.red[w]);
+    mx = max(mx, sm.red[kWarps + w]);
+  }
+  __syncthreads();
+}
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// bin of key k in [lo, lo + range): floor((k - lo) * nb / range)
+__device__ __forceinline__ uint32_t bin_of(uint32_t k, uint32_t lo, uint64_t range, uint32_t nb) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(k - lo) * nb) / range);
+}
+
+// After a histogram of `nb` bins is in sm.hist, finds the bin b holding the
+// need-th largest key.  Writes b, the count above b and the count in b to sm.sel.
+__device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need) {
+  // thread t owns bins nb-1-4t .. nb-4-4t (descending)
+  const int t = threadIdx.x;
+  uint32_t c[4], s = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int b = static_cast<int>(nb) - 1 - 4 * t - q;
+    c[q] = b >= 0 ? sm.hist[b] : 0u;
+    s += c[q];
+  }
+  uint32_t tot;
+  const uint32_t excl = block_excl_scan(s, sm.warp_tmp, &tot);
+  if (excl < need && excl + s >= need) {
+    uint32_t cum = excl;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (cum + c[q] >= need) {
+        sm.sel[0] = nb - 1 - 4 * t - q;
+        sm.sel[1] = cum;
+        sm.sel[2] = c[q];
+        break;
+      }
+      cum += c[q];
+    }
+  }
+  __syncthreads();
+}
+
+// Exact select among the sm.ncand candidate keys: the need-th largest key T
+// and how many candidates equal to T are to be kept.  Radix over (key - lo).
+__device__ __forceinline__ void select_candidates(Smem& sm, uint32_t lo, uint32_t hi, uint32_t need, uint32_t* T_out,
+                                                  uint32_t* take_eq) {
+  const uint32_t nc = sm.ncand;
+  uint32_t prefix = 0, pmask = 0;
+  const uint32_t span = hi - lo;
+  int bits = span == 0 ? 0 : 32 - __clz(span);
+  while (bits > 0) {
+    const int nb = min(8, bits);
+    const int shift = bits - nb;
+    for (int b = threadIdx.x; b < 256; b += kThreads) sm.hist[b] = 0u;
+    __syncthreads();
+    for (uint32_t j = threadIdx.x; j < nc; j += kThreads) {
+      const uint32_t x = sm.cand_key[j] - lo;
+      if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & ((1u << nb) - 1u)], 1u);
+    }
+    __syncthreads();
+    find_bin(sm, 256, need);
+    const uint32_t b = sm.sel[0], above = sm.sel[1];
+    need -= above;
+    prefix |= b << shift;
+    pmask |= ((1u << nb) - 1u) << shift;
+    bits -= nb;
+    __syncthreads();
+  }
+  *T_out = lo + prefix;
+  *take_eq = need;
+}
+
+template <bool kRegs>
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores, int64_t ld,
+                                                           int64_t row0, int topk, int32_t* __restrict__ out) {
+  __shared__ Smem sm;
+  const int tid = threadIdx.x;
   const int64_t i = row0 + blockIdx.x;
   const int n = static_cast<int>(i / 4);
   int32_t* orow = out + static_cast<int64_t>(blockIdx.x) * topk;
@@ -79,133 +176,150 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
     return;
   }
   const float* srow = scores + static_cast<int64_t>(blockIdx.x) * ld;
-  auto key_at = [&](int j) -> uint32_t { return kCached ? keys[j] : score_key(__ldg(srow + j)); };
+  // thread tid owns the contiguous segment [beg, end) of the row
+  const int seg = kRegs ? kEpt : (n + kThreads - 1) / kThreads;
+  const int beg = min(n, tid * seg), end = min(n, beg + seg);
+  uint32_t keys[kRegs ? kEpt : 1];
+  auto key_at = [&](int e) -> uint32_t {  // e-th element of this thread's segment
+    if constexpr (kRegs) {
+      return keys[e];
+    } else {
+      return score_key(__ldg(srow + beg + e));
+    }
+  };
+  const int cnt = end - beg;
 
-  // ---- pass 0: stage keys, min and max
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  const int n4 = n >> 2;
-  for (int j = tid; j < n4; j += kThreads) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(srow) + j);
-    const uint32_t k0 = score_key(f.x), k1 = score_key(f.y), k2 = score_key(f.z), k3 = score_key(f.w);
-    if (kCached) *reinterpret_cast<uint4*>(keys + 4 * j) = make_uint4(k0, k1, k2, k3);
-    kmin = min(kmin, min(min(k0, k1), min(k2, k3)));
-    kmax = max(kmax, max(max(k0, k1), max(k2, k3)));
-  }
-  for (int j = 4 * n4 + tid; j < n; j += kThreads) {
-    const uint32_t k = score_key(__ldg(srow + j));
-    if (kCached) keys[j] = k;
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
-  }
+  // ---- 1. load (register variant) and min / max
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  if constexpr (kRegs) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    for (int e4 = 0; e4 < kEpt / 4; ++e4) {
+      const int e = 4 * e4;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e + 3 < cnt) {
+        f = __ldg(reinterpret_cast<const float4*>(srow + beg + e));
+      } else {
+        if (e < cnt) f.x = __ldg(srow + beg + e);
+        if (e + 1 < cnt) f.y = __ldg(srow + beg + e + 1);
+        if (e + 2 < cnt) f.z = __ldg(srow + beg + e + 2);
+      }
+      keys[e] = score_key(f.x);
+      keys[e + 1] = score_key(f.y);
+      keys[e + 2] = score_key(f.z);
+      keys[e + 3] = score_key(f.w);
+    }
+#pragma unroll
+    for (int e = 0; e < kEpt; ++e)
+      if (e < cnt) {
+        lo = min(lo, keys[e]);
+        hi = max(hi, keys[e]);
+      }
+  } else {
+    for (int e = 0; e < cnt; ++e) {
+      const uint32_t k = key_at(e);
+      lo = min(lo, k);
+      hi = max(hi, k);
+    }
   }
-  if (lane == 0) {
-    s_minmax[warp] = kmin;
-    s_minmax[kWarps + warp] = kmax;
-  }
-  __syncthreads();
-  kmin = s_minmax[0];
-  kmax = s_minmax[kWarps];
-  for (int w = 1; w < kWarps; ++w) {
-    kmin = min(kmin, s_minmax[w]);
-    kmax = max(kmax, s_minmax[kWarps + w]);
-  }
+  block_minmax(lo, hi, sm);
 
-  // ---- radix passes over the bits below the shared prefix
-  uint32_t prefix = kmin, pmask = 0xFFFFFFFFu;
-  uint32_t remaining = static_cast<uint32_t>(topk);  // keys still to take among those matching prefix
-  if (kmin != kmax) {
-    int L = __clz(kmin ^ kmax);
-    pmask = L ? (0xFFFFFFFFu << (32 - L)) : 0u;
-    prefix = kmin & pmask;
-    while (L < 32) {
-      const int nb = min(8, 32 - L);
-      const int shift = 32 - L - nb;
-      const uint32_t dmask = (1u << nb) - 1u;
-      for (int b = tid; b < kWarps * 256; b += kThreads) hist[b] = 0u;
-      __syncthreads();
-      for (int j0 = 0; j0 < n; j0 += kThreads) {
-        const int j = j0 + tid;
-        const uint32_t k = j < n ? key_at(j) : 0u;
-        const bool cand = j < n && (k & pmask) == prefix;
-        const uint32_t d = cand ? ((k >> shift) & dmask) : 0xFFFFFFFFu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        if (cand && lane == __ffs(peers) - 1) hist[warp * 256 + d] += __popc(peers);
+  // ---- 2. narrow [lo, hi] with value histograms
+  uint32_t need = static_cast<uint32_t>(topk);
+  uint32_t T = lo, take_eq = need;
+  bool done = false;
+  while (!done) {
+    if (lo == hi) {
+      T = lo;
+      take_eq = need;
+      break;
+    }
+    const uint64_t range = static_cast<uint64_t>(hi - lo) + 1u;
+    for (int b = tid; b < kBins; b += kThreads) sm.hist[b] = 0u;
+    __syncthreads();
+    if constexpr (kRegs) {
+#pragma unroll
+      for (int e = 0; e < kEpt; ++e)
+        if (e < cnt && keys[e] >= lo && keys[e] <= hi) atomicAdd(&sm.hist[bin_of(keys[e], lo, range, kBins)], 1u);
+    } else {
+      for (int e = 0; e < cnt; ++e) {
+        const uint32_t k = key_at(e);
+        if (k >= lo && k <= hi) atomicAdd(&sm.hist[bin_of(k, lo, range, kBins)], 1u);
       }
+    }
+    __syncthreads();
+    find_bin(sm, kBins, need);
+    const uint32_t b = sm.sel[0], above = sm.sel[1], inbin = sm.sel[2];
+    need -= above;
+    // keys with bin == b: (k - lo) in [ceil(b*range/nb), ceil((b+1)*range/nb) - 1]
+    const uint32_t nlo = lo + static_cast<uint32_t>((static_cast<uint64_t>(b) * range + kBins - 1) / kBins);
+    const uint32_t nhi = lo + static_cast<uint32_t>((static_cast<uint64_t>(b + 1) * range + kBins - 1) / kBins) - 1u;
+    lo = nlo;
+    hi = nhi;
+    if (inbin <= kCap) {
+      // ---- 3. compact the bin's keys and select exactly among them
+      if (tid == 0) sm.ncand = 0;
       __syncthreads();
-      if (tid < 256) {
-        uint32_t s = 0;
+      if constexpr (kRegs) {
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += hist[w * 256 + tid];
-        hist[tid] = s;  // column tid of row 0 is read only by this thread
-      }
-      __syncthreads();
-      if (warp == 0) {
-        uint32_t c[8], s = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          c[q] = hist[255 - 8 * lane - q];
-          s += c[q];
-        }
-        uint32_t incl = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - s;
-        const unsigned hit = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
-        if (lane == __ffs(hit) - 1) {
-          uint32_t cum = excl;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (cum + c[q] >= remaining) {
-              s_sel[0] = static_cast<uint32_t>(255 - 8 * lane - q);
-              s_sel[1] = cum;
-              break;
-            }
-            cum += c[q];
+        for (int e = 0; e < kEpt; ++e)
+          if (e < cnt && keys[e] >= lo && keys[e] <= hi) {
+            const uint32_t pos = atomicAdd(&sm.ncand, 1u);
+            sm.cand_key[pos] = keys[e];
+          }
+      } else {
+        for (int e = 0; e < cnt; ++e) {
+          const uint32_t k = key_at(e);
+          if (k >= lo && k <= hi) {
+            const uint32_t pos = atomicAdd(&sm.ncand, 1u);
+            sm.cand_key[pos] = k;
           }
         }
       }
       __syncthreads();
-      const uint32_t bin = s_sel[0], above = s_sel[1];
-      remaining -= above;
-      prefix |= bin << shift;
-      pmask |= dmask << shift;
-      L += nb;
-      __syncthreads();
+      select_candidates(sm, lo, hi, need, &T, &take_eq);
+      done = true;
+    }
+    __syncthreads();
+  }
+
+  // ---- 4. keys > T, plus the first take_eq keys == T in index order
+  uint32_t n_gt = 0, n_eq = 0;
+  if constexpr (kRegs) {
+#pragma unroll
+    for (int e = 0; e < kEpt; ++e)
+      if (e < cnt) {
+        n_gt += keys[e] > T;
+        n_eq += keys[e] == T;
+      }
+  } else {
+    for (int e = 0; e < cnt; ++e) {
+      const uint32_t k = key_at(e);
+      n_gt += k > T;
+      n_eq += k == T;
     }
   }
-  const uint32_t T = prefix;  // key of the k-th largest score
-
-  // ---- final pass: keys > T, plus the first `remaining` keys == T in index order
-  int seg = (n + kThreads - 1) / kThreads;
-  seg |= 1;  // odd stride: consecutive threads start in different shared-memory banks
-  const int beg = min(n, tid * seg), end = min(n, beg + seg);
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int j = beg; j < end; ++j) {
-    const uint32_t k = key_at(j);
-    n_gt += k > T;
-    n_eq += k == T;
-  }
   uint32_t tot;
-  const uint32_t eq_before = block_excl_scan(n_eq, s_warp, &tot);
-  const uint32_t take_eq = eq_before >= remaining ? 0u : min(n_eq, remaining - eq_before);
-  const uint32_t off0 = block_excl_scan(n_gt + take_eq, s_warp, &tot);
-  uint32_t off = off0, eq_seen = 0;
-  for (int j = beg; j < end; ++j) {
-    const uint32_t k = key_at(j);
-    if (k > T || (k == T && eq_seen < take_eq)) orow[off++] = j;
-    eq_seen += k == T;
+  const uint32_t eq_before = block_excl_scan(n_eq, sm.warp_tmp, &tot);
+  const uint32_t my_eq = eq_before >= take_eq ? 0u : min(n_eq, take_eq - eq_before);
+  uint32_t off = block_excl_scan(n_gt + my_eq, sm.warp_tmp, &tot);
+  uint32_t eq_seen = 0;
+  if constexpr (kRegs) {
+#pragma unroll
+    for (int e = 0; e < kEpt; ++e)
+      if (e < cnt) {
+        const uint32_t k = keys[e];
+        if (k > T || (k == T && eq_seen < my_eq)) orow[off++] = beg + e;
+        eq_seen += k == T;
+      }
+  } else {
+    for (int e = 0; e < cnt; ++e) {
+      const uint32_t k = key_at(e);
+      if (k > T || (k == T && eq_seen < my_eq)) orow[off++] = beg + e;
+      eq_seen += k == T;
+    }
   }
-  if (tid == 0 && tot != static_cast<uint32_t>(topk)) {
-    // cannot happen for finite scores; keep the row well-formed regardless
-    for (uint32_t j = tot; j < static_cast<uint32_t>(topk); ++j) orow[j] = -1;
-  }
+  if (tid == 0)
+    for (uint32_t j = tot; j < static_cast<uint32_t>(topk); ++j) orow[j] = -1;  // unreachable for finite scores
 }
 
 }  // namespace
@@ -214,20 +328,10 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows
                         const LaunchCtx& ctx) {
   if (nrows <= 0) return cudaSuccess;
   const int64_t n_max = (row0 + nrows - 1) / 4;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (n_max <= kCacheMax) {
-    const size_t smem = kHistBytes + static_cast<size_t>(n_max) * sizeof(uint32_t);
-    if (dev < 64 && !attr_done[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kHistBytes + kCacheMax * sizeof(uint32_t)));
-      if (e != cudaSuccess) return e;
-      attr_done[dev] = 1;
-    }
-    topk_kernel<true><<<nrows, kThreads, smem, ctx.stream>>>(scores, ld, row0, topk, out);
+  if (n_max <= kRegMax) {
+    topk_kernel<true><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
   } else {
-    topk_kernel<false><<<nrows, kThreads, kHistBytes, ctx.stream>>>(scores, ld, row0, topk, out);
+    topk_kernel<false><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
   }
   return cudaGetLastError();
 }

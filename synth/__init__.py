@@ -152,6 +152,7 @@ WORKLOADS = {
     "tiny_int_s2048": Workload("tiny_int_s2048", 2048, Hi=8, topk=64, chunk=256, values="int", seed=0,
                                backward=True),
     "s16k": Workload("s16k", 16384, values="normal", seed=1),
+    "s32k": Workload("s32k", 32768, values="normal", q_idx_scale=0.125, seed=5, backward=True),
     "s128k": Workload("s128k", 131072, values="normal", q_idx_scale=0.125, seed=2, backward=True),
     "s256k_cluster": Workload("s256k_cluster", 262144, chunk=512, values="cluster", seed=3),
     "s1m_cluster": Workload("s1m_cluster", 1048576, chunk=512, values="cluster", seed=3),
