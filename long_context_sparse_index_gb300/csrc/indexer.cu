@@ -53,7 +53,7 @@ __device__ __forceinline__ int pool_tiles_of(const IndexerArgs& a, int qb) {
   return static_cast<int>((n + kBN - 1) / kBN);
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const IndexerArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -237,12 +237,12 @@ __global__ void __maxnreg__(200)
         const float wv = valid ? __ldg(wrow + h) : 0.f;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + cs * kBN + ch * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c * 32, r);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[16];
+          tmem_ld16(taddr + c * 16, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(wv, fmaxf(__uint_as_float(r[j]), 0.f), acc[c * 32 + j]);
+          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(wv, fmaxf(__uint_as_float(r[j]), 0.f), acc[c * 16 + j]);
         }
         tc_fence_before();
         __syncwarp();
