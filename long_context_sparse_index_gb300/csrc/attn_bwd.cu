@@ -26,7 +26,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kBlkPools = 16;
 constexpr int kBlkKeys = 4 * kBlkPools;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kQBytes = kHq * kD * 2;
@@ -319,31 +319,31 @@ __global__ void __launch_bounds__(kThreads, 2)
   cp_async_wait<0>();
   __syncthreads();
 
-  // ---- dq = scale * sum over the four warps' partial dq
+  // ---- dq = scale * sum over the four warps' partial dq (rows padded to
+  // 132 floats so the fragment stores spread over the banks)
+  constexpr int kRedLd = kD + 4;
   float* red = reinterpret_cast<float*>(gbase + 2 * kQBytes);  // reuses the gather ring
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = 8 * j + 2 * t4;
-    *reinterpret_cast<float2*>(red + (warp * kHq + g) * kD + col) = make_float2(dq_acc[j][0], dq_acc[j][1]);
-    *reinterpret_cast<float2*>(red + (warp * kHq + g + 8) * kD + col) = make_float2(dq_acc[j][2], dq_acc[j][3]);
+    *reinterpret_cast<float2*>(red + (warp * kHq + g) * kRedLd + col) = make_float2(dq_acc[j][0], dq_acc[j][1]);
+    *reinterpret_cast<float2*>(red + (warp * kHq + g + 8) * kRedLd + col) = make_float2(dq_acc[j][2], dq_acc[j][3]);
   }
   __syncthreads();
-  {
-    const int e0 = tid * 16;
-    uint32_t packed[8];
+  // thread tid owns element pairs e = 2 * (tid + 128 m), m = 0..7 (consecutive across threads)
+  __nv_bfloat16* dqrow = dq + i * (kHq * kD);
 #pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-      float a0 = 0.f, a1 = 0.f;
+  for (int m = 0; m < 8; ++m) {
+    const int e = 2 * (tid + kThreads * m);
+    const int r = e / kD, c = e % kD;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        a0 += red[w * kHq * kD + e0 + e];
-        a1 += red[w * kHq * kD + e0 + e + 1];
-      }
-      packed[e >> 1] = pack_bf16(scale * a0, scale * a1);
+    for (int w = 0; w < kWarps; ++w) {
+      const float2 x = *reinterpret_cast<const float2*>(red + (w * kHq + r) * kRedLd + c);
+      a0 += x.x;
+      a1 += x.y;
     }
-    uint4* dst = reinterpret_cast<uint4*>(dq + i * (kHq * kD) + e0);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    *reinterpret_cast<uint32_t*>(dqrow + e) = pack_bf16(scale * a0, scale * a1);
   }
 }
 

@@ -270,34 +270,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     fac[hh] = mine / L;
     if (warp == 0 && t4 == 0) lse[i * kHq + h] = (M + log2f(L)) * kLn2;
   }
-  // partial O (already normalised) into shared memory, one [16][128] fp32 slab per warp
+  // partial O (already normalised) into shared memory, one [16][132] fp32 slab
+  // per warp (padded rows spread the fragment stores over the banks)
+  constexpr int kRedLd = kD + 4;
   float* red = reinterpret_cast<float*>(gbase + kQBytes);  // reuses the gather ring
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = 8 * j + 2 * t4;
-    *reinterpret_cast<float2*>(red + (warp * kHq + g) * kD + col) =
+    *reinterpret_cast<float2*>(red + (warp * kHq + g) * kRedLd + col) =
         make_float2(o_acc[j][0] * fac[0], o_acc[j][1] * fac[0]);
-    *reinterpret_cast<float2*>(red + (warp * kHq + g + 8) * kD + col) =
+    *reinterpret_cast<float2*>(red + (warp * kHq + g + 8) * kRedLd + col) =
         make_float2(o_acc[j][2] * fac[1], o_acc[j][3] * fac[1]);
   }
   __syncthreads();
-  // 16 x 128 outputs, 16 per thread, written as bf16x8 vectors
-  {
-    const int e0 = tid * 16;  // flat index into [16][128]
-    uint32_t packed[8];
+  // thread tid owns element pairs e = 2 * (tid + 128 m), m = 0..7 (consecutive across threads)
+  __nv_bfloat16* orow = o + i * (kHq * kD);
 #pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-      float a0 = 0.f, a1 = 0.f;
+  for (int m = 0; m < 8; ++m) {
+    const int e = 2 * (tid + kThreads * m);
+    const int r = e / kD, c = e % kD;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        a0 += red[w * kHq * kD + e0 + e];
-        a1 += red[w * kHq * kD + e0 + e + 1];
-      }
-      packed[e >> 1] = pack_bf16(a0, a1);
+    for (int w = 0; w < kWarps; ++w) {
+      const float2 x = *reinterpret_cast<const float2*>(red + (w * kHq + r) * kRedLd + c);
+      a0 += x.x;
+      a1 += x.y;
     }
-    uint4* dst = reinterpret_cast<uint4*>(o + i * (kHq * kD) + e0);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16(a0, a1);
   }
 }
 

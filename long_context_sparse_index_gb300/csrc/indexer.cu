@@ -228,13 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      // the head weight is fetched one head ahead so its load latency hides
+      // behind the previous head's epilogue
+      float w_next = valid ? __ldg(wrow) : 0.f;
       for (int h = 0; h < a.Hi; ++h) {
+        const float wv = w_next;
+        if (h + 1 < a.Hi) w_next = valid ? __ldg(wrow + h + 1) : 0.f;
         if (!mbar_wait(bar_acc_full + 8 * cs, cph, a.limit_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float wv = valid ? __ldg(wrow + h) : 0.f;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + cs * kBN + ch * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {

@@ -7,19 +7,22 @@
 // pools whose score equals T.  Kept pools are written in ascending order,
 // then -1.
 //
-// Method (one CTA per query row).  Scores map to order-preserving 32-bit
-// keys.  The search keeps a key interval [lo, hi] known to contain T and the
-// number `need` of keys still to take inside it:
+// Method (one CTA of 512 threads per query row).  Scores map to
+// order-preserving 32-bit keys.  Element j of the row belongs to round
+// m = j / 2048, thread (j % 2048) / 4, lane q = j % 4, so every round is a
+// contiguous stretch of 2048 scores read with one float4 per thread.
 //   1. lo, hi = min, max key of the row.
 //   2. A 2048-bin histogram of the keys in [lo, hi], bins linear in key
 //      value, locates the bin holding the need-th largest key; keys in higher
-//      bins are kept, the interval shrinks to that bin.  Repeat until the bin
-//      holds at most kCap keys (or the interval is a single key).
-//   3. The bin's keys are compacted into shared memory and an exact radix
-//      select on them yields T and the number of ties at T to keep.
-//   4. A stable compaction pass writes the kept indices in index order.
-// Rows of up to kThreads * kEpt scores keep their keys in registers (one
-// read of the row); longer rows re-read the scores (L2) in each pass.
+//      bins are kept and the interval shrinks to that bin.  Repeat until the
+//      bin holds at most kCap keys (or the interval is a single key).
+//   3. That bin's keys are compacted into shared memory; an exact radix select
+//      on them gives T and the number of keys equal to T to keep.
+//   4. Round by round, one block scan of the packed counts (keys > T, keys
+//      == T) gives every thread its output offset: keys > T before it plus
+//      min(ties before it, ties to keep).
+// Rows of up to kRegRounds * 2048 scores keep their keys in registers (one
+// read of the row); longer rows re-read the scores in every pass.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -28,10 +31,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kEpt = 64;                       // keys per thread in the register-resident variant
-constexpr int kRegMax = kThreads * kEpt;       // 32768
+constexpr int kPerRound = 4 * kThreads;           // 2048 scores per round
+constexpr int kRegRounds = 16;                    // register-resident rows: n <= 32768
 constexpr int kBins = 2048;
-constexpr int kCap = 4096;                     // candidate buffer (keys + indices)
+constexpr int kCap = 2048;
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -41,15 +44,17 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 
 struct Smem {
   uint32_t hist[kBins];
-  uint32_t cand_key[kCap];
-  uint32_t warp_tmp[kWarps + 1];
+  uint32_t cand[kCap];
+  uint32_t wsum[2][kWarps];
   uint32_t red[2 * kWarps];
   uint32_t sel[4];
   uint32_t ncand;
 };
 
-// Exclusive scan of one value per thread over the block; *total gets the sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t* total) {
+// Exclusive prefix over the block of one value per thread, in thread order,
+// with a single __syncthreads; `buf` alternates between calls.  Also returns
+// the block total.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -57,24 +62,18 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp
     const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) s_warp[warp] = x;
+  if (lane == 31) buf[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t w = lane < kWarps ? s_warp[lane] : 0u;
-    uint32_t incl = w;
+  const uint32_t wt = lane < kWarps ? buf[lane] : 0u;
+  uint32_t incl = wt;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane < kWarps) s_warp[lane] = incl - w;
-    if (lane == kWarps - 1) s_warp[kWarps] = incl;
+  for (int o = 1; o < kWarps; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  __syncthreads();
-  const uint32_t r = s_warp[warp] + x - v;
-  *total = s_warp[kWarps];
-  __syncthreads();
-  return r;
+  const uint32_t warp_base = __shfl_sync(0xffffffffu, incl - wt, warp);
+  *total = __shfl_sync(0xffffffffu, incl, kWarps - 1);
+  return warp_base + x - v;
 }
 
 __device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, Smem& sm) {
@@ -89,34 +88,35 @@ __device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, Smem& s
     sm.red[kWarps + warp] = mx;
   }
   __syncthreads();
-  mn = sm.red[0];
-  mx = sm.red[kWarps];
-  for (int w = 1; w < kWarps; ++w) {
-    mn = min(mn, sm.red[w]);
-    mx = max(mx, sm.red[kWarps + w]);
+  mn = lane < kWarps ? sm.red[lane] : 0xFFFFFFFFu;
+  mx = lane < kWarps ? sm.red[kWarps + lane] : 0u;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
-  __syncthreads();
+  mn = __shfl_sync(0xffffffffu, mn, 0);
+  mx = __shfl_sync(0xffffffffu, mx, 0);
 }
 
-// bin of key k in [lo, lo + range): floor((k - lo) * nb / range)
+// floor((k - lo) * nb / range)
 __device__ __forceinline__ uint32_t bin_of(uint32_t k, uint32_t lo, uint64_t range, uint32_t nb) {
   return static_cast<uint32_t>((static_cast<uint64_t>(k - lo) * nb) / range);
 }
 
-// After a histogram of `nb` bins is in sm.hist, finds the bin b holding the
-// need-th largest key.  Writes b, the count above b and the count in b to sm.sel.
-__device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need) {
-  // thread t owns bins nb-1-4t .. nb-4-4t (descending)
+// With a histogram of nb (<= 2048) bins in sm.hist, finds the bin b holding
+// the need-th largest key: sm.sel = {b, count above b, count in b}.
+__device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need, int parity) {
   const int t = threadIdx.x;
   uint32_t c[4], s = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int b = static_cast<int>(nb) - 1 - 4 * t - q;
+    const int b = static_cast<int>(nb) - 1 - 4 * t - q;  // descending bins
     c[q] = b >= 0 ? sm.hist[b] : 0u;
     s += c[q];
   }
   uint32_t tot;
-  const uint32_t excl = block_excl_scan(s, sm.warp_tmp, &tot);
+  const uint32_t excl = block_excl_scan(s, sm.wsum[parity], &tot);
   if (excl < need && excl + s >= need) {
     uint32_t cum = excl;
 #pragma unroll
@@ -133,34 +133,17 @@ __device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need) {
   __syncthreads();
 }
 
-// Exact select among the sm.ncand candidate keys: the need-th largest key T
-// and how many candidates equal to T are to be kept.  Radix over (key - lo).
-__device__ __forceinline__ void select_candidates(Smem& sm, uint32_t lo, uint32_t hi, uint32_t need, uint32_t* T_out,
-                                                  uint32_t* take_eq) {
-  const uint32_t nc = sm.ncand;
-  uint32_t prefix = 0, pmask = 0;
-  const uint32_t span = hi - lo;
-  int bits = span == 0 ? 0 : 32 - __clz(span);
-  while (bits > 0) {
-    const int nb = min(8, bits);
-    const int shift = bits - nb;
-    for (int b = threadIdx.x; b < 256; b += kThreads) sm.hist[b] = 0u;
-    __syncthreads();
-    for (uint32_t j = threadIdx.x; j < nc; j += kThreads) {
-      const uint32_t x = sm.cand_key[j] - lo;
-      if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & ((1u << nb) - 1u)], 1u);
-    }
-    __syncthreads();
-    find_bin(sm, 256, need);
-    const uint32_t b = sm.sel[0], above = sm.sel[1];
-    need -= above;
-    prefix |= b << shift;
-    pmask |= ((1u << nb) - 1u) << shift;
-    bits -= nb;
-    __syncthreads();
+// Calls f(m) for every round m < rounds: fully unrolled (register-resident
+// keys stay in registers) or as a plain loop.
+template <bool kRegs, typename F>
+__device__ __forceinline__ void for_rounds(int rounds, F&& f) {
+  if constexpr (kRegs) {
+#pragma unroll
+    for (int m = 0; m < kRegRounds; ++m)
+      if (m < rounds) f(m);
+  } else {
+    for (int m = 0; m < rounds; ++m) f(m);
   }
-  *T_out = lo + prefix;
-  *take_eq = need;
 }
 
 template <bool kRegs>
@@ -176,58 +159,58 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     return;
   }
   const float* srow = scores + static_cast<int64_t>(blockIdx.x) * ld;
-  // thread tid owns the contiguous segment [beg, end) of the row
-  const int seg = kRegs ? kEpt : (n + kThreads - 1) / kThreads;
-  const int beg = min(n, tid * seg), end = min(n, beg + seg);
-  uint32_t keys[kRegs ? kEpt : 1];
-  auto key_at = [&](int e) -> uint32_t {  // e-th element of this thread's segment
-    if constexpr (kRegs) {
-      return keys[e];
+  const int rounds = (n + kPerRound - 1) / kPerRound;
+  constexpr uint32_t kPad = 0u;  // key of elements past the row end (below every real key's range use)
+
+  // keys of round m for this thread (4 consecutive elements at 2048 m + 4 tid)
+  auto load4 = [&](int m, uint32_t (&k)[4]) {
+    const int j = m * kPerRound + 4 * tid;
+    if (j + 3 < n) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(srow + j));
+      k[0] = score_key(f.x);
+      k[1] = score_key(f.y);
+      k[2] = score_key(f.z);
+      k[3] = score_key(f.w);
     } else {
-      return score_key(__ldg(srow + beg + e));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) k[q] = j + q < n ? score_key(__ldg(srow + j + q)) : kPad;
     }
   };
-  const int cnt = end - beg;
+  uint32_t regs[kRegs ? kRegRounds : 1][4];
+  auto keys_of = [&](int m, uint32_t (&k)[4]) {
+    if constexpr (kRegs) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) k[q] = regs[m][q];
+    } else {
+      load4(m, k);
+    }
+  };
+  auto valid = [&](int m, int q) { return m * kPerRound + 4 * tid + q < n; };
 
-  // ---- 1. load (register variant) and min / max
+  // ---- 1. load and min / max
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
   if constexpr (kRegs) {
 #pragma unroll
-    for (int e4 = 0; e4 < kEpt / 4; ++e4) {
-      const int e = 4 * e4;
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e + 3 < cnt) {
-        f = __ldg(reinterpret_cast<const float4*>(srow + beg + e));
-      } else {
-        if (e < cnt) f.x = __ldg(srow + beg + e);
-        if (e + 1 < cnt) f.y = __ldg(srow + beg + e + 1);
-        if (e + 2 < cnt) f.z = __ldg(srow + beg + e + 2);
-      }
-      keys[e] = score_key(f.x);
-      keys[e + 1] = score_key(f.y);
-      keys[e + 2] = score_key(f.z);
-      keys[e + 3] = score_key(f.w);
-    }
-#pragma unroll
-    for (int e = 0; e < kEpt; ++e)
-      if (e < cnt) {
-        lo = min(lo, keys[e]);
-        hi = max(hi, keys[e]);
-      }
-  } else {
-    for (int e = 0; e < cnt; ++e) {
-      const uint32_t k = key_at(e);
-      lo = min(lo, k);
-      hi = max(hi, k);
-    }
+    for (int m = 0; m < kRegRounds; ++m)
+      if (m < rounds) load4(m, regs[m]);
   }
+  for_rounds<kRegs>(rounds, [&](int m) {
+    uint32_t k[4];
+    keys_of(m, k);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (valid(m, q)) {
+        lo = min(lo, k[q]);
+        hi = max(hi, k[q]);
+      }
+  });
   block_minmax(lo, hi, sm);
 
-  // ---- 2. narrow [lo, hi] with value histograms
+  // ---- 2./3. narrow [lo, hi] to the k-th largest key T
   uint32_t need = static_cast<uint32_t>(topk);
   uint32_t T = lo, take_eq = need;
-  bool done = false;
-  while (!done) {
+  int parity = 0;
+  while (true) {
     if (lo == hi) {
       T = lo;
       take_eq = need;
@@ -236,90 +219,92 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     const uint64_t range = static_cast<uint64_t>(hi - lo) + 1u;
     for (int b = tid; b < kBins; b += kThreads) sm.hist[b] = 0u;
     __syncthreads();
-    if constexpr (kRegs) {
+    for_rounds<kRegs>(rounds, [&](int m) {
+      uint32_t k[4];
+      keys_of(m, k);
 #pragma unroll
-      for (int e = 0; e < kEpt; ++e)
-        if (e < cnt && keys[e] >= lo && keys[e] <= hi) atomicAdd(&sm.hist[bin_of(keys[e], lo, range, kBins)], 1u);
-    } else {
-      for (int e = 0; e < cnt; ++e) {
-        const uint32_t k = key_at(e);
-        if (k >= lo && k <= hi) atomicAdd(&sm.hist[bin_of(k, lo, range, kBins)], 1u);
-      }
-    }
+      for (int q = 0; q < 4; ++q)
+        if (valid(m, q) && k[q] >= lo && k[q] <= hi) atomicAdd(&sm.hist[bin_of(k[q], lo, range, kBins)], 1u);
+    });
     __syncthreads();
-    find_bin(sm, kBins, need);
+    find_bin(sm, kBins, need, parity);
+    parity ^= 1;
     const uint32_t b = sm.sel[0], above = sm.sel[1], inbin = sm.sel[2];
     need -= above;
-    // keys with bin == b: (k - lo) in [ceil(b*range/nb), ceil((b+1)*range/nb) - 1]
+    // keys in bin b: (k - lo) in [ceil(b*range/nb), ceil((b+1)*range/nb) - 1]
     const uint32_t nlo = lo + static_cast<uint32_t>((static_cast<uint64_t>(b) * range + kBins - 1) / kBins);
     const uint32_t nhi = lo + static_cast<uint32_t>((static_cast<uint64_t>(b + 1) * range + kBins - 1) / kBins) - 1u;
     lo = nlo;
     hi = nhi;
-    if (inbin <= kCap) {
-      // ---- 3. compact the bin's keys and select exactly among them
-      if (tid == 0) sm.ncand = 0;
-      __syncthreads();
-      if constexpr (kRegs) {
-#pragma unroll
-        for (int e = 0; e < kEpt; ++e)
-          if (e < cnt && keys[e] >= lo && keys[e] <= hi) {
-            const uint32_t pos = atomicAdd(&sm.ncand, 1u);
-            sm.cand_key[pos] = keys[e];
-          }
-      } else {
-        for (int e = 0; e < cnt; ++e) {
-          const uint32_t k = key_at(e);
-          if (k >= lo && k <= hi) {
-            const uint32_t pos = atomicAdd(&sm.ncand, 1u);
-            sm.cand_key[pos] = k;
-          }
-        }
-      }
-      __syncthreads();
-      select_candidates(sm, lo, hi, need, &T, &take_eq);
-      done = true;
-    }
+    if (inbin > kCap) continue;
+    // compact the bin's keys, then radix-select over (key - lo) exactly
+    if (tid == 0) sm.ncand = 0;
     __syncthreads();
+    for_rounds<kRegs>(rounds, [&](int m) {
+      uint32_t k[4];
+      keys_of(m, k);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (valid(m, q) && k[q] >= lo && k[q] <= hi) sm.cand[atomicAdd(&sm.ncand, 1u)] = k[q];
+    });
+    __syncthreads();
+    const uint32_t nc = sm.ncand;
+    uint32_t prefix = 0, pmask = 0;
+    const uint32_t span = hi - lo;
+    int bits = span == 0 ? 0 : 32 - __clz(span);
+    while (bits > 0) {
+      const int nb = min(8, bits);
+      const int shift = bits - nb;
+      if (tid < 256) sm.hist[tid] = 0u;
+      __syncthreads();
+      for (uint32_t j = tid; j < nc; j += kThreads) {
+        const uint32_t x = sm.cand[j] - lo;
+        if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & ((1u << nb) - 1u)], 1u);
+      }
+      __syncthreads();
+      find_bin(sm, 256, need, parity);
+      parity ^= 1;
+      const uint32_t bb = sm.sel[0], ab = sm.sel[1];
+      need -= ab;
+      prefix |= bb << shift;
+      pmask |= ((1u << nb) - 1u) << shift;
+      bits -= nb;
+      __syncthreads();
+    }
+    T = lo + prefix;
+    take_eq = need;
+    break;
   }
+  __syncthreads();
 
-  // ---- 4. keys > T, plus the first take_eq keys == T in index order
-  uint32_t n_gt = 0, n_eq = 0;
-  if constexpr (kRegs) {
+  // ---- 4. stable compaction, one packed block scan per round
+  uint32_t gt_base = 0, eq_base = 0;
+  for_rounds<kRegs>(rounds, [&](int m) {
+    uint32_t k[4];
+    keys_of(m, k);
+    uint32_t gt[4], eq[4], c_gt = 0, c_eq = 0;
 #pragma unroll
-    for (int e = 0; e < kEpt; ++e)
-      if (e < cnt) {
-        n_gt += keys[e] > T;
-        n_eq += keys[e] == T;
-      }
-  } else {
-    for (int e = 0; e < cnt; ++e) {
-      const uint32_t k = key_at(e);
-      n_gt += k > T;
-      n_eq += k == T;
+    for (int q = 0; q < 4; ++q) {
+      const bool v = valid(m, q);
+      gt[q] = v && k[q] > T;
+      eq[q] = v && k[q] == T;
+      c_gt += gt[q];
+      c_eq += eq[q];
     }
-  }
-  uint32_t tot;
-  const uint32_t eq_before = block_excl_scan(n_eq, sm.warp_tmp, &tot);
-  const uint32_t my_eq = eq_before >= take_eq ? 0u : min(n_eq, take_eq - eq_before);
-  uint32_t off = block_excl_scan(n_gt + my_eq, sm.warp_tmp, &tot);
-  uint32_t eq_seen = 0;
-  if constexpr (kRegs) {
+    uint32_t tot;
+    const uint32_t pre = block_excl_scan((c_gt << 16) | c_eq, sm.wsum[parity], &tot);
+    parity ^= 1;
+    uint32_t gt_before = gt_base + (pre >> 16), eq_before = eq_base + (pre & 0xFFFFu);
 #pragma unroll
-    for (int e = 0; e < kEpt; ++e)
-      if (e < cnt) {
-        const uint32_t k = keys[e];
-        if (k > T || (k == T && eq_seen < my_eq)) orow[off++] = beg + e;
-        eq_seen += k == T;
-      }
-  } else {
-    for (int e = 0; e < cnt; ++e) {
-      const uint32_t k = key_at(e);
-      if (k > T || (k == T && eq_seen < my_eq)) orow[off++] = beg + e;
-      eq_seen += k == T;
+    for (int q = 0; q < 4; ++q) {
+      const bool take = gt[q] || (eq[q] && eq_before < take_eq);
+      if (take) orow[gt_before + min(eq_before, take_eq)] = m * kPerRound + 4 * tid + q;
+      gt_before += gt[q];
+      eq_before += eq[q];
     }
-  }
-  if (tid == 0)
-    for (uint32_t j = tot; j < static_cast<uint32_t>(topk); ++j) orow[j] = -1;  // unreachable for finite scores
+    gt_base += tot >> 16;
+    eq_base += tot & 0xFFFFu;
+  });
 }
 
 }  // namespace
@@ -328,7 +313,7 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows
                         const LaunchCtx& ctx) {
   if (nrows <= 0) return cudaSuccess;
   const int64_t n_max = (row0 + nrows - 1) / 4;
-  if (n_max <= kRegMax) {
+  if (n_max <= static_cast<int64_t>(kRegRounds) * kPerRound) {
     topk_kernel<true><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
   } else {
     topk_kernel<false><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
