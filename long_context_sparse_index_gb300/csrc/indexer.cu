@@ -27,8 +27,9 @@ constexpr int kBStages = 2;
 constexpr uint32_t kABytes = kBM * kDi * 2;        // 16 KB: q_idx tile of one head
 constexpr uint32_t kBHalf = kBN * kDi * 2;         // 32 KB: Khat hi (or lo) tile
 constexpr uint32_t kBBytes = 2 * kBHalf;           // 64 KB
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarps = 16;                      // 4 TMEM lane quarters x 4 column quarters
+constexpr int kEpiCols = kBN / 4;                  // 64 columns per epilogue thread
+constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, 16 epilogue warps
 constexpr uint32_t kTmemCols = 512;                // 2 accumulators x 256 columns
 constexpr uint32_t kBarOff = kBStages * kBBytes + kAStages * kABytes;
 constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
@@ -213,9 +214,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;         // 0..7
-    const int lq = warp & 3;         // TMEM lane quarter this warp may access
-    const int ch = ew >> 2;          // which 128-column half of the tile
+    // Warp w (2..17) reads TMEM lanes 32*(w%4).. (its hardware lane quarter)
+    // and columns 64*((w-2)/4).. of each accumulator: one query row and 64
+    // pools per thread.  16 warps keep several TMEM loads in flight per SM
+    // sub-partition while others compute.
+    const int ew = warp - 2;
+    const int lq = warp & 3;
+    const int cq = ew >> 2;
     int cs = 0;
     uint32_t cph = 0;
     bool ok = true;
@@ -225,9 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row = a.row0 + static_cast<int64_t>(qb) * kBM + lq * 32 + lane;
       const bool valid = row < a.row0 + a.nrows;
       const float* wrow = a.w + (valid ? row : a.row0) * a.Hi;
-      float acc[128];
+      float2 acc[kEpiCols / 2];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      for (int j = 0; j < kEpiCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
       // the head weight is fetched one head ahead so its load latency hides
       // behind the previous head's epilogue
       float w_next = valid ? __ldg(wrow) : 0.f;
@@ -239,14 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + cs * kBN + ch * 128;
+        const float2 w2 = make_float2(wv, wv);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + cs * kBN + cq * kEpiCols;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kEpiCols / 16; ++c) {
           uint32_t r[16];
           tmem_ld16(taddr + c * 16, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(wv, fmaxf(__uint_as_float(r[j]), 0.f), acc[c * 16 + j]);
+          for (int j = 0; j < 8; ++j) {
+            const float2 x = make_float2(fmaxf(__uint_as_float(r[2 * j]), 0.f), fmaxf(__uint_as_float(r[2 * j + 1]), 0.f));
+            acc[c * 8 + j] = __ffma2_rn(w2, x, acc[c * 8 + j]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -259,9 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (valid) {
         float4* dst = reinterpret_cast<float4*>(a.scores + (row - a.row0) * a.ld + static_cast<int64_t>(pb) * kBN +
-                                                ch * 128);
+                                                cq * kEpiCols);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) dst[c] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        for (int c = 0; c < kEpiCols / 4; ++c)
+          dst[c] = make_float4(acc[2 * c].x, acc[2 * c].y, acc[2 * c + 1].x, acc[2 * c + 1].y);
       }
     }
     if (!ok) {

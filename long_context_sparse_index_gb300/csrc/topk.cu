@@ -8,9 +8,8 @@
 // then -1.
 //
 // Method (one CTA of 512 threads per query row).  Scores map to
-// order-preserving 32-bit keys.  Element j of the row belongs to round
-// m = j / 2048, thread (j % 2048) / 4, lane q = j % 4, so every round is a
-// contiguous stretch of 2048 scores read with one float4 per thread.
+// order-preserving 32-bit keys, staged once in shared memory when the row
+// fits (n <= kCacheMax), otherwise re-read from the scores in every pass.
 //   1. lo, hi = min, max key of the row.
 //   2. A 2048-bin histogram of the keys in [lo, hi], bins linear in key
 //      value, locates the bin holding the need-th largest key; keys in higher
@@ -18,11 +17,10 @@
 //      bin holds at most kCap keys (or the interval is a single key).
 //   3. That bin's keys are compacted into shared memory; an exact radix select
 //      on them gives T and the number of keys equal to T to keep.
-//   4. Round by round, one block scan of the packed counts (keys > T, keys
-//      == T) gives every thread its output offset: keys > T before it plus
+//   4. Round by round over stretches of 2048 keys (4 consecutive keys per
+//      thread), one block scan of the packed counts (keys > T, keys == T)
+//      gives every thread its output offset: keys > T before it plus
 //      min(ties before it, ties to keep).
-// Rows of up to kRegRounds * 2048 scores keep their keys in registers (one
-// read of the row); longer rows re-read the scores in every pass.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -31,10 +29,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPerRound = 4 * kThreads;           // 2048 scores per round
-constexpr int kRegRounds = 16;                    // register-resident rows: n <= 32768
+constexpr int kPerRound = 4 * kThreads;  // 2048 keys per round
 constexpr int kBins = 2048;
 constexpr int kCap = 2048;
+constexpr int kCacheMax = 49152;        // rows up to 192 KB of keys live in shared memory
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -51,9 +49,8 @@ struct Smem {
   uint32_t ncand;
 };
 
-// Exclusive prefix over the block of one value per thread, in thread order,
-// with a single __syncthreads; `buf` alternates between calls.  Also returns
-// the block total.
+// Exclusive prefix over the block of one value per thread (thread order),
+// with one __syncthreads; callers alternate `buf`.  *total gets the sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -74,29 +71,6 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, u
   const uint32_t warp_base = __shfl_sync(0xffffffffu, incl - wt, warp);
   *total = __shfl_sync(0xffffffffu, incl, kWarps - 1);
   return warp_base + x - v;
-}
-
-__device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, Smem& sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) {
-    sm.red[warp] = mn;
-    sm.red[kWarps + warp] = mx;
-  }
-  __syncthreads();
-  mn = lane < kWarps ? sm.red[lane] : 0xFFFFFFFFu;
-  mx = lane < kWarps ? sm.red[kWarps + lane] : 0u;
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  mn = __shfl_sync(0xffffffffu, mn, 0);
-  mx = __shfl_sync(0xffffffffu, mx, 0);
 }
 
 // floor((k - lo) * nb / range)
@@ -133,24 +107,32 @@ __device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need, i
   __syncthreads();
 }
 
-// Calls f(m) for every round m < rounds: fully unrolled (register-resident
-// keys stay in registers) or as a plain loop.
-template <bool kRegs, typename F>
-__device__ __forceinline__ void for_rounds(int rounds, F&& f) {
-  if constexpr (kRegs) {
-#pragma unroll
-    for (int m = 0; m < kRegRounds; ++m)
-      if (m < rounds) f(m);
+// Keys of elements j .. j+3 (j a multiple of 4); elements >= n read as 0.
+template <bool kCached>
+__device__ __forceinline__ uint4 keys4(const uint32_t* cache, const float* srow, int j, int n) {
+  if constexpr (kCached) {
+    return *reinterpret_cast<const uint4*>(cache + j);  // staged with the same padding
   } else {
-    for (int m = 0; m < rounds; ++m) f(m);
+    if (j + 3 < n) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(srow + j));
+      return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+    }
+    uint4 k;
+    k.x = j < n ? score_key(__ldg(srow + j)) : 0u;
+    k.y = j + 1 < n ? score_key(__ldg(srow + j + 1)) : 0u;
+    k.z = j + 2 < n ? score_key(__ldg(srow + j + 2)) : 0u;
+    k.w = j + 3 < n ? score_key(__ldg(srow + j + 3)) : 0u;
+    return k;
   }
 }
 
-template <bool kRegs>
+template <bool kCached>
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores, int64_t ld,
                                                            int64_t row0, int topk, int32_t* __restrict__ out) {
   __shared__ Smem sm;
-  const int tid = threadIdx.x;
+  extern __shared__ uint4 cache4[];
+  uint32_t* cache = reinterpret_cast<uint32_t*>(cache4);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t i = row0 + blockIdx.x;
   const int n = static_cast<int>(i / 4);
   int32_t* orow = out + static_cast<int64_t>(blockIdx.x) * topk;
@@ -160,51 +142,39 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   }
   const float* srow = scores + static_cast<int64_t>(blockIdx.x) * ld;
   const int rounds = (n + kPerRound - 1) / kPerRound;
-  constexpr uint32_t kPad = 0u;  // key of elements past the row end (below every real key's range use)
 
-  // keys of round m for this thread (4 consecutive elements at 2048 m + 4 tid)
-  auto load4 = [&](int m, uint32_t (&k)[4]) {
-    const int j = m * kPerRound + 4 * tid;
-    if (j + 3 < n) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(srow + j));
-      k[0] = score_key(f.x);
-      k[1] = score_key(f.y);
-      k[2] = score_key(f.z);
-      k[3] = score_key(f.w);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) k[q] = j + q < n ? score_key(__ldg(srow + j + q)) : kPad;
-    }
-  };
-  uint32_t regs[kRegs ? kRegRounds : 1][4];
-  auto keys_of = [&](int m, uint32_t (&k)[4]) {
-    if constexpr (kRegs) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) k[q] = regs[m][q];
-    } else {
-      load4(m, k);
-    }
-  };
-  auto valid = [&](int m, int q) { return m * kPerRound + 4 * tid + q < n; };
-
-  // ---- 1. load and min / max
+  // ---- 1. stage keys (cached variant), min and max
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-  if constexpr (kRegs) {
-#pragma unroll
-    for (int m = 0; m < kRegRounds; ++m)
-      if (m < rounds) load4(m, regs[m]);
-  }
-  for_rounds<kRegs>(rounds, [&](int m) {
-    uint32_t k[4];
-    keys_of(m, k);
+  for (int j = 4 * tid; j < n; j += kPerRound) {
+    const uint4 k = keys4<false>(nullptr, srow, j, n);
+    if constexpr (kCached) *reinterpret_cast<uint4*>(cache + j) = k;
+    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (valid(m, q)) {
-        lo = min(lo, k[q]);
-        hi = max(hi, k[q]);
+      if (j + q < n) {
+        lo = min(lo, kk[q]);
+        hi = max(hi, kk[q]);
       }
-  });
-  block_minmax(lo, hi, sm);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    sm.red[warp] = lo;
+    sm.red[kWarps + warp] = hi;
+  }
+  __syncthreads();
+  lo = lane < kWarps ? sm.red[lane] : 0xFFFFFFFFu;
+  hi = lane < kWarps ? sm.red[kWarps + lane] : 0u;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  lo = __shfl_sync(0xffffffffu, lo, 0);
+  hi = __shfl_sync(0xffffffffu, hi, 0);
 
   // ---- 2./3. narrow [lo, hi] to the k-th largest key T
   uint32_t need = static_cast<uint32_t>(topk);
@@ -219,13 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     const uint64_t range = static_cast<uint64_t>(hi - lo) + 1u;
     for (int b = tid; b < kBins; b += kThreads) sm.hist[b] = 0u;
     __syncthreads();
-    for_rounds<kRegs>(rounds, [&](int m) {
-      uint32_t k[4];
-      keys_of(m, k);
+    for (int j = 4 * tid; j < n; j += kPerRound) {
+      const uint4 k = keys4<kCached>(cache, srow, j, n);
+      const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (valid(m, q) && k[q] >= lo && k[q] <= hi) atomicAdd(&sm.hist[bin_of(k[q], lo, range, kBins)], 1u);
-    });
+        if (j + q < n && kk[q] >= lo && kk[q] <= hi) atomicAdd(&sm.hist[bin_of(kk[q], lo, range, kBins)], 1u);
+    }
     __syncthreads();
     find_bin(sm, kBins, need, parity);
     parity ^= 1;
@@ -237,16 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     lo = nlo;
     hi = nhi;
     if (inbin > kCap) continue;
-    // compact the bin's keys, then radix-select over (key - lo) exactly
     if (tid == 0) sm.ncand = 0;
     __syncthreads();
-    for_rounds<kRegs>(rounds, [&](int m) {
-      uint32_t k[4];
-      keys_of(m, k);
+    for (int j = 4 * tid; j < n; j += kPerRound) {
+      const uint4 k = keys4<kCached>(cache, srow, j, n);
+      const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (valid(m, q) && k[q] >= lo && k[q] <= hi) sm.cand[atomicAdd(&sm.ncand, 1u)] = k[q];
-    });
+        if (j + q < n && kk[q] >= lo && kk[q] <= hi) sm.cand[atomicAdd(&sm.ncand, 1u)] = kk[q];
+    }
     __syncthreads();
     const uint32_t nc = sm.ncand;
     uint32_t prefix = 0, pmask = 0;
@@ -264,9 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       __syncthreads();
       find_bin(sm, 256, need, parity);
       parity ^= 1;
-      const uint32_t bb = sm.sel[0], ab = sm.sel[1];
-      need -= ab;
-      prefix |= bb << shift;
+      need -= sm.sel[1];
+      prefix |= sm.sel[0] << shift;
       pmask |= ((1u << nb) - 1u) << shift;
       bits -= nb;
       __syncthreads();
@@ -279,15 +247,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
 
   // ---- 4. stable compaction, one packed block scan per round
   uint32_t gt_base = 0, eq_base = 0;
-  for_rounds<kRegs>(rounds, [&](int m) {
-    uint32_t k[4];
-    keys_of(m, k);
+  for (int m = 0; m < rounds; ++m) {
+    const int j = m * kPerRound + 4 * tid;
+    const uint4 k = j < n ? keys4<kCached>(cache, srow, j, n) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
     uint32_t gt[4], eq[4], c_gt = 0, c_eq = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const bool v = valid(m, q);
-      gt[q] = v && k[q] > T;
-      eq[q] = v && k[q] == T;
+      const bool v = j + q < n;
+      gt[q] = v && kk[q] > T;
+      eq[q] = v && kk[q] == T;
       c_gt += gt[q];
       c_eq += eq[q];
     }
@@ -297,14 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     uint32_t gt_before = gt_base + (pre >> 16), eq_before = eq_base + (pre & 0xFFFFu);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const bool take = gt[q] || (eq[q] && eq_before < take_eq);
-      if (take) orow[gt_before + min(eq_before, take_eq)] = m * kPerRound + 4 * tid + q;
+      if (gt[q] || (eq[q] && eq_before < take_eq)) orow[gt_before + min(eq_before, take_eq)] = j + q;
       gt_before += gt[q];
       eq_before += eq[q];
     }
     gt_base += tot >> 16;
     eq_base += tot & 0xFFFFu;
-  });
+  }
 }
 
 }  // namespace
@@ -313,8 +281,19 @@ cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows
                         const LaunchCtx& ctx) {
   if (nrows <= 0) return cudaSuccess;
   const int64_t n_max = (row0 + nrows - 1) / 4;
-  if (n_max <= static_cast<int64_t>(kRegRounds) * kPerRound) {
-    topk_kernel<true><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (n_max <= kCacheMax) {
+    if (dev < 64 && !attr_done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kCacheMax * sizeof(uint32_t)));
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = 1;
+    }
+    // the cache holds the row rounded up to a multiple of 4 keys
+    const size_t smem = static_cast<size_t>((n_max + 3) / 4 * 4) * sizeof(uint32_t);
+    topk_kernel<true><<<nrows, kThreads, smem, ctx.stream>>>(scores, ld, row0, topk, out);
   } else {
     topk_kernel<false><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
   }
