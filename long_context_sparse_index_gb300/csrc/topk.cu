@@ -7,20 +7,23 @@
 // pools whose score equals T.  Kept pools are written in ascending order,
 // then -1.
 //
-// Method (one CTA of 512 threads per query row).  Scores map to
-// order-preserving 32-bit keys, staged once in shared memory when the row
-// fits (n <= kCacheMax), otherwise re-read from the scores in every pass.
-//   1. lo, hi = min, max key of the row.
-//   2. A 2048-bin histogram of the keys in [lo, hi], bins linear in key
-//      value, locates the bin holding the need-th largest key; keys in higher
-//      bins are kept and the interval shrinks to that bin.  Repeat until the
-//      bin holds at most kCap keys (or the interval is a single key).
-//   3. That bin's keys are compacted into shared memory; an exact radix select
-//      on them gives T and the number of keys equal to T to keep.
-//   4. Round by round over stretches of 2048 keys (4 consecutive keys per
-//      thread), one block scan of the packed counts (keys > T, keys == T)
-//      gives every thread its output offset: keys > T before it plus
-//      min(ties before it, ties to keep).
+// Method (one CTA of 512 threads per query row; scores map to
+// order-preserving 32-bit keys):
+//   1. Threshold guess.  A strided sample of kSample keys is radix-selected
+//      for its r-th largest key t, with r chosen so that, for any row whose
+//      large scores are not packed into a few places, at least topk keys of
+//      the row exceed t while only a few thousand do (short rows skip this:
+//      every key is a candidate).
+//   2. One pass over the row: each warp owns a contiguous stretch and appends
+//      the keys >= t, with their indices, to its own buffer in index order.
+//   3. If there are at least topk candidates and no buffer overflowed, an
+//      exact radix select over the candidate keys gives T and the number of
+//      keys equal to T to keep; the candidates are then walked in index
+//      order (a scan over the 16 warp buffers) to write the kept indices.
+//      Every key of the row that is >= T is a candidate, so this is exact.
+//   4. Otherwise (the guess failed) the row takes the general path: value
+//      histograms over [min, max] narrow down to T, and a stable compaction
+//      pass over the whole row writes the kept indices.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -29,10 +32,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPerRound = 4 * kThreads;  // 2048 keys per round
-constexpr int kBins = 2048;
-constexpr int kCap = 2048;
-constexpr int kCacheMax = 49152;        // rows up to 192 KB of keys live in shared memory
+constexpr int kWarpCap = 256;            // candidate slots per warp
+constexpr int kSample = 2048;            // 4 sampled keys per thread
+constexpr int kBins = 2048;              // general-path histogram
+constexpr int kPerRound = 4 * kThreads;  // general-path compaction stretch
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -41,11 +44,23 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 struct Smem {
-  uint32_t hist[kBins];
-  uint32_t cand[kCap];
+  union {
+    struct {
+      uint32_t key[kWarps][kWarpCap];
+      uint32_t idx[kWarps][kWarpCap];
+    } cand;
+    uint32_t samp[kSample];
+    struct {
+      uint32_t hist[kBins];
+      uint32_t cand[kBins];
+    } gen;
+  } u;
+  uint32_t hist[256];
+  uint32_t wcount[kWarps];
   uint32_t wsum[2][kWarps];
   uint32_t red[2 * kWarps];
   uint32_t sel[4];
+  uint32_t flag;
   uint32_t ncand;
 };
 
@@ -73,24 +88,20 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, u
   return warp_base + x - v;
 }
 
-// floor((k - lo) * nb / range)
-__device__ __forceinline__ uint32_t bin_of(uint32_t k, uint32_t lo, uint64_t range, uint32_t nb) {
-  return static_cast<uint32_t>((static_cast<uint64_t>(k - lo) * nb) / range);
-}
-
-// With a histogram of nb (<= 2048) bins in sm.hist, finds the bin b holding
-// the need-th largest key: sm.sel = {b, count above b, count in b}.
-__device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need, int parity) {
+// With a histogram of nb (<= 2048) bins, finds the bin b holding the
+// need-th largest key: sm.sel = {b, count above b, count in b}.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, Smem& sm, uint32_t nb, uint32_t need, int& parity) {
   const int t = threadIdx.x;
   uint32_t c[4], s = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int b = static_cast<int>(nb) - 1 - 4 * t - q;  // descending bins
-    c[q] = b >= 0 ? sm.hist[b] : 0u;
+    c[q] = b >= 0 ? hist[b] : 0u;
     s += c[q];
   }
   uint32_t tot;
   const uint32_t excl = block_excl_scan(s, sm.wsum[parity], &tot);
+  parity ^= 1;
   if (excl < need && excl + s >= need) {
     uint32_t cum = excl;
 #pragma unroll
@@ -107,55 +118,41 @@ __device__ __forceinline__ void find_bin(Smem& sm, uint32_t nb, uint32_t need, i
   __syncthreads();
 }
 
-// Keys of elements j .. j+3 (j a multiple of 4); elements >= n read as 0.
-template <bool kCached>
-__device__ __forceinline__ uint4 keys4(const uint32_t* cache, const float* srow, int j, int n) {
-  if constexpr (kCached) {
-    return *reinterpret_cast<const uint4*>(cache + j);  // staged with the same padding
-  } else {
-    if (j + 3 < n) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(srow + j));
-      return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+// Exact radix select over keys in [lo, hi] held in shared memory: `get(j)`
+// returns (valid, key) for slot j < nslots.  Returns the need-th largest key
+// T; *need_out = how many keys equal to T are to be taken.
+template <typename Get>
+__device__ __forceinline__ uint32_t radix_select(Smem& sm, uint32_t lo, uint32_t hi, uint32_t need, int nslots,
+                                                 Get&& get, uint32_t* need_out, int& parity) {
+  uint32_t prefix = 0, pmask = 0;
+  const uint32_t span = hi - lo;
+  int bits = span == 0 ? 0 : 32 - __clz(span);
+  while (bits > 0) {
+    const int nb = min(8, bits);
+    const int shift = bits - nb;
+    if (threadIdx.x < 256) sm.hist[threadIdx.x] = 0u;
+    __syncthreads();
+    for (int j = threadIdx.x; j < nslots; j += kThreads) {
+      uint32_t k;
+      if (get(j, k)) {
+        const uint32_t x = k - lo;
+        if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & ((1u << nb) - 1u)], 1u);
+      }
     }
-    uint4 k;
-    k.x = j < n ? score_key(__ldg(srow + j)) : 0u;
-    k.y = j + 1 < n ? score_key(__ldg(srow + j + 1)) : 0u;
-    k.z = j + 2 < n ? score_key(__ldg(srow + j + 2)) : 0u;
-    k.w = j + 3 < n ? score_key(__ldg(srow + j + 3)) : 0u;
-    return k;
+    __syncthreads();
+    find_bin(sm.hist, sm, 256, need, parity);
+    need -= sm.sel[1];
+    prefix |= sm.sel[0] << shift;
+    pmask |= ((1u << nb) - 1u) << shift;
+    bits -= nb;
+    __syncthreads();
   }
+  *need_out = need;
+  return lo + prefix;
 }
 
-template <bool kCached>
-__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores, int64_t ld,
-                                                           int64_t row0, int topk, int32_t* __restrict__ out) {
-  __shared__ Smem sm;
-  extern __shared__ uint4 cache4[];
-  uint32_t* cache = reinterpret_cast<uint32_t*>(cache4);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t i = row0 + blockIdx.x;
-  const int n = static_cast<int>(i / 4);
-  int32_t* orow = out + static_cast<int64_t>(blockIdx.x) * topk;
-  if (n <= topk) {
-    for (int j = tid; j < topk; j += kThreads) orow[j] = j < n ? j : -1;
-    return;
-  }
-  const float* srow = scores + static_cast<int64_t>(blockIdx.x) * ld;
-  const int rounds = (n + kPerRound - 1) / kPerRound;
-
-  // ---- 1. stage keys (cached variant), min and max
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-  for (int j = 4 * tid; j < n; j += kPerRound) {
-    const uint4 k = keys4<false>(nullptr, srow, j, n);
-    if constexpr (kCached) *reinterpret_cast<uint4*>(cache + j) = k;
-    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (j + q < n) {
-        lo = min(lo, kk[q]);
-        hi = max(hi, kk[q]);
-      }
-  }
+__device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Smem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -175,11 +172,41 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   }
   lo = __shfl_sync(0xffffffffu, lo, 0);
   hi = __shfl_sync(0xffffffffu, hi, 0);
+  __syncthreads();
+}
 
-  // ---- 2./3. narrow [lo, hi] to the k-th largest key T
+// keys of elements j .. j+3; elements >= n read as 0
+__device__ __forceinline__ uint4 load_keys4(const float* srow, int j, int n) {
+  if (j + 3 < n) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(srow + j));
+    return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  }
+  uint4 k;
+  k.x = j < n ? score_key(__ldg(srow + j)) : 0u;
+  k.y = j + 1 < n ? score_key(__ldg(srow + j + 1)) : 0u;
+  k.z = j + 2 < n ? score_key(__ldg(srow + j + 2)) : 0u;
+  k.w = j + 3 < n ? score_key(__ldg(srow + j + 3)) : 0u;
+  return k;
+}
+
+// General path: histogram narrowing over the whole row, then a stable
+// compaction pass (re-reads the scores).
+__device__ void topk_general(Smem& sm, const float* srow, int n, int topk, int32_t* orow, int& parity) {
+  const int tid = threadIdx.x;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int j = 4 * tid; j < n; j += kPerRound) {
+    const uint4 k = load_keys4(srow, j, n);
+    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (j + q < n) {
+        lo = min(lo, kk[q]);
+        hi = max(hi, kk[q]);
+      }
+  }
+  block_minmax(lo, hi, sm);
   uint32_t need = static_cast<uint32_t>(topk);
   uint32_t T = lo, take_eq = need;
-  int parity = 0;
   while (true) {
     if (lo == hi) {
       T = lo;
@@ -187,69 +214,52 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       break;
     }
     const uint64_t range = static_cast<uint64_t>(hi - lo) + 1u;
-    for (int b = tid; b < kBins; b += kThreads) sm.hist[b] = 0u;
+    for (int b = tid; b < kBins; b += kThreads) sm.u.gen.hist[b] = 0u;
     __syncthreads();
     for (int j = 4 * tid; j < n; j += kPerRound) {
-      const uint4 k = keys4<kCached>(cache, srow, j, n);
+      const uint4 k = load_keys4(srow, j, n);
       const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (j + q < n && kk[q] >= lo && kk[q] <= hi) atomicAdd(&sm.hist[bin_of(kk[q], lo, range, kBins)], 1u);
+        if (j + q < n && kk[q] >= lo && kk[q] <= hi)
+          atomicAdd(&sm.u.gen.hist[static_cast<uint32_t>((static_cast<uint64_t>(kk[q] - lo) * kBins) / range)], 1u);
     }
     __syncthreads();
-    find_bin(sm, kBins, need, parity);
-    parity ^= 1;
-    const uint32_t b = sm.sel[0], above = sm.sel[1], inbin = sm.sel[2];
-    need -= above;
-    // keys in bin b: (k - lo) in [ceil(b*range/nb), ceil((b+1)*range/nb) - 1]
+    find_bin(sm.u.gen.hist, sm, kBins, need, parity);
+    const uint32_t b = sm.sel[0], inbin = sm.sel[2];
+    need -= sm.sel[1];
     const uint32_t nlo = lo + static_cast<uint32_t>((static_cast<uint64_t>(b) * range + kBins - 1) / kBins);
     const uint32_t nhi = lo + static_cast<uint32_t>((static_cast<uint64_t>(b + 1) * range + kBins - 1) / kBins) - 1u;
     lo = nlo;
     hi = nhi;
-    if (inbin > kCap) continue;
+    __syncthreads();
+    if (inbin > static_cast<uint32_t>(kBins)) continue;
     if (tid == 0) sm.ncand = 0;
     __syncthreads();
     for (int j = 4 * tid; j < n; j += kPerRound) {
-      const uint4 k = keys4<kCached>(cache, srow, j, n);
+      const uint4 k = load_keys4(srow, j, n);
       const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (j + q < n && kk[q] >= lo && kk[q] <= hi) sm.cand[atomicAdd(&sm.ncand, 1u)] = kk[q];
+        if (j + q < n && kk[q] >= lo && kk[q] <= hi) sm.u.gen.cand[atomicAdd(&sm.ncand, 1u)] = kk[q];
     }
     __syncthreads();
-    const uint32_t nc = sm.ncand;
-    uint32_t prefix = 0, pmask = 0;
-    const uint32_t span = hi - lo;
-    int bits = span == 0 ? 0 : 32 - __clz(span);
-    while (bits > 0) {
-      const int nb = min(8, bits);
-      const int shift = bits - nb;
-      if (tid < 256) sm.hist[tid] = 0u;
-      __syncthreads();
-      for (uint32_t j = tid; j < nc; j += kThreads) {
-        const uint32_t x = sm.cand[j] - lo;
-        if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & ((1u << nb) - 1u)], 1u);
-      }
-      __syncthreads();
-      find_bin(sm, 256, need, parity);
-      parity ^= 1;
-      need -= sm.sel[1];
-      prefix |= sm.sel[0] << shift;
-      pmask |= ((1u << nb) - 1u) << shift;
-      bits -= nb;
-      __syncthreads();
-    }
-    T = lo + prefix;
-    take_eq = need;
+    const int nc = static_cast<int>(sm.ncand);
+    T = radix_select(
+        sm, lo, hi, need, nc,
+        [&](int j, uint32_t& k) {
+          k = sm.u.gen.cand[j];
+          return true;
+        },
+        &take_eq, parity);
     break;
   }
   __syncthreads();
-
-  // ---- 4. stable compaction, one packed block scan per round
   uint32_t gt_base = 0, eq_base = 0;
+  const int rounds = (n + kPerRound - 1) / kPerRound;
   for (int m = 0; m < rounds; ++m) {
     const int j = m * kPerRound + 4 * tid;
-    const uint4 k = j < n ? keys4<kCached>(cache, srow, j, n) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 k = j < n ? load_keys4(srow, j, n) : make_uint4(0u, 0u, 0u, 0u);
     const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
     uint32_t gt[4], eq[4], c_gt = 0, c_eq = 0;
 #pragma unroll
@@ -275,28 +285,156 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   }
 }
 
+__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restrict__ scores, int64_t ld,
+                                                           int64_t row0, int topk, int32_t* __restrict__ out) {
+  __shared__ Smem sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t i = row0 + blockIdx.x;
+  const int n = static_cast<int>(i / 4);
+  int32_t* orow = out + static_cast<int64_t>(blockIdx.x) * topk;
+  if (n <= topk) {
+    for (int j = tid; j < topk; j += kThreads) orow[j] = j < n ? j : -1;
+    return;
+  }
+  const float* srow = scores + static_cast<int64_t>(blockIdx.x) * ld;
+  int parity = 0;
+  // each warp owns the stretch [seg0, seg1) of the row, a multiple of 4 long
+  const int seg = ((n + kWarps - 1) / kWarps + 3) & ~3;
+  const int seg0 = min(n, warp * seg), seg1 = min(n, seg0 + seg);
+
+  // ---- 1. threshold guess
+  uint32_t t_lo = 0u;
+  if (seg > kWarpCap) {
+#pragma unroll
+    for (int s = 0; s < kSample / kThreads; ++s) {
+      const int sj = tid + s * kThreads;
+      const int j = static_cast<int>((static_cast<int64_t>(sj) * n) / kSample);
+      sm.u.samp[sj] = score_key(__ldg(srow + j));
+    }
+    __syncthreads();
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+    for (int s = 0; s < kSample / kThreads; ++s) {
+      lo = min(lo, sm.u.samp[tid + s * kThreads]);
+      hi = max(hi, sm.u.samp[tid + s * kThreads]);
+    }
+    block_minmax(lo, hi, sm);
+    // expected keys of the row above the r-th largest sample: r * n / kSample
+    const float r0 = static_cast<float>(topk) * kSample / static_cast<float>(n);
+    const uint32_t r = min(static_cast<uint32_t>(kSample),
+                           static_cast<uint32_t>(ceilf(r0 + 4.f * sqrtf(r0) + 4.f)));
+    uint32_t dummy;
+    t_lo = radix_select(
+        sm, lo, hi, r, kSample,
+        [&](int j, uint32_t& k) {
+          k = sm.u.samp[j];
+          return true;
+        },
+        &dummy, parity);
+    __syncthreads();
+  }
+
+  // ---- 2. one pass: per-warp candidate buffers in index order
+  if (tid == 0) sm.flag = 0;
+  uint32_t cnt = 0, cmax = 0;
+  for (int base = seg0; base < seg1; base += 128) {
+    const int j = base + 4 * lane;
+    const uint4 k = j < seg1 ? load_keys4(srow, j, seg1) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
+    uint32_t f = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (j + q < seg1 && kk[q] >= t_lo) f |= 1u << q;
+    uint32_t c = __popc(f), incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t pos = cnt + incl - c;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (f & (1u << q)) {
+        if (pos < kWarpCap) {
+          sm.u.cand.key[warp][pos] = kk[q];
+          sm.u.cand.idx[warp][pos] = j + q;
+          cmax = max(cmax, kk[q]);
+        }
+        ++pos;
+      }
+    cnt += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) sm.wcount[warp] = cnt;
+  __syncthreads();
+  uint32_t total = 0;
+  bool overflow = false;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    total += sm.wcount[w];
+    overflow |= sm.wcount[w] > static_cast<uint32_t>(kWarpCap);
+  }
+  if (overflow || total < static_cast<uint32_t>(topk)) {
+    __syncthreads();
+    topk_general(sm, srow, n, topk, orow, parity);
+    return;
+  }
+
+  // ---- 3. exact select among the candidates
+  uint32_t lo = t_lo, hi = cmax;
+  {
+    uint32_t dummy_lo = 0xFFFFFFFFu;
+    block_minmax(dummy_lo, hi, sm);
+  }
+  uint32_t take_eq;
+  const uint32_t T = radix_select(
+      sm, lo, hi, topk, kWarps * kWarpCap,
+      [&](int j, uint32_t& k) {
+        const int w = j / kWarpCap, p = j % kWarpCap;
+        if (p >= static_cast<int>(sm.wcount[w])) return false;
+        k = sm.u.cand.key[w][p];
+        return true;
+      },
+      &take_eq, parity);
+
+  // walk the candidates in index order: warp w takes its own buffer
+  const int myc = static_cast<int>(sm.wcount[warp]);
+  uint32_t c_gt = 0, c_eq = 0;
+  for (int p = lane; p < myc; p += 32) {
+    const uint32_t k = sm.u.cand.key[warp][p];
+    c_gt += k > T;
+    c_eq += k == T;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
+    c_eq += __shfl_xor_sync(0xffffffffu, c_eq, o);
+  }
+  // exclusive prefix over warps of the packed (gt, eq) counts
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan(lane == 31 ? ((c_gt << 16) | c_eq) : 0u, sm.wsum[parity], &tot);
+  parity ^= 1;
+  const uint32_t wpre = __shfl_sync(0xffffffffu, pre, 31);  // exclusive prefix of this warp's totals
+  uint32_t gt_before = wpre >> 16, eq_before = wpre & 0xFFFFu;
+  for (int p0 = 0; p0 < myc; p0 += 32) {
+    const int p = p0 + lane;
+    const bool v = p < myc;
+    const uint32_t k = v ? sm.u.cand.key[warp][p] : 0u;
+    const bool gt = v && k > T, eq = v && k == T;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t below = (1u << lane) - 1u;
+    const uint32_t g_pre = gt_before + __popc(bg & below), e_pre = eq_before + __popc(be & below);
+    if (gt || (eq && e_pre < take_eq)) orow[g_pre + min(e_pre, take_eq)] = static_cast<int32_t>(sm.u.cand.idx[warp][p]);
+    gt_before += __popc(bg);
+    eq_before += __popc(be);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows, int topk, int32_t* out,
                         const LaunchCtx& ctx) {
   if (nrows <= 0) return cudaSuccess;
-  const int64_t n_max = (row0 + nrows - 1) / 4;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (n_max <= kCacheMax) {
-    if (dev < 64 && !attr_done[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kCacheMax * sizeof(uint32_t)));
-      if (e != cudaSuccess) return e;
-      attr_done[dev] = 1;
-    }
-    // the cache holds the row rounded up to a multiple of 4 keys
-    const size_t smem = static_cast<size_t>((n_max + 3) / 4 * 4) * sizeof(uint32_t);
-    topk_kernel<true><<<nrows, kThreads, smem, ctx.stream>>>(scores, ld, row0, topk, out);
-  } else {
-    topk_kernel<false><<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
-  }
+  topk_kernel<<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
   return cudaGetLastError();
 }
 
