@@ -139,6 +139,27 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
                                  float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                                  void* stream);
 
+/*
+ * Indexer + top-k for callers that cannot allocate device memory.  (The
+ * source pages have no counterpart to this call; it exists for users of the
+ * library.)
+ *
+ * Same arguments, outputs and results as dsa_index_topk, but without a
+ * workspace: the scratch lives in a fixed static device buffer of 10 MiB +
+ * 256 B inside the library, which every GPU that loads the library holds
+ * until the process exits.  That covers S <= 32768 with chunk <= 256; larger
+ * sizes return DSA_ERR_WORKSPACE (see dsa_last_error()) and nothing runs.
+ * The call allocates nothing.  The first call on a device looks up the
+ * buffer's device address (cudaGetSymbolAddress, with that device current),
+ * so that first call should come before any stream capture.  All calls on a
+ * device share the buffer and leave their contents in it; nothing needs to be
+ * zero beforehand.  Calls whose GPU work overlaps (e.g. on unordered streams)
+ * race on the buffer: order them.
+ */
+dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
+                                    int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
+                                    void* stream);
+
 /* Synchronises `stream` and returns DSA_ERR_TIMEOUT / DSA_ERR_INTERNAL if a
  * kernel has recorded a failed bounded wait or check since the last
  * dsa_clear_status(), DSA_ERR_CUDA if the stream reports an error, else

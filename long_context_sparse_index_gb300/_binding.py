@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
 # every symbol the C header declares
 EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd_workspace",
             "dsa_sparse_attn_bwd", "dsa_sync_status", "dsa_clear_status", "dsa_last_error", "dsa_version",
-            "dsa_profile_enable", "dsa_profile_read", "dsa_launch_count", "dsa_launch_count_reset")
+            "dsa_profile_enable", "dsa_profile_read", "dsa_launch_count", "dsa_launch_count_reset",
+            "dsa_index_topk_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,8 @@ def load():
             lib.dsa_profile_read.restype = ctypes.c_int
             lib.dsa_launch_count.argtypes = []
             lib.dsa_launch_count.restype = ctypes.c_int64
+            lib.dsa_index_topk_noalloc.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp]
+            lib.dsa_index_topk_noalloc.restype = ctypes.c_int
             lib.dsa_launch_count_reset.argtypes = []
             lib.dsa_launch_count_reset.restype = None
             _lib = lib
@@ -129,6 +132,27 @@ def dsa_index_topk(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int = 0, q_e
     _check(lib.dsa_index_topk(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), S, Hi, Di, chunk, topk, q_begin,
                               q_end, pool_idx.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
                               _stream_handle(stream)))
+    return pool_idx
+
+
+def dsa_index_topk_noalloc(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int = 0, q_end: int | None = None,
+                           pool_idx=None, stream=None):
+    """dsa_index_topk without a workspace, for callers that must not allocate
+    device scratch: the library's fixed built-in buffer is used instead (S up
+    to 32768 with chunk up to 256).  `pool_idx` should be passed preallocated
+    by such callers; if omitted it is allocated here for convenience."""
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    _need(k_idx, "k_idx", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    S, Hi, Di = q_idx.shape
+    if k_idx.shape != (S, Di) or w.shape != (S, Hi):
+        raise ValueError("k_idx must be [S, Di] and w [S, Hi]")
+    q_end = S if q_end is None else q_end
+    if pool_idx is None:
+        pool_idx = torch.empty((max(q_end - q_begin, 0), topk), dtype=torch.int32, device=q_idx.device)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    _check(load().dsa_index_topk_noalloc(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), S, Hi, Di, chunk, topk,
+                                         q_begin, q_end, pool_idx.data_ptr(), _stream_handle(stream)))
     return pool_idx
 
 

@@ -160,6 +160,10 @@ int64_t pools_padded(int64_t S) { return ((S / 4 + kPoolTile - 1) / kPoolTile) *
 
 }  // namespace
 
+namespace dsa {
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace dsa
+
 extern "C" {
 
 const char* dsa_last_error(void) { return g_last_error.c_str(); }

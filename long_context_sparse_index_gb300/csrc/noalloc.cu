@@ -1,0 +1,90 @@
+// noalloc.cu -- dsa_index_topk_noalloc: the indexer + top-k entry point for
+// callers that cannot allocate device memory.
+//
+// Some callers of this library cannot call cudaMalloc (or any allocating
+// routine) at the point where they need the indexer: for example a host
+// runtime that owns a fixed device-memory budget and must not let a library
+// grow it, or a latency-critical path that must not block on the device
+// allocator.  For them this file keeps the scratch the call needs in a
+// file-scope static device array of fixed size, kNoAllocScratchBytes, which
+// every GPU that loads the library holds until the process exits.  The caller
+// still passes its own inputs and outputs.
+//
+// Set-up: the first call on each device looks up that device's address of the
+// array with cudaGetSymbolAddress (with that device current).  That first call
+// per device should therefore come before any stream capture.  In host code
+// the array's name is only a stand-in, never a device address, so kernels are
+// always given the looked-up address.
+//
+// Every call on a device shares the same array, and the array keeps whatever
+// the previous call left in it.  Nothing in it needs to start at zero: each
+// call rebuilds the pooled keys and rewrites every score it reads before
+// reading it.  Two calls whose work overlaps on the GPU (different streams
+// without ordering between them) race on the array and must not be issued.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+void set_last_error(const std::string& msg);  // dsa_api.cu: the message dsa_last_error() returns
+}
+
+namespace {
+
+// 10 MiB + 256 B: enough for dsa_index_topk_workspace(S, Hi, Di, chunk, topk)
+// with S <= 32768 and chunk <= 256 (pooled keys 2 MiB + scores 8 MiB).
+constexpr size_t kNoAllocScratchBytes = (static_cast<size_t>(10) << 20) + 256;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
+                                    int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
+                                    void* stream) {
+  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk);
+  if (need == 0) {
+    // invalid sizes: let the regular entry point report the precise reason
+    return dsa_index_topk(q_idx, k_idx, w, S, Hi, Di, chunk, topk, q_begin, q_end, pool_idx, nullptr, 0, stream);
+  }
+  if (need > kNoAllocScratchBytes) {
+    dsa::set_last_error("dsa_index_topk_noalloc: these sizes need " + std::to_string(need) +
+                        " bytes of scratch but the built-in buffer holds " + std::to_string(kNoAllocScratchBytes) +
+                        " (S <= 32768 with chunk <= 256); use dsa_index_topk with a caller workspace");
+    return DSA_ERR_WORKSPACE;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    dsa::set_last_error(std::string("dsa_index_topk_noalloc: no usable current device: ") + cudaGetErrorString(e));
+    return DSA_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        dsa::set_last_error(std::string("dsa_index_topk_noalloc: cudaGetSymbolAddress failed: ") +
+                            cudaGetErrorString(e));
+        return DSA_ERR_CUDA;
+      }
+      g_scratch_ptr[dev] = p;
+    }
+    scratch = g_scratch_ptr[dev];
+  }
+  return dsa_index_topk(q_idx, k_idx, w, S, Hi, Di, chunk, topk, q_begin, q_end, pool_idx, scratch,
+                        kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"
