@@ -12,8 +12,9 @@
 // One CTA (4 warps) per query gathers K and V blocks exactly as the forward
 // does.  Per warp and 16-key slice: S and dP on mma.sync, dQ accumulated in
 // registers, and the slice's dK/dV rows (16 keys x 128 dims, already summed
-// over the 16 heads by the MMA) added into fp32 accumulators with 16-byte
-// vector reductions.  A final kernel rounds the accumulators to bf16.
+// over the 16 heads by the MMA) added straight from the MMA fragments into
+// fp32 accumulators with 16-byte reductions.  A final kernel rounds the
+// accumulators to bf16.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -63,6 +64,23 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
     const int64_t src = (ok ? row : 0) * kD + cc * 8;
     cp_async16(st + swz(kr, cc), k + src, ok);
     cp_async16(st + kTileBytes + swz(kr, cc), v + src, ok);
+  }
+}
+
+// Adds one C fragment (16 keys x 8 dims, rows = keys) into acc[row, :] with
+// 16-byte reductions: the two lanes of a pair swap halves so each lane owns
+// four consecutive columns of one key.
+__device__ __forceinline__ void red_frag(float* __restrict__ acc, const float (&c)[4], int64_t row_g, bool ok_g,
+                                         int64_t row_g8, bool ok_g8, int col0, int t4) {
+  const bool odd = t4 & 1;
+  const float s0 = odd ? c[0] : c[2];
+  const float s1 = odd ? c[1] : c[3];
+  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+  const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+  if (!odd) {
+    if (ok_g) red_add_v4(acc + row_g * kD + col0 + 2 * t4, c[0], c[1], r0, r1);
+  } else {
+    if (ok_g8) red_add_v4(acc + row_g8 * kD + col0 + 2 * t4 - 2, r0, r1, c[2], c[3]);
   }
 }
 
@@ -235,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const float* x = m == 0 ? P : dS;
+        const float mul = m == 0 ? 1.f : scale;  // the dK tiles carry scale * dS
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {
-          const uint32_t hi = pack_bf16(x[2 * qd], x[2 * qd + 1]);
+          const float x0 = mul * x[2 * qd], x1 = mul * x[2 * qd + 1];
+          const uint32_t hi = pack_bf16(x0, x1);
           const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
           tw[(2 * m) * 128 + widx[qd]] = hi;
-          tw[(2 * m + 1) * 128 + widx[qd]] = pack_bf16(x[2 * qd] - h0, x[2 * qd + 1] - h1);
+          tw[(2 * m + 1) * 128 + widx[qd]] = pack_bf16(x0 - h0, x1 - h1);
         }
       }
     }
@@ -255,66 +275,47 @@ __global__ void __launch_bounds__(kThreads, 2)
       ldsm_x4_t(sTw + 2 * kTBytes + off, dth[0], dth[1], dth[2], dth[3]);
       ldsm_x4_t(sTw + 3 * kTBytes + off, dtl[0], dtl[1], dtl[2], dtl[3]);
     }
-    // This warp's K and V rows are no longer read: they become the fp32
-    // staging tile [16 keys][128 dims] (rows 0-7 in the K slice, 8-15 in the
-    // V slice, 16-B chunks XOR-swizzled by row) so each reduction below covers
-    // one whole 512-B key row.
-    uint8_t* stage_k = gbase + (sK - base) + key0 * 256;
-    uint8_t* stage_v = gbase + (sV - base) + key0 * 256;
-    // dV rows = P^T dO, then dK rows = scale * dS^T Q   (16 keys x 128 dims)
+    // global rows of this thread's two dK/dV rows: keys g and g+8 of the slice
+    int64_t krow[2];
+    bool kok[2];
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-      const uint32_t (&ah)[4] = pass == 0 ? pth : dth;
-      const uint32_t (&al)[4] = pass == 0 ? ptl : dtl;
-      const uint32_t sB = pass == 0 ? sdO : sQ;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int mat = lane >> 3;
-        const int r = (lane & 7) + ((mat & 1) << 3);
-        const int c = 2 * j + (mat >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sB + swz(r, c), b0, b1, b2, b3);
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16_16816(c0, ah, b0, b1);
-        mma_bf16_16816(c0, al, b0, b1);
-        mma_bf16_16816(c1, ah, b2, b3);
-        mma_bf16_16816(c1, al, b2, b3);
-        // n-tile 2j covers dims 16j..16j+7, n-tile 2j+1 dims 16j+8..16j+15
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const float* cc = half == 0 ? c0 : c1;
-          const int chunk = 4 * j + 2 * half + (t4 >> 1);
-          const int sub = (t4 & 1) * 8;
-          *reinterpret_cast<float2*>(stage_k + g * 512 + ((chunk ^ g) << 4) + sub) = make_float2(cc[0], cc[1]);
-          *reinterpret_cast<float2*>(stage_v + g * 512 + ((chunk ^ g) << 4) + sub) = make_float2(cc[2], cc[3]);
-        }
+    for (int e = 0; e < 2; ++e) {
+      const int kb = key0 + g + 8 * e;
+      const int slot = b * kBlkPools + (kb >> 2);
+      if (slot < nsel) {
+        const int32_t p = slots[slot];
+        krow[e] = 4 * static_cast<int64_t>(p) + (kb & 3);
+        kok[e] = p >= 0;
+      } else {
+        krow[e] = 4 * n_elig + (kb & 3);
+        kok[e] = slot == nsel && krow[e] <= i;
       }
-      __syncwarp();
-      float* acc = pass == 0 ? dv_acc : dk_acc;
-      const float mul = pass == 0 ? 1.f : scale;
-#pragma unroll 4
-      for (int r = 0; r < 16; ++r) {
-        const int kb = key0 + r;
-        const int slot = b * kBlkPools + (kb >> 2);
-        int64_t row;
-        bool ok;
-        if (slot < nsel) {
-          const int32_t p = slots[slot];
-          row = 4 * static_cast<int64_t>(p) + (kb & 3);
-          ok = p >= 0;
-        } else {
-          row = 4 * n_elig + (kb & 3);
-          ok = slot == nsel && row <= i;
-        }
-        if (ok) {
-          const float4 x = *reinterpret_cast<const float4*>((r < 8 ? stage_k : stage_v) + (r & 7) * 512 +
-                                                             ((lane ^ (r & 7)) << 4));
-          red_add_v4(acc + row * kD + 4 * lane, mul * x.x, mul * x.y, mul * x.z, mul * x.w);
-        }
-      }
-      __syncwarp();
     }
-    __syncwarp();  // tiles are rewritten by the next slice
+    // dV rows += P^T dO ; dK rows += (scale dS)^T Q   (16 keys x 128 dims)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int mat = lane >> 3;
+      const int r = (lane & 7) + ((mat & 1) << 3);
+      const int c = 2 * j + (mat >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sdO + swz(r, c), b0, b1, b2, b3);
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16_16816(c0, pth, b0, b1);
+      mma_bf16_16816(c0, ptl, b0, b1);
+      mma_bf16_16816(c1, pth, b2, b3);
+      mma_bf16_16816(c1, ptl, b2, b3);
+      red_frag(dv_acc, c0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4);
+      red_frag(dv_acc, c1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4);
+      ldsm_x4_t(sQ + swz(r, c), b0, b1, b2, b3);
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16_16816(d0, dth, b0, b1);
+      mma_bf16_16816(d0, dtl, b0, b1);
+      mma_bf16_16816(d1, dth, b2, b3);
+      mma_bf16_16816(d1, dtl, b2, b3);
+      red_frag(dk_acc, d0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4);
+      red_frag(dk_acc, d1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4);
+    }
+    __syncwarp();  // the P / dS tiles are rewritten by the next slice
   }
   cp_async_wait<0>();
   __syncthreads();
