@@ -107,6 +107,7 @@ dsa_status_t make_ctx(void* stream, dsa::LaunchCtx* ctx) {
     }
   }
   ctx->wait_limit_ns = static_cast<uint64_t>(ms * 1e6);
+  ctx->pdl = 0;
   return DSA_OK;
 }
 
@@ -237,16 +238,26 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
     cudaError_t e = timed_launch("pool_keys", ctx.stream, [&] { return dsa::launch_pool_keys(k_idx, P, khat2, ctx); });
     if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: pool_keys launch");
   }
+  // Kernels after the first of this call may start early (programmatic
+  // dependent launch); each waits for its predecessor before touching the
+  // score buffer.
+  dsa::LaunchCtx chain = ctx;
+  chain.pdl = 1;
+  bool first = !need_indexer;  // pool_keys, when launched, is the call's first kernel
   for (int64_t c0 = q_begin; c0 < q_end; c0 += chunk) {
     const int64_t c1 = c0 + chunk < q_end ? c0 + chunk : q_end;
     const int nrows = static_cast<int>(c1 - c0);
     if ((c1 - 1) / 4 > topk) {
+      const dsa::LaunchCtx& lc = first ? ctx : chain;
+      first = false;
       cudaError_t e = timed_launch("indexer", ctx.stream,
-                                   [&] { return dsa::launch_indexer(q_map, k_map, w, scores, ld, c0, nrows, Hi, ctx); });
+                                   [&] { return dsa::launch_indexer(q_map, k_map, w, scores, ld, c0, nrows, Hi, lc); });
       if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: indexer launch");
     }
+    const dsa::LaunchCtx& lt = first ? ctx : chain;
+    first = false;
     cudaError_t e = timed_launch("topk", ctx.stream, [&] {
-      return dsa::launch_topk(scores, ld, c0, nrows, topk, pool_idx + (c0 - q_begin) * topk, ctx);
+      return dsa::launch_topk(scores, ld, c0, nrows, topk, pool_idx + (c0 - q_begin) * topk, lt);
     });
     if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: top-k launch");
   }

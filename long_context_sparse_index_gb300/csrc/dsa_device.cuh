@@ -28,6 +28,14 @@ __device__ __forceinline__ void record_status(unsigned* status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// wait: blocks until the preceding kernel in the stream has completed and its
+// memory is visible (a no-op when the launch did not allow early start).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// trigger: the following kernel may be scheduled once every CTA of this
+// kernel has issued this (or exited).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

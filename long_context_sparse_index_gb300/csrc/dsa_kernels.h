@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace dsa {
 
@@ -13,7 +14,25 @@ struct LaunchCtx {
   uint64_t wait_limit_ns;  // bound on every device-side spin-wait
   int inject_timeout;      // fault injection: producers issue no copies, so waits run out
   int num_sms;
+  int pdl;                 // launch may start early (programmatic stream serialization)
 };
+
+// Launches `kernel` on ctx.stream, allowing early start when ctx.pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ctx.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Pooled indexer keys: khat2 [P, 128] bf16, hi in columns 0..63, lo in 64..127.
 cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, const LaunchCtx& ctx);

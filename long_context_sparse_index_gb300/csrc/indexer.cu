@@ -266,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      // the preceding top-k may still be reading the score buffer
+      pdl_wait();
       if (valid) {
         float4* dst = reinterpret_cast<float4*>(a.scores + (row - a.row0) * a.ld + static_cast<int64_t>(pb) * kBN +
                                                 cq * kEpiCols);
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();  // all scores of this CTA are written
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -366,8 +369,7 @@ cudaError_t launch_indexer(const CUtensorMap& q_map, const CUtensorMap& khat_map
   }
   const int ntiles = a.nqb * a.npb_max;
   const int grid = ntiles < ctx.num_sms ? ntiles : ctx.num_sms;
-  indexer_kernel<<<grid, kThreads, kSmemBytes, ctx.stream>>>(q_map, khat_map, a);
-  return cudaGetLastError();
+  return launch_ex(ctx, indexer_kernel, dim3(grid), dim3(kThreads), kSmemBytes, q_map, khat_map, a);
 }
 
 }  // namespace dsa

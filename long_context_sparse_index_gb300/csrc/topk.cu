@@ -175,17 +175,18 @@ __device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Smem& s
   __syncthreads();
 }
 
-// keys of elements j .. j+3; elements >= n read as 0
+// keys of elements j .. j+3; elements >= n read as 0.  Loads bypass L1: the
+// score buffer is rewritten by every chunk's indexer.
 __device__ __forceinline__ uint4 load_keys4(const float* srow, int j, int n) {
   if (j + 3 < n) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(srow + j));
+    const float4 f = __ldcg(reinterpret_cast<const float4*>(srow + j));
     return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
   }
   uint4 k;
-  k.x = j < n ? score_key(__ldg(srow + j)) : 0u;
-  k.y = j + 1 < n ? score_key(__ldg(srow + j + 1)) : 0u;
-  k.z = j + 2 < n ? score_key(__ldg(srow + j + 2)) : 0u;
-  k.w = j + 3 < n ? score_key(__ldg(srow + j + 3)) : 0u;
+  k.x = j < n ? score_key(__ldcg(srow + j)) : 0u;
+  k.y = j + 1 < n ? score_key(__ldcg(srow + j + 1)) : 0u;
+  k.z = j + 2 < n ? score_key(__ldcg(srow + j + 2)) : 0u;
+  k.w = j + 3 < n ? score_key(__ldcg(srow + j + 3)) : 0u;
   return k;
 }
 
@@ -288,6 +289,11 @@ __device__ void topk_general(Smem& sm, const float* srow, int n, int topk, int32
 __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restrict__ scores, int64_t ld,
                                                            int64_t row0, int topk, int32_t* __restrict__ out) {
   __shared__ Smem sm;
+  // The next chunk's indexer may start its loads and MMAs now; it waits for
+  // this kernel before writing scores.  This kernel waits for the indexer
+  // that wrote the scores it reads.
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t i = row0 + blockIdx.x;
   const int n = static_cast<int>(i / 4);
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
     for (int s = 0; s < kSample / kThreads; ++s) {
       const int sj = tid + s * kThreads;
       const int j = static_cast<int>((static_cast<int64_t>(sj) * n) / kSample);
-      sm.u.samp[sj] = score_key(__ldg(srow + j));
+      sm.u.samp[sj] = score_key(__ldcg(srow + j));
     }
     __syncthreads();
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -434,8 +440,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
 cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows, int topk, int32_t* out,
                         const LaunchCtx& ctx) {
   if (nrows <= 0) return cudaSuccess;
-  topk_kernel<<<nrows, kThreads, 0, ctx.stream>>>(scores, ld, row0, topk, out);
-  return cudaGetLastError();
+  return launch_ex(ctx, topk_kernel, dim3(nrows), dim3(kThreads), 0, scores, ld, row0, topk, out);
 }
 
 }  // namespace dsa
