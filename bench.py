@@ -19,8 +19,11 @@ of the same workload (there is no other reference implementation).
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -88,6 +91,29 @@ def algorithmic_work(wl):
         "attn_bwd": {"bytes": keys * row_kv + S * (3 * q_bytes + 8 * Hq + 4 * k) + keys * 2 * D * 4},
         "pairs": pairs, "keys": keys,
     }
+
+
+KERNEL_SOURCE = {"indexer": "indexer.cu", "topk": "topk.cu", "attn_fwd": "attn_fwd.cu", "attn_bwd": "attn_bwd.cu"}
+
+
+def profiled_traffic(kernel, S):
+    """DRAM bytes per launch from the committed ncu summary under profiles/, only
+    while the kernel source still hashes to the one that was captured."""
+    src = KERNEL_SOURCE.get(kernel)
+    if src is None:
+        return None, "no capture for this kernel"
+    with open(os.path.join(ROOT, "long_context_sparse_index_gb300", "csrc", src), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_kernel_*.md"))):
+        with open(path) as f:
+            text = f.read()
+        m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+        t = re.search(rf"traffic_bytes_per_launch_S{S}:\s*(\d+)", text)
+        if m and t:
+            if m.group(1) == h:
+                return int(t.group(1)), os.path.basename(path)
+            return None, f"{os.path.basename(path)} was captured on an older {src}"
+    return None, "no capture for this kernel"
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -342,6 +368,9 @@ def run_ours(args):
         ach = work.get(dom, {"bytes": 0})["bytes"] / (dms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "traffic": None}
+    traffic, tsrc = profiled_traffic(dom, S)
+    roof["traffic"] = traffic
+    roof["traffic_source"] = tsrc
     roof.update({"kernel": dom, "launches_per_step": dl, "avg_launch_ms": dms / max(dl, 1),
                  "peak_source": peaks["source"] + (" (sustained bf16)" if dom == "indexer" else " (copy bandwidth)")})
 
