@@ -156,6 +156,28 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
   return e;
 }
 
+// Head ranges for one chunk's indexer launch.  A chunk with few tiles would
+// leave most SMs idle; splitting its heads into ns ranges multiplies its work
+// units by ns (each unit then costs ~1/ns of a tile plus a fixed overhead).
+// The choice depends on the shapes only (a fixed 152-SM reference, not the
+// device), so results never depend on where they were computed.  The ns
+// slices of nrows x (npb_max*256) floats must fit the chunk's score buffer.
+int choose_nsplit(int64_t tiles, int64_t npb_max, int Hi, int64_t ld) {
+  constexpr int64_t kRefSms = 152;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ns = 1; ns <= 4; ns *= 2) {
+    if (ns > Hi || ns * npb_max * kPoolTile > ld) break;
+    const double waves = static_cast<double>((ns * tiles + kRefSms - 1) / kRefSms);
+    const double cost = waves * (1.0 / ns + 0.03);
+    if (cost < best_cost - 1e-9) {
+      best = ns;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 size_t index_ws_khat(int64_t S) { return round_up(static_cast<size_t>(S / 4 > 0 ? S / 4 : 1) * 2 * kDi * 2, 256); }
 int64_t pools_padded(int64_t S) { return ((S / 4 + kPoolTile - 1) / kPoolTile) * kPoolTile + (S / 4 == 0 ? kPoolTile : 0); }
 
@@ -247,17 +269,30 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
   for (int64_t c0 = q_begin; c0 < q_end; c0 += chunk) {
     const int64_t c1 = c0 + chunk < q_end ? c0 + chunk : q_end;
     const int nrows = static_cast<int>(c1 - c0);
+    // this chunk's rows are compact: a row holds the pools of the chunk's last query, rounded to a tile
+    const int64_t npb_max = ((c1 - 1) / 4 + kPoolTile - 1) / kPoolTile;
+    const int64_t ld_c = npb_max > 0 ? npb_max * kPoolTile : kPoolTile;
+    int nsplit = 1;
     if ((c1 - 1) / 4 > topk) {
+      int64_t tiles = 0;  // tiles holding eligible pairs
+      for (int64_t q0 = c0; q0 < c1; q0 += 128) {
+        const int64_t last = (q0 + 128 < c1 ? q0 + 128 : c1) - 1;
+        tiles += (last / 4 + kPoolTile - 1) / kPoolTile;
+      }
+      nsplit = choose_nsplit(tiles, npb_max, Hi, ld);
+      const int64_t split_stride = static_cast<int64_t>(nrows) * ld_c;
       const dsa::LaunchCtx& lc = first ? ctx : chain;
       first = false;
-      cudaError_t e = timed_launch("indexer", ctx.stream,
-                                   [&] { return dsa::launch_indexer(q_map, k_map, w, scores, ld, c0, nrows, Hi, lc); });
+      cudaError_t e = timed_launch("indexer", ctx.stream, [&] {
+        return dsa::launch_indexer(q_map, k_map, w, scores, ld_c, nsplit, split_stride, c0, nrows, Hi, lc);
+      });
       if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: indexer launch");
     }
     const dsa::LaunchCtx& lt = first ? ctx : chain;
     first = false;
     cudaError_t e = timed_launch("topk", ctx.stream, [&] {
-      return dsa::launch_topk(scores, ld, c0, nrows, topk, pool_idx + (c0 - q_begin) * topk, lt);
+      return dsa::launch_topk(scores, ld_c, nsplit, static_cast<int64_t>(nrows) * ld_c, c0, nrows, topk,
+                              pool_idx + (c0 - q_begin) * topk, lt);
     });
     if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: top-k launch");
   }

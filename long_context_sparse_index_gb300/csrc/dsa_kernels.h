@@ -37,16 +37,19 @@ cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(KArgs...), dim3 grid,
 // Pooled indexer keys: khat2 [P, 128] bf16, hi in columns 0..63, lo in 64..127.
 cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, const LaunchCtx& ctx);
 
-// Scores of query rows [row0, row0 + nrows) against pools [0, floor((row0+nrows-1)/4)):
-// scores[(i - row0) * ld + p]; entries p >= floor(i/4) are not meaningful.
+// Scores of query rows [row0, row0 + nrows) against pools [0, floor((row0+nrows-1)/4)),
+// as nsplit partial sums over equal head ranges: slice s holds
+// scores[s * split_stride + (i - row0) * ld + p]; entries p >= floor(i/4) are
+// not meaningful.
 cudaError_t launch_indexer(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
-                           int64_t ld, int64_t row0, int nrows, int Hi, const LaunchCtx& ctx);
+                           int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows, int Hi,
+                           const LaunchCtx& ctx);
 size_t indexer_smem_bytes();
 
-// Per-row top-k of the scores written by launch_indexer; out rows are
-// pool_idx rows for queries row0 .. row0 + nrows - 1.
-cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows, int topk, int32_t* out,
-                        const LaunchCtx& ctx);
+// Per-row top-k of the scores written by launch_indexer (the nsplit slices
+// added in slice order); out rows are pool_idx rows for queries row0 .. row0 + nrows - 1.
+cudaError_t launch_topk(const float* scores, int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows,
+                        int topk, int32_t* out, const LaunchCtx& ctx);
 
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
                             int topk, float scale, void* o, float* lse, const LaunchCtx& ctx);

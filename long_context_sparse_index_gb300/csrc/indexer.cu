@@ -13,6 +13,12 @@
 // the product carries ~16 more mantissa bits than one bf16 rounding), and
 // the epilogue warps fold ReLU, the head weight and the sum over heads into
 // registers while the next head's MMA runs in the other TMEM buffer.
+//
+// A chunk with few tiles (early in the sequence, where queries see few pools)
+// would leave most SMs idle, so its heads may be split into nsplit equal
+// ranges, each tile of each range its own work unit: range s writes its
+// partial head-sum to its own slice of the score buffer, and the top-k adds
+// the slices in a fixed order.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -38,9 +44,11 @@ struct IndexerArgs {
   const float* w;
   float* scores;
   int64_t ld;
+  int64_t split_stride;  // floats between the partial-sum slices
   int64_t row0;
   int nrows;
   int Hi;
+  int nsplit;            // head ranges (1, 2 or 4)
   int nqb;
   int npb_max;
   unsigned* status;
@@ -98,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ntiles = a.nqb * a.npb_max;
+  const int ntiles = a.nqb * a.npb_max * a.nsplit;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -108,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t a_armed = 0, b_armed = 0, a_par = 0, b_par = 0;  // bit s: stage armed / parity armed
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const int qb = t % a.nqb, pb = t / a.nqb;
+        const int hs = t % a.nsplit, qb = (t / a.nsplit) % a.nqb, pb = t / a.nsplit / a.nqb;
         if (pb >= pool_tiles_of(a, qb)) continue;
         if (!mbar_wait(bar_b_empty + 8 * bs, bph ^ 1, a.limit_ns, abort_flag)) {
           ok = false;
@@ -126,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bph ^= 1;
         }
         const int qrow = static_cast<int>(a.row0) + qb * kBM;
-        for (int h = 0; h < a.Hi; ++h) {
+        for (int h = hs * a.Hi / a.nsplit; h < (hs + 1) * a.Hi / a.nsplit; ++h) {
           if (!mbar_wait(bar_a_empty + 8 * as, aph ^ 1, a.limit_ns, abort_flag)) {
             ok = false;
             break;
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aph = 0, bph = 0, cph = 0;
       bool ok = true, issued = false;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const int qb = t % a.nqb, pb = t / a.nqb;
+        const int hs = t % a.nsplit, qb = (t / a.nsplit) % a.nqb, pb = t / a.nsplit / a.nqb;
         if (pb >= pool_tiles_of(a, qb)) continue;
         if (!mbar_wait(bar_b_full + 8 * bs, bph, a.limit_ns, abort_flag)) {
           ok = false;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t b_hi = sB + bs * kBBytes, b_lo = b_hi + kBHalf;
-        for (int h = 0; h < a.Hi; ++h) {
+        for (int h = hs * a.Hi / a.nsplit; h < (hs + 1) * a.Hi / a.nsplit; ++h) {
           if (!mbar_wait(bar_a_full + 8 * as, aph, a.limit_ns, abort_flag) ||
               !mbar_wait(bar_acc_empty + 8 * cs, cph ^ 1, a.limit_ns, abort_flag)) {
             ok = false;
@@ -225,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t cph = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      const int qb = t % a.nqb, pb = t / a.nqb;
+      const int hs = t % a.nsplit, qb = (t / a.nsplit) % a.nqb, pb = t / a.nsplit / a.nqb;
       if (pb >= pool_tiles_of(a, qb)) continue;
+      const int h0 = hs * a.Hi / a.nsplit, h1 = (hs + 1) * a.Hi / a.nsplit;
       const int64_t row = a.row0 + static_cast<int64_t>(qb) * kBM + lq * 32 + lane;
       const bool valid = row < a.row0 + a.nrows;
       const float* wrow = a.w + (valid ? row : a.row0) * a.Hi;
@@ -235,10 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kEpiCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
       // the head weight is fetched one head ahead so its load latency hides
       // behind the previous head's epilogue
-      float w_next = valid ? __ldg(wrow) : 0.f;
-      for (int h = 0; h < a.Hi; ++h) {
+      float w_next = valid && h0 < h1 ? __ldg(wrow + h0) : 0.f;
+      for (int h = h0; h < h1; ++h) {
         const float wv = w_next;
-        if (h + 1 < a.Hi) w_next = valid ? __ldg(wrow + h + 1) : 0.f;
+        if (h + 1 < h1) w_next = valid ? __ldg(wrow + h + 1) : 0.f;
         if (!mbar_wait(bar_acc_full + 8 * cs, cph, a.limit_ns, abort_flag)) {
           ok = false;
           break;
@@ -269,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the preceding top-k may still be reading the score buffer
       pdl_wait();
       if (valid) {
-        float4* dst = reinterpret_cast<float4*>(a.scores + (row - a.row0) * a.ld + static_cast<int64_t>(pb) * kBN +
-                                                cq * kEpiCols);
+        float4* dst = reinterpret_cast<float4*>(a.scores + hs * a.split_stride + (row - a.row0) * a.ld +
+                                                static_cast<int64_t>(pb) * kBN + cq * kEpiCols);
 #pragma unroll
         for (int c = 0; c < kEpiCols / 4; ++c)
           dst[c] = make_float4(acc[2 * c].x, acc[2 * c].y, acc[2 * c + 1].x, acc[2 * c + 1].y);
@@ -344,14 +353,17 @@ cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, const La
 }
 
 cudaError_t launch_indexer(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
-                           int64_t ld, int64_t row0, int nrows, int Hi, const LaunchCtx& ctx) {
+                           int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows, int Hi,
+                           const LaunchCtx& ctx) {
   IndexerArgs a;
   a.w = w;
   a.scores = scores;
   a.ld = ld;
+  a.split_stride = split_stride;
   a.row0 = row0;
   a.nrows = nrows;
   a.Hi = Hi;
+  a.nsplit = nsplit;
   a.nqb = (nrows + kBM - 1) / kBM;
   a.npb_max = static_cast<int>(((row0 + nrows - 1) / 4 + kBN - 1) / kBN);
   a.status = ctx.status;
@@ -367,7 +379,7 @@ cudaError_t launch_indexer(const CUtensorMap& q_map, const CUtensorMap& khat_map
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
-  const int ntiles = a.nqb * a.npb_max;
+  const int ntiles = a.nqb * a.npb_max * a.nsplit;
   const int grid = ntiles < ctx.num_sms ? ntiles : ctx.num_sms;
   return launch_ex(ctx, indexer_kernel, dim3(grid), dim3(kThreads), kSmemBytes, q_map, khat_map, a);
 }

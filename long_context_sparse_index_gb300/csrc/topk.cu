@@ -9,18 +9,21 @@
 //
 // Method (one CTA of 512 threads per query row; scores map to
 // order-preserving 32-bit keys):
-//   1. Threshold guess.  A strided sample of kSample keys is radix-selected
-//      for its r-th largest key t, with r chosen so that, for any row whose
-//      large scores are not packed into a few places, at least topk keys of
-//      the row exceed t while only a few thousand do (short rows skip this:
-//      every key is a candidate).
+//   1. Threshold guess.  A strided sample of kSample keys is histogrammed on
+//      the top 11 bits of its span; the lower edge t of the bin that holds
+//      the r-th largest sample is the threshold, with r chosen so that, for
+//      any row whose large scores are not packed into a few places, at least
+//      topk keys of the row are >= t while only a few thousand are (short
+//      rows skip this: every key is a candidate).
 //   2. One pass over the row: each warp owns a contiguous stretch and appends
 //      the keys >= t, with their indices, to its own buffer in index order.
-//   3. If there are at least topk candidates and no buffer overflowed, an
-//      exact radix select over the candidate keys gives T and the number of
-//      keys equal to T to keep; the candidates are then walked in index
-//      order (a scan over the 16 warp buffers) to write the kept indices.
-//      Every key of the row that is >= T is a candidate, so this is exact.
+//   3. If there are at least topk candidates and no buffer overflowed, the
+//      exact k-th largest candidate key T (and how many keys equal to T to
+//      keep) comes from 11-bit digit rounds over the candidates; once the
+//      bin holding T has at most kSmall keys, those are ranked against each
+//      other directly.  The candidates are then walked in index order (a
+//      scan over the 16 warp buffers) to write the kept indices.  Every key
+//      of the row that is >= T is a candidate, so this is exact.
 //   4. Otherwise (the guess failed) the row takes the general path: value
 //      histograms over [min, max] narrow down to T, and a stable compaction
 //      pass over the whole row writes the kept indices.
@@ -36,6 +39,9 @@ constexpr int kWarpCap = 256;            // candidate slots per warp
 constexpr int kSample = 2048;            // 4 sampled keys per thread
 constexpr int kBins = 2048;              // general-path histogram
 constexpr int kPerRound = 4 * kThreads;  // general-path compaction stretch
+constexpr int kDigitBits = 11;           // fast-path digit: 2048 bins
+constexpr int kSmall = 64;               // a bin this small is ranked directly
+constexpr int kBatch = 2;                // float4 loads in flight per lane in the candidate pass
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -55,12 +61,14 @@ struct Smem {
       uint32_t cand[kBins];
     } gen;
   } u;
-  uint32_t hist[256];
+  uint32_t hist[kBins];
+  uint32_t small[kSmall];
+  uint32_t wmax[kWarps];
+  uint32_t nsmall;
   uint32_t wcount[kWarps];
   uint32_t wsum[2][kWarps];
   uint32_t red[2 * kWarps];
   uint32_t sel[4];
-  uint32_t flag;
   uint32_t ncand;
 };
 
@@ -175,24 +183,107 @@ __device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Smem& s
   __syncthreads();
 }
 
-// keys of elements j .. j+3; elements >= n read as 0.  Loads bypass L1: the
-// score buffer is rewritten by every chunk's indexer.
-__device__ __forceinline__ uint4 load_keys4(const float* srow, int j, int n) {
+// One row of scores: the indexer wrote it as ns partial head-sums, `stride`
+// floats apart; the score is their sum, added in slice order.
+struct RowSrc {
+  const float* p;
+  int64_t stride;
+  int ns;
+};
+
+// Loads bypass L1: the score buffer is rewritten by every chunk's indexer.
+__device__ __forceinline__ float load_score(const RowSrc& r, int j) {
+  float v = __ldcg(r.p + j);
+  for (int s = 1; s < r.ns; ++s) v = __fadd_rn(v, __ldcg(r.p + s * r.stride + j));
+  return v;
+}
+
+// keys of elements j .. j+3; elements >= n read as 0
+__device__ __forceinline__ uint4 load_keys4(const RowSrc& r, int j, int n) {
   if (j + 3 < n) {
-    const float4 f = __ldcg(reinterpret_cast<const float4*>(srow + j));
+    float4 f = __ldcg(reinterpret_cast<const float4*>(r.p + j));
+    for (int s = 1; s < r.ns; ++s) {
+      const float4 g = __ldcg(reinterpret_cast<const float4*>(r.p + s * r.stride + j));
+      f = make_float4(__fadd_rn(f.x, g.x), __fadd_rn(f.y, g.y), __fadd_rn(f.z, g.z), __fadd_rn(f.w, g.w));
+    }
     return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
   }
   uint4 k;
-  k.x = j < n ? score_key(__ldcg(srow + j)) : 0u;
-  k.y = j + 1 < n ? score_key(__ldcg(srow + j + 1)) : 0u;
-  k.z = j + 2 < n ? score_key(__ldcg(srow + j + 2)) : 0u;
-  k.w = j + 3 < n ? score_key(__ldcg(srow + j + 3)) : 0u;
+  k.x = j < n ? score_key(load_score(r, j)) : 0u;
+  k.y = j + 1 < n ? score_key(load_score(r, j + 1)) : 0u;
+  k.z = j + 2 < n ? score_key(load_score(r, j + 2)) : 0u;
+  k.w = j + 3 < n ? score_key(load_score(r, j + 3)) : 0u;
   return k;
+}
+
+// Exact select among keys held in shared memory: get(j, k) yields the key of
+// slot j < nslots (false = empty slot); every key lies in [lo, hi] and at
+// least `need` of them do.  Each round histograms the top kDigitBits bits of
+// the remaining span and keeps the bin that holds the need-th largest key;
+// once that bin has at most kSmall keys they are ranked against each other.
+// Returns T; *take_eq = how many keys equal to T are taken.
+template <typename Get>
+__device__ __forceinline__ uint32_t digit_select(Smem& sm, uint32_t lo, uint32_t hi, uint32_t need, int nslots,
+                                                 Get&& get, uint32_t* take_eq, int& parity) {
+  const int tid = threadIdx.x;
+  while (true) {
+    if (lo == hi) {
+      *take_eq = need;
+      return lo;
+    }
+    const uint32_t span = hi - lo;
+    const int bits = 32 - __clz(span);
+    const int sh = bits > kDigitBits ? bits - kDigitBits : 0;
+    const uint32_t nb = (span >> sh) + 1u;
+    for (uint32_t b = tid; b < nb; b += kThreads) sm.hist[b] = 0u;
+    if (tid == 0) sm.nsmall = 0u;
+    __syncthreads();
+    for (int j = tid; j < nslots; j += kThreads) {
+      uint32_t k;
+      if (get(j, k) && k >= lo && k <= hi) atomicAdd(&sm.hist[(k - lo) >> sh], 1u);
+    }
+    __syncthreads();
+    find_bin(sm.hist, sm, nb, need, parity);
+    const uint32_t b = sm.sel[0], inbin = sm.sel[2];
+    need -= sm.sel[1];
+    const uint32_t nlo = lo + (b << sh);
+    const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << sh) - 1ull);
+    lo = nlo;
+    hi = nhi < hi ? static_cast<uint32_t>(nhi) : hi;
+    if (sh == 0) {  // the bin is one key value
+      *take_eq = need;
+      return lo;
+    }
+    if (inbin > static_cast<uint32_t>(kSmall)) continue;
+    // few keys left in the bin (exactly inbin of them lie in [lo, hi])
+    for (int j = tid; j < nslots; j += kThreads) {
+      uint32_t k;
+      if (get(j, k) && k >= lo && k <= hi) sm.small[atomicAdd(&sm.nsmall, 1u)] = k;
+    }
+    __syncthreads();
+    const int ns = static_cast<int>(sm.nsmall);
+    if (tid < ns) {
+      const uint32_t kj = sm.small[tid];
+      uint32_t gt = 0, eq = 0;
+      for (int q = 0; q < ns; ++q) {
+        const uint32_t kq = sm.small[q];
+        gt += kq > kj;
+        eq += kq == kj;
+      }
+      if (gt < need && need <= gt + eq) {  // kj is T; every thread holding T writes the same values
+        sm.sel[0] = kj;
+        sm.sel[1] = need - gt;
+      }
+    }
+    __syncthreads();
+    *take_eq = sm.sel[1];
+    return sm.sel[0];
+  }
 }
 
 // General path: histogram narrowing over the whole row, then a stable
 // compaction pass (re-reads the scores).
-__device__ void topk_general(Smem& sm, const float* srow, int n, int topk, int32_t* orow, int& parity) {
+__device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int32_t* orow, int& parity) {
   const int tid = threadIdx.x;
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
   for (int j = 4 * tid; j < n; j += kPerRound) {
@@ -286,8 +377,9 @@ __device__ void topk_general(Smem& sm, const float* srow, int n, int topk, int32
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restrict__ scores, int64_t ld,
-                                                           int64_t row0, int topk, int32_t* __restrict__ out) {
+__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restrict__ scores, int64_t ld, int nsplit,
+                                                           int64_t split_stride, int64_t row0, int topk,
+                                                           int32_t* __restrict__ out) {
   __shared__ Smem sm;
   // The next chunk's indexer may start its loads and MMAs now; it waits for
   // this kernel before writing scores.  This kernel waits for the indexer
@@ -302,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
     for (int j = tid; j < topk; j += kThreads) orow[j] = j < n ? j : -1;
     return;
   }
-  const float* srow = scores + static_cast<int64_t>(blockIdx.x) * ld;
+  const RowSrc srow{scores + static_cast<int64_t>(blockIdx.x) * ld, split_stride, nsplit};
   int parity = 0;
   // each warp owns the stretch [seg0, seg1) of the row, a multiple of 4 long
   const int seg = ((n + kWarps - 1) / kWarps + 3) & ~3;
@@ -311,73 +403,90 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
   // ---- 1. threshold guess
   uint32_t t_lo = 0u;
   if (seg > kWarpCap) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
     for (int s = 0; s < kSample / kThreads; ++s) {
       const int sj = tid + s * kThreads;
       const int j = static_cast<int>((static_cast<int64_t>(sj) * n) / kSample);
-      sm.u.samp[sj] = score_key(__ldcg(srow + j));
+      const uint32_t k = score_key(load_score(srow, j));
+      sm.u.samp[sj] = k;
+      lo = min(lo, k);
+      hi = max(hi, k);
     }
-    __syncthreads();
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-#pragma unroll
-    for (int s = 0; s < kSample / kThreads; ++s) {
-      lo = min(lo, sm.u.samp[tid + s * kThreads]);
-      hi = max(hi, sm.u.samp[tid + s * kThreads]);
-    }
-    block_minmax(lo, hi, sm);
+    block_minmax(lo, hi, sm);  // its barriers also publish the samples
     // expected keys of the row above the r-th largest sample: r * n / kSample
     const float r0 = static_cast<float>(topk) * kSample / static_cast<float>(n);
     const uint32_t r = min(static_cast<uint32_t>(kSample),
                            static_cast<uint32_t>(ceilf(r0 + 4.f * sqrtf(r0) + 4.f)));
-    uint32_t dummy;
-    t_lo = radix_select(
-        sm, lo, hi, r, kSample,
-        [&](int j, uint32_t& k) {
-          k = sm.u.samp[j];
-          return true;
-        },
-        &dummy, parity);
-    __syncthreads();
+    t_lo = lo;
+    if (hi > lo) {
+      const uint32_t span = hi - lo;
+      const int bits = 32 - __clz(span);
+      const int sh = bits > kDigitBits ? bits - kDigitBits : 0;
+      const uint32_t nb = (span >> sh) + 1u;
+      for (uint32_t b = tid; b < nb; b += kThreads) sm.hist[b] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < kSample / kThreads; ++s) atomicAdd(&sm.hist[(sm.u.samp[tid + s * kThreads] - lo) >> sh], 1u);
+      __syncthreads();
+      find_bin(sm.hist, sm, nb, r, parity);
+      t_lo = lo + (sm.sel[0] << sh);
+    }
+    __syncthreads();  // the samples share storage with the candidate buffers
   }
 
   // ---- 2. one pass: per-warp candidate buffers in index order
-  if (tid == 0) sm.flag = 0;
   uint32_t cnt = 0, cmax = 0;
-  for (int base = seg0; base < seg1; base += 128) {
-    const int j = base + 4 * lane;
-    const uint4 k = j < seg1 ? load_keys4(srow, j, seg1) : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
-    uint32_t f = 0;
+  for (int base = seg0; base < seg1; base += 128 * kBatch) {
+    uint4 kv[kBatch];  // all of a batch's loads are issued before any is used
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (j + q < seg1 && kk[q] >= t_lo) f |= 1u << q;
-    uint32_t c = __popc(f), incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = base + 128 * u + 4 * lane;
+      kv[u] = j < seg1 ? load_keys4(srow, j, seg1) : make_uint4(0u, 0u, 0u, 0u);
     }
-    uint32_t pos = cnt + incl - c;
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (f & (1u << q)) {
-        if (pos < kWarpCap) {
-          sm.u.cand.key[warp][pos] = kk[q];
-          sm.u.cand.idx[warp][pos] = j + q;
-          cmax = max(cmax, kk[q]);
-        }
-        ++pos;
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = base + 128 * u + 4 * lane;
+      const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+      uint32_t f = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (j + q < seg1 && kk[q] >= t_lo) f |= 1u << q;
+      const uint32_t c = __popc(f);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-    cnt += __shfl_sync(0xffffffffu, incl, 31);
+      uint32_t pos = cnt + incl - c;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (f & (1u << q)) {
+          if (pos < kWarpCap) {
+            sm.u.cand.key[warp][pos] = kk[q];
+            sm.u.cand.idx[warp][pos] = j + q;
+            cmax = max(cmax, kk[q]);
+          }
+          ++pos;
+        }
+      cnt += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
-  if (lane == 0) sm.wcount[warp] = cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+  if (lane == 0) {
+    sm.wcount[warp] = cnt;
+    sm.wmax[warp] = cmax;
+  }
   __syncthreads();
-  uint32_t total = 0;
+  uint32_t total = 0, hi = 0;
   bool overflow = false;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
     total += sm.wcount[w];
     overflow |= sm.wcount[w] > static_cast<uint32_t>(kWarpCap);
+    hi = max(hi, sm.wmax[w]);
   }
   if (overflow || total < static_cast<uint32_t>(topk)) {
     __syncthreads();
@@ -386,14 +495,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
   }
 
   // ---- 3. exact select among the candidates
-  uint32_t lo = t_lo, hi = cmax;
-  {
-    uint32_t dummy_lo = 0xFFFFFFFFu;
-    block_minmax(dummy_lo, hi, sm);
-  }
   uint32_t take_eq;
-  const uint32_t T = radix_select(
-      sm, lo, hi, topk, kWarps * kWarpCap,
+  const uint32_t T = digit_select(
+      sm, t_lo, hi, topk, kWarps * kWarpCap,
       [&](int j, uint32_t& k) {
         const int w = j / kWarpCap, p = j % kWarpCap;
         if (p >= static_cast<int>(sm.wcount[w])) return false;
@@ -437,10 +541,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
 
 }  // namespace
 
-cudaError_t launch_topk(const float* scores, int64_t ld, int64_t row0, int nrows, int topk, int32_t* out,
-                        const LaunchCtx& ctx) {
+cudaError_t launch_topk(const float* scores, int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows,
+                        int topk, int32_t* out, const LaunchCtx& ctx) {
   if (nrows <= 0) return cudaSuccess;
-  return launch_ex(ctx, topk_kernel, dim3(nrows), dim3(kThreads), 0, scores, ld, row0, topk, out);
+  return launch_ex(ctx, topk_kernel, dim3(nrows), dim3(kThreads), 0, scores, ld, nsplit, split_stride, row0, topk,
+                   out);
 }
 
 }  // namespace dsa
