@@ -12,9 +12,12 @@
 // One CTA (4 warps) per query gathers K and V blocks exactly as the forward
 // does.  Per warp and 16-key slice: S and dP on mma.sync, dQ accumulated in
 // registers, and the slice's dK/dV rows (16 keys x 128 dims, already summed
-// over the 16 heads by the MMA) added straight from the MMA fragments into
-// fp32 accumulators with 16-byte reductions.  A final kernel rounds the
-// accumulators to bf16.
+// over the 16 heads by the MMA) added into fp32 accumulators with 16-byte
+// reductions.  The reductions are L2-bound, and L2 serves them best when one
+// warp instruction covers whole 128-byte lines: so each 32-dim block of the
+// slice's rows goes through a small shared tile, and each reduction
+// instruction then adds one pool's four key rows, 128 bytes of each.  A final
+// kernel rounds the accumulators to bf16.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -32,8 +35,10 @@ constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kQBytes = kHq * kD * 2;
 constexpr uint32_t kTBytes = kHq * 16 * 2;  // per-warp [16 heads][16 keys] bf16 tile
+constexpr int kStgLd = 40;                   // staged rows: 32 dims + 8 pad floats (conflict-free float2 stores)
+constexpr uint32_t kStgBytes = 2 * 16 * kStgLd * 4;  // per warp: dV and dK blocks of 16 keys x 32 dims
 constexpr int kMaxTopk = 2048;
-constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes;
+constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes + kWarps * kStgBytes;
 constexpr size_t smem_bytes(int topk) { return kSmemFixed + (topk + 8) * sizeof(int32_t); }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -67,22 +72,7 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
   }
 }
 
-// Adds one C fragment (16 keys x 8 dims, rows = keys) into acc[row, :] with
-// 16-byte reductions: the two lanes of a pair swap halves so each lane owns
-// four consecutive columns of one key.
-__device__ __forceinline__ void red_frag(float* __restrict__ acc, const float (&c)[4], int64_t row_g, bool ok_g,
-                                         int64_t row_g8, bool ok_g8, int col0, int t4) {
-  const bool odd = t4 & 1;
-  const float s0 = odd ? c[0] : c[2];
-  const float s1 = odd ? c[1] : c[3];
-  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
-  const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
-  if (!odd) {
-    if (ok_g) red_add_v4(acc + row_g * kD + col0 + 2 * t4, c[0], c[1], r0, r1);
-  } else {
-    if (ok_g8) red_add_v4(acc + row_g8 * kD + col0 + 2 * t4 - 2, r0, r1, c[2], c[3]);
-  }
-}
+__device__ __forceinline__ int warp_of_thread() { return static_cast<int>(threadIdx.x) >> 5; }
 
 __global__ void __launch_bounds__(kThreads, 2)
     attn_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ q,
@@ -99,7 +89,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sdO = base + kQBytes;
   const uint32_t sKV = base + 2 * kQBytes;
   const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P hi, P lo, dS hi, dS lo tiles
-  int32_t* slots = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes);
+  float* stg = reinterpret_cast<float*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes) +
+               warp_of_thread() * (kStgBytes / 4);  // this warp's dV block, then its dK block
+  int32_t* slots = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes +
+                                              kWarps * kStgBytes);
   __shared__ int s_nsel;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -275,45 +268,70 @@ __global__ void __launch_bounds__(kThreads, 2)
       ldsm_x4_t(sTw + 2 * kTBytes + off, dth[0], dth[1], dth[2], dth[3]);
       ldsm_x4_t(sTw + 3 * kTBytes + off, dtl[0], dtl[1], dtl[2], dtl[3]);
     }
-    // global rows of this thread's two dK/dV rows: keys g and g+8 of the slice
-    int64_t krow[2];
-    bool kok[2];
+    // staged reductions: instruction k of a block adds slot (key0/4 + k)'s pool,
+    // key (lane >> 3) of it, dims 4 * (lane & 7) .. + 3 of the block
+    int64_t rrow[4];
+    bool rok[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int kb = key0 + g + 8 * e;
-      const int slot = b * kBlkPools + (kb >> 2);
+    for (int kq = 0; kq < 4; ++kq) {
+      const int slot = b * kBlkPools + (key0 >> 2) + kq;
+      const int kr = lane >> 3;
       if (slot < nsel) {
         const int32_t p = slots[slot];
-        krow[e] = 4 * static_cast<int64_t>(p) + (kb & 3);
-        kok[e] = p >= 0;
+        rrow[kq] = 4 * static_cast<int64_t>(p) + kr;
+        rok[kq] = p >= 0;
       } else {
-        krow[e] = 4 * n_elig + (kb & 3);
-        kok[e] = slot == nsel && krow[e] <= i;
+        rrow[kq] = 4 * n_elig + kr;
+        rok[kq] = slot == nsel && rrow[kq] <= i;
       }
     }
-    // dV rows += P^T dO ; dK rows += (scale dS)^T Q   (16 keys x 128 dims)
+    float* stg_v = stg;
+    float* stg_k = stg + 16 * kStgLd;
+    // dV rows += P^T dO ; dK rows += (scale dS)^T Q   (16 keys x 128 dims, in 32-dim blocks)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int mat = lane >> 3;
-      const int r = (lane & 7) + ((mat & 1) << 3);
-      const int c = 2 * j + (mat >> 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sdO + swz(r, c), b0, b1, b2, b3);
-      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16_16816(c0, pth, b0, b1);
-      mma_bf16_16816(c0, ptl, b0, b1);
-      mma_bf16_16816(c1, pth, b2, b3);
-      mma_bf16_16816(c1, ptl, b2, b3);
-      red_frag(dv_acc, c0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4);
-      red_frag(dv_acc, c1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4);
-      ldsm_x4_t(sQ + swz(r, c), b0, b1, b2, b3);
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16_16816(d0, dth, b0, b1);
-      mma_bf16_16816(d0, dtl, b0, b1);
-      mma_bf16_16816(d1, dth, b2, b3);
-      mma_bf16_16816(d1, dtl, b2, b3);
-      red_frag(dk_acc, d0, krow[0], kok[0], krow[1], kok[1], 16 * j, t4);
-      red_frag(dk_acc, d1, krow[0], kok[0], krow[1], kok[1], 16 * j + 8, t4);
+    for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int j = 2 * jj + hh;
+        const int mat = lane >> 3;
+        const int r = (lane & 7) + ((mat & 1) << 3);
+        const int c = 2 * j + (mat >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sdO + swz(r, c), b0, b1, b2, b3);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(c0, pth, b0, b1);
+        mma_bf16_16816(c0, ptl, b0, b1);
+        mma_bf16_16816(c1, pth, b2, b3);
+        mma_bf16_16816(c1, ptl, b2, b3);
+        const int col = hh * 16 + 2 * t4;
+        *reinterpret_cast<float2*>(stg_v + g * kStgLd + col) = make_float2(c0[0], c0[1]);
+        *reinterpret_cast<float2*>(stg_v + (g + 8) * kStgLd + col) = make_float2(c0[2], c0[3]);
+        *reinterpret_cast<float2*>(stg_v + g * kStgLd + col + 8) = make_float2(c1[0], c1[1]);
+        *reinterpret_cast<float2*>(stg_v + (g + 8) * kStgLd + col + 8) = make_float2(c1[2], c1[3]);
+        ldsm_x4_t(sQ + swz(r, c), b0, b1, b2, b3);
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(d0, dth, b0, b1);
+        mma_bf16_16816(d0, dtl, b0, b1);
+        mma_bf16_16816(d1, dth, b2, b3);
+        mma_bf16_16816(d1, dtl, b2, b3);
+        *reinterpret_cast<float2*>(stg_k + g * kStgLd + col) = make_float2(d0[0], d0[1]);
+        *reinterpret_cast<float2*>(stg_k + (g + 8) * kStgLd + col) = make_float2(d0[2], d0[3]);
+        *reinterpret_cast<float2*>(stg_k + g * kStgLd + col + 8) = make_float2(d1[0], d1[1]);
+        *reinterpret_cast<float2*>(stg_k + (g + 8) * kStgLd + col + 8) = make_float2(d1[2], d1[3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int row = 4 * kq + (lane >> 3);
+        const int cc = 4 * (lane & 7);
+        const float4 xv = *reinterpret_cast<const float4*>(stg_v + row * kStgLd + cc);
+        const float4 xk = *reinterpret_cast<const float4*>(stg_k + row * kStgLd + cc);
+        if (rok[kq]) {
+          red_add_v4(dv_acc + rrow[kq] * kD + 32 * jj + cc, xv.x, xv.y, xv.z, xv.w);
+          red_add_v4(dk_acc + rrow[kq] * kD + 32 * jj + cc, xk.x, xk.y, xk.z, xk.w);
+        }
+      }
+      __syncwarp();  // the staged block is rewritten by the next one
     }
     __syncwarp();  // the P / dS tiles are rewritten by the next slice
   }
