@@ -387,16 +387,44 @@ def run_ours(args):
         bo = sum(t.numel() * t.element_size() for t in out_host.values())
         e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
+        # Copies overlap compute the way a pipelined caller would: the indexer
+        # inputs go first on the compute stream; q, k, v, dO travel on a copy
+        # stream while the indexer runs; pool_idx, o and lse come back while the
+        # backward runs; dq, dk, dv follow the backward.
+        copy_stream = torch.cuda.Stream(device=dev)
+        idx_in, attn_in = ("q_idx", "k_idx", "w"), ("q", "k", "v", "dO")
+        def e2e_step(s):
+            flush.zero_()
+            if s >= 0:
+                e2e_evs[s][0].record(stream)
+            for name in idx_in:
+                d[name].copy_(pin[name], non_blocking=True)
+            # host -> device bandwidth is shared: the attention inputs start once the indexer's have landed
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for name in attn_in:
+                    d[name].copy_(pin[name], non_blocking=True)
+            ev_in = copy_stream.record_event()
+            dsa.dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
+                               workspace=ws_idx)
+            stream.wait_event(ev_in)
+            dsa.dsa_sparse_attn_fwd(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for name, src in (("pool_idx", pool_idx), ("o", o), ("lse", lse)):
+                    out_host[name].copy_(src, non_blocking=True)
+            dsa.dsa_sparse_attn_bwd(d["dO"], d["q"], d["k"], d["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk,
+                                    dv=dv, workspace=ws_bwd)
+            for name, src in (("dq", dq), ("dk", dk), ("dv", dv)):
+                out_host[name].copy_(src, non_blocking=True)
+            stream.wait_stream(copy_stream)
+            if s >= 0:
+                e2e_evs[s][1].record(stream)
+
+        e2e_step(-1)  # untimed: first use of the copy stream and the pinned output buffers
         barrier()
         for s in range(args.steps):
-            flush.zero_()
-            e2e_evs[s][0].record(stream)
-            for name, t in pin.items():
-                d[name].copy_(t, non_blocking=True)
-            step(d)
-            for name, src in (("pool_idx", pool_idx), ("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-                out_host[name].copy_(src, non_blocking=True)
-            e2e_evs[s][1].record(stream)
+            e2e_step(s)
         barrier()
         e2e_s = sum(a.elapsed_time(b) for a, b in e2e_evs) / 1e3
         if world > 1:
@@ -404,7 +432,7 @@ def run_ours(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_s = float(t.item())
         e2e = {"value": world * S * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo}
+               "d2h_bytes_per_step": bo, "step_ms": [a.elapsed_time(b) for a, b in e2e_evs]}
 
     if rank == 0:
         cpu = None
