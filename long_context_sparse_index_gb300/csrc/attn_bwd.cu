@@ -39,7 +39,15 @@ constexpr int kStgLd = 40;                   // staged rows: 32 dims + 8 pad flo
 constexpr uint32_t kStgBytes = 2 * 16 * kStgLd * 4;  // per warp: dV and dK blocks of 16 keys x 32 dims
 constexpr int kMaxTopk = 2048;
 constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes + kWarps * kStgBytes;
-constexpr size_t smem_bytes(int topk) { return kSmemFixed + (topk + 8) * sizeof(int32_t); }
+// row table: one int32 per key of every block (topk pools + the own pool, in blocks of 16 slots)
+constexpr size_t smem_bytes(int topk) {
+  return kSmemFixed + static_cast<size_t>((topk + 1 + kBlkPools - 1) / kBlkPools) * kBlkKeys * sizeof(int32_t);
+}
+
+// Position in a block's row table of key kr (0..63): keys kr0, kr0 + 8, ...,
+// kr0 + 56 (kr0 = kr % 8) are adjacent, so the thread that gathers them
+// reads their rows with two 16-byte loads.
+__device__ __forceinline__ int row_slot(int kr) { return (kr & 7) * 8 + (kr >> 3); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -47,26 +55,20 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 256 + ((c ^ (r & 7)) << 4));
 }
 
+// Gathers the K and V rows of block `blk` into stage buffer `st` (rows as in
+// the forward: -1 = zero-filled and masked).  Thread t copies 16-byte chunk
+// t % 16 of keys t / 16 + 8u, u = 0..7.
 __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* __restrict__ k,
-                                             const __nv_bfloat16* __restrict__ v, const int32_t* slots, int nsel,
-                                             int64_t i, int blk) {
-  const int64_t m = i >> 2;
+                                             const __nv_bfloat16* __restrict__ v, const int32_t* rows, int blk) {
+  const int kr0 = threadIdx.x >> 4, cc = threadIdx.x & 15;
+  const int4 ra = *reinterpret_cast<const int4*>(rows + blk * kBlkKeys + kr0 * 8);
+  const int4 rb = *reinterpret_cast<const int4*>(rows + blk * kBlkKeys + kr0 * 8 + 4);
+  const int32_t r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
-  for (int u = 0; u < (kBlkKeys * 16) / kThreads; ++u) {
-    const int c = threadIdx.x + u * kThreads;
-    const int kr = c >> 4, cc = c & 15;
-    const int slot = blk * kBlkPools + (kr >> 2);
-    int64_t row = 0;
-    bool ok = false;
-    if (slot < nsel) {
-      const int32_t p = slots[slot];
-      row = 4 * static_cast<int64_t>(p) + (kr & 3);
-      ok = p >= 0;
-    } else if (slot == nsel) {
-      row = 4 * m + (kr & 3);
-      ok = row <= i;
-    }
-    const int64_t src = (ok ? row : 0) * kD + cc * 8;
+  for (int u = 0; u < 8; ++u) {
+    const int kr = kr0 + 8 * u;
+    const bool ok = r8[u] >= 0;
+    const int64_t src = static_cast<int64_t>(ok ? r8[u] : 0) * kD + cc * 8;
     cp_async16(st + swz(kr, cc), k + src, ok);
     cp_async16(st + kTileBytes + swz(kr, cc), v + src, ok);
   }
@@ -91,8 +93,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P hi, P lo, dS hi, dS lo tiles
   float* stg = reinterpret_cast<float*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes) +
                warp_of_thread() * (kStgBytes / 4);  // this warp's dV block, then its dK block
-  int32_t* slots = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes +
-                                              kWarps * kStgBytes);
+  int32_t* rows = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes +
+                                             kWarps * kStgBytes);
   __shared__ int s_nsel;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -103,25 +105,30 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) s_nsel = topk;
   __syncthreads();
   const int32_t* prow = pool_idx + i * topk;
-  for (int j = tid; j < topk; j += kThreads) {
-    const int32_t p = prow[j];
-    if (p < 0) atomicMin(&s_nsel, j);
-    slots[j] = p;
-  }
+  for (int j = tid; j < topk; j += kThreads)
+    if (prow[j] < 0) atomicMin(&s_nsel, j);
   __syncthreads();
   const int nsel = s_nsel;
+  const int nblk = (nsel + 1 + kBlkPools - 1) / kBlkPools;
+  // row table of every block, built and checked as in the forward
   bool bad = false;
-  for (int j = tid; j < nsel; j += kThreads) {
-    const int32_t p = prow[j];
-    if (p >= n_elig) {
-      slots[j] = -1;
-      bad = true;
-    } else if (j > 0 && p <= prow[j - 1]) {
-      bad = true;
+  for (int e = tid; e < nblk * kBlkKeys; e += kThreads) {
+    const int blk = e / kBlkKeys, pos = e % kBlkKeys;
+    const int kr = (pos & 7) * 8 + (pos >> 3);  // inverse of row_slot
+    const int slot = blk * kBlkPools + (kr >> 2);
+    int32_t row = -1;
+    if (slot < nsel) {
+      const int32_t p = prow[slot];
+      if (p < n_elig) row = 4 * p + (kr & 3);
+      else bad = true;
+      if ((kr & 3) == 0 && slot > 0 && p <= prow[slot - 1]) bad = true;
+    } else if (slot == nsel) {
+      const int64_t r = 4 * n_elig + (kr & 3);
+      if (r <= i) row = static_cast<int32_t>(r);
     }
+    rows[e] = row;
   }
   if (bad) record_status(status, kStatusInternal);
-  const int nblk = (nsel + 1 + kBlkPools - 1) / kBlkPools;
 
   {
     const __nv_bfloat16* qrow = q + i * (kHq * kD);
@@ -136,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
-    if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, slots, nsel, i, s);
+    if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, rows, s);
     cp_async_commit();
   }
 
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     {
       const int nb = b + kStages - 1;
-      if (nb < nblk) gather_block(sKV + (nb % kStages) * kStageBytes, k, v, slots, nsel, i, nb);
+      if (nb < nblk) gather_block(sKV + (nb % kStages) * kStageBytes, k, v, rows, nb);
       cp_async_commit();
     }
     const uint32_t sK = sKV + (b % kStages) * kStageBytes;
@@ -201,10 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     {
       const int kc[4] = {key0 + 2 * t4, key0 + 2 * t4 + 1, key0 + 8 + 2 * t4, key0 + 9 + 2 * t4};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int slot = b * kBlkPools + (kc[e] >> 2);
-        valid[e] = slot < nsel ? (slots[slot] >= 0) : (slot == nsel && 4 * n_elig + (kc[e] & 3) <= i);
-      }
+      for (int e = 0; e < 4; ++e) valid[e] = rows[b * kBlkKeys + row_slot(kc[e])] >= 0;
     }
     // P and dS (fragment order: e=0..3 row g / g+8 for n-tile 0, then n-tile 1)
     float P[8], dS[8];
@@ -274,16 +278,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool rok[4];
 #pragma unroll
     for (int kq = 0; kq < 4; ++kq) {
-      const int slot = b * kBlkPools + (key0 >> 2) + kq;
-      const int kr = lane >> 3;
-      if (slot < nsel) {
-        const int32_t p = slots[slot];
-        rrow[kq] = 4 * static_cast<int64_t>(p) + kr;
-        rok[kq] = p >= 0;
-      } else {
-        rrow[kq] = 4 * n_elig + kr;
-        rok[kq] = slot == nsel && rrow[kq] <= i;
-      }
+      const int32_t r = rows[b * kBlkKeys + row_slot(key0 + 4 * kq + (lane >> 3))];
+      rrow[kq] = r;
+      rok[kq] = r >= 0;
     }
     float* stg_v = stg;
     float* stg_k = stg + 16 * kStgLd;
