@@ -52,6 +52,17 @@ def parse_args():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x: the slowest rank sets the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
@@ -333,10 +344,7 @@ def run_ours(args):
     dsa.dsa_sync_status()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(total_s, dev)
     value = world * S * args.steps / total_s
 
     # ---- per-kernel device time, live, with events around every launch (one more step)
@@ -428,10 +436,7 @@ def run_ours(args):
             e2e_step(s)
         barrier()
         e2e_s = sum(a.elapsed_time(b) for a, b in e2e_evs) / 1e3
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(e2e_s, dev)
         e2e = {"value": world * S * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "step_ms": [a.elapsed_time(b) for a, b in e2e_evs]}
 

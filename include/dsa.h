@@ -140,6 +140,46 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
                                  void* stream);
 
 /*
+ * Query-range forms of the attention calls, for a rank that holds only some
+ * of the sequence's queries (context parallelism [CP-lesson §改进二: the
+ * sequence is split across GPUs by query rows, and each rank still needs all
+ * keys]).  Queries q_begin .. q_end-1 (global positions, 0 <= q_begin <
+ * q_end <= S) are processed:
+ *  q, o, dO, dq   bf16 [q_end - q_begin, Hq, D]  local rows (row r = query q_begin + r)
+ *  lse            fp32 [q_end - q_begin, Hq]     local rows
+ *  pool_idx       int32 [q_end - q_begin, topk]  local rows, as dsa_index_topk
+ *                 writes them for the same range
+ *  k, v           bf16 [S, D]                   the whole sequence
+ *  dk, dv         bf16 [S, D]                   this range's contribution only;
+ *                 summing the ranks' contributions (a reduce-scatter or
+ *                 all-reduce across ranks, which the caller runs) gives the
+ *                 full gradient
+ * The other arguments and the workspace are as in the unsharded calls, which
+ * are these calls with the range [0, S).  Results for a query do not depend
+ * on the range it is computed in (dk/dv up to fp32 summation order).
+ */
+dsa_status_t dsa_sparse_attn_fwd_range(const void* q, const void* k, const void* v, const int32_t* pool_idx,
+                                       int64_t S, int64_t q_begin, int64_t q_end, int Hq, int D, int topk,
+                                       float scale, void* o, float* lse, void* stream);
+dsa_status_t dsa_sparse_attn_bwd_range(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                       const float* lse, const int32_t* pool_idx, int64_t S, int64_t q_begin,
+                                       int64_t q_end, int Hq, int D, int topk, float scale, void* dq, void* dk,
+                                       void* dv, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Zig-zag query ranges of `rank` among `world` ranks  [CP-lesson §改进二,
+ * zig-zag pairing]: the sequence is cut into 2*world segments
+ * [j*S/(2*world), (j+1)*S/(2*world)); rank r takes segments r and
+ * 2*world-1-r, so with causal masking every rank has the same amount of work
+ * (exactly, when 2*world divides S).  Writes ranges = {b0, e0, b1, e1}
+ * (half-open, global positions; a range may be empty for tiny S).  Each
+ * range is passed to dsa_index_topk / dsa_sparse_attn_*_range as
+ * q_begin/q_end; positions stay global, so pools stay aligned with their keys.
+ * Host-only; DSA_ERR_INVALID_ARG unless S >= 1 and 0 <= rank < world.
+ */
+dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges);
+
+/*
  * Indexer + top-k for callers that cannot allocate device memory.  (The
  * source pages have no counterpart to this call; it exists for users of the
  * library.)

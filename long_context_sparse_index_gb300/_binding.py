@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
 EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd_workspace",
             "dsa_sparse_attn_bwd", "dsa_sync_status", "dsa_clear_status", "dsa_last_error", "dsa_version",
             "dsa_profile_enable", "dsa_profile_read", "dsa_launch_count", "dsa_launch_count_reset",
-            "dsa_index_topk_noalloc")
+            "dsa_index_topk_noalloc", "dsa_sparse_attn_fwd_range", "dsa_sparse_attn_bwd_range",
+            "dsa_zigzag_ranges")
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +56,12 @@ def load():
             lib.dsa_sparse_attn_bwd_workspace.restype = sz
             lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp,
                                                 sz, vp]
+            lib.dsa_sparse_attn_fwd_range.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, f32, vp, vp, vp]
+            lib.dsa_sparse_attn_bwd_range.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, f32,
+                                                      vp, vp, vp, vp, sz, vp]
+            lib.dsa_zigzag_ranges.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+            for f in (lib.dsa_sparse_attn_fwd_range, lib.dsa_sparse_attn_bwd_range, lib.dsa_zigzag_ranges):
+                f.restype = ctypes.c_int
             lib.dsa_sync_status.argtypes = [vp]
             lib.dsa_clear_status.argtypes = []
             for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_bwd, lib.dsa_sync_status,
@@ -156,41 +163,59 @@ def dsa_index_topk_noalloc(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int 
     return pool_idx
 
 
-def dsa_sparse_attn_fwd(q, k, v, pool_idx, scale: float = 0.0, o=None, lse=None, stream=None):
-    """(o [S, Hq, D] bf16, lse [S, Hq] fp32)."""
+def dsa_sparse_attn_fwd(q, k, v, pool_idx, scale: float = 0.0, o=None, lse=None, stream=None, q_begin: int = 0):
+    """(o [nq, Hq, D] bf16, lse [nq, Hq] fp32) for queries q_begin .. q_begin + nq - 1.
+
+    q, pool_idx, o and lse hold those queries' rows (nq = q.shape[0]); k and v
+    hold the whole sequence [S, D].  With q_begin = 0 and nq = S this is the
+    unsharded forward."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 2)
     _need(v, "v", torch.bfloat16, 2)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    S, Hq, D = q.shape
-    if k.shape != (S, D) or v.shape != (S, D) or pool_idx.shape[0] != S:
-        raise ValueError("k, v must be [S, D] and pool_idx [S, topk]")
+    nq, Hq, D = q.shape
+    S = k.shape[0]
+    if k.shape != (S, D) or v.shape != (S, D) or pool_idx.shape[0] != nq:
+        raise ValueError("k, v must be [S, D] and pool_idx [nq, topk]")
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check(load().dsa_sparse_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S, Hq, D,
-                                      pool_idx.shape[1], float(scale), o.data_ptr(), lse.data_ptr(),
-                                      _stream_handle(stream)))
+    lse = torch.empty((nq, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(load().dsa_sparse_attn_fwd_range(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S,
+                                            q_begin, q_begin + nq, Hq, D, pool_idx.shape[1], float(scale),
+                                            o.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
     return o, lse
 
 
 def dsa_sparse_attn_bwd(dO, q, k, v, o, lse, pool_idx, scale: float = 0.0, dq=None, dk=None, dv=None,
-                        workspace=None, stream=None):
-    """(dq [S, Hq, D], dk [S, D], dv [S, D]) in bf16."""
+                        workspace=None, stream=None, q_begin: int = 0):
+    """(dq [nq, Hq, D], dk [S, D], dv [S, D]) in bf16 for queries q_begin .. q_begin + nq - 1.
+
+    dO, q, o, lse, pool_idx and dq hold those queries' rows; k, v, dk and dv
+    the whole sequence.  dk and dv are this range's contribution (the full
+    gradient when the range is the whole sequence)."""
     for t, n, nd in ((dO, "dO", 3), (q, "q", 3), (o, "o", 3), (k, "k", 2), (v, "v", 2)):
         _need(t, n, torch.bfloat16, nd)
     _need(lse, "lse", torch.float32, 2)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    S, Hq, D = q.shape
+    nq, Hq, D = q.shape
+    S = k.shape[0]
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     lib = load()
     ws = _workspace(lib.dsa_sparse_attn_bwd_workspace(S, Hq, D), q.device, workspace)
-    _check(lib.dsa_sparse_attn_bwd(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                   lse.data_ptr(), pool_idx.data_ptr(), S, Hq, D, pool_idx.shape[1], float(scale),
-                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
-                                   ws.numel() * ws.element_size(), _stream_handle(stream)))
+    _check(lib.dsa_sparse_attn_bwd_range(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), pool_idx.data_ptr(), S, q_begin, q_begin + nq, Hq, D,
+                                         pool_idx.shape[1], float(scale), dq.data_ptr(), dk.data_ptr(),
+                                         dv.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                         _stream_handle(stream)))
     return dq, dk, dv
+
+
+def zigzag_ranges(S: int, world: int, rank: int):
+    """[(b0, e0), (b1, e1)]: the two query ranges of `rank` under zig-zag sharding (host only)."""
+    out = (ctypes.c_int64 * 4)()
+    _check(load().dsa_zigzag_ranges(S, world, rank, out))
+    return [(int(out[0]), int(out[1])), (int(out[2]), int(out[3]))]
 
 
 def dsa_sync_status(stream=None):

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     attn_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ q,
                     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                     const float* __restrict__ lse, const float* __restrict__ delta,
-                    const int32_t* __restrict__ pool_idx, int64_t S, int topk, float scale, float scale_log2,
+                    const int32_t* __restrict__ pool_idx, int64_t q0, int topk, float scale, float scale_log2,
                     __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
                     unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -99,12 +99,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int64_t i = blockIdx.x;
+  // query i (global position) is local row r of q, dO, lse, Delta, pool_idx and dq
+  const int64_t r = blockIdx.x;
+  const int64_t i = q0 + r;
   const int64_t n_elig = i >> 2;
 
   if (tid == 0) s_nsel = topk;
   __syncthreads();
-  const int32_t* prow = pool_idx + i * topk;
+  const int32_t* prow = pool_idx + r * topk;
   for (int j = tid; j < topk; j += kThreads)
     if (prow[j] < 0) atomicMin(&s_nsel, j);
   __syncthreads();
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (bad) record_status(status, kStatusInternal);
 
   {
-    const __nv_bfloat16* qrow = q + i * (kHq * kD);
-    const __nv_bfloat16* drow = dO + i * (kHq * kD);
+    const __nv_bfloat16* qrow = q + r * (kHq * kD);
+    const __nv_bfloat16* drow = dO + r * (kHq * kD);
 #pragma unroll
     for (int u = 0; u < (kHq * 16) / kThreads; ++u) {
       const int c = tid + u * kThreads;
@@ -148,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // per-row constants (rows g and g+8 of this thread's fragments = heads)
-  const float lse2_0 = lse[i * kHq + g] * kLog2e, lse2_1 = lse[i * kHq + g + 8] * kLog2e;
-  const float dl0 = delta[i * kHq + g], dl1 = delta[i * kHq + g + 8];
+  const float lse2_0 = lse[r * kHq + g] * kLog2e, lse2_1 = lse[r * kHq + g + 8] * kLog2e;
+  const float dl0 = delta[r * kHq + g], dl1 = delta[r * kHq + g + 8];
 
   float dq_acc[16][4];
 #pragma unroll
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   // thread tid owns element pairs e = 2 * (tid + 128 m), m = 0..7 (consecutive across threads)
-  __nv_bfloat16* dqrow = dq + i * (kHq * kD);
+  __nv_bfloat16* dqrow = dq + r * (kHq * kD);
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int e = 2 * (tid + kThreads * m);
@@ -402,13 +404,15 @@ __global__ void cast_kernel(const float* __restrict__ a, const float* __restrict
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t S, float* delta, float* dk_acc,
+cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx) {
-  // dk_acc and dv_acc are adjacent in the workspace: zero 2 * S * D floats from dk_acc
+  // Delta for the nq local query rows; dk_acc and dv_acc are adjacent in the
+  // workspace: zero 2 * S * D floats from dk_acc
   (void)dv_acc;
-  const int64_t rows = S * kHq;
+  const int64_t rows = nq * kHq;
   const int block = 256;
-  const int64_t grid = (rows * 16 + block - 1) / block;
+  const int64_t threads = rows * 16 > S * kD / 8 ? rows * 16 : S * kD / 8;  // each zeroes ~4 float4
+  const int64_t grid = (threads + block - 1) / block;
   bwd_pre_kernel<<<static_cast<unsigned>(grid), block, 0, ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(o), rows, delta,
       reinterpret_cast<float4*>(dk_acc), 2 * S * kD / 4);
@@ -416,8 +420,9 @@ cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t S, float*
 }
 
 cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
-                            const float* delta, const int32_t* pool_idx, int64_t S, int topk, float scale, void* dq,
-                            float* dk_acc, float* dv_acc, const LaunchCtx& ctx) {
+                            const float* delta, const int32_t* pool_idx, int64_t q_begin, int64_t q_end, int topk,
+                            float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx) {
+  if (q_end <= q_begin) return cudaSuccess;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -427,9 +432,9 @@ cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const 
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
-  attn_bwd_kernel<<<static_cast<unsigned>(S), kThreads, smem_bytes(topk), ctx.stream>>>(
+  attn_bwd_kernel<<<static_cast<unsigned>(q_end - q_begin), kThreads, smem_bytes(topk), ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(q),
-      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), lse, delta, pool_idx, S, topk,
+      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), lse, delta, pool_idx, q_begin, topk,
       scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc, ctx.status);
   return cudaGetLastError();
 }

@@ -73,7 +73,7 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
 
 __global__ void __launch_bounds__(kThreads, 2)
     attn_fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                    const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t S, int topk,
+                    const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t q0, int topk,
                     float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -87,13 +87,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int64_t i = blockIdx.x;
+  // query i (global position) is local row r of q, pool_idx, o and lse
+  const int64_t r = blockIdx.x;
+  const int64_t i = q0 + r;
   const int64_t n_elig = i >> 2;
 
   // ---- selected pools of this query (leading non-negative entries)
   if (tid == 0) s_nsel = topk;
   __syncthreads();
-  const int32_t* prow = pool_idx + i * topk;
+  const int32_t* prow = pool_idx + r * topk;
   for (int j = tid; j < topk; j += kThreads)
     if (prow[j] < 0) atomicMin(&s_nsel, j);
   __syncthreads();
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- Q tile (swizzled) and the gather pipeline prologue
   {
-    const __nv_bfloat16* qrow = q + i * (kHq * kD);
+    const __nv_bfloat16* qrow = q + r * (kHq * kD);
 #pragma unroll
     for (int u = 0; u < (kHq * 16) / kThreads; ++u) {
       const int c = tid + u * kThreads;
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int w = 0; w < kWarps; ++w) L += s_l[w][h] * exp2f(s_m[w][h] - M);
     const float mine = m_run[hh] == -INFINITY ? 0.f : exp2f(m_run[hh] - M);
     fac[hh] = mine / L;
-    if (warp == 0 && t4 == 0) lse[i * kHq + h] = (M + log2f(L)) * kLn2;
+    if (warp == 0 && t4 == 0) lse[r * kHq + h] = (M + log2f(L)) * kLn2;
   }
   // partial O (already normalised) into shared memory, one [16][132] fp32 slab
   // per warp (padded rows spread the fragment stores over the banks)
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   // thread tid owns element pairs e = 2 * (tid + 128 m), m = 0..7 (consecutive across threads)
-  __nv_bfloat16* orow = o + i * (kHq * kD);
+  __nv_bfloat16* orow = o + r * (kHq * kD);
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int e = 2 * (tid + kThreads * m);
@@ -304,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
-                            int topk, float scale, void* o, float* lse, const LaunchCtx& ctx) {
-  if (S <= 0) return cudaSuccess;
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
+                            int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx) {
+  if (q_end <= q_begin) return cudaSuccess;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -316,9 +318,9 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const i
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
-  attn_fwd_kernel<<<static_cast<unsigned>(S), kThreads, smem_bytes(topk), ctx.stream>>>(
+  attn_fwd_kernel<<<static_cast<unsigned>(q_end - q_begin), kThreads, smem_bytes(topk), ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), pool_idx, S, topk, scale * kLog2e, static_cast<__nv_bfloat16*>(o), lse,
+      static_cast<const __nv_bfloat16*>(v), pool_idx, q_begin, topk, scale * kLog2e, static_cast<__nv_bfloat16*>(o), lse,
       ctx.status);
   return cudaGetLastError();
 }

@@ -308,22 +308,38 @@ static dsa_status_t check_attn_args(const char* fn, int64_t S, int Hq, int D, in
   return DSA_OK;
 }
 
-dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
-                                 int Hq, int D, int topk, float scale, void* o, float* lse, void* stream) {
+static dsa_status_t check_range(const char* fn, int64_t S, int64_t q_begin, int64_t q_end) {
+  if (q_begin < 0 || q_end > S || q_begin >= q_end)
+    return fail(DSA_ERR_INVALID_ARG, "%s: query range [%lld, %lld) not inside [0, %lld)", fn, (long long)q_begin,
+                (long long)q_end, (long long)S);
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_fwd_range(const void* q, const void* k, const void* v, const int32_t* pool_idx,
+                                       int64_t S, int64_t q_begin, int64_t q_end, int Hq, int D, int topk,
+                                       float scale, void* o, float* lse, void* stream) {
   if (!q || !k || !v || !pool_idx || !o || !lse)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: null tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(pool_idx) || !aligned16(o) || !aligned16(lse))
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: tensor pointers must be 16-byte aligned");
   dsa_status_t st = check_attn_args("dsa_sparse_attn_fwd", S, Hq, D, topk);
   if (st != DSA_OK) return st;
+  st = check_range("dsa_sparse_attn_fwd", S, q_begin, q_end);
+  if (st != DSA_OK) return st;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
   dsa::LaunchCtx ctx;
   st = make_ctx(stream, &ctx);
   if (st != DSA_OK) return st;
-  cudaError_t e = timed_launch("attn_fwd", ctx.stream,
-                               [&] { return dsa::launch_attn_fwd(q, k, v, pool_idx, S, topk, scale, o, lse, ctx); });
+  cudaError_t e = timed_launch("attn_fwd", ctx.stream, [&] {
+    return dsa::launch_attn_fwd(q, k, v, pool_idx, q_begin, q_end, topk, scale, o, lse, ctx);
+  });
   if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_fwd: launch");
   return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                                 int Hq, int D, int topk, float scale, void* o, float* lse, void* stream) {
+  return dsa_sparse_attn_fwd_range(q, k, v, pool_idx, S, 0, S, Hq, D, topk, scale, o, lse, stream);
 }
 
 size_t dsa_sparse_attn_bwd_workspace(int64_t S, int Hq, int D) {
@@ -332,16 +348,18 @@ size_t dsa_sparse_attn_bwd_workspace(int64_t S, int Hq, int D) {
          round_up(static_cast<size_t>(S) * Hq * sizeof(float), 256);
 }
 
-dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const void* o,
-                                 const float* lse, const int32_t* pool_idx, int64_t S, int Hq, int D, int topk,
-                                 float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-                                 void* stream) {
+dsa_status_t dsa_sparse_attn_bwd_range(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                       const float* lse, const int32_t* pool_idx, int64_t S, int64_t q_begin,
+                                       int64_t q_end, int Hq, int D, int topk, float scale, void* dq, void* dk,
+                                       void* dv, void* workspace, size_t ws_bytes, void* stream) {
   if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: null tensor pointer");
   if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(pool_idx) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: tensor pointers must be 16-byte aligned");
   dsa_status_t st = check_attn_args("dsa_sparse_attn_bwd", S, Hq, D, topk);
+  if (st != DSA_OK) return st;
+  st = check_range("dsa_sparse_attn_bwd", S, q_begin, q_end);
   if (st != DSA_OK) return st;
   const size_t need = dsa_sparse_attn_bwd_workspace(S, Hq, D);
   if (!workspace || ws_bytes < need)
@@ -358,17 +376,41 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
   float* dk_acc = reinterpret_cast<float*>(ws);
   float* dv_acc = reinterpret_cast<float*>(ws + acc_bytes);
   float* delta = reinterpret_cast<float*>(ws + 2 * acc_bytes);
+  const int64_t nq = q_end - q_begin;
   // S * D floats is a multiple of 64, so acc_bytes == S * D * 4 and the accumulators are adjacent
   cudaError_t e = timed_launch("attn_bwd_pre", ctx.stream,
-                               [&] { return dsa::launch_attn_bwd_pre(dO, o, S, delta, dk_acc, dv_acc, ctx); });
+                               [&] { return dsa::launch_attn_bwd_pre(dO, o, nq, S, delta, dk_acc, dv_acc, ctx); });
   if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd: preprocess launch");
   e = timed_launch("attn_bwd", ctx.stream, [&] {
-    return dsa::launch_attn_bwd(dO, q, k, v, lse, delta, pool_idx, S, topk, scale, dq, dk_acc, dv_acc, ctx);
+    return dsa::launch_attn_bwd(dO, q, k, v, lse, delta, pool_idx, q_begin, q_end, topk, scale, dq, dk_acc, dv_acc,
+                                ctx);
   });
   if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd: launch");
   e = timed_launch("attn_bwd_cast", ctx.stream,
                    [&] { return dsa::launch_cast_dkdv(dk_acc, dv_acc, S * D, dk, dv, ctx); });
   if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd: cast launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const int32_t* pool_idx, int64_t S, int Hq, int D, int topk,
+                                 float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  return dsa_sparse_attn_bwd_range(dO, q, k, v, o, lse, pool_idx, S, 0, S, Hq, D, topk, scale, dq, dk, dv,
+                                   workspace, ws_bytes, stream);
+}
+
+dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges) {
+  if (!ranges) return fail(DSA_ERR_INVALID_ARG, "dsa_zigzag_ranges: null output");
+  if (S < 1 || world < 1 || rank < 0 || rank >= world)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_zigzag_ranges: S=%lld, world=%d, rank=%d", (long long)S, world, rank);
+  const int64_t nseg = 2 * static_cast<int64_t>(world);
+  // segment j = [j*S/nseg, (j+1)*S/nseg): equal lengths when nseg divides S
+  auto bound = [&](int64_t j) { return static_cast<int64_t>((static_cast<__int128>(j) * S) / nseg); };
+  ranges[0] = bound(rank);
+  ranges[1] = bound(rank + 1);
+  ranges[2] = bound(nseg - 1 - rank);
+  ranges[3] = bound(nseg - rank);
   return DSA_OK;
 }
 

@@ -51,14 +51,16 @@ size_t indexer_smem_bytes();
 cudaError_t launch_topk(const float* scores, int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows,
                         int topk, int32_t* out, const LaunchCtx& ctx);
 
-cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
-                            int topk, float scale, void* o, float* lse, const LaunchCtx& ctx);
+// Queries [q_begin, q_end) (global positions); q, pool_idx, o and lse hold
+// their rows locally (row r = query q_begin + r); k and v are the whole sequence.
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
+                            int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx);
 
-cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t S, float* delta, float* dk_acc,
+cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx);
 cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
-                            const float* delta, const int32_t* pool_idx, int64_t S, int topk, float scale, void* dq,
-                            float* dk_acc, float* dv_acc, const LaunchCtx& ctx);
+                            const float* delta, const int32_t* pool_idx, int64_t q_begin, int64_t q_end, int topk,
+                            float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx);
 cudaError_t launch_cast_dkdv(const float* dk_acc, const float* dv_acc, int64_t n, void* dk, void* dv,
                              const LaunchCtx& ctx);
 

@@ -97,6 +97,18 @@ def test_attention_rejects_bad_arguments(lib):
     assert b(*args[:7], 64, 16, 128, 4096, 0.0, *args[12:], FAKE, 1 << 30, None) == dsa.DSA_ERR_UNSUPPORTED
 
 
+def test_attention_ranges_are_checked(lib):
+    """The range forms reject a query range outside [0, S) before any device access."""
+    import long_context_sparse_index_gb300 as dsa
+    f = lib.dsa_sparse_attn_fwd_range
+    for qb, qe in ((0, 0), (-1, 10), (10, 65), (40, 30)):
+        assert f(FAKE, FAKE, FAKE, FAKE, 64, qb, qe, 16, 128, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_INVALID_ARG
+        assert b"query range" in lib.dsa_last_error()
+    b = lib.dsa_sparse_attn_bwd_range
+    args = [FAKE] * 7 + [64, 70, 80, 16, 128, 8, 0.0] + [FAKE] * 3 + [FAKE, 1 << 30, None]
+    assert b(*args) == dsa.DSA_ERR_INVALID_ARG
+
+
 def test_no_device_reports_cuda_error_not_crash(lib):
     """With valid arguments but no usable GPU the call fails with DSA_ERR_CUDA
     (or runs, on a GPU host) -- it never falls back to another path."""

@@ -96,6 +96,49 @@ def test_index_topk_s16k_float_selection_within_tolerance():
     assert agree > 0.99, agree
 
 
+# --------------------------------------------------------------------------- query-range sharding
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_zigzag_sharded_layer_equals_unsharded(world):
+    """Every rank's zig-zag ranges through dsa_index_topk and the range forms
+    of the attention calls (local q/o/dO/dq rows, whole-sequence k/v): pool_idx,
+    o, lse and dq equal the unsharded calls bit for bit, and the ranges' dk/dv
+    contributions add up to the unsharded gradient."""
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    qi, ki, wi = _indexer_to_gpu(q_idx, k_idx, w)
+    qt, kt, vt, dOt = _attn_to_gpu(*synth.attention_inputs(wl), synth.grad_output(wl))
+    S, scale = wl.S, 0.02
+    full_sel = dsa.dsa_index_topk(qi, ki, wi, chunk=256, topk=wl.topk)
+    o_full, lse_full = dsa.dsa_sparse_attn_fwd(qt, kt, vt, full_sel, scale=scale)
+    dq_full, dk_full, dv_full = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o_full, lse_full, full_sel, scale=scale)
+    sel = torch.full_like(full_sel, -7)
+    o, lse, dq = torch.zeros_like(o_full), torch.zeros_like(lse_full), torch.zeros_like(dq_full)
+    dk_sum = torch.zeros(dk_full.shape, dtype=torch.float32, device=DEV)
+    dv_sum, dk_abs, dv_abs = torch.zeros_like(dk_sum), torch.zeros_like(dk_sum), torch.zeros_like(dk_sum)
+    for rank in range(world):
+        for b, e in dsa.zigzag_ranges(S, world, rank):
+            if b == e:
+                continue
+            s_ = dsa.dsa_index_topk(qi, ki, wi, chunk=100, topk=wl.topk, q_begin=b, q_end=e)
+            ql, dl = qt[b:e].contiguous(), dOt[b:e].contiguous()
+            o_, l_ = dsa.dsa_sparse_attn_fwd(ql, kt, vt, s_, scale=scale, q_begin=b)
+            dq_, dk_, dv_ = dsa.dsa_sparse_attn_bwd(dl, ql, kt, vt, o_, l_, s_, scale=scale, q_begin=b)
+            sel[b:e], o[b:e], lse[b:e], dq[b:e] = s_, o_, l_, dq_
+            dk_sum += dk_.float()
+            dv_sum += dv_.float()
+            dk_abs += dk_.float().abs()
+            dv_abs += dv_.float().abs()
+    dsa.dsa_sync_status()
+    assert torch.equal(sel, full_sel)
+    assert torch.equal(o, o_full) and torch.equal(lse, lse_full) and torch.equal(dq, dq_full)
+    # each contribution is rounded to bf16 (half an ulp: 2^-9 relative) before the sum
+    for got, ref, mag in ((dk_sum, dk_full.float(), dk_abs), (dv_sum, dv_full.float(), dv_abs)):
+        assert ((got - ref).abs() <= 2 ** -8 * (mag + ref.abs()) + 1e-6).all()
+    ref_sel, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk)
+    assert np.array_equal(sel.cpu().numpy(), ref_sel)
+
+
 # --------------------------------------------------------------------------- attention forward
 
 def _fwd_check(q, k, v, sel, rows=None, scale=0.0):
