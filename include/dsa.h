@@ -34,8 +34,9 @@
  *  - Batch 1, row-major, no padding.  bf16 tensors are passed as void*.
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The
  *    library allocates no device memory; scratch comes from the caller's
- *    `workspace` (sized by the *_workspace() queries).  Pointers must be
- *    16-byte aligned.
+ *    `workspace` (sized by the *_workspace() queries).  bf16 tensors must
+ *    be 16-byte aligned; fp32 and int32 tensors (w, lse, pool_idx) 4-byte
+ *    aligned.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *    enqueue work and return; results are ready in stream order.
  *  - Arguments are checked before anything is launched; on error nothing is
@@ -178,6 +179,35 @@ dsa_status_t dsa_sparse_attn_bwd_range(const void* dO, const void* q, const void
  * Host-only; DSA_ERR_INVALID_ARG unless S >= 1 and 0 <= rank < world.
  */
 dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges);
+
+/*
+ * Packed variable-length batches.  nseq sequences lie end to end in every
+ * tensor; sequence s covers rows cu_seqlens[s] .. cu_seqlens[s+1]-1
+ * (cu_seqlens: HOST array of nseq+1 strictly increasing int64 offsets,
+ * cu_seqlens[0] = 0; the total is the packed length).  Each sequence is its
+ * own causal layer, as if passed alone: its pools, eligibility and pool_idx
+ * entries count from its first token, and no query sees another sequence's
+ * keys.  Tensors, scale and topk are as in the single-sequence calls, with
+ * the packed length in place of S; dk/dv rows of a sequence hold that
+ * sequence's gradient.  The workspace must hold the *_varlen_workspace()
+ * bytes (the single-sequence workspace of the longest sequence); the
+ * sequences run one after another on `stream`.  An invalid cu_seqlens or a
+ * short workspace returns DSA_ERR_INVALID_ARG / DSA_ERR_WORKSPACE (and, for
+ * the query functions, 0) before anything runs.  (The pages train single
+ * sequences; packing is what a training data loader hands the layer.)
+ */
+size_t dsa_index_topk_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hi, int Di, int chunk, int topk);
+dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const float* w, const int64_t* cu_seqlens,
+                                   int nseq, int Hi, int Di, int chunk, int topk, int32_t* pool_idx, void* workspace,
+                                   size_t ws_bytes, void* stream);
+dsa_status_t dsa_sparse_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* pool_idx,
+                                        const int64_t* cu_seqlens, int nseq, int Hq, int D, int topk, float scale,
+                                        void* o, float* lse, void* stream);
+size_t dsa_sparse_attn_bwd_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hq, int D);
+dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                        const float* lse, const int32_t* pool_idx, const int64_t* cu_seqlens,
+                                        int nseq, int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
+                                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Indexer + top-k for callers that cannot allocate device memory.  (The

@@ -27,7 +27,8 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_sparse_attn_bwd", "dsa_sync_status", "dsa_clear_status", "dsa_last_error", "dsa_version",
             "dsa_profile_enable", "dsa_profile_read", "dsa_launch_count", "dsa_launch_count_reset",
             "dsa_index_topk_noalloc", "dsa_sparse_attn_fwd_range", "dsa_sparse_attn_bwd_range",
-            "dsa_zigzag_ranges")
+            "dsa_zigzag_ranges", "dsa_index_topk_varlen_workspace", "dsa_index_topk_varlen",
+            "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +62,17 @@ def load():
                                                       vp, vp, vp, vp, sz, vp]
             lib.dsa_zigzag_ranges.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
             for f in (lib.dsa_sparse_attn_fwd_range, lib.dsa_sparse_attn_bwd_range, lib.dsa_zigzag_ranges):
+                f.restype = ctypes.c_int
+            pi64 = ctypes.POINTER(ctypes.c_int64)
+            lib.dsa_index_topk_varlen_workspace.argtypes = [pi64, i32, i32, i32, i32, i32]
+            lib.dsa_index_topk_varlen_workspace.restype = sz
+            lib.dsa_index_topk_varlen.argtypes = [vp, vp, vp, pi64, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+            lib.dsa_sparse_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, pi64, i32, i32, i32, i32, f32, vp, vp, vp]
+            lib.dsa_sparse_attn_bwd_varlen_workspace.argtypes = [pi64, i32, i32, i32]
+            lib.dsa_sparse_attn_bwd_varlen_workspace.restype = sz
+            lib.dsa_sparse_attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, pi64, i32, i32, i32, i32, f32, vp,
+                                                       vp, vp, vp, sz, vp]
+            for f in (lib.dsa_index_topk_varlen, lib.dsa_sparse_attn_fwd_varlen, lib.dsa_sparse_attn_bwd_varlen):
                 f.restype = ctypes.c_int
             lib.dsa_sync_status.argtypes = [vp]
             lib.dsa_clear_status.argtypes = []
@@ -208,6 +220,69 @@ def dsa_sparse_attn_bwd(dO, q, k, v, o, lse, pool_idx, scale: float = 0.0, dq=No
                                          pool_idx.shape[1], float(scale), dq.data_ptr(), dk.data_ptr(),
                                          dv.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
                                          _stream_handle(stream)))
+    return dq, dk, dv
+
+
+def _cu(cu_seqlens):
+    vals = [int(x) for x in cu_seqlens]
+    return (ctypes.c_int64 * len(vals))(*vals), len(vals) - 1
+
+
+def dsa_index_topk_varlen(q_idx, k_idx, w, cu_seqlens, chunk: int, topk: int, pool_idx=None, workspace=None,
+                          stream=None):
+    """Packed batch: pool_idx [T, topk] with each sequence's pool indices
+    counted from its own first token (cu_seqlens: nseq + 1 host offsets)."""
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    _need(k_idx, "k_idx", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    T, Hi, Di = q_idx.shape
+    cu, nseq = _cu(cu_seqlens)
+    if nseq < 1 or cu[nseq] != T:
+        raise ValueError("cu_seqlens must end at the packed length")
+    if pool_idx is None:
+        pool_idx = torch.empty((T, topk), dtype=torch.int32, device=q_idx.device)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    lib = load()
+    ws = _workspace(lib.dsa_index_topk_varlen_workspace(cu, nseq, Hi, Di, chunk, topk), q_idx.device, workspace)
+    _check(lib.dsa_index_topk_varlen(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), cu, nseq, Hi, Di, chunk, topk,
+                                     pool_idx.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                     _stream_handle(stream)))
+    return pool_idx
+
+
+def dsa_sparse_attn_fwd_varlen(q, k, v, pool_idx, cu_seqlens, scale: float = 0.0, o=None, lse=None, stream=None):
+    """Packed batch forward: (o [T, Hq, D], lse [T, Hq]), each sequence attending within itself."""
+    for t, n, nd in ((q, "q", 3), (k, "k", 2), (v, "v", 2)):
+        _need(t, n, torch.bfloat16, nd)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    T, Hq, D = q.shape
+    cu, nseq = _cu(cu_seqlens)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(load().dsa_sparse_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), cu, nseq,
+                                             Hq, D, pool_idx.shape[1], float(scale), o.data_ptr(), lse.data_ptr(),
+                                             _stream_handle(stream)))
+    return o, lse
+
+
+def dsa_sparse_attn_bwd_varlen(dO, q, k, v, o, lse, pool_idx, cu_seqlens, scale: float = 0.0, dq=None, dk=None,
+                               dv=None, workspace=None, stream=None):
+    """Packed batch backward: (dq [T, Hq, D], dk [T, D], dv [T, D])."""
+    for t, n, nd in ((dO, "dO", 3), (q, "q", 3), (o, "o", 3), (k, "k", 2), (v, "v", 2)):
+        _need(t, n, torch.bfloat16, nd)
+    _need(lse, "lse", torch.float32, 2)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    T, Hq, D = q.shape
+    cu, nseq = _cu(cu_seqlens)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = load()
+    ws = _workspace(lib.dsa_sparse_attn_bwd_varlen_workspace(cu, nseq, Hq, D), q.device, workspace)
+    _check(lib.dsa_sparse_attn_bwd_varlen(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                          lse.data_ptr(), pool_idx.data_ptr(), cu, nseq, Hq, D, pool_idx.shape[1],
+                                          float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                                          ws.numel() * ws.element_size(), _stream_handle(stream)))
     return dq, dk, dv
 
 

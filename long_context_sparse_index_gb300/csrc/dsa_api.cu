@@ -53,6 +53,8 @@ dsa_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// fp32 / int32 tensors the kernels only access element by element
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -203,8 +205,9 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
                             int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
                             void* workspace, size_t ws_bytes, void* stream) {
   if (!q_idx || !k_idx || !w || !pool_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: null tensor pointer");
-  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(pool_idx))
-    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: tensor pointers must be 16-byte aligned");
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(pool_idx))
+    return fail(DSA_ERR_INVALID_ARG,
+                "dsa_index_topk: q_idx and k_idx must be 16-byte aligned, w and pool_idx 4-byte aligned");
   if (S < 1 || S > 0x7FFFFFFFLL) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: S=%lld out of range", (long long)S);
   if (chunk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: chunk=%d must be >= 1", chunk);
   if (topk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: topk=%d must be >= 1", topk);
@@ -320,8 +323,9 @@ dsa_status_t dsa_sparse_attn_fwd_range(const void* q, const void* k, const void*
                                        float scale, void* o, float* lse, void* stream) {
   if (!q || !k || !v || !pool_idx || !o || !lse)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: null tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(pool_idx) || !aligned16(o) || !aligned16(lse))
-    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: tensor pointers must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(pool_idx) || !aligned16(o) || !aligned4(lse))
+    return fail(DSA_ERR_INVALID_ARG,
+                "dsa_sparse_attn_fwd: bf16 tensors must be 16-byte aligned, pool_idx and lse 4-byte aligned");
   dsa_status_t st = check_attn_args("dsa_sparse_attn_fwd", S, Hq, D, topk);
   if (st != DSA_OK) return st;
   st = check_range("dsa_sparse_attn_fwd", S, q_begin, q_end);
@@ -354,9 +358,10 @@ dsa_status_t dsa_sparse_attn_bwd_range(const void* dO, const void* q, const void
                                        void* dv, void* workspace, size_t ws_bytes, void* stream) {
   if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: null tensor pointer");
-  if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(pool_idx) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: tensor pointers must be 16-byte aligned");
+  if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+      !aligned4(pool_idx) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(DSA_ERR_INVALID_ARG,
+                "dsa_sparse_attn_bwd: bf16 tensors must be 16-byte aligned, pool_idx and lse 4-byte aligned");
   dsa_status_t st = check_attn_args("dsa_sparse_attn_bwd", S, Hq, D, topk);
   if (st != DSA_OK) return st;
   st = check_range("dsa_sparse_attn_bwd", S, q_begin, q_end);
@@ -411,6 +416,105 @@ dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges) 
   ranges[1] = bound(rank + 1);
   ranges[2] = bound(nseg - 1 - rank);
   ranges[3] = bound(nseg - rank);
+  return DSA_OK;
+}
+
+// ---------------------------------------------------------------- packed variable-length batches
+// Each sequence of the batch is its own causal layer: the calls below run the
+// single-sequence entry points on each sequence's rows in turn (one stream,
+// so one workspace serves them all).
+
+static dsa_status_t check_cu_seqlens(const char* fn, const int64_t* cu, int nseq) {
+  if (!cu || nseq < 1) return fail(DSA_ERR_INVALID_ARG, "%s: need cu_seqlens and nseq >= 1", fn);
+  if (cu[0] != 0) return fail(DSA_ERR_INVALID_ARG, "%s: cu_seqlens[0] must be 0", fn);
+  for (int s = 0; s < nseq; ++s)
+    if (cu[s + 1] <= cu[s])
+      return fail(DSA_ERR_INVALID_ARG, "%s: cu_seqlens must be strictly increasing (sequence %d is empty)", fn, s);
+  return DSA_OK;
+}
+
+static int64_t max_len(const int64_t* cu, int nseq) {
+  int64_t m = 0;
+  for (int s = 0; s < nseq; ++s) m = cu[s + 1] - cu[s] > m ? cu[s + 1] - cu[s] : m;
+  return m;
+}
+
+size_t dsa_index_topk_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hi, int Di, int chunk, int topk) {
+  if (check_cu_seqlens("dsa_index_topk_varlen_workspace", cu_seqlens, nseq) != DSA_OK) return 0;
+  return dsa_index_topk_workspace(max_len(cu_seqlens, nseq), Hi, Di, chunk, topk);
+}
+
+dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const float* w, const int64_t* cu_seqlens,
+                                   int nseq, int Hi, int Di, int chunk, int topk, int32_t* pool_idx, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  dsa_status_t st = check_cu_seqlens("dsa_index_topk_varlen", cu_seqlens, nseq);
+  if (st != DSA_OK) return st;
+  // checked up front, so that an error leaves every sequence untouched: the
+  // other checks are the same for every sequence and fail on the first
+  const size_t need = dsa_index_topk_varlen_workspace(cu_seqlens, nseq, Hi, Di, chunk, topk);
+  if (!workspace || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk_varlen: workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  const uint8_t* qb = static_cast<const uint8_t*>(q_idx);
+  const uint8_t* kb = static_cast<const uint8_t*>(k_idx);
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t o = cu_seqlens[s], L = cu_seqlens[s + 1] - o;
+    st = dsa_index_topk(qb ? qb + o * Hi * Di * 2 : nullptr, kb ? kb + o * Di * 2 : nullptr, w ? w + o * Hi : nullptr,
+                        L, Hi, Di, chunk, topk, 0, L, pool_idx ? pool_idx + o * topk : nullptr, workspace, ws_bytes,
+                        stream);
+    if (st != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* pool_idx,
+                                        const int64_t* cu_seqlens, int nseq, int Hq, int D, int topk, float scale,
+                                        void* o, float* lse, void* stream) {
+  dsa_status_t st = check_cu_seqlens("dsa_sparse_attn_fwd_varlen", cu_seqlens, nseq);
+  if (st != DSA_OK) return st;
+  const int64_t qrow = static_cast<int64_t>(Hq) * D * 2, krow = static_cast<int64_t>(D) * 2;
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t off = cu_seqlens[s], L = cu_seqlens[s + 1] - off;
+    auto at = [&](const void* p, int64_t row_bytes) -> const uint8_t* {
+      return p ? static_cast<const uint8_t*>(p) + off * row_bytes : nullptr;
+    };
+    st = dsa_sparse_attn_fwd(at(q, qrow), at(k, krow), at(v, krow), pool_idx ? pool_idx + off * topk : nullptr, L,
+                             Hq, D, topk, scale, o ? static_cast<uint8_t*>(o) + off * qrow : nullptr,
+                             lse ? lse + off * Hq : nullptr, stream);
+    if (st != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
+size_t dsa_sparse_attn_bwd_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hq, int D) {
+  if (check_cu_seqlens("dsa_sparse_attn_bwd_varlen_workspace", cu_seqlens, nseq) != DSA_OK) return 0;
+  return dsa_sparse_attn_bwd_workspace(max_len(cu_seqlens, nseq), Hq, D);
+}
+
+dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const void* k, const void* v, const void* o,
+                                        const float* lse, const int32_t* pool_idx, const int64_t* cu_seqlens,
+                                        int nseq, int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+  dsa_status_t st = check_cu_seqlens("dsa_sparse_attn_bwd_varlen", cu_seqlens, nseq);
+  if (st != DSA_OK) return st;
+  const size_t need = dsa_sparse_attn_bwd_varlen_workspace(cu_seqlens, nseq, Hq, D);
+  if (!workspace || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "dsa_sparse_attn_bwd_varlen: workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  const int64_t qrow = static_cast<int64_t>(Hq) * D * 2, krow = static_cast<int64_t>(D) * 2;
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t off = cu_seqlens[s], L = cu_seqlens[s + 1] - off;
+    auto at = [&](const void* p, int64_t row_bytes) -> const uint8_t* {
+      return p ? static_cast<const uint8_t*>(p) + off * row_bytes : nullptr;
+    };
+    auto atw = [&](void* p, int64_t row_bytes) -> uint8_t* {
+      return p ? static_cast<uint8_t*>(p) + off * row_bytes : nullptr;
+    };
+    st = dsa_sparse_attn_bwd(at(dO, qrow), at(q, qrow), at(k, krow), at(v, krow), at(o, qrow),
+                             lse ? lse + off * Hq : nullptr, pool_idx ? pool_idx + off * topk : nullptr, L, Hq, D,
+                             topk, scale, atw(dq, qrow), atw(dk, krow), atw(dv, krow), workspace, ws_bytes, stream);
+    if (st != DSA_OK) return st;
+  }
   return DSA_OK;
 }
 

@@ -68,7 +68,8 @@ def _idx(lib, **kw):
 def test_index_topk_rejects_bad_arguments(lib):
     import long_context_sparse_index_gb300 as dsa
     assert _idx(lib, q=None) == dsa.DSA_ERR_INVALID_ARG
-    assert _idx(lib, w=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, w=FAKE + 2) == dsa.DSA_ERR_INVALID_ARG
+    assert _idx(lib, q=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG
     assert _idx(lib, S=0) == dsa.DSA_ERR_INVALID_ARG
     assert _idx(lib, chunk=0) == dsa.DSA_ERR_INVALID_ARG
     assert _idx(lib, topk=0) == dsa.DSA_ERR_INVALID_ARG
@@ -107,6 +108,31 @@ def test_attention_ranges_are_checked(lib):
     b = lib.dsa_sparse_attn_bwd_range
     args = [FAKE] * 7 + [64, 70, 80, 16, 128, 8, 0.0] + [FAKE] * 3 + [FAKE, 1 << 30, None]
     assert b(*args) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_varlen_checks_cu_seqlens_and_workspace(lib):
+    """Packed batches: cu_seqlens must start at 0 and increase strictly; the
+    workspace queries give the longest sequence's workspace; errors come back
+    before any sequence runs."""
+    import ctypes
+    import long_context_sparse_index_gb300 as dsa
+    def cu(*v):
+        return (ctypes.c_int64 * len(v))(*v)
+    good = cu(0, 5, 1029, 1030)
+    assert lib.dsa_index_topk_varlen_workspace(good, 3, 8, 64, 256, 64) == lib.dsa_index_topk_workspace(1024, 8, 64,
+                                                                                                         256, 64)
+    assert lib.dsa_sparse_attn_bwd_varlen_workspace(good, 3, 16, 128) == lib.dsa_sparse_attn_bwd_workspace(1024, 16,
+                                                                                                           128)
+    for bad, n in ((cu(1, 5), 1), (cu(0, 5, 5), 2), (cu(0, 7, 3), 2), (cu(0), 0)):
+        assert lib.dsa_index_topk_varlen_workspace(bad, n, 8, 64, 256, 64) == 0
+        assert lib.dsa_index_topk_varlen(FAKE, FAKE, FAKE, bad, n, 8, 64, 256, 64, FAKE, FAKE, 1 << 30,
+                                         None) == dsa.DSA_ERR_INVALID_ARG
+        assert lib.dsa_sparse_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, bad, n, 16, 128, 8, 0.0, FAKE, FAKE,
+                                              None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_index_topk_varlen(FAKE, FAKE, FAKE, good, 3, 8, 64, 256, 64, FAKE, FAKE, 1000,
+                                     None) == dsa.DSA_ERR_WORKSPACE
+    args = [FAKE] * 7 + [good, 3, 16, 128, 8, 0.0] + [FAKE] * 3
+    assert lib.dsa_sparse_attn_bwd_varlen(*args, FAKE, 1000, None) == dsa.DSA_ERR_WORKSPACE
 
 
 def test_no_device_reports_cuda_error_not_crash(lib):

@@ -139,6 +139,43 @@ def test_zigzag_sharded_layer_equals_unsharded(world):
     assert np.array_equal(sel.cpu().numpy(), ref_sel)
 
 
+# --------------------------------------------------------------------------- packed variable-length batches
+
+def test_varlen_packed_batch_equals_each_sequence_alone():
+    """Five sequences packed end to end (lengths 1, 6, 1030, 3, 2051): every
+    sequence's pool_idx (counted from its own first token) equals the oracle's
+    for that sequence alone, bit for bit, and its forward and backward match
+    the oracle run on that sequence alone."""
+    lens = [1, 6, 1030, 3, 2051]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, Hi, topk, scale = int(cu[-1]), 8, 64, 0.05
+    q_idx = synth.int_bf16(T, 1, (T, Hi, 64), -3, 3)
+    k_idx = synth.int_bf16(T, 2, (T, 64), -3, 3)
+    w = synth.int_f32(T, 3, (T, Hi), -1, 3)
+    wl = synth.Workload("t", T, topk=topk, seed=17)
+    q, k, v = synth.attention_inputs(wl)
+    dO = synth.grad_output(wl)
+    qi, ki, wi = _indexer_to_gpu(q_idx, k_idx, w)
+    qt, kt, vt, dOt = _attn_to_gpu(q, k, v, dO)
+    sel = dsa.dsa_index_topk_varlen(qi, ki, wi, cu, chunk=300, topk=topk)
+    o, lse = dsa.dsa_sparse_attn_fwd_varlen(qt, kt, vt, sel, cu, scale=scale)
+    dq, dk, dv = dsa.dsa_sparse_attn_bwd_varlen(dOt, qt, kt, vt, o, lse, sel, cu, scale=scale)
+    dsa.dsa_sync_status()
+    sel, go, gl = sel.cpu().numpy(), torch_bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    gdq, gdk, gdv = torch_bf16_to_f64(dq), torch_bf16_to_f64(dk), torch_bf16_to_f64(dv)
+    for a, b in zip(cu[:-1], cu[1:]):
+        ref_sel, _ = oracle.index_topk(q_idx[a:b], k_idx[a:b], w[a:b], topk)
+        assert np.array_equal(sel[a:b], ref_sel)
+        seq = (q[a:b], k[a:b], v[a:b])
+        ro, rl = oracle.attn_fwd(*seq, ref_sel, scale=scale)
+        assert_close(go[a:b], ro, "o")
+        assert_close(gl[a:b], rl, "lse", bf16_out=False)
+        assert_close(gdq[a:b], oracle.attn_bwd_dq(dO[a:b], *seq, ref_sel, scale=scale), "dq")
+        rdk, rdv = oracle.attn_bwd_dkdv(dO[a:b], *seq, ref_sel, scale=scale)
+        assert_close(gdk[a:b], rdk, "dk")
+        assert_close(gdv[a:b], rdv, "dv")
+
+
 # --------------------------------------------------------------------------- attention forward
 
 def _fwd_check(q, k, v, sel, rows=None, scale=0.0):
