@@ -66,10 +66,14 @@ typedef enum {
   DSA_ERR_INTERNAL = 6      /* a device-side consistency check failed       */
 } dsa_status_t;
 
-/* Bytes of workspace dsa_index_topk needs for sequence length S, Hi indexer
- * heads of dim Di, query chunk `chunk` and `topk`: the pooled keys (as a bf16
- * hi/lo pair, 256 B per pool) plus one chunk of fp32 scores
- * (chunk x ceil(S/4 to 256) x 4 B; 32 MiB at S = 131072, chunk = 256).
+/* Bytes of workspace dsa_index_topk is best given for sequence length S, Hi
+ * indexer heads of dim Di, query chunk `chunk` and `topk`: 256 B of kernel
+ * words, the pooled keys (as a bf16 hi/lo pair, 256 B per pool) and a ring of
+ * min(8, ceil(S/chunk)) chunk buffers of fp32 scores, which consecutive chunks
+ * take in turn (each min(chunk, S) x ceil(S/4 to 256) x 4 B; 8 x 32 MiB at
+ * S = 131072, chunk = 256).  dsa_index_topk also accepts a smaller workspace,
+ * down to min(2, ceil(S/chunk)) buffers, and uses as many buffers as fit:
+ * fewer buffers keep fewer chunks in flight (slower), with the same result.
  * Returns 0 for invalid arguments. */
 size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
 
@@ -89,8 +93,9 @@ size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
  *  pool_idx  int32 [q_end - q_begin, topk] output: for query i the selected
  *            pools in ascending order, then -1 padding (row i holds
  *            min(topk, floor(i/4)) pools)
- *  workspace, ws_bytes  device scratch of at least
- *            dsa_index_topk_workspace(S, Hi, Di, chunk, topk) bytes
+ *  workspace, ws_bytes  device scratch: dsa_index_topk_workspace(S, Hi, Di,
+ *            chunk, topk) bytes, or fewer down to the two-buffer minimum
+ *            (see there)
  *
  * Selection is exact with respect to the fp32 scores the kernels compute
  * (bf16 inputs, fp32 accumulation, pooled keys carried as a bf16 hi/lo pair
@@ -215,7 +220,7 @@ dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const voi
  * library.)
  *
  * Same arguments, outputs and results as dsa_index_topk, but without a
- * workspace: the scratch lives in a fixed static device buffer of 10 MiB +
+ * workspace: the scratch lives in a fixed static device buffer of 18 MiB +
  * 256 B inside the library, which every GPU that loads the library holds
  * until the process exits.  That covers S <= 32768 with chunk <= 256; larger
  * sizes return DSA_ERR_WORKSPACE (see dsa_last_error()) and nothing runs.

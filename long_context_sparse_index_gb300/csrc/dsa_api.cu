@@ -2,8 +2,9 @@
 // checks, workspace carving, TMA descriptors and the query-chunk loop.
 //
 // [SkyRL-1M §1 DSA 真稀疏; Anyscale "稀疏注意力会导致二次成本"] the indexer
-// scores one chunk of queries at a time, so its scratch is one chunk of
-// scores (chunk x pools x 4 B) rather than the whole S x S/4 matrix.
+// scores one chunk of queries at a time, so its scratch is a ring of at most
+// eight chunks of scores (chunk x pools x 4 B each; two at the least) rather
+// than the whole S x S/4 matrix.
 // [Anyscale "检查每一层是否运行您认为的内核"] a shape the kernels do not
 // implement is an error, never a silent fallback.
 #include <cudaTypedefs.h>
@@ -36,6 +37,8 @@ constexpr int kD = 128;
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxHi = 64;
 constexpr int64_t kPoolTile = 256;
+constexpr size_t kSyncBytes = 256;  // the fused kernel's global words, first in the index workspace
+static_assert(dsa::kIndexSyncWords * 8 <= kSyncBytes, "sync words");
 
 dsa_status_t fail(dsa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
@@ -158,35 +161,33 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
   return e;
 }
 
-// Head ranges for one chunk's indexer launch.  A chunk with few tiles would
-// leave most SMs idle; splitting its heads into ns ranges multiplies its work
-// units by ns (each unit then costs ~1/ns of a tile plus a fixed overhead).
-// The choice depends on the shapes only (a fixed 152-SM reference, not the
-// device), so results never depend on where they were computed.  The ns
-// slices of nrows x (npb_max*256) floats must fit the chunk's score buffer.
-int choose_nsplit(int64_t tiles, int64_t npb_max, int Hi, int64_t ld) {
-  constexpr int64_t kRefSms = 152;
-  int best = 1;
-  double best_cost = 1e300;
-  for (int ns = 1; ns <= 4; ns *= 2) {
-    if (ns > Hi || ns * npb_max * kPoolTile > ld) break;
-    const double waves = static_cast<double>((ns * tiles + kRefSms - 1) / kRefSms);
-    const double cost = waves * (1.0 / ns + 0.03);
-    if (cost < best_cost - 1e-9) {
-      best = ns;
-      best_cost = cost;
-    }
-  }
-  return best;
+// Score buffers in the index workspace: a ring of chunk buffers, at least
+// min(2, chunks) and at most dsa::kMaxBufs.  The count only changes how many
+// chunks are in flight, never the result.
+int index_max_bufs(int64_t S, int chunk) {
+  const int64_t nchunks = (S + chunk - 1) / chunk;
+  return static_cast<int>(nchunks < dsa::kMaxBufs ? nchunks : dsa::kMaxBufs);
 }
+int index_min_bufs(int64_t S, int chunk) { return index_max_bufs(S, chunk) < 2 ? index_max_bufs(S, chunk) : 2; }
 
 size_t index_ws_khat(int64_t S) { return round_up(static_cast<size_t>(S / 4 > 0 ? S / 4 : 1) * 2 * kDi * 2, 256); }
 int64_t pools_padded(int64_t S) { return ((S / 4 + kPoolTile - 1) / kPoolTile) * kPoolTile + (S / 4 == 0 ? kPoolTile : 0); }
+size_t index_buf_bytes(int64_t S, int chunk) {
+  const int64_t rows = chunk < S ? chunk : S;
+  return round_up(static_cast<size_t>(rows) * pools_padded(S) * sizeof(float), 256);
+}
+size_t index_ws_bytes(int64_t S, int chunk, int nbuf) {
+  return kSyncBytes + index_ws_khat(S) + static_cast<size_t>(nbuf) * index_buf_bytes(S, chunk);
+}
 
 }  // namespace
 
 namespace dsa {
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+size_t index_topk_min_workspace(int64_t S, int chunk) {
+  if (S < 1 || chunk < 1) return 0;
+  return index_ws_bytes(S, chunk, index_min_bufs(S, chunk));
+}
 }  // namespace dsa
 
 extern "C" {
@@ -197,8 +198,7 @@ const char* dsa_version(void) { return "libdsa 0.1.0 (sm_103a)"; }
 
 size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk) {
   if (S < 1 || Hi < 1 || Di < 1 || chunk < 1 || topk < 1) return 0;
-  const int64_t rows = chunk < S ? chunk : S;
-  return index_ws_khat(S) + round_up(static_cast<size_t>(rows) * pools_padded(S) * sizeof(float), 256);
+  return index_ws_bytes(S, chunk, index_max_bufs(S, chunk));
 }
 
 dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
@@ -218,10 +218,10 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
   if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Di=%d unsupported (kernels implement Di=64)", Di);
   if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Hi=%d unsupported (max %d)", Hi, kMaxHi);
   if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: topk=%d unsupported (max %d)", topk, kMaxTopk);
-  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk);
+  const size_t need = index_ws_bytes(S, chunk, index_min_bufs(S, chunk));
   if (!workspace || ws_bytes < need)
-    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk: workspace of %zu bytes needed, %zu given", need,
-                workspace ? ws_bytes : (size_t)0);
+    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk: workspace of at least %zu bytes needed (%zu recommended), %zu given",
+                need, dsa_index_topk_workspace(S, Hi, Di, chunk, topk), workspace ? ws_bytes : (size_t)0);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: workspace must be 256-byte aligned");
 
@@ -232,10 +232,16 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
   const int64_t P = S / 4;
   const int64_t ld = pools_padded(S);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* khat2 = ws;
-  float* scores = reinterpret_cast<float*>(ws + index_ws_khat(S));
+  unsigned long long* sync_words = reinterpret_cast<unsigned long long*>(ws);
+  void* khat2 = ws + kSyncBytes;
+  float* scores = reinterpret_cast<float*>(ws + kSyncBytes + index_ws_khat(S));
+  const int64_t buf_stride = static_cast<int64_t>(index_buf_bytes(S, chunk) / sizeof(float));
+  int nbuf = index_min_bufs(S, chunk);  // as many chunk buffers as the workspace holds
+  while (nbuf < index_max_bufs(S, chunk) && index_ws_bytes(S, chunk, nbuf + 1) <= ws_bytes) ++nbuf;
 
   CUtensorMap q_map, k_map;
+  memset(&q_map, 0, sizeof(q_map));
+  memset(&k_map, 0, sizeof(k_map));
   const bool need_indexer = (q_end - 1) / 4 > topk;  // some row has more eligible pools than topk
   if (need_indexer) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
@@ -260,45 +266,18 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "dsa_index_topk: pooled-key tensor map (CUresult %d)", (int)r);
     }
-    cudaError_t e = timed_launch("pool_keys", ctx.stream, [&] { return dsa::launch_pool_keys(k_idx, P, khat2, ctx); });
-    if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: pool_keys launch");
   }
-  // Kernels after the first of this call may start early (programmatic
-  // dependent launch); each waits for its predecessor before touching the
-  // score buffer.
-  dsa::LaunchCtx chain = ctx;
-  chain.pdl = 1;
-  bool first = !need_indexer;  // pool_keys, when launched, is the call's first kernel
-  for (int64_t c0 = q_begin; c0 < q_end; c0 += chunk) {
-    const int64_t c1 = c0 + chunk < q_end ? c0 + chunk : q_end;
-    const int nrows = static_cast<int>(c1 - c0);
-    // this chunk's rows are compact: a row holds the pools of the chunk's last query, rounded to a tile
-    const int64_t npb_max = ((c1 - 1) / 4 + kPoolTile - 1) / kPoolTile;
-    const int64_t ld_c = npb_max > 0 ? npb_max * kPoolTile : kPoolTile;
-    int nsplit = 1;
-    if ((c1 - 1) / 4 > topk) {
-      int64_t tiles = 0;  // tiles holding eligible pairs
-      for (int64_t q0 = c0; q0 < c1; q0 += 128) {
-        const int64_t last = (q0 + 128 < c1 ? q0 + 128 : c1) - 1;
-        tiles += (last / 4 + kPoolTile - 1) / kPoolTile;
-      }
-      nsplit = choose_nsplit(tiles, npb_max, Hi, ld);
-      const int64_t split_stride = static_cast<int64_t>(nrows) * ld_c;
-      const dsa::LaunchCtx& lc = first ? ctx : chain;
-      first = false;
-      cudaError_t e = timed_launch("indexer", ctx.stream, [&] {
-        return dsa::launch_indexer(q_map, k_map, w, scores, ld_c, nsplit, split_stride, c0, nrows, Hi, lc);
-      });
-      if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: indexer launch");
-    }
-    const dsa::LaunchCtx& lt = first ? ctx : chain;
-    first = false;
-    cudaError_t e = timed_launch("topk", ctx.stream, [&] {
-      return dsa::launch_topk(scores, ld_c, nsplit, static_cast<int64_t>(nrows) * ld_c, c0, nrows, topk,
-                              pool_idx + (c0 - q_begin) * topk, lt);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: top-k launch");
-  }
+  // pool_keys also zeroes the fused kernel's global words, so it always runs
+  cudaError_t e = timed_launch("pool_keys", ctx.stream,
+                               [&] { return dsa::launch_pool_keys(k_idx, P, khat2, sync_words, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: pool_keys launch");
+  // one persistent kernel walks every chunk: indexer tiles and top-k rows
+  // (when no row has more than topk pools there are only rows, and no tensor map is read)
+  e = timed_launch("index_topk", ctx.stream, [&] {
+    return dsa::launch_index_topk(q_map, k_map, w, scores, ld, buf_stride, nbuf, q_begin, q_end, chunk, Hi, topk,
+                                  pool_idx, sync_words, ctx);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: index_topk launch");
   return DSA_OK;
 }
 

@@ -34,22 +34,27 @@ cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(KArgs...), dim3 grid,
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Global words of the fused indexer + top-k kernel (64-bit each), at the start
+// of its workspace, and its most score buffers.
+constexpr int kIndexSyncWords = 24;
+constexpr int kMaxBufs = 8;
+
 // Pooled indexer keys: khat2 [P, 128] bf16, hi in columns 0..63, lo in 64..127.
-cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, const LaunchCtx& ctx);
+// Also zeroes the kIndexSyncWords words at sync_words (always launch it, even
+// with P == 0, before launch_index_topk).
+cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, unsigned long long* sync_words,
+                             const LaunchCtx& ctx);
 
-// Scores of query rows [row0, row0 + nrows) against pools [0, floor((row0+nrows-1)/4)),
-// as nsplit partial sums over equal head ranges: slice s holds
-// scores[s * split_stride + (i - row0) * ld + p]; entries p >= floor(i/4) are
-// not meaningful.
-cudaError_t launch_indexer(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
-                           int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows, int Hi,
-                           const LaunchCtx& ctx);
-size_t indexer_smem_bytes();
-
-// Per-row top-k of the scores written by launch_indexer (the nsplit slices
-// added in slice order); out rows are pool_idx rows for queries row0 .. row0 + nrows - 1.
-cudaError_t launch_topk(const float* scores, int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows,
-                        int topk, int32_t* out, const LaunchCtx& ctx);
+// Indexer scores and per-row top-k for query rows [q_begin, q_end), in query
+// chunks of `chunk` rows, as one persistent cooperative kernel (one CTA per
+// SM).  scores holds nbuf chunk buffers (`chunk` rows x ld floats each,
+// buf_stride floats apart; chunk c uses buffer c % nbuf); pool_idx row r is
+// query q_begin + r.
+cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
+                              int64_t ld, int64_t buf_stride, int nbuf, int64_t q_begin, int64_t q_end, int chunk,
+                              int Hi, int topk, int32_t* pool_idx, unsigned long long* sync_words,
+                              const LaunchCtx& ctx);
+size_t index_topk_smem_bytes();
 
 // Queries [q_begin, q_end) (global positions); q, pool_idx, o and lse hold
 // their rows locally (row r = query q_begin + r); k and v are the whole sequence.

@@ -19,7 +19,8 @@
 // Every call on a device shares the same array, and the array keeps whatever
 // the previous call left in it.  Nothing in it needs to start at zero: each
 // call rebuilds the pooled keys and rewrites every score it reads before
-// reading it.  Two calls whose work overlaps on the GPU (different streams
+// reading it, and the kernel's global words are zeroed by the call's first
+// kernel.  Two calls whose work overlaps on the GPU (different streams
 // without ordering between them) race on the array and must not be issued.
 #include <cuda_runtime.h>
 
@@ -30,13 +31,16 @@
 
 namespace dsa {
 void set_last_error(const std::string& msg);  // dsa_api.cu: the message dsa_last_error() returns
+size_t index_topk_min_workspace(int64_t S, int chunk);  // dsa_api.cu: the least workspace dsa_index_topk accepts
 }
 
 namespace {
 
-// 10 MiB + 256 B: enough for dsa_index_topk_workspace(S, Hi, Di, chunk, topk)
-// with S <= 32768 and chunk <= 256 (pooled keys 2 MiB + scores 8 MiB).
-constexpr size_t kNoAllocScratchBytes = (static_cast<size_t>(10) << 20) + 256;
+// 18 MiB + 256 B: the least workspace dsa_index_topk accepts for S <= 32768
+// with chunk <= 256 (the kernel's global words 256 B, pooled keys 2 MiB, two
+// chunk buffers of scores 8 MiB each; more buffers only let more chunks be in
+// flight and never change the result).
+constexpr size_t kNoAllocScratchBytes = (static_cast<size_t>(18) << 20) + 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -51,7 +55,7 @@ extern "C" {
 dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
                                     int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
                                     void* stream) {
-  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk);
+  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk) == 0 ? 0 : dsa::index_topk_min_workspace(S, chunk);
   if (need == 0) {
     // invalid sizes: let the regular entry point report the precise reason
     return dsa_index_topk(q_idx, k_idx, w, S, Hi, Di, chunk, topk, q_begin, q_end, pool_idx, nullptr, 0, stream);

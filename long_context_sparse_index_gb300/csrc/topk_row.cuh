@@ -1,47 +1,50 @@
-// topk.cu -- per-query top-k of indexer scores.
+// topk_row.cuh -- per-query top-k of indexer scores, as a device routine run
+// by a group of 128 threads (4 warps, one named barrier) on one query row.
 //
 // [SkyRL-1M §1 DSA 真稀疏] each query keeps its highest-scoring pools and the
 // selection travels as int32 pool indices.  For query i with n = floor(i/4)
-// eligible pools the kernel keeps min(topk, n) of them: every pool whose
+// eligible pools the routine keeps min(topk, n) of them: every pool whose
 // score is larger than the k-th largest score T, plus the lowest-indexed
 // pools whose score equals T.  Kept pools are written in ascending order,
 // then -1.
 //
-// Method (one CTA of 512 threads per query row; scores map to
-// order-preserving 32-bit keys):
+// Method (scores map to order-preserving 32-bit keys):
 //   1. Threshold guess.  A strided sample of kSample keys is histogrammed on
-//      the top 11 bits of its span; the lower edge t of the bin that holds
-//      the r-th largest sample is the threshold, with r chosen so that, for
-//      any row whose large scores are not packed into a few places, at least
-//      topk keys of the row are >= t while only a few thousand are (short
+//      the top kDigitBits bits of its span; the lower edge t of the bin that
+//      holds the r-th largest sample is the threshold, with r chosen so that,
+//      unless the row's large scores are packed into a few places, at least
+//      topk keys of the row are >= t while only about a thousand are (short
 //      rows skip this: every key is a candidate).
 //   2. One pass over the row: each warp owns a contiguous stretch and appends
 //      the keys >= t, with their indices, to its own buffer in index order.
-//   3. If there are at least topk candidates and no buffer overflowed, the
-//      exact k-th largest candidate key T (and how many keys equal to T to
-//      keep) comes from 11-bit digit rounds over the candidates; once the
-//      bin holding T has at most kSmall keys, those are ranked against each
-//      other directly.  The candidates are then walked in index order (a
-//      scan over the 16 warp buffers) to write the kept indices.  Every key
-//      of the row that is >= T is a candidate, so this is exact.
+//   3. With at least topk candidates and no buffer overflowing, the exact
+//      k-th largest candidate key T comes from digit rounds over the
+//      candidates; once the bin holding T has at most kSmall keys they are
+//      ranked against each other directly.  The candidates are then walked in
+//      index order to write the kept indices.  Every key of the row that is
+//      >= T is a candidate, so the result is exact.
 //   4. Otherwise (the guess failed) the row takes the general path: value
 //      histograms over [min, max] narrow down to T, and a stable compaction
 //      pass over the whole row writes the kept indices.
+// Score loads go through L2 only (__ldcg): the score buffers are rewritten by
+// other CTAs between uses.
+#pragma once
+
 #include "dsa_device.cuh"
-#include "dsa_kernels.h"
 
 namespace dsa {
-namespace {
+namespace topk {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kWarpCap = 256;            // candidate slots per warp
-constexpr int kSample = 2048;            // 4 sampled keys per thread
-constexpr int kBins = 2048;              // general-path histogram
-constexpr int kPerRound = 4 * kThreads;  // general-path compaction stretch
-constexpr int kDigitBits = 11;           // fast-path digit: 2048 bins
+constexpr int kGT = 128;                 // threads of a group
+constexpr int kGW = kGT / 32;            // warps of a group
+constexpr int kWarpCap = 512;            // candidate slots per warp
+constexpr int kSample = 2048;            // sampled keys (16 per thread)
+constexpr int kDigitBits = 10;           // digit rounds: 1024 bins
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kGenBins = 1024;           // general-path value histogram
 constexpr int kSmall = 64;               // a bin this small is ranked directly
-constexpr int kBatch = 2;                // float4 loads in flight per lane in the candidate pass
+constexpr int kBatch = 4;                // float4 loads in flight per lane in the candidate pass
+constexpr int kPerRound = 4 * kGT;       // general-path compaction stretch
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -49,33 +52,45 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-struct Smem {
+struct alignas(16) Smem {
   union {
     struct {
-      uint32_t key[kWarps][kWarpCap];
-      uint32_t idx[kWarps][kWarpCap];
+      uint32_t key[kGW][kWarpCap];
+      uint32_t idx[kGW][kWarpCap];
     } cand;
     uint32_t samp[kSample];
     struct {
-      uint32_t hist[kBins];
-      uint32_t cand[kBins];
+      uint32_t hist[kGenBins];
+      uint32_t cand[kGenBins];
     } gen;
   } u;
   uint32_t hist[kBins];
   uint32_t small[kSmall];
-  uint32_t wmax[kWarps];
-  uint32_t nsmall;
-  uint32_t wcount[kWarps];
-  uint32_t wsum[2][kWarps];
-  uint32_t red[2 * kWarps];
+  uint32_t wcount[kGW];
+  uint32_t wmax[kGW];
+  uint32_t wsum[2][kGW];
+  uint32_t red[2 * kGW];
   uint32_t sel[4];
   uint32_t ncand;
+  uint32_t nsmall;
 };
 
-// Exclusive prefix over the block of one value per thread (thread order),
-// with one __syncthreads; callers alternate `buf`.  *total gets the sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// The group's threads: index within the group and the named barrier that
+// synchronises exactly them.
+struct Group {
+  int tid;
+  int bar_id;
+  __device__ __forceinline__ void sync() const {
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kGT) : "memory");
+  }
+  __device__ __forceinline__ int lane() const { return tid & 31; }
+  __device__ __forceinline__ int warp() const { return tid >> 5; }
+};
+
+// Exclusive prefix over the group of one value per thread (thread order),
+// with one barrier; callers alternate `buf`.  *total gets the sum.
+__device__ __forceinline__ uint32_t group_excl_scan(const Group& g, uint32_t v, uint32_t* buf, uint32_t* total) {
+  const int lane = g.lane(), warp = g.warp();
   uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -83,39 +98,39 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, u
     if (lane >= o) x += y;
   }
   if (lane == 31) buf[warp] = x;
-  __syncthreads();
-  const uint32_t wt = lane < kWarps ? buf[lane] : 0u;
-  uint32_t incl = wt;
+  g.sync();
+  uint32_t warp_base = 0, tot = 0;
 #pragma unroll
-  for (int o = 1; o < kWarps; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+  for (int w = 0; w < kGW; ++w) {
+    const uint32_t t = buf[w];
+    warp_base += w < warp ? t : 0u;
+    tot += t;
   }
-  const uint32_t warp_base = __shfl_sync(0xffffffffu, incl - wt, warp);
-  *total = __shfl_sync(0xffffffffu, incl, kWarps - 1);
+  *total = tot;
   return warp_base + x - v;
 }
 
-// With a histogram of nb (<= 2048) bins, finds the bin b holding the
-// need-th largest key: sm.sel = {b, count above b, count in b}.
-__device__ __forceinline__ void find_bin(const uint32_t* hist, Smem& sm, uint32_t nb, uint32_t need, int& parity) {
-  const int t = threadIdx.x;
-  uint32_t c[4], s = 0;
+// With a histogram of nb (<= kBins) bins, finds the bin b holding the need-th
+// largest key: sm.sel = {b, count above b, count in b}.  Ends with a barrier.
+__device__ __forceinline__ void find_bin(const Group& g, const uint32_t* hist, Smem& sm, uint32_t nb, uint32_t need,
+                                         int& parity) {
+  constexpr int kPer = kBins / kGT;  // bins per thread, in descending order
+  uint32_t c[kPer], s = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int b = static_cast<int>(nb) - 1 - 4 * t - q;  // descending bins
+  for (int q = 0; q < kPer; ++q) {
+    const int b = static_cast<int>(nb) - 1 - kPer * g.tid - q;
     c[q] = b >= 0 ? hist[b] : 0u;
     s += c[q];
   }
   uint32_t tot;
-  const uint32_t excl = block_excl_scan(s, sm.wsum[parity], &tot);
+  const uint32_t excl = group_excl_scan(g, s, sm.wsum[parity], &tot);
   parity ^= 1;
   if (excl < need && excl + s >= need) {
     uint32_t cum = excl;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kPer; ++q) {
       if (cum + c[q] >= need) {
-        sm.sel[0] = nb - 1 - 4 * t - q;
+        sm.sel[0] = nb - 1 - kPer * g.tid - q;
         sm.sel[1] = cum;
         sm.sel[2] = c[q];
         break;
@@ -123,44 +138,11 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, Smem& sm, uint32_
       cum += c[q];
     }
   }
-  __syncthreads();
+  g.sync();
 }
 
-// Exact radix select over keys in [lo, hi] held in shared memory: `get(j)`
-// returns (valid, key) for slot j < nslots.  Returns the need-th largest key
-// T; *need_out = how many keys equal to T are to be taken.
-template <typename Get>
-__device__ __forceinline__ uint32_t radix_select(Smem& sm, uint32_t lo, uint32_t hi, uint32_t need, int nslots,
-                                                 Get&& get, uint32_t* need_out, int& parity) {
-  uint32_t prefix = 0, pmask = 0;
-  const uint32_t span = hi - lo;
-  int bits = span == 0 ? 0 : 32 - __clz(span);
-  while (bits > 0) {
-    const int nb = min(8, bits);
-    const int shift = bits - nb;
-    if (threadIdx.x < 256) sm.hist[threadIdx.x] = 0u;
-    __syncthreads();
-    for (int j = threadIdx.x; j < nslots; j += kThreads) {
-      uint32_t k;
-      if (get(j, k)) {
-        const uint32_t x = k - lo;
-        if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & ((1u << nb) - 1u)], 1u);
-      }
-    }
-    __syncthreads();
-    find_bin(sm.hist, sm, 256, need, parity);
-    need -= sm.sel[1];
-    prefix |= sm.sel[0] << shift;
-    pmask |= ((1u << nb) - 1u) << shift;
-    bits -= nb;
-    __syncthreads();
-  }
-  *need_out = need;
-  return lo + prefix;
-}
-
-__device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Smem& sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ void group_minmax(const Group& g, uint32_t& lo, uint32_t& hi, Smem& sm) {
+  const int lane = g.lane(), warp = g.warp();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -168,52 +150,15 @@ __device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Smem& s
   }
   if (lane == 0) {
     sm.red[warp] = lo;
-    sm.red[kWarps + warp] = hi;
+    sm.red[kGW + warp] = hi;
   }
-  __syncthreads();
-  lo = lane < kWarps ? sm.red[lane] : 0xFFFFFFFFu;
-  hi = lane < kWarps ? sm.red[kWarps + lane] : 0u;
+  g.sync();
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  for (int w = 0; w < kGW; ++w) {
+    lo = min(lo, sm.red[w]);
+    hi = max(hi, sm.red[kGW + w]);
   }
-  lo = __shfl_sync(0xffffffffu, lo, 0);
-  hi = __shfl_sync(0xffffffffu, hi, 0);
-  __syncthreads();
-}
-
-// One row of scores: the indexer wrote it as ns partial head-sums, `stride`
-// floats apart; the score is their sum, added in slice order.
-struct RowSrc {
-  const float* p;
-  int64_t stride;
-  int ns;
-};
-
-// Loads bypass L1: the score buffer is rewritten by every chunk's indexer.
-__device__ __forceinline__ float load_score(const RowSrc& r, int j) {
-  float v = __ldcg(r.p + j);
-  for (int s = 1; s < r.ns; ++s) v = __fadd_rn(v, __ldcg(r.p + s * r.stride + j));
-  return v;
-}
-
-// keys of elements j .. j+3; elements >= n read as 0
-__device__ __forceinline__ uint4 load_keys4(const RowSrc& r, int j, int n) {
-  if (j + 3 < n) {
-    float4 f = __ldcg(reinterpret_cast<const float4*>(r.p + j));
-    for (int s = 1; s < r.ns; ++s) {
-      const float4 g = __ldcg(reinterpret_cast<const float4*>(r.p + s * r.stride + j));
-      f = make_float4(__fadd_rn(f.x, g.x), __fadd_rn(f.y, g.y), __fadd_rn(f.z, g.z), __fadd_rn(f.w, g.w));
-    }
-    return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
-  }
-  uint4 k;
-  k.x = j < n ? score_key(load_score(r, j)) : 0u;
-  k.y = j + 1 < n ? score_key(load_score(r, j + 1)) : 0u;
-  k.z = j + 2 < n ? score_key(load_score(r, j + 2)) : 0u;
-  k.w = j + 3 < n ? score_key(load_score(r, j + 3)) : 0u;
-  return k;
+  g.sync();
 }
 
 // Exact select among keys held in shared memory: get(j, k) yields the key of
@@ -223,9 +168,9 @@ __device__ __forceinline__ uint4 load_keys4(const RowSrc& r, int j, int n) {
 // once that bin has at most kSmall keys they are ranked against each other.
 // Returns T; *take_eq = how many keys equal to T are taken.
 template <typename Get>
-__device__ __forceinline__ uint32_t digit_select(Smem& sm, uint32_t lo, uint32_t hi, uint32_t need, int nslots,
-                                                 Get&& get, uint32_t* take_eq, int& parity) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ uint32_t digit_select(const Group& g, Smem& sm, uint32_t lo, uint32_t hi, uint32_t need,
+                                                 int nslots, Get&& get, uint32_t* take_eq, int& parity) {
+  const int tid = g.tid;
   while (true) {
     if (lo == hi) {
       *take_eq = need;
@@ -235,15 +180,15 @@ __device__ __forceinline__ uint32_t digit_select(Smem& sm, uint32_t lo, uint32_t
     const int bits = 32 - __clz(span);
     const int sh = bits > kDigitBits ? bits - kDigitBits : 0;
     const uint32_t nb = (span >> sh) + 1u;
-    for (uint32_t b = tid; b < nb; b += kThreads) sm.hist[b] = 0u;
+    for (uint32_t b = tid; b < nb; b += kGT) sm.hist[b] = 0u;
     if (tid == 0) sm.nsmall = 0u;
-    __syncthreads();
-    for (int j = tid; j < nslots; j += kThreads) {
+    g.sync();
+    for (int j = tid; j < nslots; j += kGT) {
       uint32_t k;
       if (get(j, k) && k >= lo && k <= hi) atomicAdd(&sm.hist[(k - lo) >> sh], 1u);
     }
-    __syncthreads();
-    find_bin(sm.hist, sm, nb, need, parity);
+    g.sync();
+    find_bin(g, sm.hist, sm, nb, need, parity);
     const uint32_t b = sm.sel[0], inbin = sm.sel[2];
     need -= sm.sel[1];
     const uint32_t nlo = lo + (b << sh);
@@ -256,11 +201,11 @@ __device__ __forceinline__ uint32_t digit_select(Smem& sm, uint32_t lo, uint32_t
     }
     if (inbin > static_cast<uint32_t>(kSmall)) continue;
     // few keys left in the bin (exactly inbin of them lie in [lo, hi])
-    for (int j = tid; j < nslots; j += kThreads) {
+    for (int j = tid; j < nslots; j += kGT) {
       uint32_t k;
       if (get(j, k) && k >= lo && k <= hi) sm.small[atomicAdd(&sm.nsmall, 1u)] = k;
     }
-    __syncthreads();
+    g.sync();
     const int ns = static_cast<int>(sm.nsmall);
     if (tid < ns) {
       const uint32_t kj = sm.small[tid];
@@ -275,16 +220,31 @@ __device__ __forceinline__ uint32_t digit_select(Smem& sm, uint32_t lo, uint32_t
         sm.sel[1] = need - gt;
       }
     }
-    __syncthreads();
+    g.sync();
     *take_eq = sm.sel[1];
     return sm.sel[0];
   }
 }
 
+// keys of elements j .. j+3; elements >= n read as 0
+__device__ __forceinline__ uint4 load_keys4(const float* srow, int j, int n) {
+  if (j + 3 < n) {
+    const float4 f = __ldcg(reinterpret_cast<const float4*>(srow + j));
+    return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  }
+  uint4 k;
+  k.x = j < n ? score_key(__ldcg(srow + j)) : 0u;
+  k.y = j + 1 < n ? score_key(__ldcg(srow + j + 1)) : 0u;
+  k.z = j + 2 < n ? score_key(__ldcg(srow + j + 2)) : 0u;
+  k.w = j + 3 < n ? score_key(__ldcg(srow + j + 3)) : 0u;
+  return k;
+}
+
 // General path: histogram narrowing over the whole row, then a stable
 // compaction pass (re-reads the scores).
-__device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int32_t* orow, int& parity) {
-  const int tid = threadIdx.x;
+__device__ __noinline__ void general(const Group& g, Smem& sm, const float* srow, int n, int topk, int32_t* orow,
+                                     int& parity) {
+  const int tid = g.tid;
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
   for (int j = 4 * tid; j < n; j += kPerRound) {
     const uint4 k = load_keys4(srow, j, n);
@@ -296,7 +256,7 @@ __device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int3
         hi = max(hi, kk[q]);
       }
   }
-  block_minmax(lo, hi, sm);
+  group_minmax(g, lo, hi, sm);
   uint32_t need = static_cast<uint32_t>(topk);
   uint32_t T = lo, take_eq = need;
   while (true) {
@@ -306,28 +266,30 @@ __device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int3
       break;
     }
     const uint64_t range = static_cast<uint64_t>(hi - lo) + 1u;
-    for (int b = tid; b < kBins; b += kThreads) sm.u.gen.hist[b] = 0u;
-    __syncthreads();
+    for (int b = tid; b < kGenBins; b += kGT) sm.u.gen.hist[b] = 0u;
+    g.sync();
     for (int j = 4 * tid; j < n; j += kPerRound) {
       const uint4 k = load_keys4(srow, j, n);
       const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (j + q < n && kk[q] >= lo && kk[q] <= hi)
-          atomicAdd(&sm.u.gen.hist[static_cast<uint32_t>((static_cast<uint64_t>(kk[q] - lo) * kBins) / range)], 1u);
+          atomicAdd(&sm.u.gen.hist[static_cast<uint32_t>((static_cast<uint64_t>(kk[q] - lo) * kGenBins) / range)],
+                    1u);
     }
-    __syncthreads();
-    find_bin(sm.u.gen.hist, sm, kBins, need, parity);
+    g.sync();
+    find_bin(g, sm.u.gen.hist, sm, kGenBins, need, parity);
     const uint32_t b = sm.sel[0], inbin = sm.sel[2];
     need -= sm.sel[1];
-    const uint32_t nlo = lo + static_cast<uint32_t>((static_cast<uint64_t>(b) * range + kBins - 1) / kBins);
-    const uint32_t nhi = lo + static_cast<uint32_t>((static_cast<uint64_t>(b + 1) * range + kBins - 1) / kBins) - 1u;
+    const uint32_t nlo = lo + static_cast<uint32_t>((static_cast<uint64_t>(b) * range + kGenBins - 1) / kGenBins);
+    const uint32_t nhi =
+        lo + static_cast<uint32_t>((static_cast<uint64_t>(b + 1) * range + kGenBins - 1) / kGenBins) - 1u;
     lo = nlo;
     hi = nhi;
-    __syncthreads();
-    if (inbin > static_cast<uint32_t>(kBins)) continue;
+    g.sync();
+    if (inbin > static_cast<uint32_t>(kGenBins)) continue;
     if (tid == 0) sm.ncand = 0;
-    __syncthreads();
+    g.sync();
     for (int j = 4 * tid; j < n; j += kPerRound) {
       const uint4 k = load_keys4(srow, j, n);
       const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
@@ -335,10 +297,10 @@ __device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int3
       for (int q = 0; q < 4; ++q)
         if (j + q < n && kk[q] >= lo && kk[q] <= hi) sm.u.gen.cand[atomicAdd(&sm.ncand, 1u)] = kk[q];
     }
-    __syncthreads();
+    g.sync();
     const int nc = static_cast<int>(sm.ncand);
-    T = radix_select(
-        sm, lo, hi, need, nc,
+    T = digit_select(
+        g, sm, lo, hi, need, nc,
         [&](int j, uint32_t& k) {
           k = sm.u.gen.cand[j];
           return true;
@@ -346,7 +308,7 @@ __device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int3
         &take_eq, parity);
     break;
   }
-  __syncthreads();
+  g.sync();
   uint32_t gt_base = 0, eq_base = 0;
   const int rounds = (n + kPerRound - 1) / kPerRound;
   for (int m = 0; m < rounds; ++m) {
@@ -363,7 +325,7 @@ __device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int3
       c_eq += eq[q];
     }
     uint32_t tot;
-    const uint32_t pre = block_excl_scan((c_gt << 16) | c_eq, sm.wsum[parity], &tot);
+    const uint32_t pre = group_excl_scan(g, (c_gt << 16) | c_eq, sm.wsum[parity], &tot);
     parity ^= 1;
     uint32_t gt_before = gt_base + (pre >> 16), eq_before = eq_base + (pre & 0xFFFFu);
 #pragma unroll
@@ -375,45 +337,37 @@ __device__ void topk_general(Smem& sm, const RowSrc& srow, int n, int topk, int3
     gt_base += tot >> 16;
     eq_base += tot & 0xFFFFu;
   }
+  g.sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restrict__ scores, int64_t ld, int nsplit,
-                                                           int64_t split_stride, int64_t row0, int topk,
-                                                           int32_t* __restrict__ out) {
-  __shared__ Smem sm;
-  // The next chunk's indexer may start its loads and MMAs now; it waits for
-  // this kernel before writing scores.  This kernel waits for the indexer
-  // that wrote the scores it reads.
-  pdl_trigger();
-  pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t i = row0 + blockIdx.x;
-  const int n = static_cast<int>(i / 4);
-  int32_t* orow = out + static_cast<int64_t>(blockIdx.x) * topk;
+// Top-k of one row: srow holds the n = floor(i/4) eligible scores of query i;
+// writes orow[0 .. topk).  All threads of the group call it together; it ends
+// with a group barrier (the shared buffers are reused by the next row).
+__device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, int n, int topk, int32_t* orow) {
+  const int tid = g.tid, lane = g.lane(), warp = g.warp();
   if (n <= topk) {
-    for (int j = tid; j < topk; j += kThreads) orow[j] = j < n ? j : -1;
+    for (int j = tid; j < topk; j += kGT) orow[j] = j < n ? j : -1;
     return;
   }
-  const RowSrc srow{scores + static_cast<int64_t>(blockIdx.x) * ld, split_stride, nsplit};
   int parity = 0;
   // each warp owns the stretch [seg0, seg1) of the row, a multiple of 4 long
-  const int seg = ((n + kWarps - 1) / kWarps + 3) & ~3;
+  const int seg = ((n + kGW - 1) / kGW + 3) & ~3;
   const int seg0 = min(n, warp * seg), seg1 = min(n, seg0 + seg);
 
   // ---- 1. threshold guess
   uint32_t t_lo = 0u;
   if (seg > kWarpCap) {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-#pragma unroll
-    for (int s = 0; s < kSample / kThreads; ++s) {
-      const int sj = tid + s * kThreads;
+#pragma unroll 4
+    for (int s = 0; s < kSample / kGT; ++s) {
+      const int sj = tid + s * kGT;
       const int j = static_cast<int>((static_cast<int64_t>(sj) * n) / kSample);
-      const uint32_t k = score_key(load_score(srow, j));
+      const uint32_t k = score_key(__ldcg(srow + j));
       sm.u.samp[sj] = k;
       lo = min(lo, k);
       hi = max(hi, k);
     }
-    block_minmax(lo, hi, sm);  // its barriers also publish the samples
+    group_minmax(g, lo, hi, sm);  // its barriers also publish the samples
     // expected keys of the row above the r-th largest sample: r * n / kSample
     const float r0 = static_cast<float>(topk) * kSample / static_cast<float>(n);
     const uint32_t r = min(static_cast<uint32_t>(kSample),
@@ -424,15 +378,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
       const int bits = 32 - __clz(span);
       const int sh = bits > kDigitBits ? bits - kDigitBits : 0;
       const uint32_t nb = (span >> sh) + 1u;
-      for (uint32_t b = tid; b < nb; b += kThreads) sm.hist[b] = 0u;
-      __syncthreads();
-#pragma unroll
-      for (int s = 0; s < kSample / kThreads; ++s) atomicAdd(&sm.hist[(sm.u.samp[tid + s * kThreads] - lo) >> sh], 1u);
-      __syncthreads();
-      find_bin(sm.hist, sm, nb, r, parity);
+      for (uint32_t b = tid; b < nb; b += kGT) sm.hist[b] = 0u;
+      g.sync();
+      for (int s = 0; s < kSample / kGT; ++s) atomicAdd(&sm.hist[(sm.u.samp[tid + s * kGT] - lo) >> sh], 1u);
+      g.sync();
+      find_bin(g, sm.hist, sm, nb, r, parity);
       t_lo = lo + (sm.sel[0] << sh);
     }
-    __syncthreads();  // the samples share storage with the candidate buffers
+    g.sync();  // the samples share storage with the candidate buffers
   }
 
   // ---- 2. one pass: per-warp candidate buffers in index order
@@ -479,25 +432,24 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
     sm.wcount[warp] = cnt;
     sm.wmax[warp] = cmax;
   }
-  __syncthreads();
+  g.sync();
   uint32_t total = 0, hi = 0;
   bool overflow = false;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < kGW; ++w) {
     total += sm.wcount[w];
     overflow |= sm.wcount[w] > static_cast<uint32_t>(kWarpCap);
     hi = max(hi, sm.wmax[w]);
   }
   if (overflow || total < static_cast<uint32_t>(topk)) {
-    __syncthreads();
-    topk_general(sm, srow, n, topk, orow, parity);
+    general(g, sm, srow, n, topk, orow, parity);
     return;
   }
 
   // ---- 3. exact select among the candidates
   uint32_t take_eq;
   const uint32_t T = digit_select(
-      sm, t_lo, hi, topk, kWarps * kWarpCap,
+      g, sm, t_lo, hi, topk, kGW * kWarpCap,
       [&](int j, uint32_t& k) {
         const int w = j / kWarpCap, p = j % kWarpCap;
         if (p >= static_cast<int>(sm.wcount[w])) return false;
@@ -521,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
   }
   // exclusive prefix over warps of the packed (gt, eq) counts
   uint32_t tot;
-  const uint32_t pre = block_excl_scan(lane == 31 ? ((c_gt << 16) | c_eq) : 0u, sm.wsum[parity], &tot);
+  const uint32_t pre = group_excl_scan(g, lane == 31 ? ((c_gt << 16) | c_eq) : 0u, sm.wsum[parity], &tot);
   parity ^= 1;
   const uint32_t wpre = __shfl_sync(0xffffffffu, pre, 31);  // exclusive prefix of this warp's totals
   uint32_t gt_before = wpre >> 16, eq_before = wpre & 0xFFFFu;
@@ -537,15 +489,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const float* __restri
     gt_before += __popc(bg);
     eq_before += __popc(be);
   }
+  g.sync();
 }
 
-}  // namespace
-
-cudaError_t launch_topk(const float* scores, int64_t ld, int nsplit, int64_t split_stride, int64_t row0, int nrows,
-                        int topk, int32_t* out, const LaunchCtx& ctx) {
-  if (nrows <= 0) return cudaSuccess;
-  return launch_ex(ctx, topk_kernel, dim3(nrows), dim3(kThreads), 0, scores, ld, nsplit, split_stride, row0, topk,
-                   out);
-}
-
+}  // namespace topk
 }  // namespace dsa

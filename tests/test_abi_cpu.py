@@ -44,13 +44,18 @@ def test_version(lib):
 
 
 def test_workspace_sizes(lib):
-    # pooled keys (256 B per pool) + one chunk of fp32 scores (pools padded to 256)
+    # 256 B of kernel words + pooled keys (256 B per pool) + a ring of up to
+    # eight chunk buffers of fp32 scores (pools padded to 256)
     S, chunk = 131072, 256
     P = S // 4
-    assert lib.dsa_index_topk_workspace(S, 32, 64, chunk, 512) == P * 256 + chunk * P * 4
+    assert lib.dsa_index_topk_workspace(S, 32, 64, chunk, 512) == 256 + P * 256 + 8 * chunk * P * 4
+    assert lib.dsa_index_topk_workspace(1024, 8, 64, 512, 64) == 256 + 256 * 256 + 2 * 512 * 256 * 4
     assert lib.dsa_index_topk_workspace(0, 32, 64, chunk, 512) == 0
-    # chunk larger than S is clamped to S rows
+    # one chunk covering the whole sequence needs one buffer of S rows
     assert lib.dsa_index_topk_workspace(1000, 8, 64, 4096, 64) == lib.dsa_index_topk_workspace(1000, 8, 64, 1000, 64)
+    assert lib.dsa_index_topk_workspace(1024, 8, 64, 1024, 64) == 256 + 256 * 256 + 1024 * 256 * 4
+    # the built-in no-alloc buffer holds the two-buffer minimum for S = 32768 with chunk 256
+    assert 256 + 8192 * 256 + 2 * 256 * 8192 * 4 <= (18 << 20) + 256
     assert lib.dsa_sparse_attn_bwd_workspace(S, 16, 128) == 2 * S * 128 * 4 + S * 16 * 4
 
 
@@ -79,6 +84,11 @@ def test_index_topk_rejects_bad_arguments(lib):
     assert _idx(lib, Hi=65) == dsa.DSA_ERR_UNSUPPORTED
     assert _idx(lib, topk=4096) == dsa.DSA_ERR_UNSUPPORTED
     assert _idx(lib, wsb=100) == dsa.DSA_ERR_WORKSPACE
+    # the two-buffer minimum passes the argument checks (and then needs a GPU); one byte less does not
+    S, chunk = 1024, 128
+    minimum = 256 + 256 * 256 + 2 * chunk * 256 * 4
+    assert _idx(lib, S=S, e=S, chunk=chunk, wsb=minimum - 1) == dsa.DSA_ERR_WORKSPACE
+    assert _idx(lib, S=S, e=S, chunk=chunk, wsb=minimum) != dsa.DSA_ERR_WORKSPACE
     assert _idx(lib, ws=None) == dsa.DSA_ERR_WORKSPACE
     assert _idx(lib, ws=FAKE + 16) == dsa.DSA_ERR_INVALID_ARG
     assert b"workspace" in lib.dsa_last_error()

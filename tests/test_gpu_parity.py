@@ -66,6 +66,23 @@ def test_index_topk_edge_shapes_int(S, Hi, topk, chunk):
     assert np.array_equal(got.cpu().numpy(), ref)
 
 
+def test_index_topk_result_does_not_depend_on_workspace_size():
+    """The workspace's chunk-buffer count only changes how many chunks are in
+    flight: the two-buffer minimum and the recommended size give the same
+    pool indices bit for bit, on float inputs too."""
+    wl = synth.WORKLOADS["s16k"]
+    q, k, w = _indexer_to_gpu(*synth.indexer_inputs(wl))
+    S = wl.S
+    full = dsa.dsa_index_topk(q, k, w, chunk=wl.chunk, topk=wl.topk)
+    P = S // 4
+    minimum = 256 + P * 256 + 2 * wl.chunk * ((P + 255) // 256 * 256) * 4
+    assert minimum < dsa.index_topk_workspace_size(S, wl.Hi, 64, wl.chunk, wl.topk)
+    ws = torch.empty(minimum, dtype=torch.uint8, device=DEV)
+    small = dsa.dsa_index_topk(q, k, w, chunk=wl.chunk, topk=wl.topk, workspace=ws)
+    dsa.dsa_sync_status()
+    assert torch.equal(small, full)
+
+
 def test_index_topk_all_ties_take_lowest_pools():
     """All scores equal (zero queries): every row keeps pools 0..topk-1."""
     S, Hi, topk = 1500, 4, 17
