@@ -295,7 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           iph ^= 1;
         }
         if (it.kind == kItemEnd) break;
-        if (it.kind != kItemTile) continue;
+        if (it.kind == kItemRows) {
+          // The rows' scores may have left L2 (the ring is larger than L2):
+          // start bringing them back while the epilogue finishes earlier work.
+          // (Their tiles may not all be stored yet; L2 keeps them coherent.)
+          const Chunk ch = chunk_of(a, it.chunk);
+          const float* buf = a.scores + static_cast<int64_t>(it.chunk % a.nbuf) * a.buf_stride;
+          for (int r = it.a; r < it.a + it.b; ++r) {
+            const int64_t n = (ch.row0 + r) / 4;
+            if (n > a.topk) bulk_prefetch_l2(buf + static_cast<int64_t>(r) * a.ld, static_cast<uint32_t>((n * 4 + 15) & ~15ll));
+          }
+          continue;
+        }
         if (!maps_ready) {
           tma_prefetch_map(&q_map);
           tma_prefetch_map(&k_map);

@@ -358,12 +358,14 @@ __device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, in
   uint32_t t_lo = 0u;
   if (seg > kWarpCap) {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-#pragma unroll 4
+    float sv[kSample / kGT];  // every sample load in flight at once
+#pragma unroll
+    for (int s = 0; s < kSample / kGT; ++s)
+      sv[s] = __ldcg(srow + static_cast<int>((static_cast<int64_t>(tid + s * kGT) * n) / kSample));
+#pragma unroll
     for (int s = 0; s < kSample / kGT; ++s) {
-      const int sj = tid + s * kGT;
-      const int j = static_cast<int>((static_cast<int64_t>(sj) * n) / kSample);
-      const uint32_t k = score_key(__ldcg(srow + j));
-      sm.u.samp[sj] = k;
+      const uint32_t k = score_key(sv[s]);
+      sm.u.samp[tid + s * kGT] = k;
       lo = min(lo, k);
       hi = max(hi, k);
     }
@@ -390,17 +392,20 @@ __device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, in
 
   // ---- 2. one pass: per-warp candidate buffers in index order
   uint32_t cnt = 0, cmax = 0;
+  // Loads are plain 16-byte loads with no branch, issued for the whole batch
+  // before any is converted; a load past the stretch is clamped to its last
+  // aligned quad (rows are allocated in whole 256-float tiles, so the quad is
+  // inside the row) and its elements are masked below.
+  const int jmax = seg1 > 0 ? ((seg1 - 1) & ~3) : 0;
   for (int base = seg0; base < seg1; base += 128 * kBatch) {
-    uint4 kv[kBatch];  // all of a batch's loads are issued before any is used
+    float4 fv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      fv[u] = __ldcg(reinterpret_cast<const float4*>(srow + min(base + 128 * u + 4 * lane, jmax)));
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int j = base + 128 * u + 4 * lane;
-      kv[u] = j < seg1 ? load_keys4(srow, j, seg1) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = base + 128 * u + 4 * lane;
-      const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+      const uint32_t kk[4] = {score_key(fv[u].x), score_key(fv[u].y), score_key(fv[u].z), score_key(fv[u].w)};
       uint32_t f = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
