@@ -145,6 +145,34 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
                                  float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                                  void* stream);
 
+/* Bytes of workspace dsa_sparse_attn_bwd_deterministic needs: fp32 dK and dV
+ * accumulators (2 x S x D x 4 B), Delta (S x Hq x 4 B), the per-pool query
+ * lists (S x topk x 4 B) and their counters (at most 128 x S bytes).  0 for
+ * an unsupported shape, or when S x topk exceeds 2^31 - 1. */
+size_t dsa_sparse_attn_bwd_deterministic_workspace(int64_t S, int Hq, int D, int topk);
+
+/*
+ * Sparse attention backward with bit-reproducible dk and dv  [SkyRL-1M
+ * §模型与瓶颈: the selected-key attention is trained end to end].  The
+ * arguments, shapes and results are those of dsa_sparse_attn_bwd, for the
+ * whole sequence (no query range); the workspace is
+ * dsa_sparse_attn_bwd_deterministic_workspace(S, Hq, D, topk) bytes,
+ * 256-byte aligned.
+ * dK/dV are summed key-major in a fixed order with no atomics: the selection
+ * is transposed into the list of selecting queries of every pool
+ * (ascending); then, span of 4096 queries by span in ascending order, one
+ * warp per pool adds the span's contributions (its own partial-pool queries
+ * first, then its selecting queries in order) into the pool's fp32 rows.
+ * The same inputs give the same dq, dk and dv bits on every run.  It reads
+ * q and dO (8 KB) per (query, pool) pair, from L2 while a span is resident,
+ * where the default gathers K/V and scatters with atomics.  Returns
+ * DSA_ERR_UNSUPPORTED when S x topk exceeds 2^31 - 1.
+ */
+dsa_status_t dsa_sparse_attn_bwd_deterministic(const void* dO, const void* q, const void* k, const void* v,
+                                               const void* o, const float* lse, const int32_t* pool_idx, int64_t S,
+                                               int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
+                                               void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * Query-range forms of the attention calls, for a rank that holds only some
  * of the sequence's queries (context parallelism [CP-lesson §改进二: the

@@ -28,7 +28,8 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_profile_enable", "dsa_profile_read", "dsa_launch_count", "dsa_launch_count_reset",
             "dsa_index_topk_noalloc", "dsa_sparse_attn_fwd_range", "dsa_sparse_attn_bwd_range",
             "dsa_zigzag_ranges", "dsa_index_topk_varlen_workspace", "dsa_index_topk_varlen",
-            "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen")
+            "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen",
+            "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic")
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +75,11 @@ def load():
                                                        vp, vp, vp, sz, vp]
             for f in (lib.dsa_index_topk_varlen, lib.dsa_sparse_attn_fwd_varlen, lib.dsa_sparse_attn_bwd_varlen):
                 f.restype = ctypes.c_int
+            lib.dsa_sparse_attn_bwd_deterministic_workspace.argtypes = [i64, i32, i32, i32]
+            lib.dsa_sparse_attn_bwd_deterministic_workspace.restype = sz
+            lib.dsa_sparse_attn_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp,
+                                                              vp, vp, vp, sz, vp]
+            lib.dsa_sparse_attn_bwd_deterministic.restype = ctypes.c_int
             lib.dsa_sync_status.argtypes = [vp]
             lib.dsa_clear_status.argtypes = []
             for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_bwd, lib.dsa_sync_status,
@@ -220,6 +226,34 @@ def dsa_sparse_attn_bwd(dO, q, k, v, o, lse, pool_idx, scale: float = 0.0, dq=No
                                          pool_idx.shape[1], float(scale), dq.data_ptr(), dk.data_ptr(),
                                          dv.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
                                          _stream_handle(stream)))
+    return dq, dk, dv
+
+
+def sparse_attn_bwd_deterministic_workspace_size(S: int, Hq: int, D: int, topk: int) -> int:
+    return int(load().dsa_sparse_attn_bwd_deterministic_workspace(S, Hq, D, topk))
+
+
+def dsa_sparse_attn_bwd_deterministic(dO, q, k, v, o, lse, pool_idx, scale: float = 0.0, dq=None, dk=None,
+                                      dv=None, workspace=None, stream=None):
+    """(dq [S, Hq, D], dk [S, D], dv [S, D]) in bf16 for the whole sequence,
+    with dk and dv summed in a fixed order (the same bits on every run)."""
+    for t, n, nd in ((dO, "dO", 3), (q, "q", 3), (o, "o", 3), (k, "k", 2), (v, "v", 2)):
+        _need(t, n, torch.bfloat16, nd)
+    _need(lse, "lse", torch.float32, 2)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    S, Hq, D = q.shape
+    topk = pool_idx.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = load()
+    need = lib.dsa_sparse_attn_bwd_deterministic_workspace(S, Hq, D, topk)
+    ws = _workspace(int(need), q.device, workspace)
+    _check(lib.dsa_sparse_attn_bwd_deterministic(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                 o.data_ptr(), lse.data_ptr(), pool_idx.data_ptr(), S, Hq, D, topk,
+                                                 float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                                 ws.data_ptr(), ws.numel() * ws.element_size(),
+                                                 _stream_handle(stream)))
     return dq, dk, dv
 
 

@@ -242,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_bf16_16816(dq_acc[2 * j + 1], dsa, b2, b3);
     }
 
+    if (dk_acc == nullptr) continue;  // dq only: the deterministic backward adds dK/dV key by key
+
     // P and dS as [16 heads][16 keys] bf16 tiles, each split into hi + lo
     // (x = hi + lo to ~2^-17): the dK/dV sums run over thousands of queries
     // for popular keys, where a single bf16 rounding of P or dS accumulates
@@ -407,15 +409,16 @@ __global__ void cast_kernel(const float* __restrict__ a, const float* __restrict
 cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx) {
   // Delta for the nq local query rows; dk_acc and dv_acc are adjacent in the
-  // workspace: zero 2 * S * D floats from dk_acc
+  // workspace: zero 2 * S * D floats from dk_acc (nothing when dk_acc is null)
   (void)dv_acc;
   const int64_t rows = nq * kHq;
   const int block = 256;
-  const int64_t threads = rows * 16 > S * kD / 8 ? rows * 16 : S * kD / 8;  // each zeroes ~4 float4
+  const int64_t nzero4 = dk_acc != nullptr ? 2 * S * kD / 4 : 0;
+  const int64_t threads = rows * 16 > nzero4 / 4 ? rows * 16 : nzero4 / 4;  // each zeroes ~4 float4
   const int64_t grid = (threads + block - 1) / block;
   bwd_pre_kernel<<<static_cast<unsigned>(grid), block, 0, ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(o), rows, delta,
-      reinterpret_cast<float4*>(dk_acc), 2 * S * kD / 4);
+      reinterpret_cast<float4*>(dk_acc), nzero4);
   return cudaGetLastError();
 }
 

@@ -140,10 +140,11 @@ struct ProfRec {
 };
 std::vector<ProfRec> g_prof;
 
-// Runs one launcher (each launches exactly one kernel), counting it and, when
-// profiling is on, bracketing it with events on the launch stream.
+// Runs one launcher, counting its kernels (one unless the caller says how
+// many it launched) and, when profiling is on, bracketing it with events on
+// the launch stream.
 template <typename F>
-cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
+cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch, int kernels = 1) {
   const bool prof = g_profiling.load(std::memory_order_relaxed) != 0;
   ProfRec rec{name, nullptr, nullptr};
   if (prof) {
@@ -152,7 +153,7 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
     cudaEventRecord(rec.start, stream);
   }
   cudaError_t e = launch();
-  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e == cudaSuccess) g_launches.fetch_add(kernels, std::memory_order_relaxed);
   if (prof) {
     cudaEventRecord(rec.stop, stream);
     std::lock_guard<std::mutex> lk(g_prof_mu);
@@ -382,6 +383,104 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
                                  void* stream) {
   return dsa_sparse_attn_bwd_range(dO, q, k, v, o, lse, pool_idx, S, 0, S, Hq, D, topk, scale, dq, dk, dv,
                                    workspace, ws_bytes, stream);
+}
+
+namespace {
+// pieces of the deterministic backward's workspace, each 256-byte aligned;
+// the two fp32 accumulators first and adjacent (the preprocess kernel zeroes
+// them as one range)
+struct DetLayout {
+  size_t dk_acc, dv_acc, delta, nsel, cnt, bsum, qlist, tickets, total;
+};
+DetLayout det_layout(int64_t S, int Hq, int topk, const dsa::DetPlan& d) {
+  DetLayout l;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round_up(bytes, 256);
+    return at;
+  };
+  l.dk_acc = take(static_cast<size_t>(S) * kD * sizeof(float));
+  l.dv_acc = take(static_cast<size_t>(S) * kD * sizeof(float));
+  l.delta = take(static_cast<size_t>(S) * Hq * sizeof(float));
+  l.nsel = take(static_cast<size_t>(S) * sizeof(int32_t));
+  l.cnt = take(static_cast<size_t>(d.cnt_n) * sizeof(uint32_t));
+  l.bsum = take(static_cast<size_t>(d.bsum_n) * sizeof(uint32_t));
+  l.qlist = take(static_cast<size_t>(S) * topk * sizeof(int32_t));
+  l.tickets = take(static_cast<size_t>(d.nspan) * sizeof(uint32_t));
+  l.total = off;
+  return l;
+}
+// list positions are 32-bit
+constexpr int64_t kDetMaxEntries = (int64_t{1} << 31) - 1;
+}  // namespace
+
+size_t dsa_sparse_attn_bwd_deterministic_workspace(int64_t S, int Hq, int D, int topk) {
+  if (S < 1 || Hq != kHq || D != kD || topk < 1 || topk > kMaxTopk) return 0;
+  if (S > kDetMaxEntries / topk) return 0;
+  const dsa::DetPlan d = dsa::det_plan(S, topk);
+  if (d.cnt_n > dsa::det_scan_max_elems()) return 0;
+  return det_layout(S, Hq, topk, d).total;
+}
+
+dsa_status_t dsa_sparse_attn_bwd_deterministic(const void* dO, const void* q, const void* k, const void* v,
+                                               const void* o, const float* lse, const int32_t* pool_idx, int64_t S,
+                                               int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
+                                               void* workspace, size_t ws_bytes, void* stream) {
+  const char* fn = "dsa_sparse_attn_bwd_deterministic";
+  if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
+    return fail(DSA_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+      !aligned4(pool_idx) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned, pool_idx and lse 4-byte aligned", fn);
+  dsa_status_t st = check_attn_args(fn, S, Hq, D, topk);
+  if (st != DSA_OK) return st;
+  const size_t need = dsa_sparse_attn_bwd_deterministic_workspace(S, Hq, D, topk);
+  if (need == 0)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: S x topk = %lld x %d is beyond its 2^31 - 1 list entries", fn,
+                static_cast<long long>(S), topk);
+  if (!workspace || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace ? ws_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  const dsa::DetPlan d = dsa::det_plan(S, topk);
+  const DetLayout l = det_layout(S, Hq, topk, d);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* delta = reinterpret_cast<float*>(ws + l.delta);
+  dsa::DetBuffers b;
+  b.nsel = reinterpret_cast<int32_t*>(ws + l.nsel);
+  b.cnt = reinterpret_cast<uint32_t*>(ws + l.cnt);
+  b.bsum = reinterpret_cast<uint32_t*>(ws + l.bsum);
+  b.qlist = reinterpret_cast<int32_t*>(ws + l.qlist);
+  b.tickets = reinterpret_cast<uint32_t*>(ws + l.tickets);
+  b.dk_acc = reinterpret_cast<float*>(ws + l.dk_acc);
+  b.dv_acc = reinterpret_cast<float*>(ws + l.dv_acc);
+  // Delta, and the accumulators zeroed (S * D floats is a multiple of 64, so they are adjacent)
+  cudaError_t e = timed_launch("attn_bwd_pre", ctx.stream, [&] {
+    return dsa::launch_attn_bwd_pre(dO, o, S, S, delta, b.dk_acc, b.dv_acc, ctx);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_deterministic: preprocess launch");
+  e = timed_launch("attn_bwd", ctx.stream, [&] {
+    return dsa::launch_attn_bwd(dO, q, k, v, lse, delta, pool_idx, 0, S, topk, scale, dq, nullptr, nullptr, ctx);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_deterministic: dq launch");
+  e = timed_launch("det_lists", ctx.stream, [&] { return dsa::launch_det_lists(pool_idx, S, topk, d, b, ctx); },
+                   dsa::det_lists_kernels(d));
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_deterministic: list launch");
+  for (int sp = 0; sp < d.nspan; ++sp) {
+    e = timed_launch("det_span", ctx.stream,
+                     [&] { return dsa::launch_det_span(dO, q, k, v, lse, delta, S, scale, d, b, sp, ctx); });
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_deterministic: span launch");
+  }
+  e = timed_launch("attn_bwd_cast", ctx.stream,
+                   [&] { return dsa::launch_cast_dkdv(b.dk_acc, b.dv_acc, S * D, dk, dv, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_deterministic: cast launch");
+  return DSA_OK;
 }
 
 dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges) {

@@ -61,11 +61,45 @@ size_t index_topk_smem_bytes();
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
                             int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx);
 
+// Delta for nq query rows, and zeroing of the two fp32 accumulators (skipped when dk_acc is null).
 cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx);
+// dq for queries [q_begin, q_end); dK/dV added into dk_acc/dv_acc unless they are null (dq only).
 cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
                             const float* delta, const int32_t* pool_idx, int64_t q_begin, int64_t q_end, int topk,
                             float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx);
+// Deterministic dK/dV (attn_bwd_det.cu): sizes of the pieces of its workspace.
+struct DetPlan {
+  int64_t P;         // pools that can be selected: floor(S/4)
+  int64_t nP;        // pools with keys: ceil(S/4)
+  int qb;            // queries per counting block
+  int nb;            // counting blocks
+  int G;             // counting blocks per span (one launch each)
+  int nspan;         // spans
+  int64_t cnt_n;     // P * nb counters
+  int64_t bsum_n;    // scan tile totals
+};
+struct DetBuffers {
+  int32_t* nsel;     // [S]
+  uint32_t* cnt;     // [cnt_n] counts, then offsets, then cell ends
+  uint32_t* bsum;    // [bsum_n]
+  int32_t* qlist;    // [S * topk]
+  uint32_t* tickets; // [nspan]
+  float* dk_acc;     // [S][128] fp32, zero before the first span
+  float* dv_acc;     // [S][128]
+};
+DetPlan det_plan(int64_t S, int topk);
+// largest array the two-level scan handles
+int64_t det_scan_max_elems();
+// 1. per-(pool, counting block) lists of selecting queries, ascending
+cudaError_t launch_det_lists(const int32_t* pool_idx, int64_t S, int topk, const DetPlan& d, const DetBuffers& w,
+                             const LaunchCtx& ctx);
+int det_lists_kernels(const DetPlan& d);  // kernels launch_det_lists launches
+// 2. span sp (spans in ascending order): every pool's dK/dV rows += the span's queries' contributions
+cudaError_t launch_det_span(const void* dO, const void* q, const void* k, const void* v, const float* lse,
+                            const float* delta, int64_t S, float scale, const DetPlan& d, const DetBuffers& w, int sp,
+                            const LaunchCtx& ctx);
+
 cudaError_t launch_cast_dkdv(const float* dk_acc, const float* dv_acc, int64_t n, void* dk, void* dv,
                              const LaunchCtx& ctx);
 

@@ -120,6 +120,31 @@ def test_attention_ranges_are_checked(lib):
     assert b(*args) == dsa.DSA_ERR_INVALID_ARG
 
 
+def test_deterministic_backward_workspace_and_checks(lib):
+    """The deterministic backward's workspace holds at least its fp32 dK/dV
+    accumulators, Delta and the per-pool query lists (S x topk int32), and at
+    most 128 S bytes more for the (pool, query block) counters (at most 128
+    blocks) and padding; shapes it cannot index with 32-bit list positions
+    give 0 and DSA_ERR_UNSUPPORTED, before any device access."""
+    import long_context_sparse_index_gb300 as dsa
+    ws = lib.dsa_sparse_attn_bwd_deterministic_workspace
+    S, topk = 131072, 512
+    need = ws(S, 16, 128, topk)
+    floor = 2 * S * 128 * 4 + S * 16 * 4 + S * topk * 4
+    assert floor <= need <= floor + 132 * S + (1 << 20)
+    assert ws(1, 16, 128, 1) > 0 and ws(5, 16, 128, 3) > 0
+    assert ws(S, 8, 128, topk) == 0 and ws(S, 16, 64, topk) == 0 and ws(S, 16, 128, 4096) == 0
+    assert ws(0, 16, 128, topk) == 0
+    assert ws((1 << 31) // 2048, 16, 128, 2048) == 0 and ws((1 << 31) // 2048 - 1, 16, 128, 2048) > 0
+    b = lib.dsa_sparse_attn_bwd_deterministic
+    args = [FAKE] * 7 + [64, 16, 128, 8, 0.0] + [FAKE] * 3
+    assert b(*args, FAKE, 16, None) == dsa.DSA_ERR_WORKSPACE
+    assert b(*args, None, 1 << 30, None) == dsa.DSA_ERR_WORKSPACE
+    assert b(*args, FAKE + 16, 1 << 30, None) == dsa.DSA_ERR_INVALID_ARG  # workspace not 256-byte aligned
+    assert b(*args[:7], 1 << 21, 16, 128, 1024, 0.0, *args[12:], FAKE, 1 << 40, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert b(None, *args[1:], FAKE, 1 << 30, None) == dsa.DSA_ERR_INVALID_ARG
+
+
 def test_varlen_checks_cu_seqlens_and_workspace(lib):
     """Packed batches: cu_seqlens must start at 0 and increase strictly; the
     workspace queries give the longest sequence's workspace; errors come back

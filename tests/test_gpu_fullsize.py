@@ -77,13 +77,14 @@ def test_s1m_cluster_index_topk_and_forward_sampled():
     assert_close(lse[torch.from_numpy(rows).to(DEV)].cpu().numpy().astype(np.float64), rl, "lse", bf16_out=False)
 
 
-def _check_fwd_bwd(wl, sel, q_rows, key_rows):
+def _check_fwd_bwd(wl, sel, q_rows, key_rows, deterministic=False):
     q, k, v = synth.attention_inputs(wl)
     dO = synth.grad_output(wl)
     qt, kt, vt, dOt = (bits_to_torch(a, DEV) for a in (q, k, v, dO))
     st = torch.from_numpy(sel).to(DEV)
     o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, st, scale=wl.scale)
-    dq, dk, dv = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st, scale=wl.scale)
+    bwd = dsa.dsa_sparse_attn_bwd_deterministic if deterministic else dsa.dsa_sparse_attn_bwd
+    dq, dk, dv = bwd(dOt, qt, kt, vt, o, lse, st, scale=wl.scale)
     dsa.dsa_sync_status()
     qi = torch.from_numpy(q_rows).to(DEV)
     ki = torch.from_numpy(key_rows).to(DEV)
@@ -108,9 +109,11 @@ def test_s128k_attention_forward_backward_sampled():
     _check_fwd_bwd(wl, sel, q_rows, key_rows)
 
 
-def test_s64k_zipf_forward_backward_popular_pool():
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_s64k_zipf_forward_backward_popular_pool(deterministic):
     """Zipf-popular pools: every query that may see them selects them, so their
-    dK/dV rows take the most reduction contention."""
+    dK/dV rows take the most reduction contention (the default's atomics) or
+    the longest query lists (the deterministic backward's segments)."""
     wl = synth.WORKLOADS["s64k_zipf"]
     hot = synth.hot_pools(wl)
     sel = synth.stand_in_selection(wl)
@@ -119,4 +122,4 @@ def test_s64k_zipf_forward_backward_popular_pool():
     assert counts >= (wl.S - 4 * p) // 2, counts
     q_rows = _sample_rows(wl.S, 24, 6, extra=(4 * p + 4, 4 * p + 5))
     key_rows = np.array([4 * p, 4 * p + 1, 4 * p + 2, 4 * p + 3, wl.S - 1], np.int64)
-    _check_fwd_bwd(wl, sel, q_rows, key_rows)
+    _check_fwd_bwd(wl, sel, q_rows, key_rows, deterministic)

@@ -83,6 +83,26 @@ def test_index_topk_result_does_not_depend_on_workspace_size():
     assert torch.equal(small, full)
 
 
+@pytest.mark.parametrize("nbuf", [2, 3, 5, 8])
+@pytest.mark.parametrize("chunk", [1, 37, 128])
+def test_index_topk_every_buffer_ring_size_bit_exact(nbuf, chunk):
+    """The fused kernel's item dependencies for every score-ring size the
+    workspace can give (2 to 8 chunk buffers; rows handed out min(2, nbuf-1)
+    chunks after their tiles): integer inputs give the oracle's pool indices
+    bit for bit."""
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    S = wl.S
+    P = S // 4
+    ld = (P + 255) // 256 * 256
+    nbytes = 256 + P * 256 + nbuf * min(chunk, S) * ld * 4
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=chunk, topk=wl.topk, workspace=ws)
+    dsa.dsa_sync_status()
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
 def test_index_topk_all_ties_take_lowest_pools():
     """All scores equal (zero queries): every row keeps pools 0..topk-1."""
     S, Hi, topk = 1500, 4, 17
@@ -224,11 +244,12 @@ def test_attn_fwd_normal_edge_shapes(S, topk):
 
 # --------------------------------------------------------------------------- attention backward
 
-def _bwd_check(q, k, v, dO, sel, q_rows=None, key_rows=None, scale=0.0):
+def _bwd_check(q, k, v, dO, sel, q_rows=None, key_rows=None, scale=0.0, deterministic=False):
     qt, kt, vt, dOt = _attn_to_gpu(q, k, v, dO)
     st = torch.from_numpy(sel).to(DEV)
     o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, st, scale=scale)
-    dq, dk, dv = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st, scale=scale)
+    bwd = dsa.dsa_sparse_attn_bwd_deterministic if deterministic else dsa.dsa_sparse_attn_bwd
+    dq, dk, dv = bwd(dOt, qt, kt, vt, o, lse, st, scale=scale)
     dsa.dsa_sync_status()
     rdq = oracle.attn_bwd_dq(dO, q, k, v, sel, scale=scale, rows=q_rows)
     rdk, rdv = oracle.attn_bwd_dkdv(dO, q, k, v, sel, scale=scale, key_rows=key_rows)
@@ -271,6 +292,57 @@ def test_attn_bwd_repeatable_within_rounding():
         assert (x.float() - y.float()).abs().max().item() <= 2 ** -6 * max(1.0, x.float().abs().max().item())
 
 
+# --------------------------------------------------------------------------- deterministic backward
+
+def test_attn_bwd_deterministic_tiny_int():
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    sel, _ = oracle.index_topk(*synth.indexer_inputs(wl), wl.topk)
+    q, k, v = synth.attention_inputs(wl)
+    _bwd_check(q, k, v, synth.grad_output(wl), sel, scale=0.02, deterministic=True)
+
+
+# S < 4 (no selectable pool), a ragged last pool, pool lists longer than one
+# 1024-query segment (S=4096, 2051 at top 256/512), and a topk that is not a
+# power of two
+@pytest.mark.parametrize("S,topk", [(1, 1), (3, 2), (6, 2), (67, 4), (4096, 256), (2051, 512), (5003, 37)])
+def test_attn_bwd_deterministic_normal_edge_shapes(S, topk):
+    wl = synth.Workload("t", S, topk=topk, seed=200 + S)
+    q, k, v = synth.attention_inputs(wl)
+    _bwd_check(q, k, v, synth.grad_output(wl), synth.stand_in_selection(wl), deterministic=True)
+
+
+def test_attn_bwd_deterministic_bit_reproducible_and_near_default():
+    """Zipf-popular pools (the longest per-pool query lists): two runs give the
+    same bits for dq, dk and dv, and they agree with the atomic default within
+    the parity tolerance."""
+    wl = synth.Workload("t", 8192, topk=256, seed=11, values="zipf")
+    q, k, v = synth.attention_inputs(wl)
+    qt, kt, vt, dOt = _attn_to_gpu(q, k, v, synth.grad_output(wl))
+    st = torch.from_numpy(synth.stand_in_selection(wl)).to(DEV)
+    o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, st)
+    a = dsa.dsa_sparse_attn_bwd_deterministic(dOt, qt, kt, vt, o, lse, st)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    b = dsa.dsa_sparse_attn_bwd_deterministic(dOt, qt, kt, vt, o, lse, st)
+    ref = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st)
+    dsa.dsa_sync_status()
+    for x, y, r, name in zip(a, b, ref, ("dq", "dk", "dv")):
+        assert torch.equal(x, y), name
+        assert_close(torch_bf16_to_f64(x), torch_bf16_to_f64(r), name)
+
+
+def test_attn_bwd_deterministic_rejects_small_workspace():
+    wl = synth.Workload("t", 256, topk=8, seed=4)
+    q, k, v = _attn_to_gpu(*synth.attention_inputs(wl))
+    st = torch.from_numpy(synth.stand_in_selection(wl)).to(DEV)
+    o, lse = dsa.dsa_sparse_attn_fwd(q, k, v, st)
+    need = dsa.sparse_attn_bwd_deterministic_workspace_size(256, 16, 128, 8)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(dsa.DsaError) as ei:
+        dsa.dsa_sparse_attn_bwd_deterministic(q, q, k, v, o, lse, st, workspace=ws)
+    assert ei.value.status == dsa.DSA_ERR_WORKSPACE
+
+
 # --------------------------------------------------------------------------- device status / bounded waits
 
 def test_bounded_wait_timeout_reports_status():
@@ -304,6 +376,15 @@ def test_malformed_selection_is_reported_not_read():
     sel[200, 0] = 10 ** 6
     dsa.dsa_clear_status()
     dsa.dsa_sparse_attn_fwd(q, k, v, torch.from_numpy(sel).to(DEV))
+    with pytest.raises(dsa.DsaError) as ei:
+        dsa.dsa_sync_status()
+    assert ei.value.status == dsa.DSA_ERR_INTERNAL
+    dsa.dsa_clear_status()
+    # the deterministic backward leaves the entry out of its lists and reports it too
+    good = torch.from_numpy(synth.stand_in_selection(wl)).to(DEV)
+    o, lse = dsa.dsa_sparse_attn_fwd(q, k, v, good)
+    dsa.dsa_sync_status()
+    dsa.dsa_sparse_attn_bwd_deterministic(q, q, k, v, o, lse, torch.from_numpy(sel).to(DEV))
     with pytest.raises(dsa.DsaError) as ei:
         dsa.dsa_sync_status()
     assert ei.value.status == dsa.DSA_ERR_INTERNAL
