@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="s128k")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward through dsa_sparse_attn_bwd_deterministic (bit-reproducible dK/dV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time for the CPU baseline sample")
     return ap.parse_args()
@@ -102,12 +104,16 @@ def algorithmic_work(wl):
         "attn_fwd": {"bytes": keys * row_kv + S * (2 * q_bytes + 4 * Hq + 4 * k)},
         # gather K,V + read q, dO, lse, Delta, idx + write dq + fp32 dK/dV reductions (2 x 512 B per key)
         "attn_bwd": {"bytes": keys * row_kv + S * (3 * q_bytes + 8 * Hq + 4 * k) + keys * 2 * D * 4},
+        # deterministic backward's span kernel: q and dO per (query, pool) pair, own partial pool included
+        "det_span": {"bytes": (int(np.minimum(np.arange(S, dtype=np.int64) // 4, k).sum()) + S) * 2 * q_bytes},
         "pairs": pairs, "keys": keys,
     }
 
 
 KERNEL_SOURCE = {"index_topk": ("index_topk.cu", "topk_row.cuh"), "attn_fwd": ("attn_fwd.cu",),
-                 "attn_bwd": ("attn_bwd.cu",)}
+                 "attn_bwd": ("attn_bwd.cu",), "det_span": ("attn_bwd_det.cu",)}
+# profile summary file stem of a timed launcher whose kernel has another name
+PROFILE_STEM = {"det_span": "det_item"}
 
 
 def profiled_traffic(kernel, S):
@@ -122,7 +128,8 @@ def profiled_traffic(kernel, S):
             sha.update(f.read())
     h = sha.hexdigest()[:16]
     src = " + ".join(srcs)
-    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_kernel_*.md"))):
+    stem = PROFILE_STEM.get(kernel, kernel)
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"{stem}_kernel_*.md"))):
         with open(path) as f:
             text = f.read()
         m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
@@ -131,6 +138,8 @@ def profiled_traffic(kernel, S):
             if m.group(1) == h:
                 return int(t.group(1)), os.path.basename(path)
             return None, f"{os.path.basename(path)} was captured on an older {src}"
+        if m:
+            return None, f"{os.path.basename(path)} gives no DRAM traffic for S={S}"
     return None, "no capture for this kernel"
 
 
@@ -310,7 +319,13 @@ def run_ours(args):
     dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
     ws_idx = torch.empty(dsa.index_topk_workspace_size(S, wl.Hi, wl.Di, wl.chunk, topk), dtype=torch.uint8,
                          device=dev)
-    ws_bwd = torch.empty(dsa.sparse_attn_bwd_workspace_size(S, wl.Hq, wl.D), dtype=torch.uint8, device=dev)
+    if args.deterministic:
+        bwd = dsa.dsa_sparse_attn_bwd_deterministic
+        ws_bwd_bytes = dsa.sparse_attn_bwd_deterministic_workspace_size(S, wl.Hq, wl.D, topk)
+    else:
+        bwd = dsa.dsa_sparse_attn_bwd
+        ws_bwd_bytes = dsa.sparse_attn_bwd_workspace_size(S, wl.Hq, wl.D)
+    ws_bwd = torch.empty(ws_bwd_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -318,8 +333,7 @@ def run_ours(args):
         dsa.dsa_index_topk(t["q_idx"], t["k_idx"], t["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
                            workspace=ws_idx)
         dsa.dsa_sparse_attn_fwd(t["q"], t["k"], t["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
-        dsa.dsa_sparse_attn_bwd(t["dO"], t["q"], t["k"], t["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk,
-                                dv=dv, workspace=ws_bwd)
+        bwd(t["dO"], t["q"], t["k"], t["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv, workspace=ws_bwd)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -369,7 +383,7 @@ def run_ours(args):
             tf = work["index_topk"]["flops"] / (ms * 1e-3) / 1e12
             entry.update({"algorithmic_tflops": tf, "frac_of_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
                           "executed_tensor_flops_factor": 2.0, "includes": "indexer tiles and top-k rows"})
-        elif name in ("attn_fwd", "attn_bwd"):
+        elif name in ("attn_fwd", "attn_bwd", "det_span"):
             gbs = work[name]["bytes"] / (ms * 1e-3) / 1e9
             entry.update({"algorithmic_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]})
         kernels[name] = entry
@@ -400,52 +414,87 @@ def run_ours(args):
                     "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
         bi = sum(t.numel() * t.element_size() for t in pin.values())
         bo = sum(t.numel() * t.element_size() for t in out_host.values())
-        e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)]
-        # Copies overlap compute the way a pipelined caller would: the indexer
-        # inputs go first on the compute stream; q, k, v, dO travel on a copy
-        # stream while the indexer runs; pool_idx, o and lse come back while the
-        # backward runs; dq, dk, dv follow the backward.
-        copy_stream = torch.cuda.Stream(device=dev)
+        # Pipelined the way a training loop with prefetch runs it, every copy
+        # inside the timed region: step s+1's indexer inputs upload while step s
+        # runs its attention (the indexer is done with their buffers); q, k, v,
+        # dO upload while the indexer runs, once the previous backward is done
+        # with them; pool_idx, o and lse come back while the backward runs; dq,
+        # dk and dv come back while the next step's indexer runs (the last
+        # step's before the end event).  Host-to-device and device-to-host
+        # copies run on their own streams.
+        h2d = torch.cuda.Stream(device=dev)
+        d2h = torch.cuda.Stream(device=dev)
         idx_in, attn_in = ("q_idx", "k_idx", "w"), ("q", "k", "v", "dO")
-        def e2e_step(s):
-            flush.zero_()
-            if s >= 0:
-                e2e_evs[s][0].record(stream)
-            for name in idx_in:
-                d[name].copy_(pin[name], non_blocking=True)
-            # host -> device bandwidth is shared: the attention inputs start once the indexer's have landed
-            copy_stream.wait_stream(stream)
-            with torch.cuda.stream(copy_stream):
-                for name in attn_in:
-                    d[name].copy_(pin[name], non_blocking=True)
-            ev_in = copy_stream.record_event()
-            dsa.dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
-                               workspace=ws_idx)
-            stream.wait_event(ev_in)
-            dsa.dsa_sparse_attn_fwd(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
-            copy_stream.wait_stream(stream)
-            with torch.cuda.stream(copy_stream):
-                for name, src in (("pool_idx", pool_idx), ("o", o), ("lse", lse)):
-                    out_host[name].copy_(src, non_blocking=True)
-            dsa.dsa_sparse_attn_bwd(d["dO"], d["q"], d["k"], d["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk,
-                                    dv=dv, workspace=ws_bwd)
-            for name, src in (("dq", dq), ("dk", dk), ("dv", dv)):
-                out_host[name].copy_(src, non_blocking=True)
-            stream.wait_stream(copy_stream)
-            if s >= 0:
-                e2e_evs[s][1].record(stream)
 
-        for _ in range(args.warmup):  # untimed, like the device loop's warm-up
-            e2e_step(-1)
+        def upload(names):
+            with torch.cuda.stream(h2d):
+                for name in names:
+                    d[name].copy_(pin[name], non_blocking=True)
+            return h2d.record_event()
+
+        def download(pairs):
+            with torch.cuda.stream(d2h):
+                for name, src in pairs:
+                    out_host[name].copy_(src, non_blocking=True)
+            return d2h.record_event()
+
+        def e2e_run(nsteps, start=None, marks=None):
+            if nsteps == 0:
+                return
+            if start is not None:
+                start.record(stream)
+            h2d.wait_stream(stream)
+            d2h.wait_stream(stream)
+            ev_idx_in = upload(idx_in)
+            ev_bwd = ev_small_out = ev_grads_out = None
+            for s in range(nsteps):
+                flush.zero_()
+                stream.wait_event(ev_idx_in)
+                if ev_small_out is not None:
+                    stream.wait_event(ev_small_out)  # pool_idx, o, lse of the previous step are on the host
+                dsa.dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
+                                   workspace=ws_idx)
+                ev_idx_done = stream.record_event()
+                if ev_bwd is not None:
+                    h2d.wait_event(ev_bwd)  # the previous backward is done with q, k, v, dO
+                    d2h.wait_event(ev_bwd)
+                    ev_grads_out = download((("dq", dq), ("dk", dk), ("dv", dv)))
+                ev_attn_in = upload(attn_in)
+                stream.wait_event(ev_attn_in)
+                dsa.dsa_sparse_attn_fwd(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
+                d2h.wait_stream(stream)
+                ev_small_out = download((("pool_idx", pool_idx), ("o", o), ("lse", lse)))
+                if s + 1 < nsteps:
+                    h2d.wait_event(ev_idx_done)
+                    ev_idx_in = upload(idx_in)
+                if ev_grads_out is not None:
+                    stream.wait_event(ev_grads_out)  # dq, dk, dv of the previous step are on the host
+                bwd(d["dO"], d["q"], d["k"], d["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv,
+                    workspace=ws_bwd)
+                ev_bwd = stream.record_event()
+                if marks is not None:
+                    marks[s].record(stream)
+            d2h.wait_event(ev_bwd)
+            download((("dq", dq), ("dk", dk), ("dv", dv)))
+            stream.wait_stream(d2h)
+            stream.wait_stream(h2d)
+
+        e2e_run(args.warmup)  # untimed, like the device loop's warm-up
         barrier()
-        for s in range(args.steps):
-            e2e_step(s)
+        e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e2e_run(args.steps, e2e_start, marks)
+        e2e_end.record(stream)
         barrier()
-        e2e_s = sum(a.elapsed_time(b) for a, b in e2e_evs) / 1e3
+        e2e_s = e2e_start.elapsed_time(e2e_end) / 1e3
         e2e_s = max_over_ranks(e2e_s, dev)
+        bounds = [e2e_start] + marks
         e2e = {"value": world * S * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "step_ms": [a.elapsed_time(b) for a, b in e2e_evs]}
+               "d2h_bytes_per_step": bo, "ms_per_step": 1e3 * e2e_s / args.steps,
+               "step_ms": [a.elapsed_time(b) for a, b in zip(bounds[:-1], bounds[1:])],
+               "last_step_tail_ms": marks[-1].elapsed_time(e2e_end),
+               "pipelining": "next step's indexer inputs upload during this step's attention; this step's dq/dk/dv "
+                             "download during the next step's indexer; all copies inside the timed region"}
 
     if rank == 0:
         cpu = None
@@ -454,7 +503,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
+                "config": dict(workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
+                               backward="deterministic" if args.deterministic else "atomic dK/dV"),
                 "parallelism": f"replicas x{world} (one independent sequence per GPU)",
                 "clocks": clocks, "gpu_launches": gpu_launches, "e2e": e2e, "roofline": roof,
                 "kernels": kernels, "cpu_baseline": cpu, "wall_s_timed_region": wall,
