@@ -147,8 +147,9 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
 
 /* Bytes of workspace dsa_sparse_attn_bwd_deterministic needs: fp32 dK and dV
  * accumulators (2 x S x D x 4 B), Delta (S x Hq x 4 B), the per-pool query
- * lists (S x topk x 4 B) and their counters (at most 128 x S bytes).  0 for
- * an unsupported shape, or when S x topk exceeds 2^31 - 1. */
+ * lists (S x topk x 4 B) and their per-(pool, 1024-query block) counters
+ * (about S^2 / 1024 bytes, at most 256 MiB).  0 for an unsupported shape, or
+ * when S x topk exceeds 2^31 - 1. */
 size_t dsa_sparse_attn_bwd_deterministic_workspace(int64_t S, int Hq, int D, int topk);
 
 /*
@@ -160,9 +161,11 @@ size_t dsa_sparse_attn_bwd_deterministic_workspace(int64_t S, int Hq, int D, int
  * 256-byte aligned.
  * dK/dV are summed key-major in a fixed order with no atomics: the selection
  * is transposed into the list of selecting queries of every pool
- * (ascending); then, span of 4096 queries by span in ascending order, one
- * warp per pool adds the span's contributions (its own partial-pool queries
- * first, then its selecting queries in order) into the pool's fp32 rows.
+ * (ascending); then, span of 4096 queries by span (more per span beyond
+ * S = 2^20) in ascending order, one CTA per pool adds the span's
+ * contributions (its own partial-pool queries first, then its selecting
+ * queries in order, split into four fixed quarters summed in order) into
+ * the pool's fp32 rows.
  * The same inputs give the same dq, dk and dv bits on every run.  It reads
  * q and dO (8 KB) per (query, pool) pair, from L2 while a span is resident,
  * where the default gathers K/V and scatters with atomics.  Returns

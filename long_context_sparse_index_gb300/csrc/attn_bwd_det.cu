@@ -415,11 +415,16 @@ cudaError_t scan_inplace(uint32_t* a, int64_t n, uint32_t* bsum, uint32_t* total
 
 }  // namespace
 
+int64_t det_scan_max_elems() { return static_cast<int64_t>(kScanThreads) * 16 * kScanTile; }
+
 DetPlan det_plan(int64_t S, int topk) {
   DetPlan d;
   d.P = S / 4;
   d.nP = (S + 3) / 4;
-  d.qb = static_cast<int>(S / 128 > 1024 ? (S + 127) / 128 : 1024);  // at most 128 counting blocks
+  // counting blocks of 1024 queries, coarser where P * blocks would outgrow
+  // the scan (finer blocks, tried at 256, only add counters)
+  d.qb = 1024;
+  while (d.P * ((S + d.qb - 1) / d.qb) > det_scan_max_elems()) d.qb *= 2;
   d.nb = static_cast<int>((S + d.qb - 1) / d.qb);
   d.G = d.qb < kSpan ? kSpan / d.qb : 1;  // spans of 4096 queries (or one counting block)
   d.nspan = (d.nb + d.G - 1) / d.G;
@@ -428,8 +433,6 @@ DetPlan det_plan(int64_t S, int topk) {
   (void)topk;
   return d;
 }
-
-int64_t det_scan_max_elems() { return static_cast<int64_t>(kScanThreads) * 16 * kScanTile; }
 
 int det_lists_kernels(const DetPlan& d) { return 1 + (d.cnt_n > 0 ? 4 : 0); }
 

@@ -122,16 +122,16 @@ def test_attention_ranges_are_checked(lib):
 
 def test_deterministic_backward_workspace_and_checks(lib):
     """The deterministic backward's workspace holds at least its fp32 dK/dV
-    accumulators, Delta and the per-pool query lists (S x topk int32), and at
-    most 128 S bytes more for the (pool, query block) counters (at most 128
-    blocks) and padding; shapes it cannot index with 32-bit list positions
-    give 0 and DSA_ERR_UNSUPPORTED, before any device access."""
+    accumulators, Delta and the per-pool query lists (S x topk int32), plus
+    the (pool, 1024-query block) counters (S/4 x S/1024 x 4 B, capped at
+    256 MiB) and a little padding; shapes it cannot index with 32-bit list
+    positions give 0 and DSA_ERR_UNSUPPORTED, before any device access."""
     import long_context_sparse_index_gb300 as dsa
     ws = lib.dsa_sparse_attn_bwd_deterministic_workspace
     S, topk = 131072, 512
     need = ws(S, 16, 128, topk)
-    floor = 2 * S * 128 * 4 + S * 16 * 4 + S * topk * 4
-    assert floor <= need <= floor + 132 * S + (1 << 20)
+    floor = 2 * S * 128 * 4 + S * 16 * 4 + S * topk * 4 + (S // 4) * (S // 1024) * 4
+    assert floor <= need <= floor + 4 * S + (1 << 20)
     assert ws(1, 16, 128, 1) > 0 and ws(5, 16, 128, 3) > 0
     assert ws(S, 8, 128, topk) == 0 and ws(S, 16, 64, topk) == 0 and ws(S, 16, 128, 4096) == 0
     assert ws(0, 16, 128, topk) == 0
