@@ -12,9 +12,9 @@
 // Work items.  A chunk's indexer work is its (128-query x 256-pool) tiles; its
 // top-k work is its query rows, four to an item.  Items are handed out in the
 // order
-//     tiles(0), tiles(1), tiles(2), rows(0), tiles(3), rows(1), tiles(4), ...
+//     tiles(0), tiles(1), tiles(2), tiles(3), rows(0), tiles(4), rows(1), ...
 // (a chunk's rows `lag` chunks after its tiles, so that its tiles are done;
-// lag = 2 here, less when there are fewer than three score buffers)
+// lag = 3 here, less when there are fewer than four score buffers)
 // from one global ticket counter to one CTA per SM (cooperative launch, so
 // every CTA is resident).  A CTA processes its items in ticket order:
 //   tile    TMA brings the 64 KB Khat hi/lo tile and, per head h, the q_idx
@@ -27,7 +27,8 @@
 //           buffer (a ring of up to eight chunk buffers);
 //   rows    the same 16 warps split into four groups of four; each group
 //           selects one row's top-k (topk_row.cuh), once every tile of its
-//           chunk has been stored.
+//           chunk has been stored.  Handing out a row item brings the scores
+//           of the row item two tickets later into L2.
 // Dependencies run only from later tickets to earlier ones -- rows wait for
 // their chunk's tiles, and a tile of chunk c waits, before it stores, for the
 // rows of chunk c-nbuf that read the same buffer -- so the lowest unfinished
@@ -52,7 +53,8 @@ constexpr int kDi = 64;            // indexer head dim
 constexpr int kAStages = 4;
 constexpr int kItems = 2;          // work-item ring between the roles (the item in work + one prefetched)
 constexpr int kRowsPerItem = 4;    // one per top-k group
-constexpr int kMaxRowLag = 2;      // a chunk's rows are handed out after the tiles of the chunk this far ahead
+constexpr int kPrefetchItems = 2;  // row items whose scores are brought into L2 ahead of their turn
+constexpr int kMaxRowLag = 3;      // a chunk's rows are handed out after the tiles of the chunk this far ahead
 constexpr uint32_t kABytes = kBM * kDi * 2;        // 16 KB: q_idx tile of one head
 constexpr uint32_t kBHalf = kBN * kDi * 2;         // 32 KB: Khat hi (or lo) tile
 constexpr uint32_t kBBytes = 2 * kBHalf;           // 64 KB, one stage
@@ -297,11 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.kind == kItemEnd) break;
         if (it.kind == kItemRows) {
           // The rows' scores may have left L2 (the ring is larger than L2):
-          // start bringing them back while the epilogue finishes earlier work.
-          // (Their tiles may not all be stored yet; L2 keeps them coherent.)
+          // bring back those of the chunk's row item kPrefetchItems tickets
+          // ahead, whichever CTA will take it (the first items of a chunk
+          // also fetch their own rows).  (Their tiles may not all be stored
+          // yet; L2 keeps them coherent.)
           const Chunk ch = chunk_of(a, it.chunk);
           const float* buf = a.scores + static_cast<int64_t>(it.chunk % a.nbuf) * a.buf_stride;
-          for (int r = it.a; r < it.a + it.b; ++r) {
+          const int ahead = kPrefetchItems * kRowsPerItem;
+          const int f0 = it.a < ahead ? it.a : it.a + ahead;
+          const int f1 = min(ch.nrows, it.a + ahead + kRowsPerItem);
+          for (int r = f0; r < f1; ++r) {
             const int64_t n = (ch.row0 + r) / 4;
             if (n > a.topk) bulk_prefetch_l2(buf + static_cast<int64_t>(r) * a.ld, static_cast<uint32_t>((n * 4 + 15) & ~15ll));
           }

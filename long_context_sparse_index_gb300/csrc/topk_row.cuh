@@ -9,14 +9,16 @@
 // then -1.
 //
 // Method (scores map to order-preserving 32-bit keys):
-//   1. Threshold guess.  A strided sample of kSample keys is histogrammed on
-//      the top kDigitBits bits of its span; the lower edge t of the bin that
-//      holds the r-th largest sample is the threshold, with r chosen so that,
-//      unless the row's large scores are packed into a few places, at least
-//      topk keys of the row are >= t while only about a thousand are (short
-//      rows skip this: every key is a candidate).
+//   1. Threshold guess.  A strided sample of kSample keys (read as 16-byte
+//      quads) is histogrammed on the top kDigitBits bits of its span; the
+//      lower edge t of the bin that holds the r-th largest sample is the
+//      threshold, with r chosen so that, unless the row's large scores are
+//      packed into a few places, at least topk keys of the row are >= t while
+//      only about a thousand are (short rows skip this: every key is a
+//      candidate).
 //   2. One pass over the row: each warp owns a contiguous stretch and appends
-//      the keys >= t, with their indices, to its own buffer in index order.
+//      the keys >= t, with their indices, to its own buffer in index order
+//      (slots from ballots; loads one batch ahead).
 //   3. With at least topk candidates and no buffer overflowing, the exact
 //      k-th largest candidate key T comes from digit rounds over the
 //      candidates; once the bin holding T has at most kSmall keys they are
@@ -38,7 +40,7 @@ namespace topk {
 constexpr int kGT = 128;                 // threads of a group
 constexpr int kGW = kGT / 32;            // warps of a group
 constexpr int kWarpCap = 512;            // candidate slots per warp
-constexpr int kSample = 2048;            // sampled keys (16 per thread)
+constexpr int kSample = 2048;            // sampled keys (4 quads per thread)
 constexpr int kDigitBits = 10;           // digit rounds: 1024 bins
 constexpr int kBins = 1 << kDigitBits;
 constexpr int kGenBins = 1024;           // general-path value histogram
@@ -50,6 +52,15 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
   if ((u & 0x7FFFFFFFu) == 0u) u = 0u;  // -0 == +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// A float t with f >= t exactly when score_key(f) >= k, for every non-NaN
+// f: the float whose key is k; -inf for k at or below the key of -inf (the
+// keys below it are NaN patterns); -0 for k = 0x7FFFFFFF, the one key no
+// score has (just below +0's).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  if (k <= 0x007FFFFFu) return -INFINITY;
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 struct alignas(16) Smem {
@@ -358,16 +369,24 @@ __device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, in
   uint32_t t_lo = 0u;
   if (seg > kWarpCap) {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    float sv[kSample / kGT];  // every sample load in flight at once
+    // kSample keys as kSample / 4 strided 16-byte quads (whole quads of the
+    // row; n > 2048 here, so they are distinct), every load in flight at once
+    constexpr int kQuads = kSample / 4, kQPer = kQuads / kGT;
+    const int64_t nq = n >> 2;
+    float4 sv[kQPer];
 #pragma unroll
-    for (int s = 0; s < kSample / kGT; ++s)
-      sv[s] = __ldcg(srow + static_cast<int>((static_cast<int64_t>(tid + s * kGT) * n) / kSample));
+    for (int s = 0; s < kQPer; ++s)
+      sv[s] = __ldcg(reinterpret_cast<const float4*>(srow) +
+                     static_cast<int>((static_cast<int64_t>(tid + s * kGT) * nq) / kQuads));
 #pragma unroll
-    for (int s = 0; s < kSample / kGT; ++s) {
-      const uint32_t k = score_key(sv[s]);
-      sm.u.samp[tid + s * kGT] = k;
-      lo = min(lo, k);
-      hi = max(hi, k);
+    for (int s = 0; s < kQPer; ++s) {
+      const uint32_t k4[4] = {score_key(sv[s].x), score_key(sv[s].y), score_key(sv[s].z), score_key(sv[s].w)};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sm.u.samp[4 * (tid + s * kGT) + q] = k4[q];
+        lo = min(lo, k4[q]);
+        hi = max(hi, k4[q]);
+      }
     }
     group_minmax(g, lo, hi, sm);  // its barriers also publish the samples
     // expected keys of the row above the r-th largest sample: r * n / kSample
@@ -392,43 +411,55 @@ __device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, in
 
   // ---- 2. one pass: per-warp candidate buffers in index order
   uint32_t cnt = 0, cmax = 0;
-  // Loads are plain 16-byte loads with no branch, issued for the whole batch
-  // before any is converted; a load past the stretch is clamped to its last
-  // aligned quad (rows are allocated in whole 256-float tiles, so the quad is
-  // inside the row) and its elements are masked below.
+  // Scores are compared as floats against the threshold's float (the key
+  // order is the float order, -0 and +0 being one key), and only candidates
+  // are turned into keys.  A candidate's slot is the warp's count so far plus
+  // the candidates of lower lanes (four ballots, one per quad element) plus
+  // its own earlier ones: no shuffle chain.
+  // Loads are plain 16-byte loads with no branch, issued a whole batch ahead
+  // of the batch being compared; a load past the stretch is clamped to its
+  // last aligned quad (rows are allocated in whole 256-float tiles, so the
+  // quad is inside the row) and its elements are masked below.
+  const float t_f = key_score(t_lo);
+  const uint32_t lt = (1u << lane) - 1u;
   const int jmax = seg1 > 0 ? ((seg1 - 1) & ~3) : 0;
+  float4 nx[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u)
+    nx[u] = __ldcg(reinterpret_cast<const float4*>(srow + min(seg0 + 128 * u + 4 * lane, jmax)));
   for (int base = seg0; base < seg1; base += 128 * kBatch) {
     float4 fv[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      fv[u] = __ldcg(reinterpret_cast<const float4*>(srow + min(base + 128 * u + 4 * lane, jmax)));
+    for (int u = 0; u < kBatch; ++u) {
+      fv[u] = nx[u];
+      nx[u] = __ldcg(reinterpret_cast<const float4*>(srow + min(base + 128 * (kBatch + u) + 4 * lane, jmax)));
+    }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int j = base + 128 * u + 4 * lane;
-      const uint32_t kk[4] = {score_key(fv[u].x), score_key(fv[u].y), score_key(fv[u].z), score_key(fv[u].w)};
-      uint32_t f = 0;
+      const float v[4] = {fv[u].x, fv[u].y, fv[u].z, fv[u].w};
+      bool hit[4];
+      uint32_t below = 0, total = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (j + q < seg1 && kk[q] >= t_lo) f |= 1u << q;
-      const uint32_t c = __popc(f);
-      uint32_t incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+      for (int q = 0; q < 4; ++q) {
+        hit[q] = j + q < seg1 && v[q] >= t_f;
+        const uint32_t b = __ballot_sync(0xffffffffu, hit[q]);
+        below += __popc(b & lt);
+        total += __popc(b);
       }
-      uint32_t pos = cnt + incl - c;
+      uint32_t pos = cnt + below;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (f & (1u << q)) {
+        if (hit[q]) {
           if (pos < kWarpCap) {
-            sm.u.cand.key[warp][pos] = kk[q];
+            const uint32_t k = score_key(v[q]);
+            sm.u.cand.key[warp][pos] = k;
             sm.u.cand.idx[warp][pos] = j + q;
-            cmax = max(cmax, kk[q]);
+            cmax = max(cmax, k);
           }
           ++pos;
         }
-      cnt += __shfl_sync(0xffffffffu, incl, 31);
+      cnt += total;
     }
   }
 #pragma unroll
