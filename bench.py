@@ -503,8 +503,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": dict(workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
-                               backward="deterministic" if args.deterministic else "atomic dK/dV"),
+                "config": workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
+                "backward": "deterministic (key-major, fixed order)" if args.deterministic else "atomic dK/dV",
                 "parallelism": f"replicas x{world} (one independent sequence per GPU)",
                 "clocks": clocks, "gpu_launches": gpu_launches, "e2e": e2e, "roofline": roof,
                 "kernels": kernels, "cpu_baseline": cpu, "wall_s_timed_region": wall,
