@@ -20,6 +20,7 @@ of the same workload (there is no other reference implementation).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import glob
 import hashlib
 import json
@@ -50,6 +51,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="backward through dsa_sparse_attn_bwd_deterministic (bit-reproducible dK/dV)")
+    ap.add_argument("--varlen", type=int, default=0, metavar="N",
+                    help="time the S tokens as N packed sequences of a seeded length mix (varlen calls)")
+    ap.add_argument("--zigzag", type=int, default=0, metavar="N",
+                    help="time the N zig-zag query shards of the sequence one after another (range calls)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time for the CPU baseline sample")
     return ap.parse_args()
@@ -514,10 +519,135 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- packed batches and shards
+
+def varlen_lengths(S, n, seed=7):
+    """A seeded mix of n sequence lengths (multiples of 256) summing to S."""
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, S // 256), size=n - 1, replace=False)) * 256
+    return np.diff(np.concatenate([[0], cuts, [S]])).astype(np.int64)
+
+
+def run_layout(args):
+    """--varlen N: the workload's S tokens as N packed sequences (cu_seqlens),
+    through the varlen calls.  --zigzag N: the N zig-zag query shards of the
+    one sequence, each through the range calls, one after another on this GPU
+    (what each of N ranks would run, before the all-gather of pool indices and
+    the reduce-scatter of dK/dV that the caller adds).  Both time the device
+    with CUDA events, inputs resident, L2 flushed between steps."""
+    import torch
+    import synth
+    import long_context_sparse_index_gb300 as dsa
+    from long_context_sparse_index_gb300 import build as libbuild
+
+    libbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    wl = synth.WORKLOADS[args.workload]
+    S, topk = wl.S, wl.topk
+    q_idx_h, k_idx_h, w_h, q_h, k_h, v_h, dO_h = host_inputs(wl)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q_idx, k_idx, q, k, v, dO = (bf16(a) for a in (q_idx_h, k_idx_h, q_h, k_h, v_h, dO_h))
+    w = torch.from_numpy(w_h).to(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    lib = dsa.load()
+    extra = {}
+    if args.varlen:
+        lens = varlen_lengths(S, args.varlen)
+        cu = [0] + np.cumsum(lens).tolist()
+        cu_c = (ctypes.c_int64 * len(cu))(*cu)
+        ws_i = torch.empty(max(256, lib.dsa_index_topk_varlen_workspace(cu_c, args.varlen, wl.Hi, wl.Di, wl.chunk, topk)),
+                           dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(max(256, lib.dsa_sparse_attn_bwd_varlen_workspace(cu_c, args.varlen, wl.Hq, wl.D)),
+                           dtype=torch.uint8, device=dev)
+        pool_idx = torch.empty((S, topk), dtype=torch.int32, device=dev)
+        o, lse = torch.empty_like(q), torch.empty((S, wl.Hq), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def parts():
+            def run():
+                dsa.dsa_index_topk_varlen(q_idx, k_idx, w, cu, chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
+                                          workspace=ws_i)
+                dsa.dsa_sparse_attn_fwd_varlen(q, k, v, pool_idx, cu, scale=wl.scale, o=o, lse=lse)
+                dsa.dsa_sparse_attn_bwd_varlen(dO, q, k, v, o, lse, pool_idx, cu, scale=wl.scale, dq=dq, dk=dk, dv=dv,
+                                               workspace=ws_b)
+            return [run]
+        workload = f"dsa_layer_fwd_bwd_varlen{args.varlen}_T{S}"
+        extra["seq_lens"] = lens.tolist()
+    else:
+        n = args.zigzag
+        ws_i = torch.empty(dsa.index_topk_workspace_size(S, wl.Hi, wl.Di, wl.chunk, topk), dtype=torch.uint8,
+                           device=dev)
+        ws_b = torch.empty(dsa.sparse_attn_bwd_workspace_size(S, wl.Hq, wl.D), dtype=torch.uint8, device=dev)
+        pool_idx = torch.empty((S, topk), dtype=torch.int32, device=dev)
+        o, lse = torch.empty_like(q), torch.empty((S, wl.Hq), dtype=torch.float32, device=dev)
+        dq = torch.empty_like(q)
+        dks = [(torch.empty_like(k), torch.empty_like(v)) for _ in range(2)]
+
+        def rank_step(r):
+            def run():
+                for j, (b, e) in enumerate(dsa.zigzag_ranges(S, n, r)):
+                    if e <= b:
+                        continue
+                    sel = pool_idx[b:e]
+                    dsa.dsa_index_topk(q_idx, k_idx, w, chunk=wl.chunk, topk=topk, q_begin=b, q_end=e, pool_idx=sel,
+                                       workspace=ws_i)
+                    dsa.dsa_sparse_attn_fwd(q[b:e], k, v, sel, scale=wl.scale, o=o[b:e], lse=lse[b:e], q_begin=b)
+                    dsa.dsa_sparse_attn_bwd(dO[b:e], q[b:e], k, v, o[b:e], lse[b:e], sel, scale=wl.scale, dq=dq[b:e],
+                                            dk=dks[j][0], dv=dks[j][1], workspace=ws_b, q_begin=b)
+            return run
+
+        def parts():
+            return [rank_step(r) for r in range(n)]
+        workload = f"dsa_layer_fwd_bwd_zigzag{n}_S{S}"
+        extra["ranges"] = [dsa.zigzag_ranges(S, n, r) for r in range(n)]
+
+    fns = parts()
+    for _ in range(args.warmup):
+        flush.zero_()
+        for f in fns:
+            f()
+    dsa.dsa_sync_status()
+    torch.cuda.synchronize()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in fns]
+           for _ in range(args.steps)]
+    dsa.launch_count_reset()
+    for st in range(args.steps):
+        flush.zero_()
+        for f, (a, b) in zip(fns, evs[st]):
+            a.record(stream)
+            f()
+            b.record(stream)
+    torch.cuda.synchronize()
+    launches = dsa.launch_count()
+    dsa.dsa_sync_status()
+    part_ms = np.array([[a.elapsed_time(b) for a, b in row] for row in evs]).mean(0)
+    total_ms = float(part_ms.sum())
+    line = {"metric": METRIC, "value": S / (total_ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
+                           workload=workload),
+            "gpu_launches": launches, "e2e": None}
+    if args.zigzag:
+        line["rank_ms"] = part_ms.tolist()
+        line["rank_balance_max_over_mean"] = float(part_ms.max() / part_ms.mean())
+        line["note"] = ("value = S / (sum of the N shards' times): the N shards run back to back on one GPU; "
+                        "N ranks would each take one rank_ms, plus the caller's collectives")
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.varlen or args.zigzag:
+        run_layout(args)
     else:
         run_ours(args)
 
