@@ -9,8 +9,11 @@
 //
 // Layout of the work: one CTA (4 warps) per query.  The key list is walked in
 // blocks of 16 pool slots (64 keys); 128 threads gather the K and V rows of a
-// block with 16-byte cp.async copies into a 3-stage ring in shared memory
+// block with 16-byte cp.async copies into a 2-stage ring in shared memory
 // (rows XOR-swizzled in 16-B chunks so ldmatrix reads are conflict-free).
+// The Q tile sits in the ring's second stage until it is read into
+// registers, so a CTA takes 74 KB and three run per SM (12 warps), which
+// hides more of the MMA and gather latency than a deeper ring at two per SM.
 // Warp w owns keys 16w..16w+15 of every block: S = Q K^T and O += P V run on
 // bf16 mma.sync (m16n8k16, M = the 16 heads), with the running max, the
 // normaliser and O in fp32 registers.  The four warps' partial softmax
@@ -27,12 +30,15 @@ constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kBlkPools = 16;
 constexpr int kBlkKeys = 4 * kBlkPools;       // 64
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;   // 16 KB (K or V of one block)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;     // 32 KB
 constexpr uint32_t kQBytes = kHq * kD * 2;           // 4 KB
 constexpr int kMaxTopk = 2048;
-constexpr size_t kSmemFixed = 128 + kQBytes + kStages * kStageBytes;
+// Q lives inside stage 1 of the ring until it is read into registers (before
+// block 1 is gathered), so a CTA needs 74 KB at topk = 512 and three fit per SM
+constexpr size_t kSmemFixed = 128 + kStages * kStageBytes;
+static_assert(kQBytes <= kStageBytes, "Q fits in a stage");
 // row table: one int32 per key of every block (topk pools + the own pool, in blocks of 16 slots)
 constexpr size_t smem_bytes(int topk) {
   return kSmemFixed + static_cast<size_t>((topk + 1 + kBlkPools - 1) / kBlkPools) * kBlkKeys * sizeof(int32_t);
@@ -71,7 +77,7 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     attn_fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t q0, int topk,
                     float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* status) {
@@ -79,9 +85,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 127u) & ~127u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base;
-  const uint32_t sKV = base + kQBytes;
-  int32_t* rows = reinterpret_cast<int32_t*>(gbase + kQBytes + kStages * kStageBytes);
+  const uint32_t sKV = base;
+  const uint32_t sQ = base + kStageBytes;  // inside stage 1: read before block 1 is gathered
+  int32_t* rows = reinterpret_cast<int32_t*>(gbase + kStages * kStageBytes);
   __shared__ int s_nsel;
   __shared__ float s_m[kWarps][kHq], s_l[kWarps][kHq];
 
@@ -158,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int c = 2 * kk + (mat >> 1);
         ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
+      __syncthreads();  // every warp has Q: block 1 may overwrite it
     }
     {
       const int nb = b + kStages - 1;
@@ -277,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // partial O (already normalised) into shared memory, one [16][132] fp32 slab
   // per warp (padded rows spread the fragment stores over the banks)
   constexpr int kRedLd = kD + 4;
-  float* red = reinterpret_cast<float*>(gbase + kQBytes);  // reuses the gather ring
+  float* red = reinterpret_cast<float*>(gbase);  // reuses the gather ring
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = 8 * j + 2 * t4;
