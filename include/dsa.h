@@ -149,7 +149,7 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
  * accumulators (2 x S x D x 4 B), Delta (S x Hq x 4 B), the per-pool query
  * lists (S x topk x 4 B) and their per-(pool, 1024-query block) counters
  * (about S^2 / 1024 bytes, at most 256 MiB).  0 for an unsupported shape, or
- * when S x topk exceeds 2^31 - 1. */
+ * when S x topk exceeds 2^31 - 1 or S / 4 exceeds 2^26. */
 size_t dsa_sparse_attn_bwd_deterministic_workspace(int64_t S, int Hq, int D, int topk);
 
 /*
@@ -169,7 +169,7 @@ size_t dsa_sparse_attn_bwd_deterministic_workspace(int64_t S, int Hq, int D, int
  * The same inputs give the same dq, dk and dv bits on every run.  It reads
  * q and dO (8 KB) per (query, pool) pair, from L2 while a span is resident,
  * where the default gathers K/V and scatters with atomics.  Returns
- * DSA_ERR_UNSUPPORTED when S x topk exceeds 2^31 - 1.
+ * DSA_ERR_UNSUPPORTED when S x topk exceeds 2^31 - 1 or S / 4 exceeds 2^26.
  */
 dsa_status_t dsa_sparse_attn_bwd_deterministic(const void* dO, const void* q, const void* k, const void* v,
                                                const void* o, const float* lse, const int32_t* pool_idx, int64_t S,

@@ -422,9 +422,11 @@ DetPlan det_plan(int64_t S, int topk) {
   d.P = S / 4;
   d.nP = (S + 3) / 4;
   // counting blocks of 1024 queries, coarser where P * blocks would outgrow
-  // the scan (finer blocks, tried at 256, only add counters)
-  d.qb = 1024;
-  while (d.P * ((S + d.qb - 1) / d.qb) > det_scan_max_elems()) d.qb *= 2;
+  // the scan (finer blocks, tried at 256, only add counters); one block at
+  // most (then P itself may exceed the scan: the caller rejects that shape)
+  int64_t qb = 1024;
+  while (qb < S && d.P * ((S + qb - 1) / qb) > det_scan_max_elems()) qb *= 2;
+  d.qb = static_cast<int>(qb < S ? qb : (S > 0 ? S : 1));
   d.nb = static_cast<int>((S + d.qb - 1) / d.qb);
   d.G = d.qb < kSpan ? kSpan / d.qb : 1;  // spans of 4096 queries (or one counting block)
   d.nspan = (d.nb + d.G - 1) / d.G;

@@ -437,8 +437,9 @@ dsa_status_t dsa_sparse_attn_bwd_deterministic(const void* dO, const void* q, co
   if (st != DSA_OK) return st;
   const size_t need = dsa_sparse_attn_bwd_deterministic_workspace(S, Hq, D, topk);
   if (need == 0)
-    return fail(DSA_ERR_UNSUPPORTED, "%s: S x topk = %lld x %d is beyond its 2^31 - 1 list entries", fn,
-                static_cast<long long>(S), topk);
+    return fail(DSA_ERR_UNSUPPORTED,
+                "%s: S = %lld with topk = %d is beyond its limits (S x topk < 2^31 list entries, S / 4 <= 2^26 "
+                "pools)", fn, static_cast<long long>(S), topk);
   if (!workspace || ws_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? ws_bytes : (size_t)0);

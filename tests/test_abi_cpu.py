@@ -136,6 +136,8 @@ def test_deterministic_backward_workspace_and_checks(lib):
     assert ws(S, 8, 128, topk) == 0 and ws(S, 16, 64, topk) == 0 and ws(S, 16, 128, 4096) == 0
     assert ws(0, 16, 128, topk) == 0
     assert ws((1 << 31) // 2048, 16, 128, 2048) == 0 and ws((1 << 31) // 2048 - 1, 16, 128, 2048) > 0
+    # more pools than the counter scan holds, even in one counting block (topk = 1 keeps S x topk legal)
+    assert ws(4 * (1 << 26) + 4, 16, 128, 1) == 0 and ws(4 * (1 << 26), 16, 128, 1) > 0
     b = lib.dsa_sparse_attn_bwd_deterministic
     args = [FAKE] * 7 + [64, 16, 128, 8, 0.0] + [FAKE] * 3
     assert b(*args, FAKE, 16, None) == dsa.DSA_ERR_WORKSPACE
