@@ -426,15 +426,9 @@ cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const 
                             const float* delta, const int32_t* pool_idx, int64_t q_begin, int64_t q_end, int topk,
                             float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx) {
   if (q_end <= q_begin) return cudaSuccess;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes(kMaxTopk)));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = 1;
-  }
+  static std::atomic<bool> attr_done[kAttrDevices];
+  const cudaError_t e = set_smem_limit_once(attn_bwd_kernel, static_cast<int>(smem_bytes(kMaxTopk)), attr_done);
+  if (e != cudaSuccess) return e;
   attn_bwd_kernel<<<static_cast<unsigned>(q_end - q_begin), kThreads, smem_bytes(topk), ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(q),
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), lse, delta, pool_idx, q_begin, topk,

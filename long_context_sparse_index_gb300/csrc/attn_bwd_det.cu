@@ -480,15 +480,9 @@ cudaError_t launch_det_span(const void* dO, const void* q, const void* k, const 
   a.dk_acc = w.dk_acc;
   a.dv_acc = w.dv_acc;
   a.tickets = w.tickets;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> attr_done[kAttrDevices];
+  const cudaError_t e = set_smem_limit_once(det_item_kernel, static_cast<int>(kItemSmem), attr_done);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(det_item_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kItemSmem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
-  }
   det_item_kernel<<<static_cast<unsigned>(ctx.num_sms * 3), 32 * kSegWarps, kItemSmem, ctx.stream>>>(a, sp);
   return cudaGetLastError();
 }

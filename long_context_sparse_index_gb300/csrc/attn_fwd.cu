@@ -316,15 +316,9 @@ __global__ void __launch_bounds__(kThreads, 3)
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
                             int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx) {
   if (q_end <= q_begin) return cudaSuccess;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes(kMaxTopk)));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = 1;
-  }
+  static std::atomic<bool> attr_done[kAttrDevices];
+  const cudaError_t e = set_smem_limit_once(attn_fwd_kernel, static_cast<int>(smem_bytes(kMaxTopk)), attr_done);
+  if (e != cudaSuccess) return e;
   attn_fwd_kernel<<<static_cast<unsigned>(q_end - q_begin), kThreads, smem_bytes(topk), ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), pool_idx, q_begin, topk, scale * kLog2e, static_cast<__nv_bfloat16*>(o), lse,

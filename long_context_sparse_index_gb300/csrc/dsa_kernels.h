@@ -3,10 +3,28 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 #include <utility>
 
 namespace dsa {
+
+// Raises `kernel`'s dynamic shared memory limit to `bytes` on the current
+// device, once per device and call site: `done` holds one flag per device
+// ordinal (atomic, so host threads racing here at worst repeat the
+// idempotent call; ordinals past the array are set on every call).
+constexpr int kAttrDevices = 64;
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<bool> (&done)[kAttrDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kAttrDevices;
+  if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 struct LaunchCtx {
   cudaStream_t stream;

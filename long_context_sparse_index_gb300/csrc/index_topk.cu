@@ -662,14 +662,10 @@ cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_
   a.status = ctx.status;
   a.limit_ns = ctx.wait_limit_ns;
   a.inject = ctx.inject_timeout;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(index_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+  static std::atomic<bool> attr_done[kAttrDevices];
+  {
+    const cudaError_t e = set_smem_limit_once(index_topk_kernel, static_cast<int>(kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctx.num_sms);  // one CTA per SM, all resident: the items' waits need it
