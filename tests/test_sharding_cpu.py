@@ -164,3 +164,16 @@ def _max_worker(rank, world, port):
 def test_two_gloo_ranks_benchmark_takes_the_slowest_rank():
     """bench.py times N ranks as the slowest rank's time (max over ranks)."""
     torch.multiprocessing.spawn(_max_worker, args=(2, _free_port()), nprocs=2, join=True)
+
+
+@pytest.mark.parametrize("n", [1, 2, 8, 64])
+def test_benchmark_varlen_mix_partitions_the_tokens(n):
+    """bench.py --varlen N packs the workload's S tokens as N sequences of a
+    seeded length mix: positive multiples of 256 that sum to S, the same mix
+    on every run."""
+    import bench
+    S = 131072
+    lens = bench.varlen_lengths(S, n)
+    assert len(lens) == n and int(lens.sum()) == S
+    assert (lens > 0).all() and (lens % 256 == 0).all()
+    assert (bench.varlen_lengths(S, n) == lens).all()
