@@ -119,6 +119,9 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the kernels run on the current device "
+                         f"cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
     if t.dim() != ndim or not t.is_contiguous():
@@ -134,9 +137,46 @@ def sparse_attn_bwd_workspace_size(S: int, Hq: int, D: int) -> int:
 
 
 def _workspace(nbytes: int, device, given):
+    """A caller's workspace must be a contiguous CUDA tensor on the current
+    device (the library checks its size); None allocates one."""
     if given is not None:
+        _need(given, "workspace", given.dtype, given.dim())
         return given
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _shape(t: torch.Tensor, name: str, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
+
+
+def _attn_shapes(q, k, v, pool_idx, o=None, lse=None, dO=None):
+    """q, o, dO [nq, Hq, D]; lse [nq, Hq]; pool_idx [nq, topk]; k, v [S, D]:
+    the kernels index every one of them by these extents."""
+    nq, Hq, D = q.shape
+    S = k.shape[0]
+    _shape(k, "k", (S, D))
+    _shape(v, "v", (S, D))
+    if pool_idx.shape[0] != nq:
+        raise ValueError(f"pool_idx must have {nq} rows (got {pool_idx.shape[0]})")
+    for t, name in ((o, "o"), (dO, "dO")):
+        if t is not None:
+            _shape(t, name, (nq, Hq, D))
+    if lse is not None:
+        _shape(lse, "lse", (nq, Hq))
+    return nq, Hq, D, S
+
+
+def _out(given, name: str, shape, dtype, device):
+    """A caller-supplied output must be a contiguous CUDA tensor of the given
+    dtype and shape on the current device (the kernels write through its
+    pointer); None allocates one."""
+    if given is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    _need(given, name, dtype, len(shape))
+    if tuple(given.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(given.shape)})")
+    return given
 
 
 def dsa_index_topk(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int = 0, q_end: int | None = None,
@@ -149,9 +189,7 @@ def dsa_index_topk(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int = 0, q_e
     if k_idx.shape != (S, Di) or w.shape != (S, Hi):
         raise ValueError("k_idx must be [S, Di] and w [S, Hi]")
     q_end = S if q_end is None else q_end
-    if pool_idx is None:
-        pool_idx = torch.empty((max(q_end - q_begin, 0), topk), dtype=torch.int32, device=q_idx.device)
-    _need(pool_idx, "pool_idx", torch.int32, 2)
+    pool_idx = _out(pool_idx, "pool_idx", (max(q_end - q_begin, 0), topk), torch.int32, q_idx.device)
     lib = load()
     ws = _workspace(lib.dsa_index_topk_workspace(S, Hi, Di, chunk, topk), q_idx.device, workspace)
     _check(lib.dsa_index_topk(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), S, Hi, Di, chunk, topk, q_begin,
@@ -173,9 +211,7 @@ def dsa_index_topk_noalloc(q_idx, k_idx, w, chunk: int, topk: int, q_begin: int 
     if k_idx.shape != (S, Di) or w.shape != (S, Hi):
         raise ValueError("k_idx must be [S, Di] and w [S, Hi]")
     q_end = S if q_end is None else q_end
-    if pool_idx is None:
-        pool_idx = torch.empty((max(q_end - q_begin, 0), topk), dtype=torch.int32, device=q_idx.device)
-    _need(pool_idx, "pool_idx", torch.int32, 2)
+    pool_idx = _out(pool_idx, "pool_idx", (max(q_end - q_begin, 0), topk), torch.int32, q_idx.device)
     _check(load().dsa_index_topk_noalloc(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), S, Hi, Di, chunk, topk,
                                          q_begin, q_end, pool_idx.data_ptr(), _stream_handle(stream)))
     return pool_idx
@@ -191,12 +227,9 @@ def dsa_sparse_attn_fwd(q, k, v, pool_idx, scale: float = 0.0, o=None, lse=None,
     _need(k, "k", torch.bfloat16, 2)
     _need(v, "v", torch.bfloat16, 2)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    nq, Hq, D = q.shape
-    S = k.shape[0]
-    if k.shape != (S, D) or v.shape != (S, D) or pool_idx.shape[0] != nq:
-        raise ValueError("k, v must be [S, D] and pool_idx [nq, topk]")
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((nq, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    nq, Hq, D, S = _attn_shapes(q, k, v, pool_idx)
+    o = _out(o, "o", q.shape, torch.bfloat16, q.device)
+    lse = _out(lse, "lse", (nq, Hq), torch.float32, q.device)
     _check(load().dsa_sparse_attn_fwd_range(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S,
                                             q_begin, q_begin + nq, Hq, D, pool_idx.shape[1], float(scale),
                                             o.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
@@ -214,11 +247,10 @@ def dsa_sparse_attn_bwd(dO, q, k, v, o, lse, pool_idx, scale: float = 0.0, dq=No
         _need(t, n, torch.bfloat16, nd)
     _need(lse, "lse", torch.float32, 2)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    nq, Hq, D = q.shape
-    S = k.shape[0]
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    nq, Hq, D, S = _attn_shapes(q, k, v, pool_idx, o=o, lse=lse, dO=dO)
+    dq = _out(dq, "dq", q.shape, torch.bfloat16, q.device)
+    dk = _out(dk, "dk", k.shape, torch.bfloat16, q.device)
+    dv = _out(dv, "dv", v.shape, torch.bfloat16, q.device)
     lib = load()
     ws = _workspace(lib.dsa_sparse_attn_bwd_workspace(S, Hq, D), q.device, workspace)
     _check(lib.dsa_sparse_attn_bwd_range(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
@@ -241,11 +273,13 @@ def dsa_sparse_attn_bwd_deterministic(dO, q, k, v, o, lse, pool_idx, scale: floa
         _need(t, n, torch.bfloat16, nd)
     _need(lse, "lse", torch.float32, 2)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    S, Hq, D = q.shape
+    S, Hq, D, _ = _attn_shapes(q, k, v, pool_idx, o=o, lse=lse, dO=dO)
+    if k.shape[0] != S:
+        raise ValueError("the deterministic backward takes the whole sequence: q and k need the same rows")
     topk = pool_idx.shape[1]
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = _out(dq, "dq", q.shape, torch.bfloat16, q.device)
+    dk = _out(dk, "dk", k.shape, torch.bfloat16, q.device)
+    dv = _out(dv, "dv", v.shape, torch.bfloat16, q.device)
     lib = load()
     need = lib.dsa_sparse_attn_bwd_deterministic_workspace(S, Hq, D, topk)
     ws = _workspace(int(need), q.device, workspace)
@@ -270,12 +304,12 @@ def dsa_index_topk_varlen(q_idx, k_idx, w, cu_seqlens, chunk: int, topk: int, po
     _need(k_idx, "k_idx", torch.bfloat16, 2)
     _need(w, "w", torch.float32, 2)
     T, Hi, Di = q_idx.shape
+    _shape(k_idx, "k_idx", (T, Di))
+    _shape(w, "w", (T, Hi))
     cu, nseq = _cu(cu_seqlens)
     if nseq < 1 or cu[nseq] != T:
         raise ValueError("cu_seqlens must end at the packed length")
-    if pool_idx is None:
-        pool_idx = torch.empty((T, topk), dtype=torch.int32, device=q_idx.device)
-    _need(pool_idx, "pool_idx", torch.int32, 2)
+    pool_idx = _out(pool_idx, "pool_idx", (T, topk), torch.int32, q_idx.device)
     lib = load()
     ws = _workspace(lib.dsa_index_topk_varlen_workspace(cu, nseq, Hi, Di, chunk, topk), q_idx.device, workspace)
     _check(lib.dsa_index_topk_varlen(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), cu, nseq, Hi, Di, chunk, topk,
@@ -289,10 +323,11 @@ def dsa_sparse_attn_fwd_varlen(q, k, v, pool_idx, cu_seqlens, scale: float = 0.0
     for t, n, nd in ((q, "q", 3), (k, "k", 2), (v, "v", 2)):
         _need(t, n, torch.bfloat16, nd)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    T, Hq, D = q.shape
+    T, Hq, D, _ = _attn_shapes(q, k, v, pool_idx)
+    _shape(k, "k", (T, D))
     cu, nseq = _cu(cu_seqlens)
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    o = _out(o, "o", q.shape, torch.bfloat16, q.device)
+    lse = _out(lse, "lse", (T, Hq), torch.float32, q.device)
     _check(load().dsa_sparse_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), cu, nseq,
                                              Hq, D, pool_idx.shape[1], float(scale), o.data_ptr(), lse.data_ptr(),
                                              _stream_handle(stream)))
@@ -306,11 +341,12 @@ def dsa_sparse_attn_bwd_varlen(dO, q, k, v, o, lse, pool_idx, cu_seqlens, scale:
         _need(t, n, torch.bfloat16, nd)
     _need(lse, "lse", torch.float32, 2)
     _need(pool_idx, "pool_idx", torch.int32, 2)
-    T, Hq, D = q.shape
+    T, Hq, D, _ = _attn_shapes(q, k, v, pool_idx, o=o, lse=lse, dO=dO)
+    _shape(k, "k", (T, D))
     cu, nseq = _cu(cu_seqlens)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = _out(dq, "dq", q.shape, torch.bfloat16, q.device)
+    dk = _out(dk, "dk", k.shape, torch.bfloat16, q.device)
+    dv = _out(dv, "dv", v.shape, torch.bfloat16, q.device)
     lib = load()
     ws = _workspace(lib.dsa_sparse_attn_bwd_varlen_workspace(cu, nseq, Hq, D), q.device, workspace)
     _check(lib.dsa_sparse_attn_bwd_varlen(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),

@@ -389,3 +389,27 @@ def test_malformed_selection_is_reported_not_read():
         dsa.dsa_sync_status()
     assert ei.value.status == dsa.DSA_ERR_INTERNAL
     dsa.dsa_clear_status()
+
+
+def test_binding_refuses_bad_outputs_and_shapes():
+    """Caller-supplied outputs and workspaces must be contiguous CUDA tensors
+    of the right dtype and shape, and the inputs' extents must agree: a host
+    pointer or a short buffer never reaches a kernel."""
+    wl = synth.Workload("t", 64, topk=8, seed=5)
+    q, k, v = _attn_to_gpu(*synth.attention_inputs(wl))
+    st = torch.from_numpy(synth.stand_in_selection(wl)).to(DEV)
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_attn_fwd(q, k, v, st, o=torch.empty(q.shape, dtype=torch.bfloat16))  # host tensor
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_attn_fwd(q, k, v, st, lse=torch.empty((63, 16), dtype=torch.float32, device=DEV))
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_attn_fwd(q, k, v, st[:32])
+    o, lse = dsa.dsa_sparse_attn_fwd(q, k, v, st)
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_attn_bwd(q, q, k, v, o, lse[:32], st)
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_attn_bwd(q, q, k, v, o, lse, st, workspace=torch.empty(1 << 20, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_attn_bwd_deterministic(q, q, k, v, o, lse, st, dk=torch.empty((64, 64), dtype=torch.bfloat16,
+                                                                                       device=DEV))
+    dsa.dsa_sync_status()
