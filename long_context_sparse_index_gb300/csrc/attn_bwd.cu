@@ -10,8 +10,9 @@
 // The forward's lse lets P be recomputed instead of stored.
 //
 // One CTA (4 warps) per query gathers K and V blocks exactly as the forward
-// does.  Per warp and 16-key slice: S and dP on mma.sync, dQ accumulated in
-// registers, and the slice's dK/dV rows (16 keys x 128 dims, already summed
+// does.  Per warp and 16-key slice: S and dP on mma.sync (the Q and dO
+// A fragments are read from shared memory once per query and stay in
+// registers), dQ accumulated in registers, and the slice's dK/dV rows (16 keys x 128 dims, already summed
 // over the 16 heads by the MMA) added into fp32 accumulators with 16-byte
 // reductions.  The reductions are L2-bound, and L2 serves them best when one
 // warp instruction covers whole 128-byte lines: so each 32-dim block of the
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float dq_acc[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j) dq_acc[j][0] = dq_acc[j][1] = dq_acc[j][2] = dq_acc[j][3] = 0.f;
-  uint32_t qa[8][4];
+  uint32_t qa[8][4], dga[8][4];  // Q and dO A fragments, read once per query
   const uint32_t sTw = sT + warp * 4 * kTBytes;
   uint8_t* gT = gbase + (sTw - base);
 
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int r = (lane & 7) + ((mat & 1) << 3);
         const int c = 2 * kk + (mat >> 1);
         ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        ldsm_x4(sdO + swz(r, c), dga[kk][0], dga[kk][1], dga[kk][2], dga[kk][3]);
       }
     }
     {
@@ -193,15 +195,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       ldsm_x4(sK + swz(r, c), b0, b1, b2, b3);
       mma_bf16_16816(s0, qa[kk], b0, b1);
       mma_bf16_16816(s1, qa[kk], b2, b3);
-      uint32_t da[4];
-      {
-        const int ra = (lane & 7) + ((mat & 1) << 3);
-        const int ca = 2 * kk + (mat >> 1);
-        ldsm_x4(sdO + swz(ra, ca), da[0], da[1], da[2], da[3]);
-      }
       ldsm_x4(sV + swz(r, c), b0, b1, b2, b3);
-      mma_bf16_16816(p0, da, b0, b1);
-      mma_bf16_16816(p1, da, b2, b3);
+      mma_bf16_16816(p0, dga[kk], b0, b1);
+      mma_bf16_16816(p1, dga[kk], b2, b3);
     }
 
     // key validity and global rows of this thread's columns (2t, 2t+1, 8+2t, 9+2t)
