@@ -177,3 +177,17 @@ def test_benchmark_varlen_mix_partitions_the_tokens(n):
     assert len(lens) == n and int(lens.sum()) == S
     assert (lens > 0).all() and (lens % 256 == 0).all()
     assert (bench.varlen_lengths(S, n) == lens).all()
+
+
+@pytest.mark.parametrize("S,topk", [(1, 1), (7, 2), (1030, 64), (4099, 512)])
+def test_benchmark_work_counts_match_brute_force(S, topk):
+    """The roofline's units: query i scores floor(i/4) pools and attends to
+    4 * min(topk, floor(i/4)) selected keys plus its own i mod 4 + 1."""
+    import bench
+    import synth
+    wl = synth.Workload("t", S, topk=topk, seed=1)
+    pairs, keys = bench.workload_counts(wl)
+    assert pairs == sum(i // 4 for i in range(S))
+    assert keys == sum(4 * min(topk, i // 4) + (i - 4 * (i // 4)) + 1 for i in range(S))
+    w = bench.algorithmic_work(wl)
+    assert w["index_topk"]["flops"] == 2 * wl.Hi * wl.Di * pairs
