@@ -42,6 +42,16 @@ METRIC = "DSA layer fwd+bwd tokens/s at S=128k; indexer TFLOP/s & attn GB/s vs p
 UNIT = "tokens/s"
 
 
+def metric_for(wl):
+    """The headline metric for the fwd+bwd workloads; the forward-only workloads
+    (planted-cluster keys at S = 262144 and 1048576, S = 16384) report the
+    forward pass: indexer + top-k + sparse attention forward."""
+    if wl.backward:
+        return METRIC
+    return (f"DSA layer fwd tokens/s at S={wl.S} (indexer+top-k+sparse attn fwd); "
+            "indexer TFLOP/s & attn GB/s vs peak")
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -222,7 +232,8 @@ def oracle_sample_step(wl, host, rows):
     full = np.full((wl.S, wl.topk), -1, np.int32)
     full[rows] = sel
     oracle.attn_fwd(q, k, v, full, scale=wl.scale, rows=rows)
-    oracle.attn_bwd_rows(dO, q, k, v, full, scale=wl.scale, rows=rows)
+    if wl.backward:
+        oracle.attn_bwd_rows(dO, q, k, v, full, scale=wl.scale, rows=rows)
 
 
 def cpu_baseline(wl, host, seconds, seed=12345):
@@ -239,7 +250,8 @@ def cpu_baseline(wl, host, seconds, seed=12345):
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} query rows drawn uniformly from the S={wl.S} sequence (seed {seed}); each row: indexer "
-                      f"scores over its floor(i/4) pools + top-{wl.topk} by full sort, forward and backward over its "
+                      f"scores over its floor(i/4) pools + top-{wl.topk} by full sort, "
+                      f"{'forward and backward' if wl.backward else 'forward'} over its "
                       f"key set; tokens/s = rows / oracle seconds ({dt:.1f} s)"}
 
 
@@ -247,15 +259,18 @@ def host_inputs(wl):
     import synth
     q_idx, k_idx, w = synth.indexer_inputs(wl)
     q, k, v = synth.attention_inputs(wl)
-    dO = synth.grad_output(wl)
+    dO = synth.grad_output(wl) if wl.backward else None
     return q_idx, k_idx, w, q, k, v, dO
 
 
 def workload_config(wl, l2_note):
-    return {"workload": f"dsa_layer_fwd_bwd_S{wl.S}", "S": wl.S, "batch": 1, "indexer_heads": wl.Hi,
+    name = f"dsa_layer_fwd_bwd_S{wl.S}" if wl.backward else f"dsa_layer_fwd_S{wl.S}_{wl.values}"
+    return {"workload": name, "S": wl.S, "batch": 1, "indexer_heads": wl.Hi,
             "indexer_dim": wl.Di, "pool_size": 4, "topk_pools": wl.topk, "query_chunk": wl.chunk,
             "q_heads": wl.Hq, "kv_heads": 1, "head_dim": wl.D, "max_keys_per_query": 4 * wl.topk + 4,
-            "inputs": "seeded bf16 N(0,1); indexer queries x %g; head weights U(0,1) fp32" % wl.q_idx_scale,
+            "inputs": ("seeded bf16 N(0,1); indexer queries x %g; head weights U(0,1) fp32" % wl.q_idx_scale) +
+                      ("; indexer keys with 8 planted clusters (1/16 of pools)" if wl.values == "cluster" else "") +
+                      ("; Zipf-ranked pool magnitudes" if wl.values == "zipf" else ""),
             "l2": l2_note}
 
 
@@ -279,8 +294,9 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     value = rows_per_step * args.steps / dt
     sample = (f"{rows_per_step} query rows per step drawn uniformly from the S={wl.S} sequence; each row: indexer + "
-              f"top-{wl.topk}, forward and backward over its key set; tokens/s = rows / oracle seconds")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+              f"top-{wl.topk}, {'forward and backward' if wl.backward else 'forward'} over its key set; "
+              f"tokens/s = rows / oracle seconds")
+    line = {"impl": "reference", "metric": metric_for(wl), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(wl, "n/a (CPU)"),
@@ -291,6 +307,18 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- our arm
+
+def measure_l2_peaks(dsa, torch, dev):
+    """L2 rates of the attention kernels' access shapes, on a 64 MiB buffer
+    (L2-resident): streaming reads, random 1 KB pool gathers, and 16-byte fp32
+    vector reductions four rows x 128 B per warp instruction."""
+    buf = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
+    out = {"buffer_mib": 64}
+    for kind, name in ((0, "stream_read_gbs"), (1, "gather_1kb_gbs"), (2, "red_v4_gbs")):
+        out[name] = max(dsa.measure_l2(kind, buf, iters=20) for _ in range(3))
+    del buf
+    return out
+
 
 def run_ours(args):
     import torch
@@ -307,7 +335,9 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     libbuild.build()
     wl = synth.WORKLOADS[args.workload]
+    backward = wl.backward
     peaks = load_peaks()
+    l2 = measure_l2_peaks(dsa, torch, dev)
 
     host = host_inputs(wl)
     q_idx_h, k_idx_h, w_h, q_h, k_h, v_h, dO_h = host
@@ -316,22 +346,30 @@ def run_ours(args):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
 
     pin = {"q_idx": pinned_bf16(q_idx_h), "k_idx": pinned_bf16(k_idx_h), "w": torch.from_numpy(w_h).pin_memory(),
-           "q": pinned_bf16(q_h), "k": pinned_bf16(k_h), "v": pinned_bf16(v_h), "dO": pinned_bf16(dO_h)}
+           "q": pinned_bf16(q_h), "k": pinned_bf16(k_h), "v": pinned_bf16(v_h)}
+    if backward:
+        pin["dO"] = pinned_bf16(dO_h)
+    del host, q_idx_h, q_h, dO_h
+
+    def host_view(name):
+        t = pin[name]
+        return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
     d = {name: t.to(dev) for name, t in pin.items()}
     S, topk = wl.S, wl.topk
     pool_idx = torch.empty((S, topk), dtype=torch.int32, device=dev)
     o = torch.empty_like(d["q"])
     lse = torch.empty((S, wl.Hq), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
     ws_idx = torch.empty(dsa.index_topk_workspace_size(S, wl.Hi, wl.Di, wl.chunk, topk), dtype=torch.uint8,
                          device=dev)
-    if args.deterministic:
-        bwd = dsa.dsa_sparse_attn_bwd_deterministic
-        ws_bwd_bytes = dsa.sparse_attn_bwd_deterministic_workspace_size(S, wl.Hq, wl.D, topk)
-    else:
-        bwd = dsa.dsa_sparse_attn_bwd
-        ws_bwd_bytes = dsa.sparse_attn_bwd_workspace_size(S, wl.Hq, wl.D)
-    ws_bwd = torch.empty(ws_bwd_bytes, dtype=torch.uint8, device=dev)
+    if backward:
+        dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+        if args.deterministic:
+            bwd = dsa.dsa_sparse_attn_bwd_deterministic
+            ws_bwd_bytes = dsa.sparse_attn_bwd_deterministic_workspace_size(S, wl.Hq, wl.D, topk)
+        else:
+            bwd = dsa.dsa_sparse_attn_bwd
+            ws_bwd_bytes = dsa.sparse_attn_bwd_workspace_size(S, wl.Hq, wl.D)
+        ws_bwd = torch.empty(ws_bwd_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -339,7 +377,9 @@ def run_ours(args):
         dsa.dsa_index_topk(t["q_idx"], t["k_idx"], t["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
                            workspace=ws_idx)
         dsa.dsa_sparse_attn_fwd(t["q"], t["k"], t["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
-        bwd(t["dO"], t["q"], t["k"], t["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv, workspace=ws_bwd)
+        if backward:
+            bwd(t["dO"], t["q"], t["k"], t["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv,
+                workspace=ws_bwd)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -372,6 +412,7 @@ def run_ours(args):
     clocks = sampler.stop()
     gpu_launches = dsa.launch_count()
     dsa.dsa_sync_status()
+    index_stats = dsa.index_topk_stats(ws_idx)
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) / 1e3
     total_s = max_over_ranks(total_s, dev)
@@ -392,9 +433,17 @@ def run_ours(args):
             tf = work["index_topk"]["flops"] / (ms * 1e-3) / 1e12
             entry.update({"algorithmic_tflops": tf, "frac_of_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
                           "executed_tensor_flops_factor": 2.0, "includes": "indexer tiles and top-k rows"})
+            traffic, tsrc = profiled_traffic("index_topk", S)
+            entry.update({"dram_bytes_per_launch": traffic, "dram_bytes_source": tsrc})
         elif name in ("attn_fwd", "attn_bwd", "det_span"):
             gbs = work[name]["bytes"] / (ms * 1e-3) / 1e9
             entry.update({"algorithmic_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]})
+            if name == "attn_fwd":
+                # the gather and the per-query streams read through L2 (K/V is L2-resident up to S ~ 2^17)
+                entry["frac_of_l2_gather"] = gbs / l2["gather_1kb_gbs"]
+            if name == "attn_bwd":
+                red = work["keys"] * 2 * wl.D * 4 / (ms * 1e-3) / 1e9
+                entry.update({"reduction_gbs": red, "frac_of_l2_red": red / l2["red_v4_gbs"]})
         kernels[name] = entry
     dom = max(prof.items(), key=lambda kv: kv[1][0])[0]
     dms, dl = prof[dom]
@@ -411,29 +460,33 @@ def run_ours(args):
     roof["traffic_source"] = tsrc
     roof.update({"kernel": dom, "launches_per_step": dl, "avg_launch_ms": dms / max(dl, 1),
                  "peak_source": peaks["source"] + (" (sustained bf16)" if dom == "index_topk" else " (copy bandwidth)")})
+    if dom in kernels:
+        for key in ("frac_of_l2_red", "reduction_gbs", "frac_of_l2_gather"):
+            if key in kernels[dom]:
+                roof[key] = kernels[dom][key]
+    roof["l2_peaks_measured"] = l2
 
-    # ---- end to end through the public API: pinned host -> device, the three calls, device -> host
+    # ---- end to end through the public API: pinned host -> device, the calls, device -> host
     e2e = None
     if not args.no_e2e:
-        out_host = {"pool_idx": torch.empty(pool_idx.shape, dtype=pool_idx.dtype).pin_memory(),
-                    "o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
-                    "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
-                    "dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
-                    "dk": torch.empty(dk.shape, dtype=dk.dtype).pin_memory(),
-                    "dv": torch.empty(dv.shape, dtype=dv.dtype).pin_memory()}
+        out_names = [("pool_idx", pool_idx), ("o", o), ("lse", lse)]
+        grad_names = [("dq", dq), ("dk", dk), ("dv", dv)] if backward else []
+        out_host = {name: torch.empty(t.shape, dtype=t.dtype).pin_memory() for name, t in out_names + grad_names}
         bi = sum(t.numel() * t.element_size() for t in pin.values())
         bo = sum(t.numel() * t.element_size() for t in out_host.values())
         # Pipelined the way a training loop with prefetch runs it, every copy
         # inside the timed region: step s+1's indexer inputs upload while step s
-        # runs its attention (the indexer is done with their buffers); q, k, v,
-        # dO upload while the indexer runs, once the previous backward is done
-        # with them; pool_idx, o and lse come back while the backward runs; dq,
-        # dk and dv come back while the next step's indexer runs (the last
-        # step's before the end event).  Host-to-device and device-to-host
-        # copies run on their own streams.
+        # runs its attention (the indexer is done with their buffers); q, k, v
+        # (and dO) upload while the indexer runs, once the previous step's
+        # attention is done with them; pool_idx, o and lse come back while the
+        # backward (or the next step's indexer) runs; dq, dk and dv come back
+        # while the next step's indexer runs (the last step's before the end
+        # event).  Host-to-device and device-to-host copies run on their own
+        # streams.
         h2d = torch.cuda.Stream(device=dev)
         d2h = torch.cuda.Stream(device=dev)
-        idx_in, attn_in = ("q_idx", "k_idx", "w"), ("q", "k", "v", "dO")
+        idx_in = ("q_idx", "k_idx", "w")
+        attn_in = ("q", "k", "v", "dO") if backward else ("q", "k", "v")
 
         def upload(names):
             with torch.cuda.stream(h2d):
@@ -455,7 +508,7 @@ def run_ours(args):
             h2d.wait_stream(stream)
             d2h.wait_stream(stream)
             ev_idx_in = upload(idx_in)
-            ev_bwd = ev_small_out = ev_grads_out = None
+            ev_attn_done = ev_small_out = ev_grads_out = None
             for s in range(nsteps):
                 flush.zero_()
                 stream.wait_event(ev_idx_in)
@@ -464,27 +517,30 @@ def run_ours(args):
                 dsa.dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
                                    workspace=ws_idx)
                 ev_idx_done = stream.record_event()
-                if ev_bwd is not None:
-                    h2d.wait_event(ev_bwd)  # the previous backward is done with q, k, v, dO
-                    d2h.wait_event(ev_bwd)
-                    ev_grads_out = download((("dq", dq), ("dk", dk), ("dv", dv)))
+                if ev_attn_done is not None:
+                    h2d.wait_event(ev_attn_done)  # the previous step's attention is done with q, k, v (, dO)
+                    if backward:
+                        d2h.wait_event(ev_attn_done)
+                        ev_grads_out = download(grad_names)
                 ev_attn_in = upload(attn_in)
                 stream.wait_event(ev_attn_in)
                 dsa.dsa_sparse_attn_fwd(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
                 d2h.wait_stream(stream)
-                ev_small_out = download((("pool_idx", pool_idx), ("o", o), ("lse", lse)))
+                ev_small_out = download(out_names)
                 if s + 1 < nsteps:
                     h2d.wait_event(ev_idx_done)
                     ev_idx_in = upload(idx_in)
-                if ev_grads_out is not None:
-                    stream.wait_event(ev_grads_out)  # dq, dk, dv of the previous step are on the host
-                bwd(d["dO"], d["q"], d["k"], d["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv,
-                    workspace=ws_bwd)
-                ev_bwd = stream.record_event()
+                if backward:
+                    if ev_grads_out is not None:
+                        stream.wait_event(ev_grads_out)  # dq, dk, dv of the previous step are on the host
+                    bwd(d["dO"], d["q"], d["k"], d["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv,
+                        workspace=ws_bwd)
+                ev_attn_done = stream.record_event()
                 if marks is not None:
                     marks[s].record(stream)
-            d2h.wait_event(ev_bwd)
-            download((("dq", dq), ("dk", dk), ("dv", dv)))
+            if backward:
+                d2h.wait_event(ev_attn_done)
+                download(grad_names)
             stream.wait_stream(d2h)
             stream.wait_stream(h2d)
 
@@ -507,22 +563,24 @@ def run_ours(args):
                "d2h_bytes_per_step": bo, "ms_per_step": 1e3 * e2e_s / args.steps,
                "step_ms": [a.elapsed_time(b) for a, b in zip(bounds[:-1], bounds[1:])],
                "last_step_tail_ms": marks[-1].elapsed_time(e2e_end),
-               "pipelining": "next step's indexer inputs upload during this step's attention; this step's dq/dk/dv "
-                             "download during the next step's indexer; all copies inside the timed region"}
+               "pipelining": "next step's indexer inputs upload during this step's attention; this step's outputs "
+                             "download during the next step's work; all copies inside the timed region"}
 
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            cpu = cpu_baseline(wl, host, args.cpu_seconds)
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            cpu = cpu_baseline(wl, tuple(host_view(n) if n in pin else None
+                                         for n in ("q_idx", "k_idx", "w", "q", "k", "v", "dO")), args.cpu_seconds)
+        line = {"metric": metric_for(wl), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": workload_config(wl, "flushed between timed steps (512 MiB write outside the events)"),
-                "backward": "deterministic (key-major, fixed order)" if args.deterministic else "atomic dK/dV",
                 "parallelism": f"replicas x{world} (one independent sequence per GPU)",
                 "clocks": clocks, "gpu_launches": gpu_launches, "e2e": e2e, "roofline": roof,
-                "kernels": kernels, "cpu_baseline": cpu, "wall_s_timed_region": wall,
-                "step_ms": step_ms}
+                "kernels": kernels, "index_topk_stats": index_stats, "cpu_baseline": cpu,
+                "wall_s_timed_region": wall, "step_ms": step_ms}
+        if backward:
+            line["backward"] = "deterministic (key-major, fixed order)" if args.deterministic else "atomic dK/dV"
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -14,9 +14,11 @@
  *              and sharded by query, exchanging int32 selected-pool indices.
  *  [Anyscale]  "How Lila Sciences and Anyscale Scaled GLM-5.3-Flash
  *              Training", lessons "检查每一层是否运行您认为的内核" (a sparse
- *              kernel that silently fell back to dense attention) and
- *              "稀疏注意力会导致二次成本" (a few hundred queries scored at a
- *              time keeps the score matrix under 2 GiB).
+ *              kernel that silently fell back to dense attention) and the
+ *              second lesson, on the indexer: sparse attention moves its
+ *              quadratic cost into the indexer rather than removing it, and
+ *              scoring a few hundred queries at a time keeps the score
+ *              matrix under 2 GiB).
  *  [CP-lesson] "128K 的序列,激活放在哪?" (context-parallel lesson),
  *              §改进二 and evidence row ②: blockwise online softmax equals
  *              the one-shot softmax.
@@ -78,8 +80,8 @@ typedef enum {
 size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
 
 /*
- * Indexer + top-k  [SkyRL-1M §模型与瓶颈, §1 DSA 真稀疏; Anyscale lesson
- * "稀疏注意力会导致二次成本"].
+ * Indexer + top-k  [SkyRL-1M §模型与瓶颈, §1 DSA 真稀疏; Anyscale, second
+ * lesson (the indexer's quadratic cost)].
  *
  *  q_idx     bf16 [S, Hi, Di]  indexer queries (rows q_begin..q_end-1 read)
  *  k_idx     bf16 [S, Di]      indexer keys
@@ -251,20 +253,39 @@ dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const voi
  * library.)
  *
  * Same arguments, outputs and results as dsa_index_topk, but without a
- * workspace: the scratch lives in a fixed static device buffer of 18 MiB +
- * 256 B inside the library, which every GPU that loads the library holds
- * until the process exits.  That covers S <= 32768 with chunk <= 256; larger
- * sizes return DSA_ERR_WORKSPACE (see dsa_last_error()) and nothing runs.
- * The call allocates nothing.  The first call on a device looks up the
- * buffer's device address (cudaGetSymbolAddress, with that device current),
- * so that first call should come before any stream capture.  All calls on a
- * device share the buffer and leave their contents in it; nothing needs to be
- * zero beforehand.  Calls whose GPU work overlaps (e.g. on unordered streams)
- * race on the buffer: order them.
+ * workspace: the scratch lives in a fixed static device array of 18 MiB +
+ * 256 B inside the library.  Sizes run when dsa_index_topk's least workspace
+ * for them (two chunk buffers) fits in it -- S <= 32768 with chunk <= 256,
+ * for example, or S = 65536 with chunk <= 64; other sizes return
+ * DSA_ERR_WORKSPACE (see dsa_last_error()) and nothing runs.  At the largest
+ * sizes that fit, only two chunks are in flight, so the call is slower than
+ * dsa_index_topk with its recommended workspace (same result).
+ * Under CUDA's default lazy module loading a device reserves the array when
+ * the library's module holding it is first loaded there, which happens in
+ * the first call on that device (that call looks up the array's device
+ * address with cudaGetSymbolAddress, with the device current); the device
+ * then holds the array until the process exits.  So make the first call on
+ * each device outside any region that must not allocate and before any
+ * stream capture; later calls allocate nothing.  The address is cached per
+ * CUDA context and looked up again after a device reset.  All calls on a
+ * device share the array and leave their contents in it; nothing needs to be
+ * zero beforehand.  Calls whose GPU work overlaps (e.g. on unordered
+ * streams) race on the array: order them.
  */
 dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
                                     int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
                                     void* stream);
+
+/*
+ * Counters of the last dsa_index_topk call that used `workspace` (a
+ * measurement helper; no part of the layer's arithmetic).  Synchronises
+ * `stream` (the stream of that call), then writes up to `max_stats` values:
+ *   stats[0]  query rows whose top-k had to take the full-row path (the
+ *             fast path's threshold guess did not hold for the row)
+ * Returns the number of values written, or -1 (with dsa_last_error()) for a
+ * null or short workspace or a CUDA error.
+ */
+int dsa_index_topk_stats(const void* workspace, size_t ws_bytes, int64_t* stats, int max_stats, void* stream);
 
 /* Synchronises `stream` and returns DSA_ERR_TIMEOUT / DSA_ERR_INTERNAL if a
  * kernel has recorded a failed bounded wait or check since the last
@@ -295,6 +316,22 @@ const char* dsa_version(void);
  * in this process since dsa_launch_count_reset(), whether or not profiling
  * is enabled.
  */
+/*
+ * L2 rate probes (measurement helper).  Runs one probe kernel `iters` times
+ * (after one untimed warm-up pass) on the caller's device buffer `buf` of
+ * `bytes` bytes (16-byte aligned, >= 4096; size it below L2 to measure L2)
+ * on `stream`, times it with CUDA events (synchronising), and returns the
+ * rate in GB/s of bytes moved, or -1.0 on error:
+ *   kind 0  streaming 16-byte loads over the buffer
+ *   kind 1  random 1 KB blocks read whole by one warp each (the attention
+ *           kernels' gather of one key pool's four 256-byte rows)
+ *   kind 2  red.global.add.v4.f32 on random 2 KB blocks, each warp
+ *           instruction adding 128 bytes to each of a block's four 512-byte
+ *           rows (the backward's dK/dV reductions); counts bytes added
+ * Kind 2 adds into the buffer's contents.
+ */
+double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream);
+
 void dsa_profile_enable(int on);
 int dsa_profile_read(char* names, int name_len, double* ms, int64_t* launches, int max_kernels);
 int64_t dsa_launch_count(void);

@@ -29,7 +29,8 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_index_topk_noalloc", "dsa_sparse_attn_fwd_range", "dsa_sparse_attn_bwd_range",
             "dsa_zigzag_ranges", "dsa_index_topk_varlen_workspace", "dsa_index_topk_varlen",
             "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen",
-            "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic")
+            "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic",
+            "dsa_index_topk_stats", "dsa_measure_l2")
 
 _lock = threading.Lock()
 _lib = None
@@ -100,6 +101,10 @@ def load():
             lib.dsa_index_topk_noalloc.restype = ctypes.c_int
             lib.dsa_launch_count_reset.argtypes = []
             lib.dsa_launch_count_reset.restype = None
+            lib.dsa_index_topk_stats.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, vp]
+            lib.dsa_index_topk_stats.restype = ctypes.c_int
+            lib.dsa_measure_l2.argtypes = [ctypes.c_int, vp, sz, ctypes.c_int, vp]
+            lib.dsa_measure_l2.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -393,6 +398,27 @@ def profile_read() -> dict:
         nm = raw[j * name_len:(j + 1) * name_len].split(b"\0", 1)[0].decode()
         out[nm] = (float(ms[j]), int(cnt[j]))
     return out
+
+
+def index_topk_stats(workspace: torch.Tensor, stream=None) -> dict:
+    """Counters of the last dsa_index_topk call on `workspace` (synchronises)."""
+    lib = load()
+    out = (ctypes.c_int64 * 8)()
+    n = lib.dsa_index_topk_stats(workspace.data_ptr(), workspace.numel() * workspace.element_size(), out, 8,
+                                 _stream_handle(stream))
+    if n < 0:
+        raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
+    names = ("general_path_rows",)
+    return {names[j]: int(out[j]) for j in range(min(n, len(names)))}
+
+
+def measure_l2(kind: int, buf: torch.Tensor, iters: int = 20, stream=None) -> float:
+    """GB/s of an L2 probe kernel on `buf` (kind 0 stream read, 1 1-KB gather, 2 red.v4 reductions)."""
+    lib = load()
+    r = lib.dsa_measure_l2(kind, buf.data_ptr(), buf.numel() * buf.element_size(), iters, _stream_handle(stream))
+    if r < 0:
+        raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
+    return float(r)
 
 
 def launch_count() -> int:

@@ -1,7 +1,7 @@
 // dsa_api.cu -- the C ABI of libdsa (declared in include/dsa.h): argument
 // checks, workspace carving, TMA descriptors and the query-chunk loop.
 //
-// [SkyRL-1M §1 DSA 真稀疏; Anyscale "稀疏注意力会导致二次成本"] the indexer
+// [SkyRL-1M §1 DSA 真稀疏; Anyscale, second lesson (the indexer)] the indexer
 // scores one chunk of queries at a time, so its scratch is a ring of at most
 // eight chunks of scores (chunk x pools x 4 B each; two at the least) rather
 // than the whole S x S/4 matrix.
@@ -23,6 +23,13 @@
 #include "../../include/dsa.h"
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
+
+namespace dsa {
+// Unique id of the calling thread's current CUDA context, or 0 when there is
+// none (or the driver cannot say).  Device addresses looked up in a context
+// are cached under its id.
+unsigned long long current_context_id();
+}  // namespace dsa
 
 namespace {
 
@@ -64,6 +71,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct DeviceInfo {
   int num_sms = 0;
   unsigned* status = nullptr;
+  unsigned long long ctx = 0;  // context the status address was looked up in
 };
 
 std::mutex g_dev_mu;
@@ -76,6 +84,10 @@ dsa_status_t device_info(DeviceInfo* out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
+  // a device reset replaces the context, and with it the module that holds
+  // the status word: look its address up again in the new context
+  const unsigned long long ctx = dsa::current_context_id();
+  if (d.num_sms != 0 && (ctx == 0 || ctx != d.ctx)) d.num_sms = 0;
   if (d.num_sms == 0) {
     int major = 0, minor = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -89,6 +101,7 @@ dsa_status_t device_info(DeviceInfo* out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
     d.status = static_cast<unsigned*>(p);
     d.num_sms = sms;
+    d.ctx = dsa::current_context_id();  // the lookup made the context current if it was not
   }
   *out = d;
   return DSA_OK;
@@ -185,6 +198,30 @@ size_t index_ws_bytes(int64_t S, int chunk, int nbuf) {
 
 namespace dsa {
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 size_t index_topk_min_workspace(int64_t S, int chunk) {
   if (S < 1 || chunk < 1) return 0;
   return index_ws_bytes(S, chunk, index_min_bufs(S, chunk));
@@ -613,6 +650,23 @@ dsa_status_t dsa_clear_status(void) {
   cudaError_t e = cudaMemcpyToSymbol(g_dsa_status, &z, sizeof(z));
   if (e != cudaSuccess) return cuda_fail(e, "dsa_clear_status");
   return DSA_OK;
+}
+
+int dsa_index_topk_stats(const void* workspace, size_t ws_bytes, int64_t* stats, int max_stats, void* stream) {
+  if (!workspace || ws_bytes < kSyncBytes || !stats || max_stats < 1) {
+    fail(DSA_ERR_INVALID_ARG, "dsa_index_topk_stats: null or short workspace, or no room for results");
+    return -1;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned long long words[dsa::kIndexSyncWords];
+  cudaError_t e = cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "dsa_index_topk_stats: read counters");
+    return -1;
+  }
+  stats[0] = static_cast<int64_t>(words[dsa::kIndexGeneralRowsWord]);
+  return 1;
 }
 
 void dsa_profile_enable(int on) { g_profiling.store(on ? 1 : 0); }

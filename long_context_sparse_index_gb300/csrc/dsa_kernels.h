@@ -56,6 +56,9 @@ cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(KArgs...), dim3 grid,
 // of its workspace, and its most score buffers.
 constexpr int kIndexSyncWords = 24;
 constexpr int kMaxBufs = 8;
+// word counting the rows whose top-k took the general (full-row) path; it
+// survives the call (the next call's key pooling zeroes it)
+constexpr int kIndexGeneralRowsWord = 20;
 
 // Pooled indexer keys: khat2 [P, 128] bf16, hi in columns 0..63, lo in 64..127.
 // Also zeroes the kIndexSyncWords words at sync_words (always launch it, even

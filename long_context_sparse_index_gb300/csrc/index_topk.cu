@@ -2,7 +2,7 @@
 // its per-query top-k as one persistent kernel.
 //
 // [SkyRL-1M §模型与瓶颈] the indexer scores every query against every earlier
-// 4-token key pool; [§1 DSA 真稀疏; Anyscale "稀疏注意力会导致二次成本"] it
+// 4-token key pool; [§1 DSA 真稀疏; Anyscale, second lesson (the indexer)] it
 // does so one query chunk at a time so the score matrix is never whole, and
 // keeps each query's best pools as int32 indices.
 //
@@ -94,7 +94,7 @@ struct Item {
 // global 64-bit words, zeroed by pool_keys_kernel before each launch; the
 // done counters are per buffer (chunk c uses buffer c % nbuf) and cumulative
 enum : int { kTicket = 0, kTilesDone = 1 /* kMaxBufs words */, kRowsDone = 1 + kMaxBufs, kGAbort = 1 + 2 * kMaxBufs };
-static_assert(kGAbort < kIndexSyncWords, "global words");
+static_assert(kGAbort < kIndexSyncWords && kIndexGeneralRowsWord > kGAbort, "global words");
 
 struct Args {
   const float* w;
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (gid < nr) {
           const int64_t i = ch.row0 + r0 + gid;
           topk::row(grp, tsm[gid], buf + static_cast<int64_t>(r0 + gid) * a.ld, static_cast<int>(i / 4), a.topk,
-                    a.pool_idx + (i - a.q_begin) * a.topk);
+                    a.pool_idx + (i - a.q_begin) * a.topk, a.sync + kIndexGeneralRowsWord);
         }
         epi_sync();
         if (etid == 0) atomicAdd(a.sync + kRowsDone + bi, static_cast<unsigned long long>(nr));

@@ -6,15 +6,22 @@
 // runtime that owns a fixed device-memory budget and must not let a library
 // grow it, or a latency-critical path that must not block on the device
 // allocator.  For them this file keeps the scratch the call needs in a
-// file-scope static device array of fixed size, kNoAllocScratchBytes, which
-// every GPU that loads the library holds until the process exits.  The caller
-// still passes its own inputs and outputs.
+// file-scope static device array of fixed size, kNoAllocScratchBytes.  The
+// caller still passes its own inputs and outputs.
 //
-// Set-up: the first call on each device looks up that device's address of the
-// array with cudaGetSymbolAddress (with that device current).  That first call
-// per device should therefore come before any stream capture.  In host code
-// the array's name is only a stand-in, never a device address, so kernels are
-// always given the looked-up address.
+// When the array is reserved: this file is its own CUDA module, and under
+// the runtime's default lazy module loading a device reserves the array when
+// the module is first loaded on it -- during the first call on that device
+// (the address lookup below loads it).  From then on the device holds the
+// array until the process exits.  So the first call on each device belongs
+// outside any region that must not allocate, and before any stream capture.
+//
+// Set-up: that first call on each device looks up the device's address of
+// the array with cudaGetSymbolAddress (with that device current) and caches
+// it under the current context's id; a later call in a new context (after a
+// device reset, say) looks it up again.  In host code the array's name is
+// only a stand-in, never a device address, so kernels are always given the
+// looked-up address.
 //
 // Every call on a device shares the same array, and the array keeps whatever
 // the previous call left in it.  Nothing in it needs to start at zero: each
@@ -32,14 +39,18 @@
 namespace dsa {
 void set_last_error(const std::string& msg);  // dsa_api.cu: the message dsa_last_error() returns
 size_t index_topk_min_workspace(int64_t S, int chunk);  // dsa_api.cu: the least workspace dsa_index_topk accepts
+unsigned long long current_context_id();  // dsa_api.cu: id of the current CUDA context (0: none)
 }
 
 namespace {
 
-// 18 MiB + 256 B: the least workspace dsa_index_topk accepts for S <= 32768
-// with chunk <= 256 (the kernel's global words 256 B, pooled keys 2 MiB, two
-// chunk buffers of scores 8 MiB each; more buffers only let more chunks be in
-// flight and never change the result).
+// 18 MiB + 256 B.  The call runs the sizes whose least workspace (the one
+// dsa_index_topk accepts at the minimum, two chunk buffers of scores) fits:
+// for example S <= 32768 with chunk <= 256 (kernel words 256 B, pooled keys
+// 2 MiB, two chunk buffers of 8 MiB), or S = 65536 with chunk <= 64.  It
+// always hands dsa_index_topk the whole array, so at the largest sizes only
+// two chunks are in flight (slower than dsa_index_topk with its recommended
+// workspace; the result is the same).
 constexpr size_t kNoAllocScratchBytes = (static_cast<size_t>(18) << 20) + 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -47,6 +58,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};  // context each address was looked up in
 
 }  // namespace
 
@@ -63,7 +75,8 @@ dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const 
   if (need > kNoAllocScratchBytes) {
     dsa::set_last_error("dsa_index_topk_noalloc: these sizes need " + std::to_string(need) +
                         " bytes of scratch but the built-in buffer holds " + std::to_string(kNoAllocScratchBytes) +
-                        " (S <= 32768 with chunk <= 256); use dsa_index_topk with a caller workspace");
+                        " (enough for S <= 32768 with chunk <= 256, for example); use dsa_index_topk with a "
+                        "caller workspace");
     return DSA_ERR_WORKSPACE;
   }
   int dev = 0;
@@ -75,7 +88,8 @@ dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const 
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    const unsigned long long ctx = dsa::current_context_id();
+    if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || p == nullptr) {
@@ -84,6 +98,7 @@ dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const 
         return DSA_ERR_CUDA;
       }
       g_scratch_ptr[dev] = p;
+      g_scratch_ctx[dev] = dsa::current_context_id();  // the lookup made a context current if none was
     }
     scratch = g_scratch_ptr[dev];
   }

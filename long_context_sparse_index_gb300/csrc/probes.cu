@@ -1,0 +1,139 @@
+// probes.cu -- measurement kernels for the ceilings the attention kernels
+// meet when their working set sits in L2 (no part of the layer's arithmetic).
+//
+// The sparse attention gathers 1 KB key pools (four 256-byte K or V rows)
+// chosen by the selection, and the backward adds each (query, key) pair's
+// dK/dV rows into fp32 accumulators with 16-byte vector reductions, one
+// pool's four rows x 128 bytes per warp instruction.  At S = 131072 both K/V
+// (64 MiB) and the accumulators (128 MiB) are L2-sized, so HBM bandwidth does
+// not bound those kernels; these probes measure the L2 rates of the same
+// access shapes on the caller's buffer:
+//   kind 0  streaming 16-byte loads over the whole buffer, repeated
+//   kind 1  random 1 KB blocks, each read by one warp (two 16-byte loads a lane)
+//   kind 2  red.global.add.v4.f32 on random 2 KB blocks (4 rows x 512 B):
+//           each warp instruction adds 128 bytes to each of the 4 rows
+// All three report bytes moved (read, or added) per second.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/dsa.h"
+#include "dsa_device.cuh"
+
+namespace dsa {
+void set_last_error(const std::string& msg);
+}
+
+namespace {
+
+__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+  // a 32-bit integer hash (xorshift-multiply rounds) picking pseudo-random blocks
+  x ^= x >> 16;
+  x *= 0x7feb352du;
+  x ^= x >> 15;
+  x *= 0x846ca68bu;
+  x ^= x >> 16;
+  return x;
+}
+
+__global__ void probe_stream_kernel(const float4* __restrict__ buf, int64_t n4, int iters, float* sink) {
+  float acc = 0.f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int it = 0; it < iters; ++it)
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4; j += stride) {
+      const float4 v = __ldcg(buf + j);
+      acc += v.x + v.y + v.z + v.w;
+    }
+  if (acc == 1.2345f) sink[0] = acc;  // a data-dependent store (practically never taken) keeps the loads
+}
+
+__global__ void probe_gather_kernel(const uint4* __restrict__ buf, uint32_t nblocks, int per_warp, float* sink) {
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t acc = 0;
+  for (int it = 0; it < per_warp; it += 4) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // four blocks in flight per warp
+      const uint32_t b = mix32(warp * 0x9E3779B9u + static_cast<uint32_t>(it + u)) % nblocks;
+      const uint4* src = buf + static_cast<int64_t>(b) * 64 + lane;
+      v[2 * u] = __ldcg(src);
+      v[2 * u + 1] = __ldcg(src + 32);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  if (acc == 0x12345678u) sink[0] = 1.f;
+}
+
+__global__ void probe_red_kernel(float* __restrict__ buf, uint32_t nblocks, int per_warp) {
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int it = 0; it < per_warp; ++it) {
+    const uint32_t h = mix32(warp * 0x9E3779B9u + static_cast<uint32_t>(it));
+    const uint32_t b = h % nblocks;
+    const int jj = static_cast<int>((h >> 28) & 3u);  // 32-dim block of the rows
+    float* dst = buf + static_cast<int64_t>(b) * 512 + (lane >> 3) * 128 + 32 * jj + 4 * (lane & 7);
+    dsa::red_add_v4(dst, 1.f, 1.f, 1.f, 1.f);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream) {
+  if (!buf || bytes < 4096 || iters < 1 || kind < 0 || kind > 2 || (reinterpret_cast<uintptr_t>(buf) & 15u)) {
+    dsa::set_last_error("dsa_measure_l2: kind must be 0..2, buf 16-byte aligned, bytes >= 4096, iters >= 1");
+    return -1.0;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    dsa::set_last_error("dsa_measure_l2: no device");
+    return -1.0;
+  }
+  const int block = 256;
+  const int grid = sms * 8;
+  const int warps = grid * block / 32;
+  float* sink = static_cast<float*>(buf);
+  double moved = 0.0;
+  auto launch = [&](int reps) {
+    if (kind == 0) {
+      const int64_t n4 = static_cast<int64_t>(bytes / 16);
+      probe_stream_kernel<<<grid, block, 0, st>>>(static_cast<const float4*>(buf), n4, reps, sink);
+      moved = static_cast<double>(n4) * 16.0 * reps;
+    } else if (kind == 1) {
+      const uint32_t nb = static_cast<uint32_t>(bytes / 1024);
+      const int per_warp = 64 * reps;
+      probe_gather_kernel<<<grid, block, 0, st>>>(static_cast<const uint4*>(buf), nb, per_warp, sink);
+      moved = static_cast<double>(warps) * per_warp * 1024.0;
+    } else {
+      const uint32_t nb = static_cast<uint32_t>(bytes / 2048);
+      const int per_warp = 64 * reps;
+      probe_red_kernel<<<grid, block, 0, st>>>(static_cast<float*>(buf), nb, per_warp);
+      moved = static_cast<double>(warps) * per_warp * 512.0;
+    }
+  };
+  cudaEvent_t a, b;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  launch(1);  // warm-up: brings the buffer into L2
+  cudaEventRecord(a, st);
+  launch(iters);
+  cudaEventRecord(b, st);
+  cudaError_t e = cudaEventSynchronize(b);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  if (e != cudaSuccess || ms <= 0.f) {
+    dsa::set_last_error(std::string("dsa_measure_l2: ") + cudaGetErrorString(e));
+    return -1.0;
+  }
+  return moved / (ms * 1e-3) / 1e9;
+}
+
+}  // extern "C"

@@ -353,8 +353,10 @@ __device__ __noinline__ void general(const Group& g, Smem& sm, const float* srow
 
 // Top-k of one row: srow holds the n = floor(i/4) eligible scores of query i;
 // writes orow[0 .. topk).  All threads of the group call it together; it ends
-// with a group barrier (the shared buffers are reused by the next row).
-__device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, int n, int topk, int32_t* orow) {
+// with a group barrier (the shared buffers are reused by the next row).  A
+// row that takes the general path adds one to *general_rows.
+__device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, int n, int topk, int32_t* orow,
+                                 unsigned long long* general_rows) {
   const int tid = g.tid, lane = g.lane(), warp = g.warp();
   if (n <= topk) {
     for (int j = tid; j < topk; j += kGT) orow[j] = j < n ? j : -1;
@@ -478,6 +480,7 @@ __device__ __noinline__ void row(const Group& g, Smem& sm, const float* srow, in
     hi = max(hi, sm.wmax[w]);
   }
   if (overflow || total < static_cast<uint32_t>(topk)) {
+    if (tid == 0) atomicAdd(general_rows, 1ull);
     general(g, sm, srow, n, topk, orow, parity);
     return;
   }

@@ -17,7 +17,7 @@
  *              (2051 selected keys, no positional encoding, query-chunked
  *              indexer, int32 selected-pool indices).
  *  [Anyscale]  "How Lila Sciences and Anyscale Scaled GLM-5.3-Flash
- *              Training", lesson "稀疏注意力会导致二次成本" (selection scores
+ *              Training", second lesson, on the indexer (selection scores
  *              each query against the whole sequence; scores computed a few
  *              hundred queries at a time).
  *  [CP-lesson] "128K 的序列,激活放在哪?" (context-parallel lesson),

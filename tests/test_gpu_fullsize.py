@@ -6,6 +6,9 @@ benchmark times, on sampled outputs the oracle computes one by one.
   s256k_cluster  S=262144, planted key clusters, chunk 512 (indexer + top-k)
   s1m_cluster    S=1048576, planted key clusters, chunk 512 (indexer + top-k,
                  attention forward)
+  s16k, s256k_cluster   the forward configurations at S=16384 and S=262144:
+                 the attention forward on the oracle's own selection of the
+                 sampled rows
   s64k_zipf      S=65536, Zipf-ranked pool popularity; forward and backward,
                  with dK/dV checked on a popular pool
 """
@@ -75,6 +78,37 @@ def test_s1m_cluster_index_topk_and_forward_sampled():
     ro, rl = oracle.attn_fwd(q, k, v, sel, scale=wl.scale, rows=rows)
     assert_close(torch_bf16_to_f64(o[torch.from_numpy(rows).to(DEV)]), ro, "o")
     assert_close(lse[torch.from_numpy(rows).to(DEV)].cpu().numpy().astype(np.float64), rl, "lse", bf16_out=False)
+
+
+def _check_forward_on_oracle_selection(wl, n_rows, seed):
+    """Sparse attention forward at the workload's full size on the selection
+    the oracle makes for sampled query rows (every other row keeps the seeded
+    stand-in selection, so the launch has the full size); o and lse of the
+    sampled rows against the oracle's forward over the same key sets."""
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    rows = _sample_rows(wl.S, n_rows, seed)
+    ref_sel, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk, rows=rows)
+    del q_idx
+    sel = synth.stand_in_selection(wl)
+    sel[rows] = ref_sel
+    q, k, v = synth.attention_inputs(wl)
+    o, lse = dsa.dsa_sparse_attn_fwd(bits_to_torch(q, DEV), bits_to_torch(k, DEV), bits_to_torch(v, DEV),
+                                     torch.from_numpy(sel).to(DEV), scale=wl.scale)
+    dsa.dsa_sync_status()
+    ri = torch.from_numpy(rows).to(DEV)
+    ro, rl = oracle.attn_fwd(q, k, v, sel, scale=wl.scale, rows=rows)
+    assert_close(torch_bf16_to_f64(o[ri]), ro, "o")
+    assert_close(lse[ri].cpu().numpy().astype(np.float64), rl, "lse", bf16_out=False)
+
+
+def test_s16k_forward_on_oracle_selection_sampled():
+    """The S=16384 forward configuration (32 indexer heads, top 512 pools)."""
+    _check_forward_on_oracle_selection(synth.WORKLOADS["s16k"], 32, 7)
+
+
+def test_s256k_cluster_forward_on_oracle_selection_sampled():
+    """The S=262144 forward configuration with planted key clusters."""
+    _check_forward_on_oracle_selection(synth.WORKLOADS["s256k_cluster"], 24, 8)
 
 
 def _check_fwd_bwd(wl, sel, q_rows, key_rows, deterministic=False):

@@ -289,7 +289,12 @@ def test_attn_bwd_repeatable_within_rounding():
     b = dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st)
     assert torch.equal(a[0], b[0])
     for x, y in zip(a[1:], b[1:]):
-        assert (x.float() - y.float()).abs().max().item() <= 2 ** -6 * max(1.0, x.float().abs().max().item())
+        # element by element: the fp32 sums differ only in rounding order, so
+        # after the bf16 rounding two runs differ by at most one bf16 step of
+        # the element itself (a lost or doubled contribution would not)
+        xf, yf = x.float(), y.float()
+        bound = 2 ** -7 * torch.maximum(xf.abs(), yf.abs()) + 1e-6 * xf.abs().max()
+        assert bool(((xf - yf).abs() <= bound).all())
 
 
 # --------------------------------------------------------------------------- deterministic backward

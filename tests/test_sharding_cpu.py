@@ -151,6 +151,50 @@ def test_two_gloo_ranks_zigzag_sharded_indexer_and_forward(dsa):
     torch.multiprocessing.spawn(_sharded_layer_worker, args=(2, _free_port()), nprocs=2, join=True)
 
 
+def _sharded_backward_worker(rank, world, port):
+    """One rank: the backward of its zig-zag ranges through the oracle (its dq
+    rows and its contribution to every key's dK/dV), then the two exchanges a
+    context-parallel backward needs: an all-reduce that sums the ranks' dK/dV
+    contributions and an all-gather of the dq rows; every rank checks the sums
+    against the unsharded oracle backward."""
+    import long_context_sparse_index_gb300 as d
+    _init(rank, world, port)
+    try:
+        wl = synth.WORKLOADS["tiny_int_s2048"]
+        sel, _ = oracle.index_topk(*synth.indexer_inputs(wl), wl.topk)
+        q, k, v = synth.attention_inputs(wl)
+        dO = synth.grad_output(wl)
+        S = wl.S
+        rows = np.concatenate([np.arange(b, e) for b, e in d.zigzag_ranges(S, world, rank)]).astype(np.int64)
+        dq_mine, dk_mine, dv_mine = oracle.attn_bwd_rows(dO, q, k, v, sel, scale=0.02, rows=rows)
+        dk_t, dv_t = torch.from_numpy(dk_mine.copy()), torch.from_numpy(dv_mine.copy())
+        torch.distributed.all_reduce(dk_t)
+        torch.distributed.all_reduce(dv_t)
+        g_rows = [torch.empty(rows.size, dtype=torch.int64) for _ in range(world)]
+        g_dq = [torch.empty(dq_mine.shape, dtype=torch.float64) for _ in range(world)]
+        torch.distributed.all_gather(g_rows, torch.from_numpy(rows))
+        torch.distributed.all_gather(g_dq, torch.from_numpy(dq_mine))
+        ref_dq, ref_dk, ref_dv = oracle.attn_bwd_rows(dO, q, k, v, sel, scale=0.02)
+        dq = np.full_like(ref_dq, np.nan)
+        for r_, g_ in zip(g_rows, g_dq):
+            dq[r_.numpy()] = g_.numpy()
+        assert np.array_equal(dq, ref_dq)
+        # integer inputs: every contribution is a dyadic rational far from fp64
+        # rounding, so the two-term sum is the unsharded sum up to rounding order
+        scale = np.abs(ref_dk).max() + np.abs(ref_dv).max()
+        assert np.abs(dk_t.numpy() - ref_dk).max() <= 1e-12 * scale
+        assert np.abs(dv_t.numpy() - ref_dv).max() <= 1e-12 * scale
+        # each rank's contribution alone is not the whole gradient
+        assert np.abs(dk_mine - ref_dk).max() > 1e-3
+        torch.distributed.barrier()
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_two_gloo_ranks_zigzag_sharded_backward_sums_dkdv(dsa):
+    torch.multiprocessing.spawn(_sharded_backward_worker, args=(2, _free_port()), nprocs=2, join=True)
+
+
 def _max_worker(rank, world, port):
     import bench
     _init(rank, world, port)

@@ -63,6 +63,23 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, name):
 
 
 @pytest.mark.gpu
+def test_noalloc_matches_oracle_on_integer_inputs(lib):
+    """On the integer workload every score is exact, so the selection is
+    unique: the built-in-buffer call must give the oracle's pool indices bit
+    for bit, on two calls in a row."""
+    import oracle
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk)
+    q, k, wt = _bf16(q_idx), _bf16(k_idx), torch.from_numpy(w).cuda()
+    for _ in range(2):
+        got = _noalloc(lib, q, k, wt, wl.S, wl.Hi, wl.chunk, wl.topk)
+        torch.cuda.synchronize()
+        assert lib.dsa_sync_status(None) == 0, lib.dsa_last_error()
+        assert np.array_equal(got.cpu().numpy(), ref)
+
+
+@pytest.mark.gpu
 def test_noalloc_rejects_sizes_beyond_its_buffer(lib):
     import long_context_sparse_index_gb300 as dsa
     S, Hi = 65536, 8
