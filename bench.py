@@ -66,6 +66,9 @@ def parse_args():
                     help="time the S tokens as N packed sequences of a seeded length mix (varlen calls)")
     ap.add_argument("--zigzag", type=int, default=0, metavar="N",
                     help="time the N zig-zag query shards of the sequence one after another (range calls)")
+    ap.add_argument("--trace", action="store_true",
+                    help="indexer item trace: one dsa_index_topk call through the DSA_ITEM_TRACE build, "
+                         "time per work-item kind (fold, dependency wait, rest) and per-CTA idle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time for the CPU baseline sample")
     return ap.parse_args()
@@ -709,10 +712,106 @@ def run_layout(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- indexer item trace
+
+TRACE_KINDS = ("sample", "thresh", "tile", "rows")
+
+
+def summarize_trace(rec, num_sms):
+    """Per-kind and per-CTA time from the item records (see dsa_trace_configure)."""
+    kind = rec["kind_sm"] & 0xFF
+    sm = rec["kind_sm"] >> 8
+    t0, t1, t2, t3 = (rec[f].astype(np.int64) for f in ("t0", "t1", "t2", "t3"))
+    start, end = int(t0.min()), int(t3.max())
+    out = {"records": int(rec.size), "span_ms": (end - start) / 1e6, "ctas": int(np.unique(sm).size), "kinds": {}}
+    ctas = max(out["ctas"], 1)
+    for k, name in enumerate(TRACE_KINDS):
+        m = kind == k
+        if not m.any():
+            continue
+        out["kinds"][name] = {
+            "items": int(m.sum()),
+            "fold_ms_per_cta": float((t1[m] - t0[m]).sum()) / 1e6 / ctas,
+            "wait_ms_per_cta": float((t2[m] - t1[m]).sum()) / 1e6 / ctas,
+            "rest_ms_per_cta": float((t3[m] - t2[m]).sum()) / 1e6 / ctas,
+            "mean_us": float((t3[m] - t0[m]).mean()) / 1e3,
+        }
+    # time between one item's end and the next item's start on the same SM,
+    # plus the lead before an SM's first item and the tail after its last
+    gaps = 0
+    for s_ in np.unique(sm):
+        m = sm == s_
+        a, b = np.sort(t0[m]), np.sort(t3[m])
+        gaps += int(np.clip(a[1:] - b[:-1], 0, None).sum()) + int(a[0] - start) + int(end - b[-1])
+    out["between_items_ms_per_cta"] = gaps / 1e6 / ctas
+    return out
+
+
+def run_trace(args):
+    import torch
+    import synth
+    from long_context_sparse_index_gb300 import build as libbuild
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    path = libbuild.build(trace=True)
+    lib = ctypes.CDLL(path)
+    i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    lib.dsa_index_topk_workspace.argtypes = [i64, i32, i32, i32, i32]
+    lib.dsa_index_topk_workspace.restype = sz
+    lib.dsa_index_topk.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp, sz, vp]
+    lib.dsa_trace_configure.argtypes = [vp, sz]
+    lib.dsa_sync_status.argtypes = [vp]
+    lib.dsa_last_error.restype = ctypes.c_char_p
+    wl = synth.WORKLOADS[args.workload]
+    q_idx, k_idx, w = synth.indexer_inputs(wl)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, wt = to(q_idx), to(k_idx), torch.from_numpy(w).to(dev)
+    del q_idx
+    S = wl.S
+    out = torch.empty((S, wl.topk), dtype=torch.int32, device=dev)
+    ws = torch.empty(lib.dsa_index_topk_workspace(S, wl.Hi, wl.Di, wl.chunk, wl.topk), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        rc = lib.dsa_index_topk(q.data_ptr(), k.data_ptr(), wt.data_ptr(), S, wl.Hi, wl.Di, wl.chunk, wl.topk, 0, S,
+                                out.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+        if rc != 0:
+            raise RuntimeError(lib.dsa_last_error().decode())
+
+    for _ in range(max(1, args.warmup)):
+        call()
+    rec_dtype = np.dtype([("kind_sm", np.uint32), ("chunk", np.uint32), ("t0", np.uint64), ("t1", np.uint64),
+                          ("t2", np.uint64), ("t3", np.uint64)])
+    pairs, _ = workload_counts(wl)
+    cap = int(pairs // (128 * 256) * 2 + 4 * S // 4 + 100000)
+    buf = torch.zeros(64 + cap * rec_dtype.itemsize, dtype=torch.uint8, device=dev)
+    if lib.dsa_trace_configure(buf.data_ptr(), buf.numel()) != 0:
+        raise RuntimeError("trace build did not accept the buffer")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    call()
+    ev1.record()
+    torch.cuda.synchronize()
+    lib.dsa_trace_configure(None, 0)
+    assert lib.dsa_sync_status(None) == 0, lib.dsa_last_error()
+    host = buf.cpu().numpy()
+    n = int(host[:8].view(np.uint64)[0])
+    rec = host[64:64 + min(n, cap) * rec_dtype.itemsize].view(rec_dtype)
+    summary = summarize_trace(rec, torch.cuda.get_device_properties(0).multi_processor_count)
+    summary.update({"workload": args.workload, "S": S, "call_ms": ev0.elapsed_time(ev1), "records_dropped": max(0, n - cap),
+                    "note": "DSA_ITEM_TRACE build (measurement only): epilogue thread 0 stamps each work item; "
+                            "fold = taking the item to the end of its fold over heads (waits on the MMAs included), "
+                            "wait = its dependency wait, rest = selection / append / store and publish"})
+    print(json.dumps({"trace": summary}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.trace:
+        run_trace(args)
     elif args.varlen or args.zigzag:
         run_layout(args)
     else:

@@ -69,15 +69,26 @@ typedef enum {
 } dsa_status_t;
 
 /* Bytes of workspace dsa_index_topk is best given for sequence length S, Hi
- * indexer heads of dim Di, query chunk `chunk` and `topk`: 256 B of kernel
- * words, the pooled keys (as a bf16 hi/lo pair, 256 B per pool) and a ring of
- * min(8, ceil(S/chunk)) chunk buffers of fp32 scores, which consecutive chunks
- * take in turn (each min(chunk, S) x ceil(S/4 to 256) x 4 B; 8 x 32 MiB at
- * S = 131072, chunk = 256).  dsa_index_topk also accepts a smaller workspace,
- * down to min(2, ceil(S/chunk)) buffers, and uses as many buffers as fit:
- * fewer buffers keep fewer chunks in flight (slower), with the same result.
- * Returns 0 for invalid arguments. */
+ * indexer heads of dim Di, query chunk `chunk` and `topk`: 512 B of kernel
+ * words; the pooled keys (as a bf16 hi/lo pair and as fp32, 512 B per pool);
+ * a list of rows for the fallback path (4 B per query) and its 64 scratch rows
+ * of scores (4 B per pool each); and a ring of min(8, ceil(S/chunk)) chunk
+ * slots, which consecutive chunks take in turn.  A slot holds, for each of
+ * min(chunk, S) rows (thresholds and counts padded to 128 rows), the scores of every sigma-th pool (sigma = max(2^
+ * floor(log2(topk/16)), 2^ceil(log2(ceil(S/4 / 4096)))), 32 at S = 131072,
+ * topk = 512), a threshold, a candidate count and up to `cap` candidates of
+ * 8 B (cap = 4096 for topk <= 512).  97 MB in all at S = 131072, chunk 256,
+ * topk 512; 388 MB at S = 1048576, chunk 512.  dsa_index_topk also accepts a
+ * smaller workspace, down to min(2, ceil(S/chunk)) slots, and uses as many
+ * slots as fit: fewer slots keep fewer chunks in flight (slower), with the
+ * same result.  Returns 0 for invalid arguments. */
 size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
+
+/* Bytes of an index workspace that holds exactly `slots` chunk slots (1 ..
+ * min(8, ceil(S/chunk))); dsa_index_topk_workspace() is this for the most
+ * slots, and the least workspace dsa_index_topk accepts is this for
+ * min(2, ceil(S/chunk)).  Returns 0 for invalid arguments. */
+size_t dsa_index_topk_workspace_slots(int64_t S, int Hi, int Di, int chunk, int topk, int slots);
 
 /*
  * Indexer + top-k  [SkyRL-1M §模型与瓶颈, §1 DSA 真稀疏; Anyscale, second
@@ -88,7 +99,7 @@ size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
  *  w         fp32 [S, Hi]      per-query head weights (any sign)
  *  S         sequence length, 1 <= S <= 2^31 - 1
  *  Hi, Di    indexer heads (1..64) and head dim (must be 64)
- *  chunk     queries scored per pass (>= 1): bounds the score scratch
+ *  chunk     queries scored per pass (>= 1): bounds the per-chunk scratch
  *  topk      pools kept per query (1..2048)
  *  q_begin, q_end   query range to process, 0 <= q_begin < q_end <= S; a
  *            shard of a sequence passes its own range (rows are independent)
@@ -96,12 +107,19 @@ size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk);
  *            pools in ascending order, then -1 padding (row i holds
  *            min(topk, floor(i/4)) pools)
  *  workspace, ws_bytes  device scratch: dsa_index_topk_workspace(S, Hi, Di,
- *            chunk, topk) bytes, or fewer down to the two-buffer minimum
- *            (see there)
+ *            chunk, topk) bytes, or fewer down to the two-slot minimum (see
+ *            there); 256-byte aligned
  *
+ * The score matrix is never stored.  Each row keeps, as candidates, the
+ * pools whose (score, -index) is at or above a threshold taken from the
+ * scores of every sigma-th pool; the row's top-k is then selected from its
+ * candidates, which is exact whenever at least topk pools are candidates.
+ * Rows that fall short (or overflow the candidate list) are recomputed in
+ * full by a fallback kernel; dsa_index_topk_stats() counts them.
  * Selection is exact with respect to the fp32 scores the kernels compute
  * (bf16 inputs, fp32 accumulation, pooled keys carried as a bf16 hi/lo pair
- * so the product keeps ~16 more bits than a single bf16 rounding).
+ * so the product keeps ~16 more bits than a single bf16 rounding; a fallback
+ * row's scores are fp32 dot products with the fp32 pooled keys).
  */
 dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
                             int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
@@ -253,13 +271,13 @@ dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const voi
  * library.)
  *
  * Same arguments, outputs and results as dsa_index_topk, but without a
- * workspace: the scratch lives in a fixed static device array of 18 MiB +
- * 256 B inside the library.  Sizes run when dsa_index_topk's least workspace
- * for them (two chunk buffers) fits in it -- S <= 32768 with chunk <= 256,
- * for example, or S = 65536 with chunk <= 64; other sizes return
- * DSA_ERR_WORKSPACE (see dsa_last_error()) and nothing runs.  At the largest
- * sizes that fit, only two chunks are in flight, so the call is slower than
- * dsa_index_topk with its recommended workspace (same result).
+ * workspace: the scratch lives in a fixed static device array of 32 MiB
+ * inside the library.  Sizes run when dsa_index_topk's least workspace for
+ * them (two chunk slots) fits in it -- every S <= 32768 with chunk <= 256 and
+ * topk <= 512, for example; other sizes return DSA_ERR_WORKSPACE (see
+ * dsa_last_error()) and nothing runs.  At the largest sizes that fit, only
+ * two chunks are in flight, so the call is slower than dsa_index_topk with
+ * its recommended workspace (same result).
  * Under CUDA's default lazy module loading a device reserves the array when
  * the library's module holding it is first loaded there, which happens in
  * the first call on that device (that call looks up the array's device
@@ -280,8 +298,9 @@ dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const 
  * Counters of the last dsa_index_topk call that used `workspace` (a
  * measurement helper; no part of the layer's arithmetic).  Synchronises
  * `stream` (the stream of that call), then writes up to `max_stats` values:
- *   stats[0]  query rows whose top-k had to take the full-row path (the
- *             fast path's threshold guess did not hold for the row)
+ *   stats[0]  query rows whose candidates could not certify the top-k
+ *             (fewer than topk, or more than the list holds), so the
+ *             fallback kernel recomputed all their scores
  * Returns the number of values written, or -1 (with dsa_last_error()) for a
  * null or short workspace or a CUDA error.
  */
@@ -331,6 +350,21 @@ const char* dsa_version(void);
  * Kind 2 adds into the buffer's contents.
  */
 double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream);
+
+/*
+ * Item trace of the persistent indexer (measurement helper; only the trace
+ * build of the library, libdsa_trace.so, compiled with DSA_ITEM_TRACE, records
+ * anything -- the default build returns -1).  `buf` is a device buffer of
+ * `bytes`: a 64-byte header whose first 8 bytes count the records (the
+ * caller zeroes it before the call it wants traced), then records of 40 bytes
+ * {uint32 kind | sm << 8, uint32 chunk, uint64 t0, t1, t2, t3}: the
+ * globaltimer (ns) when the epilogue took the item, ended its fold over heads
+ * (= t0 for row items), ended its dependency wait, and published it.  kind:
+ * 0 sample tile, 1 thresholds, 2 indexer tile, 3 top-k rows.  Records past
+ * the buffer are dropped (the count keeps counting).  NULL stops tracing.
+ * Returns 0, or -1.
+ */
+int dsa_trace_configure(void* buf, size_t bytes);
 
 void dsa_profile_enable(int on);
 int dsa_profile_read(char* names, int name_len, double* ms, int64_t* launches, int max_kernels);

@@ -30,7 +30,7 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_zigzag_ranges", "dsa_index_topk_varlen_workspace", "dsa_index_topk_varlen",
             "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen",
             "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic",
-            "dsa_index_topk_stats", "dsa_measure_l2")
+            "dsa_index_topk_stats", "dsa_measure_l2", "dsa_index_topk_workspace_slots", "dsa_trace_configure")
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +53,8 @@ def load():
             i64, i32, vp, sz, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
             lib.dsa_index_topk_workspace.argtypes = [i64, i32, i32, i32, i32]
             lib.dsa_index_topk_workspace.restype = sz
+            lib.dsa_index_topk_workspace_slots.argtypes = [i64, i32, i32, i32, i32, i32]
+            lib.dsa_index_topk_workspace_slots.restype = sz
             lib.dsa_index_topk.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp, sz, vp]
             lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
             lib.dsa_sparse_attn_bwd_workspace.argtypes = [i64, i32, i32]
@@ -133,8 +135,11 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be a contiguous {ndim}-d tensor (got shape {tuple(t.shape)})")
 
 
-def index_topk_workspace_size(S: int, Hi: int, Di: int, chunk: int, topk: int) -> int:
-    return int(load().dsa_index_topk_workspace(S, Hi, Di, chunk, topk))
+def index_topk_workspace_size(S: int, Hi: int, Di: int, chunk: int, topk: int, slots: int | None = None) -> int:
+    """Recommended index workspace bytes, or the bytes for exactly `slots` chunk slots."""
+    if slots is None:
+        return int(load().dsa_index_topk_workspace(S, Hi, Di, chunk, topk))
+    return int(load().dsa_index_topk_workspace_slots(S, Hi, Di, chunk, topk, slots))
 
 
 def sparse_attn_bwd_workspace_size(S: int, Hq: int, D: int) -> int:
@@ -408,7 +413,7 @@ def index_topk_stats(workspace: torch.Tensor, stream=None) -> dict:
                                  _stream_handle(stream))
     if n < 0:
         raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
-    names = ("general_path_rows",)
+    names = ("fallback_rows",)
     return {names[j]: int(out[j]) for j in range(min(n, len(names)))}
 
 

@@ -44,7 +44,7 @@ constexpr int kD = 128;
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxHi = 64;
 constexpr int64_t kPoolTile = 256;
-constexpr size_t kSyncBytes = 256;  // the fused kernel's global words, first in the index workspace
+constexpr size_t kSyncBytes = 512;  // the fused kernel's global words, first in the index workspace
 static_assert(dsa::kIndexSyncWords * 8 <= kSyncBytes, "sync words");
 
 dsa_status_t fail(dsa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -143,6 +143,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// ---------------------------------------------------------------- item trace (measurement build)
+#ifdef DSA_ITEM_TRACE
+std::mutex g_trace_mu;
+void* g_trace_buf = nullptr;
+size_t g_trace_bytes = 0;
+#endif
+
 // ---------------------------------------------------------------- launch accounting
 std::atomic<int64_t> g_launches{0};
 std::atomic<int> g_profiling{0};
@@ -175,23 +182,91 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch, int 
   return e;
 }
 
-// Score buffers in the index workspace: a ring of chunk buffers, at least
-// min(2, chunks) and at most dsa::kMaxBufs.  The count only changes how many
-// chunks are in flight, never the result.
+// The index workspace: kernel words, pooled keys (bf16 hi/lo and fp32), the
+// fallback kernel's row list and scratch rows, then a ring of per-chunk slots
+// (sampled scores, thresholds, candidate counts and candidate lists), at least
+// min(2, chunks) and at most dsa::kMaxBufs.  The slot count only changes how
+// many chunks are in flight, never the result.
 int index_max_bufs(int64_t S, int chunk) {
   const int64_t nchunks = (S + chunk - 1) / chunk;
   return static_cast<int>(nchunks < dsa::kMaxBufs ? nchunks : dsa::kMaxBufs);
 }
 int index_min_bufs(int64_t S, int chunk) { return index_max_bufs(S, chunk) < 2 ? index_max_bufs(S, chunk) : 2; }
 
-size_t index_ws_khat(int64_t S) { return round_up(static_cast<size_t>(S / 4 > 0 ? S / 4 : 1) * 2 * kDi * 2, 256); }
-int64_t pools_padded(int64_t S) { return ((S / 4 + kPoolTile - 1) / kPoolTile) * kPoolTile + (S / 4 == 0 ? kPoolTile : 0); }
-size_t index_buf_bytes(int64_t S, int chunk) {
-  const int64_t rows = chunk < S ? chunk : S;
-  return round_up(static_cast<size_t>(rows) * pools_padded(S) * sizeof(float), 256);
+int64_t pow2_ceil(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
 }
-size_t index_ws_bytes(int64_t S, int chunk, int nbuf) {
-  return kSyncBytes + index_ws_khat(S) + static_cast<size_t>(nbuf) * index_buf_bytes(S, chunk);
+int64_t pow2_floor(int64_t x) {
+  int64_t p = 1;
+  while (2 * p <= x) p <<= 1;
+  return p;
+}
+
+constexpr int kCandBase = 4096;  // rows with at most this many pools keep every pool as a candidate
+constexpr int kFallbackCtas = 64;
+
+// Sampling and candidate sizes.  sigma: every sigma-th pool is sampled, with
+// at least 16 samples expected above a row's k-th largest score (sigma <=
+// topk/16) and at most kCandBase samples per row.  A threshold at the rsel-th
+// largest sample leaves about c = rsel * sigma pools at or above it; c is
+// chosen so that c - 4 sqrt(sigma c) = topk (fewer than topk candidates is a
+// four-sigma event of the sampling), and cap holds c + 4 sqrt(sigma c).
+dsa::IndexPlan index_plan(int64_t S, int chunk, int topk) {
+  dsa::IndexPlan pl;
+  pl.P = S / 4;
+  pl.Ppad = ((pl.P + kPoolTile - 1) / kPoolTile) * kPoolTile + (pl.P == 0 ? kPoolTile : 0);
+  const int64_t sig_min = pow2_floor(topk / 16 > 1 ? topk / 16 : 1);
+  const int64_t sig_p = pow2_ceil((pl.P + kCandBase - 1) / kCandBase);
+  pl.sigma = static_cast<int>(sig_min > sig_p ? sig_min : sig_p);
+  const double sg = pl.sigma;
+  const double rc = 2.0 * std::sqrt(sg) + std::sqrt(4.0 * sg + topk);
+  const double c = rc * rc;
+  pl.rsel = static_cast<int>(std::ceil(c / sg));
+  const int64_t hold = pow2_ceil(static_cast<int64_t>(std::ceil(c + 4.0 * std::sqrt(sg * c))));
+  pl.cap = static_cast<int>(hold > kCandBase ? hold : kCandBase);
+  const int64_t G = (pl.P + pl.sigma - 1) / pl.sigma;
+  pl.samp_ld = ((G + kPoolTile - 1) / kPoolTile) * kPoolTile + (G == 0 ? kPoolTile : 0);
+  pl.slot_rows = chunk < S ? chunk : S;
+  pl.thr_ld = (pl.slot_rows + 127) / 128 * 128;
+  pl.samp_slot = pl.slot_rows * pl.samp_ld;
+  pl.cand_slot = pl.slot_rows * pl.cap;
+  pl.fb_ctas = kFallbackCtas;
+  pl.fb_ld = pl.Ppad;
+  return pl;
+}
+
+struct IndexLayout {
+  size_t khat2, khat32, fb_rows, fb_scratch, samples, thr, cnt, cands, total;
+};
+
+IndexLayout index_layout(int64_t S, const dsa::IndexPlan& pl, int nbuf) {
+  IndexLayout L;
+  const size_t P1 = static_cast<size_t>(pl.P > 0 ? pl.P : 1);
+  size_t off = kSyncBytes;
+  L.khat2 = off;
+  off += round_up(P1 * 2 * kDi * 2, 256);
+  L.khat32 = off;
+  off += round_up(P1 * kDi * 4, 256);
+  L.fb_rows = off;
+  off += round_up(static_cast<size_t>(S) * 4, 256);
+  L.fb_scratch = off;
+  off += round_up(static_cast<size_t>(pl.fb_ctas) * pl.fb_ld * 4, 256);
+  L.samples = off;
+  off += round_up(static_cast<size_t>(nbuf) * pl.samp_slot * 4, 256);
+  L.thr = off;
+  off += round_up(static_cast<size_t>(nbuf) * pl.thr_ld * 8, 256);
+  L.cnt = off;
+  off += round_up(static_cast<size_t>(nbuf) * pl.thr_ld * 4, 256);
+  L.cands = off;
+  off += round_up(static_cast<size_t>(nbuf) * pl.cand_slot * 8, 256);
+  L.total = off;
+  return L;
+}
+
+size_t index_ws_bytes(int64_t S, int chunk, int topk, int nbuf) {
+  return index_layout(S, index_plan(S, chunk, topk), nbuf).total;
 }
 
 }  // namespace
@@ -222,9 +297,9 @@ unsigned long long current_context_id() {
   if (get_current(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS) return 0;
   return id;
 }
-size_t index_topk_min_workspace(int64_t S, int chunk) {
-  if (S < 1 || chunk < 1) return 0;
-  return index_ws_bytes(S, chunk, index_min_bufs(S, chunk));
+size_t index_topk_min_workspace(int64_t S, int chunk, int topk) {
+  if (S < 1 || chunk < 1 || topk < 1) return 0;
+  return index_ws_bytes(S, chunk, topk, index_min_bufs(S, chunk));
 }
 }  // namespace dsa
 
@@ -236,7 +311,12 @@ const char* dsa_version(void) { return "libdsa 0.1.0 (sm_103a)"; }
 
 size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk) {
   if (S < 1 || Hi < 1 || Di < 1 || chunk < 1 || topk < 1) return 0;
-  return index_ws_bytes(S, chunk, index_max_bufs(S, chunk));
+  return index_ws_bytes(S, chunk, topk, index_max_bufs(S, chunk));
+}
+
+size_t dsa_index_topk_workspace_slots(int64_t S, int Hi, int Di, int chunk, int topk, int slots) {
+  if (S < 1 || Hi < 1 || Di < 1 || chunk < 1 || topk < 1 || slots < 1 || slots > index_max_bufs(S, chunk)) return 0;
+  return index_ws_bytes(S, chunk, topk, slots);
 }
 
 dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
@@ -256,7 +336,7 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
   if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Di=%d unsupported (kernels implement Di=64)", Di);
   if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Hi=%d unsupported (max %d)", Hi, kMaxHi);
   if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: topk=%d unsupported (max %d)", topk, kMaxTopk);
-  const size_t need = index_ws_bytes(S, chunk, index_min_bufs(S, chunk));
+  const size_t need = index_ws_bytes(S, chunk, topk, index_min_bufs(S, chunk));
   if (!workspace || ws_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "dsa_index_topk: workspace of at least %zu bytes needed (%zu recommended), %zu given",
                 need, dsa_index_topk_workspace(S, Hi, Di, chunk, topk), workspace ? ws_bytes : (size_t)0);
@@ -267,19 +347,41 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
   dsa_status_t st = make_ctx(stream, &ctx);
   if (st != DSA_OK) return st;
 
-  const int64_t P = S / 4;
-  const int64_t ld = pools_padded(S);
+  const dsa::IndexPlan pl = index_plan(S, chunk, topk);
+  const int64_t P = pl.P;
+  int nbuf = index_min_bufs(S, chunk);  // as many chunk slots as the workspace holds
+  while (nbuf < index_max_bufs(S, chunk) && index_layout(S, pl, nbuf + 1).total <= ws_bytes) ++nbuf;
+  const IndexLayout L = index_layout(S, pl, nbuf);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  unsigned long long* sync_words = reinterpret_cast<unsigned long long*>(ws);
-  void* khat2 = ws + kSyncBytes;
-  float* scores = reinterpret_cast<float*>(ws + kSyncBytes + index_ws_khat(S));
-  const int64_t buf_stride = static_cast<int64_t>(index_buf_bytes(S, chunk) / sizeof(float));
-  int nbuf = index_min_bufs(S, chunk);  // as many chunk buffers as the workspace holds
-  while (nbuf < index_max_bufs(S, chunk) && index_ws_bytes(S, chunk, nbuf + 1) <= ws_bytes) ++nbuf;
+  dsa::IndexBuffers b;
+  b.sync = reinterpret_cast<unsigned long long*>(ws);
+  b.khat2 = ws + L.khat2;
+  b.khat32 = reinterpret_cast<float*>(ws + L.khat32);
+  b.fb_rows = reinterpret_cast<int32_t*>(ws + L.fb_rows);
+  b.fb_scratch = reinterpret_cast<float*>(ws + L.fb_scratch);
+  b.samples = reinterpret_cast<float*>(ws + L.samples);
+  b.thr = reinterpret_cast<uint2*>(ws + L.thr);
+  b.cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
+  b.cands = reinterpret_cast<uint2*>(ws + L.cands);
+  b.nbuf = nbuf;
+  b.trace = nullptr;
+  b.trace_count = nullptr;
+  b.trace_cap = 0;
+#ifdef DSA_ITEM_TRACE
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (g_trace_buf != nullptr) {
+      b.trace_count = static_cast<unsigned long long*>(g_trace_buf);
+      b.trace = reinterpret_cast<dsa::IndexTraceRec*>(static_cast<uint8_t*>(g_trace_buf) + 64);
+      b.trace_cap = static_cast<int64_t>((g_trace_bytes - 64) / sizeof(dsa::IndexTraceRec));
+    }
+  }
+#endif
 
-  CUtensorMap q_map, k_map;
+  CUtensorMap q_map, k_map, s_map;
   memset(&q_map, 0, sizeof(q_map));
   memset(&k_map, 0, sizeof(k_map));
+  memset(&s_map, 0, sizeof(s_map));
   const bool need_indexer = (q_end - 1) / 4 > topk;  // some row has more eligible pools than topk
   if (need_indexer) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
@@ -299,23 +401,42 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
       cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * kDi) * 2};
       cuuint32_t box[2] = {static_cast<cuuint32_t>(kDi), static_cast<cuuint32_t>(kPoolTile)};
       cuuint32_t estr[2] = {1u, 1u};
-      CUresult r = enc(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, khat2, dims, strides, box, estr,
+      CUresult r = enc(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b.khat2, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "dsa_index_topk: pooled-key tensor map (CUresult %d)", (int)r);
     }
+    {
+      // every sigma-th pooled key: row g of this map is pool g * sigma
+      const int64_t G = (P + pl.sigma - 1) / pl.sigma;
+      cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * kDi), static_cast<cuuint64_t>(G)};
+      cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * kDi) * 2 * static_cast<cuuint64_t>(pl.sigma)};
+      cuuint32_t box[2] = {static_cast<cuuint32_t>(kDi), static_cast<cuuint32_t>(kPoolTile)};
+      cuuint32_t estr[2] = {1u, 1u};
+      CUresult r = enc(&s_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b.khat2, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "dsa_index_topk: sampled-key tensor map (CUresult %d)", (int)r);
+    }
   }
   // pool_keys also zeroes the fused kernel's global words, so it always runs
-  cudaError_t e = timed_launch("pool_keys", ctx.stream,
-                               [&] { return dsa::launch_pool_keys(k_idx, P, khat2, sync_words, ctx); });
+  cudaError_t e = timed_launch("pool_keys", ctx.stream, [&] {
+    return dsa::launch_pool_keys(k_idx, P, b.khat2, b.khat32, b.sync, ctx);
+  });
   if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: pool_keys launch");
-  // one persistent kernel walks every chunk: indexer tiles and top-k rows
-  // (when no row has more than topk pools there are only rows, and no tensor map is read)
+  // one persistent kernel walks every chunk: samples, thresholds, indexer
+  // tiles and top-k rows (when no row has more than topk pools there are only
+  // rows, and no tensor map is read); then the rows it could not certify
   e = timed_launch("index_topk", ctx.stream, [&] {
-    return dsa::launch_index_topk(q_map, k_map, w, scores, ld, buf_stride, nbuf, q_begin, q_end, chunk, Hi, topk,
-                                  pool_idx, sync_words, ctx);
+    return dsa::launch_index_topk(q_map, k_map, s_map, pl, b, w, q_begin, q_end, chunk, Hi, topk, pool_idx, ctx);
   });
   if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: index_topk launch");
+  if (need_indexer) {
+    e = timed_launch("index_fallback", ctx.stream, [&] {
+      return dsa::launch_index_fallback(q_idx, pl, b, w, q_begin, Hi, topk, pool_idx, ctx);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: index_fallback launch");
+  }
   return DSA_OK;
 }
 
@@ -665,8 +786,22 @@ int dsa_index_topk_stats(const void* workspace, size_t ws_bytes, int64_t* stats,
     cuda_fail(e, "dsa_index_topk_stats: read counters");
     return -1;
   }
-  stats[0] = static_cast<int64_t>(words[dsa::kIndexGeneralRowsWord]);
+  stats[0] = static_cast<int64_t>(words[dsa::kIndexFallbackRowsWord]);
   return 1;
+}
+
+int dsa_trace_configure(void* buf, size_t bytes) {
+#ifdef DSA_ITEM_TRACE
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (buf != nullptr && bytes < 64 + sizeof(dsa::IndexTraceRec)) return -1;
+  g_trace_buf = buf;
+  g_trace_bytes = buf ? bytes : 0;
+  return 0;
+#else
+  (void)buf, (void)bytes;
+  fail(DSA_ERR_UNSUPPORTED, "dsa_trace_configure: this library was built without DSA_ITEM_TRACE");
+  return -1;
+#endif
 }
 
 void dsa_profile_enable(int on) { g_profiling.store(on ? 1 : 0); }

@@ -53,28 +53,70 @@ cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(KArgs...), dim3 grid,
 }
 
 // Global words of the fused indexer + top-k kernel (64-bit each), at the start
-// of its workspace, and its most score buffers.
-constexpr int kIndexSyncWords = 24;
+// of its workspace, and its most per-chunk buffer slots.
+constexpr int kIndexSyncWords = 40;
 constexpr int kMaxBufs = 8;
-// word counting the rows whose top-k took the general (full-row) path; it
-// survives the call (the next call's key pooling zeroes it)
-constexpr int kIndexGeneralRowsWord = 20;
+// word counting the rows listed for the fallback kernel (their candidates
+// could not certify the top-k); it survives the call (the next call's key
+// pooling zeroes it)
+constexpr int kIndexFallbackRowsWord = 36;
 
-// Pooled indexer keys: khat2 [P, 128] bf16, hi in columns 0..63, lo in 64..127.
+// Sizes of the indexer's per-chunk buffers and scratch, from S, chunk and topk.
+struct IndexPlan {
+  int64_t P;          // selectable pools, floor(S/4)
+  int64_t Ppad;       // P rounded up to 256 (at least 256)
+  int sigma;          // sample stride in pools (power of two)
+  int rsel;           // the row threshold is the rsel-th largest sample
+  int cap;            // candidate slots per row
+  int64_t samp_ld;    // sampled scores per row: ceil(P / sigma) rounded up to 256
+  int64_t slot_rows;  // rows per slot: min(chunk, S)
+  int64_t thr_ld;     // thresholds and counts per slot: slot_rows rounded up to 128
+  int64_t samp_slot;  // floats of samples per slot
+  int64_t cand_slot;  // candidates per slot
+  int fb_ctas;        // CTAs of the fallback kernel
+  int64_t fb_ld;      // floats per fallback scratch row (Ppad)
+};
+// One work item of the persistent indexer, recorded by the item-trace build
+// (DSA_ITEM_TRACE): globaltimer stamps when its epilogue took it (t0), when
+// the fold over heads ended (t1; = t0 for row items), when its dependency wait
+// ended (t2) and when it was published (t3).
+struct IndexTraceRec {
+  uint32_t kind_sm;   // item kind in bits 0..7, SM id in bits 8..
+  uint32_t chunk;
+  uint64_t t0, t1, t2, t3;
+};
+struct IndexBuffers {
+  unsigned long long* sync;
+  IndexTraceRec* trace;            // item-trace build only: records, and
+  unsigned long long* trace_count; // their count (caller zeroes it); null: none
+  int64_t trace_cap;
+  void* khat2;        // [P, 128] bf16: hi in columns 0..63, lo in 64..127
+  float* khat32;      // [P, 64] fp32
+  float* samples;     // [nbuf][slot_rows][samp_ld]
+  uint2* thr;         // [nbuf][thr_ld]
+  unsigned* cnt;      // [nbuf][thr_ld]
+  uint2* cands;       // [nbuf][slot_rows][cap]
+  int nbuf;
+  int32_t* fb_rows;   // [rows of the call]
+  float* fb_scratch;  // [fb_ctas][fb_ld]
+};
+
+// Pooled indexer keys: khat2 [P, 128] bf16 (hi, lo) and khat32 [P, 64] fp32.
 // Also zeroes the kIndexSyncWords words at sync_words (always launch it, even
 // with P == 0, before launch_index_topk).
-cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, unsigned long long* sync_words,
+cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, float* khat32, unsigned long long* sync_words,
                              const LaunchCtx& ctx);
 
 // Indexer scores and per-row top-k for query rows [q_begin, q_end), in query
 // chunks of `chunk` rows, as one persistent cooperative kernel (one CTA per
-// SM).  scores holds nbuf chunk buffers (`chunk` rows x ld floats each,
-// buf_stride floats apart; chunk c uses buffer c % nbuf); pool_idx row r is
-// query q_begin + r.
-cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
-                              int64_t ld, int64_t buf_stride, int nbuf, int64_t q_begin, int64_t q_end, int chunk,
-                              int Hi, int topk, int32_t* pool_idx, unsigned long long* sync_words,
-                              const LaunchCtx& ctx);
+// SM); chunk c uses slot c % b.nbuf of the per-chunk buffers; pool_idx row r
+// is query q_begin + r.  Rows it cannot certify are listed in b.fb_rows for
+// launch_index_fallback, which must follow it on the same stream.
+cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_map, const CUtensorMap& samp_map,
+                              const IndexPlan& pl, const IndexBuffers& b, const float* w, int64_t q_begin,
+                              int64_t q_end, int chunk, int Hi, int topk, int32_t* pool_idx, const LaunchCtx& ctx);
+cudaError_t launch_index_fallback(const void* q_idx, const IndexPlan& pl, const IndexBuffers& b, const float* w,
+                                  int64_t q_begin, int Hi, int topk, int32_t* pool_idx, const LaunchCtx& ctx);
 size_t index_topk_smem_bytes();
 
 // Queries [q_begin, q_end) (global positions); q, pool_idx, o and lse hold

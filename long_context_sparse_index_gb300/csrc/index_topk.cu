@@ -1,5 +1,7 @@
 // index_topk.cu -- pooled indexer keys, and the causal pooled indexer with
-// its per-query top-k as one persistent kernel.
+// its per-query top-k as one persistent kernel that never stores the score
+// matrix: each tile's scores are compared in the epilogue against the row's
+// threshold, and only the pools at or above it are kept, as candidates.
 //
 // [SkyRL-1M §模型与瓶颈] the indexer scores every query against every earlier
 // 4-token key pool; [§1 DSA 真稀疏; Anyscale, second lesson (the indexer)] it
@@ -9,40 +11,52 @@
 //   Khat_p     = ((k[4p] + k[4p+1]) + (k[4p+2] + k[4p+3])) * 0.25    (fp32)
 //   score(i,p) = sum_h w[i,h] * ReLU(q_idx[i,h,:] . Khat_p)
 //
-// Work items.  A chunk's indexer work is its (128-query x 256-pool) tiles; its
-// top-k work is its query rows, four to an item.  Items are handed out in the
-// order
-//     tiles(0), tiles(1), tiles(2), tiles(3), rows(0), tiles(4), rows(1), ...
-// (a chunk's rows `lag` chunks after its tiles, so that its tiles are done;
-// lag = 3 here, less when there are fewer than four score buffers)
-// from one global ticket counter to one CTA per SM (cooperative launch, so
-// every CTA is resident).  A CTA processes its items in ticket order:
-//   tile    TMA brings the 64 KB Khat hi/lo tile and, per head h, the q_idx
-//           tile of head h; one 128x256x128 bf16 tcgen05 MMA chain per head
-//           accumulates q_h . [Khat_hi ; Khat_lo] in TMEM (Khat kept as a bf16
-//           hi/lo pair, so the product keeps ~16 more mantissa bits than one
-//           bf16 rounding); 16 epilogue warps fold ReLU, the head weight and
-//           the sum over heads into registers while the next head's MMA fills
-//           the other TMEM buffer; the tile's scores go to the chunk's score
-//           buffer (a ring of up to eight chunk buffers);
-//   rows    the same 16 warps split into four groups of four; each group
-//           selects one row's top-k (topk_row.cuh), once every tile of its
-//           chunk has been stored.  Handing out a row item brings the scores
-//           of the row item two tickets later into L2.
-// Dependencies run only from later tickets to earlier ones -- rows wait for
-// their chunk's tiles, and a tile of chunk c waits, before it stores, for the
-// rows of chunk c-nbuf that read the same buffer -- so the lowest unfinished
-// ticket can always proceed (rows of chunk c-nbuf are handed out in step
-// c-nbuf+lag < c).  With two buffers, tiles waited on rows handed out just
-// before them (84 us per tile on average at S = 131072); more buffers put
-// chunks of work between a buffer's readers and its next writers.
-// There is no barrier per chunk: a CTA that has finished its part of one
-// chunk takes the next chunk's work, so SMs do not idle on a chunk whose tile
-// count is not a multiple of the SM count, and the chunk size only bounds the
-// score scratch.
+// Pools are ranked by the composite key (score desc, index asc).  For query i
+// with n = floor(i/4) eligible pools (n > topk; shorter rows keep all pools):
+//   * n <= cap: every eligible pool is a candidate;
+//   * n > cap: the threshold is the rsel-th largest composite key among the
+//     row's sampled pools (every sigma-th pool); about rsel * sigma pools of
+//     the row lie above it, which is more than topk and fewer than cap.
+// The row's candidates are the pools at or above its threshold.  When there
+// are at least topk of them (and no more than cap), the row's top-k is among
+// them, and selecting from the candidates is exact; otherwise the row is
+// listed for the fallback kernel, which recomputes all its scores.
+//
+// Work items, for each query chunk c (rows row0 .. row0+nrows-1):
+//   sample  (128-query block, 256 sampled pools): the block's scores against
+//           every sigma-th pool, stored in the chunk's sample buffer;
+//   thresh  four rows: each row's threshold from its samples; zeroes its
+//           candidate count;
+//   tile    (128-query block, 256-pool tile): the indexer scores; the
+//           epilogue appends the row's pools at or above its threshold to
+//           its candidate list (slots from one atomic add per thread);
+//   rows    four rows: each row's top-k from its candidate list.
+// A sample or tile item: TMA brings the 64 KB Khat hi/lo tile and, per head
+// h, the q_idx tile of head h; one 128x256x128 bf16 tcgen05 MMA chain per head
+// accumulates q_h . [Khat_hi ; Khat_lo] in TMEM (Khat as a bf16 hi/lo pair:
+// the product keeps ~16 more mantissa bits than one bf16 rounding); 16
+// epilogue warps fold ReLU, the head weight and the sum over heads into
+// registers while the next head's MMA fills the other TMEM buffer.  For
+// thresh and rows items the 16 warps form four 128-thread groups, one row
+// each (topk_cand.cuh).
+//
+// Items come from one global ticket counter, step by step; step s holds
+//     sample(s), thresh(s-1), tile(s-2), rows(s-2-lag)
+// and chunk c uses slot c % nbuf of a ring of per-chunk buffers (samples,
+// thresholds, candidate counts and lists).  Every wait is on an earlier
+// ticket: a sample item waits (before storing) for the thresh items of chunk
+// c-nbuf to be done reading the slot's samples; thresh(c) waits for the
+// samples of c and for the rows of c-nbuf (done with the slot's candidates,
+// step c-nbuf+2+lag <= c since lag <= nbuf-2); a tile waits (before
+// appending) for thresh(c); rows(c) wait for the tiles of c.  With one CTA
+// per SM (cooperative launch: all resident), the lowest unfinished ticket can
+// always proceed.  There is no barrier per chunk, and the chunk size only
+// bounds the per-chunk buffers.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
+#include "topk_cand.cuh"
 #include "topk_row.cuh"
+#include "topk_warp.cuh"
 
 namespace dsa {
 namespace {
@@ -52,63 +66,90 @@ constexpr int kBN = 256;           // pools per tile (TMEM columns per buffer)
 constexpr int kDi = 64;            // indexer head dim
 constexpr int kAStages = 4;
 constexpr int kItems = 2;          // work-item ring between the roles (the item in work + one prefetched)
-constexpr int kRowsPerItem = 4;    // one per top-k group
-constexpr int kPrefetchItems = 2;  // row items whose scores are brought into L2 ahead of their turn
-constexpr int kMaxRowLag = 3;      // a chunk's rows are handed out after the tiles of the chunk this far ahead
+constexpr int kRowsPerGroupItem = 4;   // topk > 512: one row per 128-thread group
+constexpr int kRowsPerWarpItem = 16;   // topk <= 512: one row per epilogue warp
+constexpr int kMaxLag = 2;         // rows of chunk c come in step c + 2 + lag
 constexpr uint32_t kABytes = kBM * kDi * 2;        // 16 KB: q_idx tile of one head
 constexpr uint32_t kBHalf = kBN * kDi * 2;         // 32 KB: Khat hi (or lo) tile
 constexpr uint32_t kBBytes = 2 * kBHalf;           // 64 KB, one stage
 constexpr int kEpiWarps = 16;                      // 4 TMEM lane quarters x 4 column quarters
 constexpr int kEpiCols = kBN / 4;                  // 64 columns per epilogue thread
-constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, 16 epilogue warps
+constexpr int kEpiWarp0 = 3;                       // first epilogue warp
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);  // TMA warp, MMA warp, scheduler warp, 16 epilogue warps
 constexpr uint32_t kTmemCols = 512;                // 2 accumulators x 256 columns
 constexpr uint32_t kCtlOff = kBBytes + kAStages * kABytes;
 constexpr uint32_t kCtlBytes = 512;
-constexpr uint32_t kTopkOff = kCtlOff + kCtlBytes;
-constexpr size_t kSmemBytes = 1024 + kTopkOff + kRowsPerItem * sizeof(topk::Smem);
-static_assert(kRowsPerItem * topk::kGT == 32 * kEpiWarps, "the epilogue warps form the top-k groups");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(sizeof(topk::Smem) % 16 == 0, "top-k group buffers stay 16-byte aligned");
-
-constexpr int kEpiBar = 1;   // named barrier of the 512 epilogue threads; the groups use 2..5
-// Tile stores go through a per-warp staging tile (32 rows x 32 columns, rows
-// padded to 36 floats) in the top-k buffers, which tiles do not otherwise use,
-// so that each warp store covers four rows x 128 contiguous bytes.
+constexpr uint32_t kThrOff = kCtlOff + kCtlBytes;   // thresholds of a tile's rows, per ring slot
+constexpr uint32_t kThrBytes = kItems * kBM * 8;
+constexpr uint32_t kGrpOff = kThrOff + kThrBytes;
+// Sample stores go through a per-warp staging tile (32 rows x 32 columns,
+// rows padded to 36 floats), so that each warp store covers four rows x 128
+// contiguous bytes; it shares space with the groups' selection buffers.
 constexpr int kStgLd = 36;
 constexpr uint32_t kStgBytes = 32 * kStgLd * 4;
-static_assert(kEpiWarps * kStgBytes <= kRowsPerItem * sizeof(topk::Smem), "staging fits the top-k buffers");
+constexpr size_t cmax(size_t x, size_t y) { return x > y ? x : y; }
+constexpr size_t kGrpBytes =
+    cmax(cmax(kRowsPerGroupItem * sizeof(cand::Smem), kEpiWarps * kStgBytes), kEpiWarps * sizeof(wsel::Smem));
+constexpr size_t kSmemBytes = 1024 + kGrpOff + kGrpBytes;
+static_assert(kRowsPerGroupItem * topk::kGT == 32 * kEpiWarps, "the epilogue warps form the top-k groups");
+static_assert(kRowsPerWarpItem == kEpiWarps, "one row per epilogue warp");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(sizeof(cand::Smem) % 16 == 0, "group buffers stay 16-byte aligned");
+
+constexpr int kEpiBar = 1;  // named barrier of the 512 epilogue threads; the groups use 2..5
 
 // control block offsets (bytes from kCtlOff)
 constexpr uint32_t kBarAFull = 0, kBarAEmpty = 32, kBarBFull = 64, kBarBEmpty = 72, kBarAccFull = 80,
-                   kBarAccEmpty = 96, kBarDrain = 112, kBarItemFull = 120, kBarItemEmpty = 152;
-constexpr uint32_t kTmemSlot = 184, kAbort = 188, kGroupOk = 192, kWaitOk = 196, kItemData = 256;  // 4 x 16 B
+                   kBarAccEmpty = 96, kBarDrain = 112, kBarItemFull = 120, kBarItemEmpty = 136, kBarDeps = 152,
+                   kBarDone = 168;
+constexpr uint32_t kTmemSlot = 184, kAbort = 188, kGroupOk = 192, kWaitOk = 196, kItemData = 256;  // kItems x 16 B
+static_assert(kItems == 2 && kItemData + kItems * 16 <= kCtlBytes, "control block");
 
-enum : int { kItemTile = 0, kItemRows = 1, kItemEnd = 2 };
+enum : int { kItemSample = 0, kItemThresh = 1, kItemTile = 2, kItemRows = 3, kItemEnd = 4 };
 struct Item {
   int kind;
   int chunk;
-  int a;  // tile: qb   rows: first row within the chunk
-  int b;  // tile: pb   rows: number of rows (1..4)
+  int a;  // sample, tile: qb        thresh, rows: first row within the chunk
+  int b;  // sample: sample tile     tile: pb      thresh, rows: number of rows (1..4)
 };
 
 // global 64-bit words, zeroed by pool_keys_kernel before each launch; the
-// done counters are per buffer (chunk c uses buffer c % nbuf) and cumulative
-enum : int { kTicket = 0, kTilesDone = 1 /* kMaxBufs words */, kRowsDone = 1 + kMaxBufs, kGAbort = 1 + 2 * kMaxBufs };
-static_assert(kGAbort < kIndexSyncWords && kIndexGeneralRowsWord > kGAbort, "global words");
+// done counters are per slot (chunk c uses slot c % nbuf) and cumulative
+enum : int {
+  kTicket = 0,
+  kSampDone = 1,                 // kMaxBufs words: sample tiles stored
+  kThrDone = 1 + kMaxBufs,       // rows whose threshold is set
+  kTilesDone = 1 + 2 * kMaxBufs, // tiles appended
+  kRowsDone = 1 + 3 * kMaxBufs,  // rows selected
+  kGAbort = 1 + 4 * kMaxBufs
+};
+static_assert(kGAbort < kIndexFallbackRowsWord && kIndexFallbackRowsWord < kIndexSyncWords, "global words");
 
 struct Args {
   const float* w;
-  float* scores;        // nbuf buffers of `chunk` rows x ld floats
-  int64_t ld;
-  int64_t buf_stride;   // floats between consecutive buffers
-  int nbuf;             // 1 .. kMaxBufs
-  int lag;              // min(kMaxRowLag, nbuf - 1): rows of chunk c come in step c + lag
+  float* samples;       // per slot: slot_rows rows x samp_ld sampled scores
+  int64_t samp_ld, samp_slot;
+  uint2* cands;         // per slot: slot_rows rows x cap candidates (score key, pool)
+  int64_t cand_slot;
+  uint2* thr;           // per slot: thr_ld thresholds (score key, pool), one per row
+  unsigned* cnt;        // per slot: thr_ld candidate counts
+  int64_t thr_ld;       // slot rows rounded up to 128 (a tile's 128 thresholds are 16-byte aligned)
+  int cap;
+  int sigma;            // sample stride in pools
+  int rsel;             // the threshold is the rsel-th largest sample
+  int rpi;              // rows per thresh / rows item: 16 (one per warp, topk <= 512) or 4 (one per group)
+  int nbuf;             // slots, 1 .. kMaxBufs
+  int lag;              // min(kMaxLag, nbuf - 2), at least 0
   int64_t q_begin, q_end;
   int chunk;
   int nchunks;
   int Hi;
   int topk;
   int32_t* pool_idx;
+  int32_t* fb_rows;     // rows listed for the fallback kernel
+  IndexTraceRec* trace;  // item-trace build only (DSA_ITEM_TRACE)
+  unsigned long long* trace_count;
+  int64_t trace_cap;
   unsigned long long* sync;
   unsigned* status;
   uint64_t limit_ns;
@@ -134,10 +175,28 @@ __device__ __forceinline__ Chunk chunk_of(const Args& a, int c) {
   return ch;
 }
 
-__device__ __forceinline__ int pool_tiles_of(const Chunk& ch, int qb) {
+// pools eligible for the last query of block qb
+__device__ __forceinline__ int64_t block_pools(const Chunk& ch, int qb) {
   const int64_t end = min(ch.row0 + static_cast<int64_t>(qb + 1) * kBM, ch.row0 + ch.nrows);
-  const int64_t n = (end - 1) / 4;  // pools eligible for the last query of the block
-  return static_cast<int>((n + kBN - 1) / kBN);
+  return (end - 1) / 4;
+}
+
+__device__ __forceinline__ int pool_tiles_of(const Chunk& ch, int qb) {
+  return static_cast<int>((block_pools(ch, qb) + kBN - 1) / kBN);
+}
+
+// sample tiles of block qb: only blocks with a row past cap pools need samples
+__device__ __forceinline__ int sample_tiles_of(const Args& a, const Chunk& ch, int qb) {
+  const int64_t n = block_pools(ch, qb);
+  if (ch.ntiles == 0 || n <= a.cap) return 0;
+  const int64_t G = (n + a.sigma - 1) / a.sigma;
+  return static_cast<int>((G + kBN - 1) / kBN);
+}
+
+__device__ __forceinline__ int sample_tiles(const Args& a, const Chunk& ch) {
+  int n = 0;
+  for (int qb = 0; qb < ch.nqb; ++qb) n += sample_tiles_of(a, ch, qb);
+  return n;
 }
 
 // Tiles of the chunk that hold eligible pairs (the ones that are computed).
@@ -175,27 +234,68 @@ __device__ __forceinline__ void raise_abort(const Args& a, volatile int* local_a
   record_status(a.status, kStatusTimeout);
 }
 
+// Item-trace build: epilogue thread 0 records each item (see IndexTraceRec).
+__device__ __forceinline__ void trace_item(const Args& a, int kind, int chunk, uint64_t t0, uint64_t t1, uint64_t t2) {
+#ifdef DSA_ITEM_TRACE
+  if (a.trace == nullptr) return;
+  const uint64_t t3 = globaltimer_ns();
+  const unsigned long long slot = atomicAdd(a.trace_count, 1ull);
+  if (static_cast<int64_t>(slot) >= a.trace_cap) return;
+  uint32_t sm;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+  IndexTraceRec r;
+  r.kind_sm = static_cast<uint32_t>(kind) | (sm << 8);
+  r.chunk = static_cast<uint32_t>(chunk);
+  r.t0 = t0;
+  r.t1 = t1;
+  r.t2 = t2;
+  r.t3 = t3;
+  a.trace[slot] = r;
+#else
+  (void)a, (void)kind, (void)chunk, (void)t0, (void)t1, (void)t2;
+#endif
+}
+
+#ifdef DSA_ITEM_TRACE
+#define DSA_STAMP(v) v = globaltimer_ns()
+#else
+#define DSA_STAMP(v) (void)0
+#endif
+
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(kEpiBar), "n"(32 * kEpiWarps) : "memory");
 }
 
-// The ticket taker's view of the sequence: step s holds the tiles of chunk s
-// (s < nchunks) followed by the row items of chunk s - lag.
+// Rows of chunks c' <= c that use slot c % nbuf, every such chunk before the
+// last of the call being full (thresh and rows items count rows).
+__device__ __forceinline__ unsigned long long rows_through(const Args& a, int c) {
+  return static_cast<unsigned long long>(c / a.nbuf) * a.chunk + chunk_of(a, c).nrows;
+}
+
+// The ticket taker's view of the sequence: step s holds the sample items of
+// chunk s, the thresh items of chunk s-1, the tiles of chunk s-2 and the row
+// items of chunk s-2-lag.
 struct Cursor {
   int s;
-  int64_t base;  // first ticket of step s
-  int nt, nr;    // tile and row items in step s
+  int64_t base;        // first ticket of step s
+  int ns, nh, nt, nr;  // sample, thresh, tile and row items in step s
 };
 
+__device__ __forceinline__ int steps(const Args& a) { return a.nchunks + 2 + a.lag; }
+
 __device__ __forceinline__ void cursor_load(const Args& a, Cursor& cur) {
-  cur.nt = cur.s < a.nchunks ? chunk_of(a, cur.s).ntiles : 0;
-  const int rc = cur.s - a.lag;
-  cur.nr = rc >= 0 && rc < a.nchunks ? (chunk_of(a, rc).nrows + kRowsPerItem - 1) / kRowsPerItem : 0;
+  const int cs = cur.s, ch_ = cur.s - 1, ct = cur.s - 2, cr = cur.s - 2 - a.lag;
+  cur.ns = cs < a.nchunks ? sample_tiles(a, chunk_of(a, cs)) : 0;
+  cur.nh = ch_ >= 0 && ch_ < a.nchunks ? (chunk_of(a, ch_).nrows + a.rpi - 1) / a.rpi : 0;
+  cur.nt = ct >= 0 && ct < a.nchunks ? chunk_of(a, ct).ntiles : 0;
+  cur.nr = cr >= 0 && cr < a.nchunks ? (chunk_of(a, cr).nrows + a.rpi - 1) / a.rpi : 0;
 }
+
+__device__ __forceinline__ int cursor_items(const Cursor& cur) { return cur.ns + cur.nh + cur.nt + cur.nr; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     index_topk_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                      const Args a) {
+                      const __grid_constant__ CUtensorMap s_map, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-B swizzle atoms need 1024-B alignment
@@ -209,12 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acc_full = sCtl + kBarAccFull, bar_acc_empty = sCtl + kBarAccEmpty;
   const uint32_t bar_drain = sCtl + kBarDrain;
   const uint32_t bar_item_full = sCtl + kBarItemFull, bar_item_empty = sCtl + kBarItemEmpty;
+  const uint32_t bar_deps = sCtl + kBarDeps, bar_done = sCtl + kBarDone;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gctl + kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctl + kAbort);
   volatile int* group_ok = reinterpret_cast<volatile int*>(gctl + kGroupOk);
   volatile int* wait_ok = reinterpret_cast<volatile int*>(gctl + kWaitOk);
   volatile Item* items = reinterpret_cast<volatile Item*>(gctl + kItemData);
-  topk::Smem* tsm = reinterpret_cast<topk::Smem*>(gbase + kTopkOff);
+  uint2* thr_s = reinterpret_cast<uint2*>(gbase + kThrOff);  // [kItems][kBM] thresholds of a tile's rows
+  cand::Smem* csm = reinterpret_cast<cand::Smem*>(gbase + kGrpOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -231,8 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_acc_empty + 8 * s, kEpiWarps);
     }
     for (int s = 0; s < kItems; ++s) {
-      mbar_init(bar_item_full + 8 * s, 1);
-      mbar_init(bar_item_empty + 8 * s, 1 + kEpiWarps);  // the MMA thread and one lane per epilogue warp
+      mbar_init(bar_item_full + 8 * s, 1);   // the scheduler wrote the item
+      mbar_init(bar_item_empty + 8 * s, 3);  // the TMA and MMA threads read it; the publisher published it
+      mbar_init(bar_deps + 8 * s, 1);        // the scheduler found its dependencies met
+      mbar_init(bar_done + 8 * s, kEpiWarps);  // every epilogue warp finished it
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -247,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- ticket taker + TMA producer
+    // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       int as = 0, is = 0;
       uint32_t aph = 0, bph = 0, iph = 0;
@@ -255,68 +359,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool b_armed = false;
       uint32_t b_par = 0;
       bool ok = true, maps_ready = false;
-      Cursor cur{0, 0, 0, 0};
-      cursor_load(a, cur);
       while (ok) {
-        // A ticket is taken only once the ring has room for its item: a CTA
-        // never holds work it cannot start soon, so tickets are served close
-        // to their order and the items that wait on earlier ones find them done.
-        if (!mbar_wait(bar_item_empty + 8 * is, iph ^ 1, a.limit_ns, abort_flag)) {
+        if (!mbar_wait(bar_item_full + 8 * is, iph, a.limit_ns, abort_flag)) {
           ok = false;
           break;
         }
-        Item it{kItemEnd, 0, 0, 0};
-        while (true) {
-          const int64_t t = static_cast<int64_t>(atomicAdd(a.sync + kTicket, 1ull));
-          while (t >= cur.base + cur.nt + cur.nr && cur.s < a.nchunks + a.lag) {
-            cur.base += cur.nt + cur.nr;
-            ++cur.s;
-            cursor_load(a, cur);
-          }
-          if (cur.s >= a.nchunks + a.lag) break;  // no work left: the end item
-          if (t - cur.base < cur.nt) {
-            const Chunk ch = chunk_of(a, cur.s);
-            const int tt = static_cast<int>(t - cur.base);
-            const int qb = tt % ch.nqb, pb = tt / ch.nqb;
-            if (pb >= pool_tiles_of(ch, qb)) continue;  // past the causal edge: nothing to compute
-            it = Item{kItemTile, cur.s, qb, pb};
-          } else {
-            const Chunk ch = chunk_of(a, cur.s - a.lag);
-            const int r0 = static_cast<int>(t - cur.base - cur.nt) * kRowsPerItem;
-            it = Item{kItemRows, cur.s - a.lag, r0, min(kRowsPerItem, ch.nrows - r0)};
-          }
-          break;
-        }
-        items[is].kind = it.kind;
-        items[is].chunk = it.chunk;
-        items[is].a = it.a;
-        items[is].b = it.b;
-        mbar_arrive(bar_item_full + 8 * is);  // release: the item's fields are visible to the waiters
+        const Item it{items[is].kind, items[is].chunk, items[is].a, items[is].b};
+        mbar_arrive(bar_item_empty + 8 * is);
         if (++is == kItems) {
           is = 0;
           iph ^= 1;
         }
         if (it.kind == kItemEnd) break;
-        if (it.kind == kItemRows) {
-          // The rows' scores may have left L2 (the ring is larger than L2):
-          // bring back those of the chunk's row item kPrefetchItems tickets
-          // ahead, whichever CTA will take it (the first items of a chunk
-          // also fetch their own rows).  (Their tiles may not all be stored
-          // yet; L2 keeps them coherent.)
-          const Chunk ch = chunk_of(a, it.chunk);
-          const float* buf = a.scores + static_cast<int64_t>(it.chunk % a.nbuf) * a.buf_stride;
-          const int ahead = kPrefetchItems * kRowsPerItem;
-          const int f0 = it.a < ahead ? it.a : it.a + ahead;
-          const int f1 = min(ch.nrows, it.a + ahead + kRowsPerItem);
-          for (int r = f0; r < f1; ++r) {
-            const int64_t n = (ch.row0 + r) / 4;
-            if (n > a.topk) bulk_prefetch_l2(buf + static_cast<int64_t>(r) * a.ld, static_cast<uint32_t>((n * 4 + 15) & ~15ll));
-          }
-          continue;
-        }
+        if (it.kind != kItemSample && it.kind != kItemTile) continue;
         if (!maps_ready) {
           tma_prefetch_map(&q_map);
           tma_prefetch_map(&k_map);
+          tma_prefetch_map(&s_map);
           maps_ready = true;
         }
         if (!mbar_wait(bar_b_empty, bph ^ 1, a.limit_ns, abort_flag)) {
@@ -324,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (!a.inject) {
+          // tile: pools pb*256 ..; sample: sampled pools (st*256 + j) * sigma
+          const CUtensorMap* bm = it.kind == kItemTile ? &k_map : &s_map;
           mbar_arrive_expect_tx(bar_b_full, kBBytes);
-          tma_load_2d(sB, &k_map, bar_b_full, 0, it.b * kBN);
-          tma_load_2d(sB + kBHalf, &k_map, bar_b_full, kDi, it.b * kBN);
+          tma_load_2d(sB, bm, bar_b_full, 0, it.b * kBN);
+          tma_load_2d(sB + kBHalf, bm, bar_b_full, kDi, it.b * kBN);
           b_armed = true;
           b_par = bph;
         }
@@ -374,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           iph ^= 1;
         }
         if (kind == kItemEnd) break;
-        if (kind != kItemTile) continue;
+        if (kind != kItemTile && kind != kItemSample) continue;
         if (!mbar_wait(bar_b_full, bph, a.limit_ns, abort_flag)) {
           ok = false;
           break;
@@ -418,28 +479,177 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar_drain, 0, a.limit_ns, nullptr);
       }
     }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- scheduler: tickets and dependencies
+      // Takes the next ticket once the ring has a free slot (a CTA never
+      // holds work it cannot start soon, so tickets are served close to their
+      // order), then waits until the item's dependencies -- earlier tickets,
+      // published by other CTAs -- are met, and for a tile brings the
+      // thresholds of its 128 rows into shared memory.  The epilogue then
+      // waits only on shared-memory barriers.
+      int is = 0;
+      uint32_t iph = 0;
+      bool ok = true;
+      Cursor cur{0, 0, 0, 0, 0, 0};
+      cursor_load(a, cur);
+      const int nsteps = steps(a);
+      unsigned long long tiles_cum[kMaxBufs], samp_cum[kMaxBufs];
+#pragma unroll
+      for (int q = 0; q < kMaxBufs; ++q) tiles_cum[q] = samp_cum[q] = 0ull;
+      int tiles_upto = -1, samp_upto = -1;
+      while (ok) {
+        if (!mbar_wait(bar_item_empty + 8 * is, iph ^ 1, a.limit_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        Item it{kItemEnd, 0, 0, 0};
+        while (true) {
+          const int64_t t = static_cast<int64_t>(atomicAdd(a.sync + kTicket, 1ull));
+          while (t >= cur.base + cursor_items(cur) && cur.s < nsteps) {
+            cur.base += cursor_items(cur);
+            ++cur.s;
+            cursor_load(a, cur);
+          }
+          if (cur.s >= nsteps) break;  // no work left: the end item
+          int off = static_cast<int>(t - cur.base);
+          if (off < cur.ns) {
+            const Chunk ch = chunk_of(a, cur.s);
+            int qb = 0;
+            while (qb + 1 < ch.nqb) {
+              const int n = sample_tiles_of(a, ch, qb);
+              if (off < n) break;
+              off -= n;
+              ++qb;
+            }
+            it = Item{kItemSample, cur.s, qb, off};
+            break;
+          }
+          off -= cur.ns;
+          if (off < cur.nh) {
+            const Chunk ch = chunk_of(a, cur.s - 1);
+            const int r0 = off * a.rpi;
+            it = Item{kItemThresh, cur.s - 1, r0, min(a.rpi, ch.nrows - r0)};
+            break;
+          }
+          off -= cur.nh;
+          if (off < cur.nt) {
+            const Chunk ch = chunk_of(a, cur.s - 2);
+            const int qb = off % ch.nqb, pb = off / ch.nqb;
+            if (pb >= pool_tiles_of(ch, qb)) continue;  // past the causal edge: nothing to compute
+            it = Item{kItemTile, cur.s - 2, qb, pb};
+            break;
+          }
+          off -= cur.nt;
+          const Chunk ch = chunk_of(a, cur.s - 2 - a.lag);
+          const int r0 = off * a.rpi;
+          it = Item{kItemRows, cur.s - 2 - a.lag, r0, min(a.rpi, ch.nrows - r0)};
+          break;
+        }
+        items[is].kind = it.kind;
+        items[is].chunk = it.chunk;
+        items[is].a = it.a;
+        items[is].b = it.b;
+        mbar_arrive(bar_item_full + 8 * is);  // release: the item's fields are visible to the waiters
+        if (it.kind != kItemEnd) {
+          const int bi = it.chunk % a.nbuf;
+          const Chunk ch = chunk_of(a, it.chunk);
+          bool go = true;
+          if (it.kind == kItemSample) {
+            // the thresh items of chunks c-nbuf, ... are done reading the slot's samples
+            if (it.chunk >= a.nbuf) go = wait_counter(a, a.sync + kThrDone + bi, rows_through(a, it.chunk - a.nbuf));
+          } else if (it.kind == kItemThresh) {
+            if (ch.row0 + it.a + it.b - 1 > 4ll * a.cap + 3) {  // some row has more than cap pools: its samples
+              while (samp_upto < it.chunk) {
+                const int c = ++samp_upto;
+                samp_cum[c % a.nbuf] += static_cast<unsigned long long>(sample_tiles(a, chunk_of(a, c)));
+              }
+              go = wait_counter(a, a.sync + kSampDone + bi, samp_cum[bi]);
+            }
+            // the rows of chunks c-nbuf, ... are done with the slot's candidates
+            if (go && it.chunk >= a.nbuf) go = wait_counter(a, a.sync + kRowsDone + bi, rows_through(a, it.chunk - a.nbuf));
+          } else if (it.kind == kItemTile) {
+            // the thresholds of chunk c are set (and its candidate counts zeroed)
+            go = wait_counter(a, a.sync + kThrDone + bi, rows_through(a, it.chunk));
+            if (go) {
+              // thresholds of the tile's 128 rows (rows past the chunk read padding)
+              const uint2* src = a.thr + static_cast<int64_t>(bi) * a.thr_ld + static_cast<int64_t>(it.a) * kBM;
+              const uint32_t dst = smem_u32(thr_s + is * kBM);
+#pragma unroll 8
+              for (int j = 0; j < kBM / 2; ++j) cp_async16(dst + 16 * j, src + 2 * j, true);
+              cp_async_commit();
+              cp_async_wait<0>();
+            }
+          } else if (ch.row0 + it.a + it.b - 1 > 4ll * a.topk + 3) {
+            // rows: some row reads candidates, so its chunk's tiles must be appended
+            while (tiles_upto < it.chunk) {
+              const int c = ++tiles_upto;
+              tiles_cum[c % a.nbuf] += valid_tiles(chunk_of(a, c));
+            }
+            go = wait_counter(a, a.sync + kTilesDone + bi, tiles_cum[bi]);
+          }
+          if (!go) {
+            ok = false;
+            raise_abort(a, abort_flag);
+          }
+        }
+        mbar_arrive(bar_deps + 8 * is);  // release: the thresholds are visible to the epilogue
+        if (++is == kItems) {
+          is = 0;
+          iph ^= 1;
+        }
+        if (it.kind == kItemEnd) break;
+      }
+      if (!ok) raise_abort(a, abort_flag);
+    } else if (lane == 1) {
+      // -------------------------------------------------------------- publisher
+      // Once every epilogue warp has finished an item (their arrivals order
+      // its writes before this thread's fence, whose effect is cumulative),
+      // adds it to the chunk slot's done counter and frees its ring slot.
+      int is = 0;
+      uint32_t iph = 0;
+      bool ok = true;
+      while (ok) {
+        if (!mbar_wait(bar_item_full + 8 * is, iph, a.limit_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const Item it{items[is].kind, items[is].chunk, items[is].a, items[is].b};
+        if (it.kind == kItemEnd) break;
+        if (!mbar_wait(bar_done + 8 * is, iph, a.limit_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        __threadfence();
+        const int bi = it.chunk % a.nbuf;
+        if (it.kind == kItemSample) atomicAdd(a.sync + kSampDone + bi, 1ull);
+        else if (it.kind == kItemTile) atomicAdd(a.sync + kTilesDone + bi, 1ull);
+        else if (it.kind == kItemThresh) atomicAdd(a.sync + kThrDone + bi, static_cast<unsigned long long>(it.b));
+        else atomicAdd(a.sync + kRowsDone + bi, static_cast<unsigned long long>(it.b));
+        mbar_arrive(bar_item_empty + 8 * is);
+        if (++is == kItems) {
+          is = 0;
+          iph ^= 1;
+        }
+      }
+      if (!ok) raise_abort(a, abort_flag);
+    }
   } else {
-    // ---------------------------------------------------------------- epilogue + top-k
-    // Warp w (2..17) reads TMEM lanes 32*(w%4).. (its hardware lane quarter)
-    // and columns 64*((w-2)/4).. of each accumulator: one query row and 64
-    // pools per thread.  For row items, warps 2+4g .. 5+4g form top-k group g.
-    // Decisions that steer the 512-thread barrier are taken by epilogue
-    // thread 0 and read by all from shared memory, so every epilogue thread
-    // takes the same branch; the two decision words alternate so that a
-    // write never overtakes a reader of the previous value.
-    const int etid = static_cast<int>(threadIdx.x) - 64;
-    const int ew = warp - 2;
+    // ---------------------------------------------------------------- epilogue + thresholds + top-k
+    // Warp w (3..18) reads TMEM lanes 32*(w%4).. (its hardware lane quarter)
+    // and columns 64*((w-3)/4).. of each accumulator: one query row and 64
+    // pools per thread.  For thresh and rows items, warps 3+4g .. 6+4g form
+    // group g.  Decisions that steer the 512-thread barrier are taken by
+    // epilogue thread 0 and read by all from shared memory, so every epilogue
+    // thread takes the same branch.
+    const int etid = static_cast<int>(threadIdx.x) - 32 * kEpiWarp0;
+    const int ew = warp - kEpiWarp0;
     const int lq = warp & 3;
     const int cq = ew >> 2;
     const int gid = ew >> 2;
     const topk::Group grp{etid - gid * topk::kGT, 2 + gid};
     int cs = 0, is = 0;
     uint32_t cph = 0, iph = 0;
-    // cumulative valid-tile counts of chunks 0..tc_upto by buffer (epilogue thread 0 only)
-    unsigned long long tiles_cum[kMaxBufs];
-#pragma unroll
-    for (int q = 0; q < kMaxBufs; ++q) tiles_cum[q] = 0ull;
-    int tc_upto = -1;
     while (true) {
       bool ok = mbar_wait(bar_item_full + 8 * is, iph, a.limit_ns, abort_flag);
       Item it{kItemEnd, 0, 0, 0};
@@ -448,12 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.chunk = items[is].chunk;
         it.a = items[is].a;
         it.b = items[is].b;
-      }
-      __syncwarp();
-      if (ok && lane == 0) mbar_arrive(bar_item_empty + 8 * is);
-      if (++is == kItems) {
-        is = 0;
-        iph ^= 1;
       }
       if (!ok) raise_abort(a, abort_flag);
       // every warp saw the same item (or an abort): agree before branching
@@ -464,9 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const Chunk ch = chunk_of(a, it.chunk);
       const int bi = it.chunk % a.nbuf;
-      float* buf = a.scores + static_cast<int64_t>(bi) * a.buf_stride;
-      if (it.kind == kItemTile) {
-        const int qb = it.a, pb = it.b;
+      uint64_t ts0 = 0, ts1 = 0, ts2 = 0;
+      DSA_STAMP(ts0);
+      ts1 = ts0;
+      if (it.kind == kItemTile || it.kind == kItemSample) {
+        const int qb = it.a;
         const int64_t row = ch.row0 + static_cast<int64_t>(qb) * kBM + lq * 32 + lane;
         const bool valid = row < ch.row0 + ch.nrows;
         const float* wrow = a.w + (valid ? row : ch.row0) * a.Hi;
@@ -506,22 +712,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             cph ^= 1;
           }
         }
+        DSA_STAMP(ts1);
+        // the item's dependencies (met long ago, as a rule)
+        if (ok) ok = mbar_wait(bar_deps + 8 * is, iph, a.limit_ns, abort_flag);
         if (!ok) raise_abort(a, abort_flag);
-        epi_sync();
-        if (etid == 0) {
-          // the rows of chunks c-nbuf, c-2*nbuf, ... (same buffer) must be done reading it
-          bool go = !*abort_flag;
-          if (go && it.chunk >= a.nbuf)
-            go = wait_counter(a, a.sync + kRowsDone + bi,
-                              static_cast<unsigned long long>(it.chunk / a.nbuf) * a.chunk);
-          if (!go) raise_abort(a, abort_flag);
-          *wait_ok = go;
-        }
-        epi_sync();
-        if (!*wait_ok) break;
-        {
-          float* stg = reinterpret_cast<float*>(gbase + kTopkOff + ew * kStgBytes);
-          const int64_t rbase = ch.row0 + static_cast<int64_t>(qb) * kBM + lq * 32;  // this warp's first row
+        DSA_STAMP(ts2);
+        const int64_t rloc = row - ch.row0;
+        if (!ok) {
+          // nothing is written; the publisher times out and the call reports it
+        } else if (it.kind == kItemSample) {
+          float* stg = reinterpret_cast<float*>(gbase + kGrpOff + ew * kStgBytes);
+          float* buf = a.samples + static_cast<int64_t>(bi) * a.samp_slot;
+          const int64_t rbase = static_cast<int64_t>(qb) * kBM + lq * 32;  // this warp's first row in the chunk
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             // lane holds row rbase + lane: columns 32*half .. +31 of its 64
@@ -535,45 +737,142 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 8; ++k) {
               const int r = 4 * k + (lane >> 3), c = 4 * (lane & 7);
               const float4 x = *reinterpret_cast<const float4*>(stg + r * kStgLd + c);
-              if (rbase + r < ch.row0 + ch.nrows)
-                *reinterpret_cast<float4*>(buf + (rbase + r - ch.row0) * a.ld + static_cast<int64_t>(pb) * kBN +
+              if (rbase + r < ch.nrows)
+                *reinterpret_cast<float4*>(buf + (rbase + r) * a.samp_ld + static_cast<int64_t>(it.b) * kBN +
                                            cq * kEpiCols + 32 * half + c) = x;
             }
             __syncwarp();
           }
-        }
-        // publish: the barrier orders every thread's stores before thread 0's
-        // fence, whose effect is cumulative, then the count (only thread 0 waits)
-        epi_sync();
-        if (etid == 0) {
-          __threadfence();
-          atomicAdd(a.sync + kTilesDone + bi, 1ull);
+        } else {
+          // append this row's pools at or above its threshold
+          const int64_t n_r = row / 4;
+          if (valid && n_r > a.topk) {
+            const uint2 th = thr_s[is * kBM + lq * 32 + lane];
+            const uint32_t pbase = static_cast<uint32_t>(it.b) * kBN + cq * kEpiCols;
+            // pool pbase + j is a candidate when j < jn (eligible) and its
+            // score is above the threshold's, or equal with j <= jt; the key
+            // order is the float order (-0 and +0 being one key), so the
+            // scores are compared as floats
+            const float tf = topk::key_score(th.x);
+            const int jn = static_cast<int>(min(n_r - static_cast<int64_t>(pbase), static_cast<int64_t>(kEpiCols)));
+            const int jt = static_cast<int>(
+                min(static_cast<int64_t>(th.y) - static_cast<int64_t>(pbase), static_cast<int64_t>(kEpiCols)));
+            // bit j of `hit`: pool pbase + j is a candidate
+            unsigned long long hit = 0ull;
+#pragma unroll
+            for (int j = 0; j < kEpiCols; ++j) {
+              const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
+              if (j < jn && (v > tf || (v == tf && j <= jt))) hit |= 1ull << j;
+            }
+            if (hit != 0ull) {
+              unsigned pos = atomicAdd(a.cnt + static_cast<int64_t>(bi) * a.thr_ld + rloc,
+                                       static_cast<unsigned>(__popcll(hit)));
+              uint2* dst = a.cands + static_cast<int64_t>(bi) * a.cand_slot + rloc * a.cap;
+              const unsigned cap = static_cast<unsigned>(a.cap);
+#pragma unroll
+              for (int j = 0; j < kEpiCols; ++j) {
+                if ((hit >> j) & 1ull) {
+                  const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
+                  if (pos < cap) dst[pos] = make_uint2(topk::score_key(v), pbase + j);
+                  ++pos;
+                }
+              }
+            }
+          }
         }
       } else {
-        // ---- up to four top-k rows, one per group
-        const int r0 = it.a, nr = it.b;
-        const int64_t i_last = ch.row0 + r0 + nr - 1;
-        if (i_last / 4 > a.topk) {  // some row reads scores: its chunk's tiles must be stored
-          if (etid == 0) {
-            while (tc_upto < it.chunk) {
-              ++tc_upto;
-              tiles_cum[tc_upto % a.nbuf] += valid_tiles(chunk_of(a, tc_upto));
-            }
-            const bool go = wait_counter(a, a.sync + kTilesDone + bi, tiles_cum[bi]);
-            if (!go) raise_abort(a, abort_flag);
-            *wait_ok = go;
-            __threadfence();
-          }
-          epi_sync();
-          if (!*wait_ok) break;
-        }
-        if (gid < nr) {
-          const int64_t i = ch.row0 + r0 + gid;
-          topk::row(grp, tsm[gid], buf + static_cast<int64_t>(r0 + gid) * a.ld, static_cast<int>(i / 4), a.topk,
-                    a.pool_idx + (i - a.q_begin) * a.topk, a.sync + kIndexGeneralRowsWord);
-        }
+        // ---- thresh or rows: up to four rows, one per group, once the
+        // item's dependencies are met (all warps agree before the groups'
+        // barriers)
+        bool dep = mbar_wait(bar_deps + 8 * is, iph, a.limit_ns, abort_flag);
+        if (!dep) raise_abort(a, abort_flag);
         epi_sync();
-        if (etid == 0) atomicAdd(a.sync + kRowsDone + bi, static_cast<unsigned long long>(nr));
+        if (etid == 0) *wait_ok = !*abort_flag;
+        epi_sync();
+        if (!*wait_ok) break;
+        DSA_STAMP(ts2);
+        const int r0 = it.a, nr = it.b;
+        if (a.rpi == kRowsPerWarpItem) {
+          // one row per warp (topk <= 512)
+          if (ew < nr) {
+            wsel::Smem& wsm = reinterpret_cast<wsel::Smem*>(gbase + kGrpOff)[ew];
+            const int64_t rloc = r0 + ew;
+            const int64_t i = ch.row0 + rloc;
+            const int64_t n = i / 4;
+            if (it.kind == kItemThresh) {
+              if (n > a.topk) {
+                uint2 th = make_uint2(0u, 0x7FFFFFFFu);  // every eligible pool
+                if (n > a.cap) {
+                  const int G = static_cast<int>((n + a.sigma - 1) / a.sigma);
+                  th = wsel::threshold(wsm, lane, a.samples + static_cast<int64_t>(bi) * a.samp_slot + rloc * a.samp_ld,
+                                       G, a.rsel, a.sigma);
+                }
+                if (lane == 0) {
+                  a.thr[static_cast<int64_t>(bi) * a.thr_ld + rloc] = th;
+                  a.cnt[static_cast<int64_t>(bi) * a.thr_ld + rloc] = 0u;
+                }
+              }
+            } else {
+              int32_t* orow = a.pool_idx + (i - a.q_begin) * a.topk;
+              if (n <= a.topk) {
+                for (int j = lane; j < a.topk; j += 32) orow[j] = j < n ? j : -1;
+              } else {
+                const unsigned count = __ldcg(a.cnt + static_cast<int64_t>(bi) * a.thr_ld + rloc);
+                bool done = false;
+                if (count >= static_cast<unsigned>(a.topk) && count <= static_cast<unsigned>(a.cap))
+                  done = wsel::topk(wsm, lane, a.cands + static_cast<int64_t>(bi) * a.cand_slot + rloc * a.cap,
+                                    static_cast<int>(count), a.topk, orow);
+                if (!done && lane == 0) {
+                  const unsigned long long f = atomicAdd(a.sync + kIndexFallbackRowsWord, 1ull);
+                  a.fb_rows[f] = static_cast<int32_t>(i);
+                }
+              }
+            }
+          }
+        } else if (gid < nr) {
+          // one row per 128-thread group (topk > 512)
+          const int64_t rloc = r0 + gid;
+          const int64_t i = ch.row0 + rloc;
+          const int64_t n = i / 4;
+          if (it.kind == kItemThresh) {
+            if (n > a.topk) {
+              uint2 th = make_uint2(0u, 0x7FFFFFFFu);  // every eligible pool
+              if (n > a.cap) {
+                const int G = static_cast<int>((n + a.sigma - 1) / a.sigma);
+                th = cand::sample_threshold(grp, csm[gid],
+                                            a.samples + static_cast<int64_t>(bi) * a.samp_slot + rloc * a.samp_ld, G,
+                                            a.rsel, a.sigma);
+              }
+              if (grp.tid == 0) {
+                a.thr[static_cast<int64_t>(bi) * a.thr_ld + rloc] = th;
+                a.cnt[static_cast<int64_t>(bi) * a.thr_ld + rloc] = 0u;
+              }
+            }
+          } else {
+            int32_t* orow = a.pool_idx + (i - a.q_begin) * a.topk;
+            if (n <= a.topk) {
+              for (int j = grp.tid; j < a.topk; j += topk::kGT) orow[j] = j < n ? j : -1;
+            } else {
+              const unsigned count = __ldcg(a.cnt + static_cast<int64_t>(bi) * a.thr_ld + rloc);
+              bool done = false;
+              if (count >= static_cast<unsigned>(a.topk) && count <= static_cast<unsigned>(a.cap))
+                done = cand::select(grp, csm[gid], a.cands + static_cast<int64_t>(bi) * a.cand_slot + rloc * a.cap,
+                                    static_cast<int>(count), a.topk, orow);
+              if (!done && grp.tid == 0) {
+                const unsigned long long f = atomicAdd(a.sync + kIndexFallbackRowsWord, 1ull);
+                a.fb_rows[f] = static_cast<int32_t>(i);
+              }
+            }
+          }
+        }
+      }
+      // this warp is done with the item: the publisher counts it once all are
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_done + 8 * is);
+      if (etid == 0) trace_item(a, it.kind, it.chunk, ts0, ts1, ts2 == 0 ? ts1 : ts2);
+      if (++is == kItems) {
+        is = 0;
+        iph ^= 1;
       }
     }
   }
@@ -584,11 +883,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Khat in fp32 with the fixed summation order, then split into bf16 hi + lo.
-// One thread per (pool, 8-dim group); Di = 64.  The first threads also zero
-// index_topk_kernel's global words.
+// Rows the main kernel could not certify (fewer than topk candidates, or
+// more than cap): all n = floor(i/4) scores of the row are recomputed on the
+// CUDA cores -- fp32 dot products of q_idx with the fp32 pooled keys, ReLU,
+// head weight, sum over heads in head order -- into this CTA's scratch row,
+// and the row's top-k is taken from them (topk_row.cuh).  CTAs take the
+// listed rows in turn.
+constexpr int kFbThreads = 256;
+constexpr int kMaxHi = 64;
+
+__global__ void __launch_bounds__(kFbThreads)
+    index_fallback_kernel(const __nv_bfloat16* __restrict__ q_idx, const float* __restrict__ khat32,
+                          const float* __restrict__ w, int Hi, int topk, int64_t q_begin, int32_t* __restrict__ pool_idx,
+                          const int32_t* __restrict__ fb_rows, const unsigned long long* __restrict__ sync,
+                          float* __restrict__ scratch, int64_t scratch_ld) {
+  __shared__ topk::Smem tsm;
+  __shared__ float qs[kMaxHi * kDi];
+  __shared__ float ws[kMaxHi];
+  __shared__ unsigned long long general_rows;
+  const unsigned long long nfb = sync[kIndexFallbackRowsWord];
+  float* srow = scratch + static_cast<int64_t>(blockIdx.x) * scratch_ld;
+  for (unsigned long long f = blockIdx.x; f < nfb; f += gridDim.x) {
+    const int64_t i = fb_rows[f];
+    const int n = static_cast<int>(i / 4);
+    for (int e = threadIdx.x; e < Hi * kDi; e += kFbThreads)
+      qs[e] = __bfloat162float(q_idx[i * Hi * kDi + e]);
+    for (int h = threadIdx.x; h < Hi; h += kFbThreads) ws[h] = w[i * Hi + h];
+    __syncthreads();
+    for (int p = threadIdx.x; p < n; p += kFbThreads) {
+      float kh[kDi];
+      const float4* src = reinterpret_cast<const float4*>(khat32 + static_cast<int64_t>(p) * kDi);
+#pragma unroll
+      for (int d4 = 0; d4 < kDi / 4; ++d4) {
+        const float4 v = src[d4];
+        kh[4 * d4] = v.x;
+        kh[4 * d4 + 1] = v.y;
+        kh[4 * d4 + 2] = v.z;
+        kh[4 * d4 + 3] = v.w;
+      }
+      float acc = 0.f;
+      for (int h = 0; h < Hi; ++h) {
+        float x = 0.f;
+#pragma unroll
+        for (int d = 0; d < kDi; ++d) x = fmaf(qs[h * kDi + d], kh[d], x);
+        acc = fmaf(ws[h], fmaxf(x, 0.f), acc);
+      }
+      srow[p] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x < topk::kGT) {
+      const topk::Group grp{static_cast<int>(threadIdx.x), 1};
+      topk::row(grp, tsm, srow, n, topk, pool_idx + (i - q_begin) * topk, &general_rows);
+    }
+    __syncthreads();
+  }
+}
+
+// Khat in fp32 with the fixed summation order, stored as fp32 and split into
+// bf16 hi + lo.  One thread per (pool, 8-dim group); Di = 64.  The first
+// threads also zero index_topk_kernel's global words.
 __global__ void pool_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t P,
-                                 __nv_bfloat16* __restrict__ khat2, unsigned long long* sync_words) {
+                                 __nv_bfloat16* __restrict__ khat2, float* __restrict__ khat32,
+                                 unsigned long long* sync_words) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t < kIndexSyncWords) sync_words[t] = 0ull;
   const int64_t p = t >> 3;
@@ -599,6 +955,7 @@ __global__ void pool_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_
 #pragma unroll
   for (int r = 0; r < 4; ++r) rows[r] = src[r * (kDi / 8)];
   uint32_t hi[4], lo[4];
+  float kf[8];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     float v[4][2];
@@ -615,6 +972,8 @@ __global__ void pool_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_
       const float s23 = __fadd_rn(v[2][c], v[3][c]);
       kh[c] = __fmul_rn(__fadd_rn(s01, s23), 0.25f);
     }
+    kf[2 * e] = kh[0];
+    kf[2 * e + 1] = kh[1];
     const __nv_bfloat162 h2 = __floats2bfloat162_rn(kh[0], kh[1]);
     const float2 hf = __bfloat1622float2(h2);
     const __nv_bfloat162 l2 = __floats2bfloat162_rn(__fsub_rn(kh[0], hf.x), __fsub_rn(kh[1], hf.y));
@@ -624,33 +983,44 @@ __global__ void pool_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_
   uint4* dst = reinterpret_cast<uint4*>(khat2 + p * (2 * kDi));
   dst[g] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
   dst[8 + g] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  float4* d32 = reinterpret_cast<float4*>(khat32 + p * kDi + 8 * g);
+  d32[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
+  d32[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
 }
 
 }  // namespace
 
 size_t index_topk_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, unsigned long long* sync_words,
+cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, float* khat32, unsigned long long* sync_words,
                              const LaunchCtx& ctx) {
   const int64_t threads = P * 8 > kIndexSyncWords ? P * 8 : kIndexSyncWords;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
   pool_keys_kernel<<<static_cast<unsigned>(grid), block, 0, ctx.stream>>>(
-      static_cast<const __nv_bfloat16*>(k_idx), P, static_cast<__nv_bfloat16*>(khat2), sync_words);
+      static_cast<const __nv_bfloat16*>(k_idx), P, static_cast<__nv_bfloat16*>(khat2), khat32, sync_words);
   return cudaGetLastError();
 }
 
-cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_map, const float* w, float* scores,
-                              int64_t ld, int64_t buf_stride, int nbuf, int64_t q_begin, int64_t q_end, int chunk,
-                              int Hi, int topk, int32_t* pool_idx, unsigned long long* sync_words,
-                              const LaunchCtx& ctx) {
+cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_map, const CUtensorMap& samp_map,
+                              const IndexPlan& pl, const IndexBuffers& b, const float* w, int64_t q_begin,
+                              int64_t q_end, int chunk, int Hi, int topk, int32_t* pool_idx, const LaunchCtx& ctx) {
   Args a;
   a.w = w;
-  a.scores = scores;
-  a.ld = ld;
-  a.buf_stride = buf_stride;
-  a.nbuf = nbuf;
-  a.lag = nbuf - 1 < kMaxRowLag ? nbuf - 1 : kMaxRowLag;
+  a.samples = b.samples;
+  a.samp_ld = pl.samp_ld;
+  a.samp_slot = pl.samp_slot;
+  a.cands = b.cands;
+  a.cand_slot = pl.cand_slot;
+  a.thr = b.thr;
+  a.cnt = b.cnt;
+  a.thr_ld = pl.thr_ld;
+  a.cap = pl.cap;
+  a.sigma = pl.sigma;
+  a.rsel = pl.rsel;
+  a.rpi = topk <= wsel::kMaxK ? kRowsPerWarpItem : kRowsPerGroupItem;
+  a.nbuf = b.nbuf;
+  a.lag = b.nbuf - 2 < kMaxLag ? (b.nbuf - 2 > 0 ? b.nbuf - 2 : 0) : kMaxLag;
   a.q_begin = q_begin;
   a.q_end = q_end;
   a.chunk = chunk;
@@ -658,7 +1028,11 @@ cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_
   a.Hi = Hi;
   a.topk = topk;
   a.pool_idx = pool_idx;
-  a.sync = sync_words;
+  a.fb_rows = b.fb_rows;
+  a.trace = b.trace;
+  a.trace_count = b.trace_count;
+  a.trace_cap = b.trace_cap;
+  a.sync = b.sync;
   a.status = ctx.status;
   a.limit_ns = ctx.wait_limit_ns;
   a.inject = ctx.inject_timeout;
@@ -677,7 +1051,15 @@ cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, index_topk_kernel, q_map, khat_map, a);
+  return cudaLaunchKernelEx(&cfg, index_topk_kernel, q_map, khat_map, samp_map, a);
+}
+
+cudaError_t launch_index_fallback(const void* q_idx, const IndexPlan& pl, const IndexBuffers& b, const float* w,
+                                  int64_t q_begin, int Hi, int topk, int32_t* pool_idx, const LaunchCtx& ctx) {
+  index_fallback_kernel<<<pl.fb_ctas, kFbThreads, 0, ctx.stream>>>(
+      static_cast<const __nv_bfloat16*>(q_idx), b.khat32, w, Hi, topk, q_begin, pool_idx, b.fb_rows, b.sync,
+      b.fb_scratch, pl.fb_ld);
+  return cudaGetLastError();
 }
 
 }  // namespace dsa

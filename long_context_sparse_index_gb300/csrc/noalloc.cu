@@ -38,20 +38,21 @@
 
 namespace dsa {
 void set_last_error(const std::string& msg);  // dsa_api.cu: the message dsa_last_error() returns
-size_t index_topk_min_workspace(int64_t S, int chunk);  // dsa_api.cu: the least workspace dsa_index_topk accepts
+size_t index_topk_min_workspace(int64_t S, int chunk, int topk);  // dsa_api.cu: the least workspace dsa_index_topk accepts
 unsigned long long current_context_id();  // dsa_api.cu: id of the current CUDA context (0: none)
 }
 
 namespace {
 
-// 18 MiB + 256 B.  The call runs the sizes whose least workspace (the one
-// dsa_index_topk accepts at the minimum, two chunk buffers of scores) fits:
-// for example S <= 32768 with chunk <= 256 (kernel words 256 B, pooled keys
-// 2 MiB, two chunk buffers of 8 MiB), or S = 65536 with chunk <= 64.  It
-// always hands dsa_index_topk the whole array, so at the largest sizes only
-// two chunks are in flight (slower than dsa_index_topk with its recommended
-// workspace; the result is the same).
-constexpr size_t kNoAllocScratchBytes = (static_cast<size_t>(18) << 20) + 256;
+// 32 MiB.  The call runs the sizes whose least workspace (the one
+// dsa_index_topk accepts at the minimum, two chunk slots) fits: every
+// S <= 32768 with chunk <= 256 and topk <= 512, for example (at most ~30.2
+// MiB: kernel words, pooled keys as bf16 hi/lo and fp32, the fallback rows'
+// list and scratch, and two slots of sampled scores, thresholds and candidate
+// lists).  It always hands dsa_index_topk the whole array, so at the largest
+// sizes only two chunks are in flight (slower than dsa_index_topk with its
+// recommended workspace; the result is the same).
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -67,7 +68,7 @@ extern "C" {
 dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
                                     int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
                                     void* stream) {
-  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk) == 0 ? 0 : dsa::index_topk_min_workspace(S, chunk);
+  const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk) == 0 ? 0 : dsa::index_topk_min_workspace(S, chunk, topk);
   if (need == 0) {
     // invalid sizes: let the regular entry point report the precise reason
     return dsa_index_topk(q_idx, k_idx, w, S, Hi, Di, chunk, topk, q_begin, q_end, pool_idx, nullptr, 0, stream);
@@ -75,8 +76,8 @@ dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const 
   if (need > kNoAllocScratchBytes) {
     dsa::set_last_error("dsa_index_topk_noalloc: these sizes need " + std::to_string(need) +
                         " bytes of scratch but the built-in buffer holds " + std::to_string(kNoAllocScratchBytes) +
-                        " (enough for S <= 32768 with chunk <= 256, for example); use dsa_index_topk with a "
-                        "caller workspace");
+                        " (enough for S <= 32768 with chunk <= 256 and topk <= 512, for example); use "
+                        "dsa_index_topk with a caller workspace");
     return DSA_ERR_WORKSPACE;
   }
   int dev = 0;

@@ -123,7 +123,9 @@ __device__ __forceinline__ uint32_t group_excl_scan(const Group& g, uint32_t v, 
 
 // With a histogram of nb (<= kBins) bins, finds the bin b holding the need-th
 // largest key: sm.sel = {b, count above b, count in b}.  Ends with a barrier.
-__device__ __forceinline__ void find_bin(const Group& g, const uint32_t* hist, Smem& sm, uint32_t nb, uint32_t need,
+// (SM: any shared-memory struct with the wsum and sel members of Smem.)
+template <typename SM>
+__device__ __forceinline__ void find_bin(const Group& g, const uint32_t* hist, SM& sm, uint32_t nb, uint32_t need,
                                          int& parity) {
   constexpr int kPer = kBins / kGT;  // bins per thread, in descending order
   uint32_t c[kPer], s = 0;
@@ -152,7 +154,8 @@ __device__ __forceinline__ void find_bin(const Group& g, const uint32_t* hist, S
   g.sync();
 }
 
-__device__ __forceinline__ void group_minmax(const Group& g, uint32_t& lo, uint32_t& hi, Smem& sm) {
+template <typename SM>
+__device__ __forceinline__ void group_minmax(const Group& g, uint32_t& lo, uint32_t& hi, SM& sm) {
   const int lane = g.lane(), warp = g.warp();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -178,8 +181,8 @@ __device__ __forceinline__ void group_minmax(const Group& g, uint32_t& lo, uint3
 // the remaining span and keeps the bin that holds the need-th largest key;
 // once that bin has at most kSmall keys they are ranked against each other.
 // Returns T; *take_eq = how many keys equal to T are taken.
-template <typename Get>
-__device__ __forceinline__ uint32_t digit_select(const Group& g, Smem& sm, uint32_t lo, uint32_t hi, uint32_t need,
+template <typename SM, typename Get>
+__device__ __forceinline__ uint32_t digit_select(const Group& g, SM& sm, uint32_t lo, uint32_t hi, uint32_t need,
                                                  int nslots, Get&& get, uint32_t* take_eq, int& parity) {
   const int tid = g.tid;
   while (true) {

@@ -2,6 +2,7 @@
 every entry point include/dsa.h declares, and rejects bad arguments with the
 documented status codes before touching the device."""
 import ctypes
+import math
 import os
 import re
 
@@ -43,19 +44,53 @@ def test_version(lib):
     assert lib.dsa_version().startswith(b"libdsa")
 
 
-def test_workspace_sizes(lib):
-    # 256 B of kernel words + pooled keys (256 B per pool) + a ring of up to
-    # eight chunk buffers of fp32 scores (pools padded to 256)
-    S, chunk = 131072, 256
+def _pow2_ceil(x):
+    p = 1
+    while p < x:
+        p <<= 1
+    return p
+
+
+def _pow2_floor(x):
+    p = 1
+    while 2 * p <= x:
+        p <<= 1
+    return p
+
+
+def _index_ws(S, chunk, topk, nbuf):
+    """The index workspace as the header describes it, each part rounded up to 256 B."""
+    r = lambda x: (x + 255) // 256 * 256
     P = S // 4
-    assert lib.dsa_index_topk_workspace(S, 32, 64, chunk, 512) == 256 + P * 256 + 8 * chunk * P * 4
-    assert lib.dsa_index_topk_workspace(1024, 8, 64, 512, 64) == 256 + 256 * 256 + 2 * 512 * 256 * 4
+    P1 = max(P, 1)
+    Ppad = r(P) if P else 256
+    sigma = max(_pow2_floor(max(1, topk // 16)), _pow2_ceil((P + 4095) // 4096))
+    c = (2 * math.sqrt(sigma) + math.sqrt(4 * sigma + topk)) ** 2
+    cap = max(4096, _pow2_ceil(math.ceil(c + 4 * math.sqrt(sigma * c))))
+    G = (P + sigma - 1) // sigma
+    samp_ld = r(G) if G else 256
+    rows = min(chunk, S)
+    thr_ld = (rows + 127) // 128 * 128
+    return (512 + 2 * r(P1 * 256) + r(S * 4) + r(64 * Ppad * 4) + r(nbuf * rows * samp_ld * 4) + r(nbuf * thr_ld * 8)
+            + r(nbuf * thr_ld * 4) + r(nbuf * rows * cap * 8))
+
+
+def test_workspace_sizes(lib):
+    S, chunk = 131072, 256
+    assert lib.dsa_index_topk_workspace(S, 32, 64, chunk, 512) == _index_ws(S, chunk, 512, 8)
+    # the slot's candidate lists: 4096 per row for topk 512, sampled every 32nd pool
+    assert _index_ws(S, chunk, 512, 8) - _index_ws(S, chunk, 512, 7) == 256 * 1024 * 4 + 256 * 12 + 256 * 4096 * 8
+    assert lib.dsa_index_topk_workspace(1048576, 32, 64, 512, 512) == _index_ws(1048576, 512, 512, 8)
+    assert lib.dsa_index_topk_workspace(1024, 8, 64, 512, 64) == _index_ws(1024, 512, 64, 2)
+    assert lib.dsa_index_topk_workspace(1024, 8, 64, 100, 2048) == _index_ws(1024, 100, 2048, 8)
     assert lib.dsa_index_topk_workspace(0, 32, 64, chunk, 512) == 0
-    # one chunk covering the whole sequence needs one buffer of S rows
+    # one chunk covering the whole sequence needs one slot of S rows
     assert lib.dsa_index_topk_workspace(1000, 8, 64, 4096, 64) == lib.dsa_index_topk_workspace(1000, 8, 64, 1000, 64)
-    assert lib.dsa_index_topk_workspace(1024, 8, 64, 1024, 64) == 256 + 256 * 256 + 1024 * 256 * 4
-    # the built-in no-alloc buffer holds the two-buffer minimum for S = 32768 with chunk 256
-    assert 256 + 8192 * 256 + 2 * 256 * 8192 * 4 <= (18 << 20) + 256
+    assert lib.dsa_index_topk_workspace(1024, 8, 64, 1024, 64) == _index_ws(1024, 1024, 64, 1)
+    # the built-in no-alloc buffer holds the two-slot minimum for S <= 32768 with chunk <= 256, topk <= 512
+    need = max(_index_ws(S_, c_, k_, min(2, (S_ + c_ - 1) // c_)) for S_ in (4097, 16388, 20000, 32768)
+               for c_ in (1, 64, 256) for k_ in (1, 8, 64, 255, 512))
+    assert need <= 32 << 20
     assert lib.dsa_sparse_attn_bwd_workspace(S, 16, 128) == 2 * S * 128 * 4 + S * 16 * 4
 
 
@@ -84,9 +119,9 @@ def test_index_topk_rejects_bad_arguments(lib):
     assert _idx(lib, Hi=65) == dsa.DSA_ERR_UNSUPPORTED
     assert _idx(lib, topk=4096) == dsa.DSA_ERR_UNSUPPORTED
     assert _idx(lib, wsb=100) == dsa.DSA_ERR_WORKSPACE
-    # the two-buffer minimum passes the argument checks (and then needs a GPU); one byte less does not
+    # the two-slot minimum passes the argument checks (and then needs a GPU); one byte less does not
     S, chunk = 1024, 128
-    minimum = 256 + 256 * 256 + 2 * chunk * 256 * 4
+    minimum = _index_ws(S, chunk, 64, 2)
     assert _idx(lib, S=S, e=S, chunk=chunk, wsb=minimum - 1) == dsa.DSA_ERR_WORKSPACE
     assert _idx(lib, S=S, e=S, chunk=chunk, wsb=minimum) != dsa.DSA_ERR_WORKSPACE
     assert _idx(lib, ws=None) == dsa.DSA_ERR_WORKSPACE

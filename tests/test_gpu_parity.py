@@ -53,7 +53,8 @@ def test_index_topk_query_range_shards_concatenate():
 
 @pytest.mark.parametrize("S,Hi,topk,chunk", [(1, 1, 1, 1), (2, 3, 1, 5), (3, 1, 4, 2), (4, 2, 1, 4), (5, 1, 1, 3),
                                              (9, 4, 1, 4), (37, 5, 3, 10), (255, 1, 2, 300), (257, 8, 16, 64),
-                                             (1023, 2, 64, 129), (1030, 8, 255, 500), (3001, 16, 100, 1000)])
+                                             (1023, 2, 64, 129), (1030, 8, 255, 500), (3001, 16, 100, 1000),
+                                             (3001, 4, 600, 256), (9001, 2, 2048, 700)])
 def test_index_topk_edge_shapes_int(S, Hi, topk, chunk):
     """Ragged S (not a multiple of 4, smaller than a tile), topk larger than
     the available pools, chunk not dividing S, a single head."""
@@ -67,15 +68,15 @@ def test_index_topk_edge_shapes_int(S, Hi, topk, chunk):
 
 
 def test_index_topk_result_does_not_depend_on_workspace_size():
-    """The workspace's chunk-buffer count only changes how many chunks are in
-    flight: the two-buffer minimum and the recommended size give the same
-    pool indices bit for bit, on float inputs too."""
-    wl = synth.WORKLOADS["s16k"]
+    """The workspace's slot count only changes how many chunks are in flight:
+    the two-slot minimum and the recommended size give the same pool indices
+    bit for bit, on float inputs too (S = 20480 also takes the sampled
+    thresholds: rows past 4096 pools)."""
+    wl = synth.Workload("t", 20480, seed=21)
     q, k, w = _indexer_to_gpu(*synth.indexer_inputs(wl))
     S = wl.S
     full = dsa.dsa_index_topk(q, k, w, chunk=wl.chunk, topk=wl.topk)
-    P = S // 4
-    minimum = 256 + P * 256 + 2 * wl.chunk * ((P + 255) // 256 * 256) * 4
+    minimum = dsa.index_topk_workspace_size(S, wl.Hi, 64, wl.chunk, wl.topk, slots=2)
     assert minimum < dsa.index_topk_workspace_size(S, wl.Hi, 64, wl.chunk, wl.topk)
     ws = torch.empty(minimum, dtype=torch.uint8, device=DEV)
     small = dsa.dsa_index_topk(q, k, w, chunk=wl.chunk, topk=wl.topk, workspace=ws)
@@ -86,21 +87,74 @@ def test_index_topk_result_does_not_depend_on_workspace_size():
 @pytest.mark.parametrize("nbuf", [2, 3, 5, 8])
 @pytest.mark.parametrize("chunk", [1, 37, 128])
 def test_index_topk_every_buffer_ring_size_bit_exact(nbuf, chunk):
-    """The fused kernel's item dependencies for every score-ring size the
-    workspace can give (2 to 8 chunk buffers; rows handed out min(2, nbuf-1)
-    chunks after their tiles): integer inputs give the oracle's pool indices
+    """The fused kernel's item dependencies for every slot-ring size the
+    workspace can give (2 to 8 chunk slots; rows handed out min(2, nbuf-2)
+    steps after their tiles): integer inputs give the oracle's pool indices
     bit for bit."""
     wl = synth.WORKLOADS["tiny_int_s2048"]
     q_idx, k_idx, w = synth.indexer_inputs(wl)
     S = wl.S
-    P = S // 4
-    ld = (P + 255) // 256 * 256
-    nbytes = 256 + P * 256 + nbuf * min(chunk, S) * ld * 4
+    nbytes = dsa.index_topk_workspace_size(S, wl.Hi, 64, chunk, wl.topk, slots=nbuf)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=chunk, topk=wl.topk, workspace=ws)
     dsa.dsa_sync_status()
     ref, _ = oracle.index_topk(q_idx, k_idx, w, wl.topk)
     assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def _int_indexer(S, Hi, seed, w_lo=0, w_hi=3):
+    return (synth.int_bf16(seed, 1, (S, Hi, 64), -3, 3), synth.int_bf16(seed, 2, (S, 64), -3, 3),
+            synth.int_f32(seed, 3, (S, Hi), w_lo, w_hi))
+
+
+@pytest.mark.parametrize("S,Hi,topk,chunk,slots", [(24577, 8, 64, 256, None), (24577, 8, 512, 256, None),
+                                                    (24577, 8, 100, 300, 2), (24577, 8, 512, 1000, 3),
+                                                    (40001, 2, 1024, 256, None), (40001, 2, 600, 384, 2)])
+def test_index_topk_sampled_thresholds_bit_exact(S, Hi, topk, chunk, slots):
+    """Rows past `cap` pools (4096, or 8192 for topk 1024) take their
+    candidates from a threshold on every sigma-th pool's score.  Integer inputs
+    make every score exact and tie often, so the composite (score, -index)
+    threshold and the tie cut at the k-th score are both exercised, for one
+    warp per row (topk <= 512) and one 128-thread group per row (topk > 512);
+    pool indices equal the oracle's bit for bit, whatever the slot count."""
+    q_idx, k_idx, w = _int_indexer(S, Hi, 31 + topk)
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, topk)
+    ws = None
+    if slots is not None:
+        ws = torch.empty(dsa.index_topk_workspace_size(S, Hi, 64, chunk, topk, slots=slots), dtype=torch.uint8,
+                         device=DEV)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=chunk, topk=topk, workspace=ws)
+    dsa.dsa_sync_status()
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("mode", ["hot_samples", "cold_samples"])
+def test_index_topk_fallback_rows_bit_exact(mode):
+    """Keys built so that the sampled threshold cannot certify rows: with
+    every 64th pool far above the rest ("hot_samples"), the threshold lands
+    among those pools and fewer than topk pools reach it; with every 4th pool
+    far below the rest ("cold_samples"), nearly every pool reaches it and the
+    candidate list overflows.  Those rows go to the fallback kernel, which
+    recomputes their scores in full: pool indices still equal the oracle's bit
+    for bit, and the call reports the rows it sent there.  (Hot pools all
+    tie, so the top-k keeps the lowest-indexed of them.)"""
+    S, Hi, topk = 24577, 4, 64
+    q_idx = synth.int_bf16(41, 1, (S, Hi, 64), 0, 2)      # non-negative queries and keys: nearly
+    k_idx = synth.int_bf16(41, 2, (S, 64), 0, 2)          # every score is positive
+    pools = np.arange(S) // 4
+    big = np.uint16(0x4100)    # bf16 8.0
+    small = np.uint16(0xC100)  # bf16 -8.0
+    if mode == "hot_samples":
+        k_idx[(pools % 64 == 0)] = big
+    else:
+        k_idx[(pools % 4 == 0)] = small
+    w = np.ones((S, Hi), np.float32)
+    ref, _ = oracle.index_topk(q_idx, k_idx, w, topk)
+    ws = torch.empty(dsa.index_topk_workspace_size(S, Hi, 64, 256, topk), dtype=torch.uint8, device=DEV)
+    got = dsa.dsa_index_topk(*_indexer_to_gpu(q_idx, k_idx, w), chunk=256, topk=topk, workspace=ws)
+    dsa.dsa_sync_status()
+    assert np.array_equal(got.cpu().numpy(), ref)
+    assert dsa.index_topk_stats(ws)["fallback_rows"] > 0
 
 
 def test_index_topk_all_ties_take_lowest_pools():
