@@ -799,6 +799,17 @@ def run_trace(args):
     n = int(host[:8].view(np.uint64)[0])
     rec = host[64:64 + min(n, cap) * rec_dtype.itemsize].view(rec_dtype)
     summary = summarize_trace(rec, torch.cuda.get_device_properties(0).multi_processor_count)
+    # SM-cycle sums of the trace build (kernel words 37..43): epilogue thread 0 of
+    # each CTA and the MMA issuer
+    words = ws[:64 * 8].cpu().numpy().view(np.uint64)
+    fheads, mheads = max(int(words[43]), 1), max(int(words[42]), 1)
+    summary["fold_cycles"] = {"per_head_folded": int(words[38]) / fheads,
+                              "acc_wait_per_head": int(words[37]) / fheads,
+                              "mma_q_tile_wait_per_head": int(words[39]) / mheads,
+                              "mma_acc_free_wait_per_head": int(words[40]) / mheads,
+                              "mma_key_tile_wait_per_head": int(words[41]) / mheads,
+                              "heads_issued": int(words[42]), "heads_folded_thread0": int(words[43]),
+                              "fallback_rows": int(words[36])}
     summary.update({"workload": args.workload, "S": S, "call_ms": ev0.elapsed_time(ev1), "records_dropped": max(0, n - cap),
                     "note": "DSA_ITEM_TRACE build (measurement only): epilogue thread 0 stamps each work item; "
                             "fold = taking the item to the end of its fold over heads (waits on the MMAs included), "

@@ -54,7 +54,7 @@ cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(KArgs...), dim3 grid,
 
 // Global words of the fused indexer + top-k kernel (64-bit each), at the start
 // of its workspace, and its most per-chunk buffer slots.
-constexpr int kIndexSyncWords = 40;
+constexpr int kIndexSyncWords = 48;
 constexpr int kMaxBufs = 8;
 // word counting the rows listed for the fallback kernel (their candidates
 // could not certify the top-k); it survives the call (the next call's key

@@ -262,6 +262,40 @@ __device__ __forceinline__ void trace_item(const Args& a, int kind, int chunk, u
 #define DSA_STAMP(v) (void)0
 #endif
 
+// Item-trace build: SM-cycle sums of the fold's and the MMA issuer's waits,
+// in the kernel words after the fallback count (zero cost otherwise).
+enum : int {
+  kCycFoldWait = kIndexFallbackRowsWord + 1,  // epilogue thread 0: waiting for a head's accumulator
+  kCycFold,                                   // ... folding tiles and samples, waits included
+  kCycMmaA,                                   // MMA issuer: waiting for a head's query tile
+  kCycMmaAcc,                                 // ... for a free accumulator
+  kCycMmaB,                                   // ... for a pooled-key tile
+  kCycMmaHeads,                               // heads issued (a count)
+  kCycFoldHeads                               // heads folded by epilogue thread 0 (a count)
+};
+static_assert(kCycFoldHeads < kIndexSyncWords, "trace words");
+
+struct CycleSum {
+#ifdef DSA_ITEM_TRACE
+  long long sum = 0, t = 0;
+  __device__ __forceinline__ void start() { t = clock64(); }
+  __device__ __forceinline__ void stop() { sum += clock64() - t; }
+  __device__ __forceinline__ void add(long long n) { sum += n; }
+#else
+  __device__ __forceinline__ void start() {}
+  __device__ __forceinline__ void stop() {}
+  __device__ __forceinline__ void add(long long) {}
+#endif
+};
+
+__device__ __forceinline__ void cycles_publish(const Args& a, int word, const CycleSum& c) {
+#ifdef DSA_ITEM_TRACE
+  if (a.trace != nullptr && c.sum != 0) atomicAdd(a.sync + word, static_cast<unsigned long long>(c.sum));
+#else
+  (void)a, (void)word, (void)c;
+#endif
+}
+
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(kEpiBar), "n"(32 * kEpiWarps) : "memory");
 }
@@ -423,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int as = 0, cs = 0, is = 0;
       uint32_t aph = 0, bph = 0, cph = 0, iph = 0;
       bool ok = true, issued = false;
+      CycleSum cyc_a, cyc_acc, cyc_b, cyc_heads;
       while (ok) {
         if (!mbar_wait(bar_item_full + 8 * is, iph, a.limit_ns, abort_flag)) {
           ok = false;
@@ -436,18 +471,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kind == kItemEnd) break;
         if (kind != kItemTile && kind != kItemSample) continue;
+        cyc_b.start();
         if (!mbar_wait(bar_b_full, bph, a.limit_ns, abort_flag)) {
           ok = false;
           break;
         }
+        cyc_b.stop();
         tc_fence_after();
         const uint32_t b_hi = sB, b_lo = sB + kBHalf;
         for (int h = 0; h < a.Hi; ++h) {
-          if (!mbar_wait(bar_a_full + 8 * as, aph, a.limit_ns, abort_flag) ||
-              !mbar_wait(bar_acc_empty + 8 * cs, cph ^ 1, a.limit_ns, abort_flag)) {
+          cyc_a.start();
+          const bool got_a = mbar_wait(bar_a_full + 8 * as, aph, a.limit_ns, abort_flag);
+          cyc_a.stop();
+          cyc_acc.start();
+          if (!got_a || !mbar_wait(bar_acc_empty + 8 * cs, cph ^ 1, a.limit_ns, abort_flag)) {
             ok = false;
             break;
           }
+          cyc_acc.stop();
+          cyc_heads.add(1);
           tc_fence_after();
           const uint32_t d = tmem + cs * kBN;
           const uint32_t aa = sA + as * kABytes;
@@ -474,6 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bph ^= 1;
       }
       if (!ok) raise_abort(a, abort_flag);
+      cycles_publish(a, kCycMmaA, cyc_a);
+      cycles_publish(a, kCycMmaAcc, cyc_acc);
+      cycles_publish(a, kCycMmaB, cyc_b);
+      cycles_publish(a, kCycMmaHeads, cyc_heads);
       if (issued) {  // all MMAs done before TMEM and shared memory are released
         umma_commit(bar_drain);
         mbar_wait(bar_drain, 0, a.limit_ns, nullptr);
@@ -650,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const topk::Group grp{etid - gid * topk::kGT, 2 + gid};
     int cs = 0, is = 0;
     uint32_t cph = 0, iph = 0;
+    CycleSum cyc_fw, cyc_fold, cyc_fheads;
     while (true) {
       bool ok = mbar_wait(bar_item_full + 8 * is, iph, a.limit_ns, abort_flag);
       Item it{kItemEnd, 0, 0, 0};
@@ -682,21 +729,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the head weight is fetched one head ahead so its load latency hides
         // behind the previous head's epilogue
         float w_next = valid ? __ldg(wrow) : 0.f;
+        cyc_fold.start();
         for (int h = 0; h < a.Hi; ++h) {
           const float wv = w_next;
           if (h + 1 < a.Hi) w_next = valid ? __ldg(wrow + h + 1) : 0.f;
+          cyc_fw.start();
           if (!mbar_wait(bar_acc_full + 8 * cs, cph, a.limit_ns, abort_flag)) {
             ok = false;
             break;
           }
+          cyc_fw.stop();
+          cyc_fheads.add(1);
           tc_fence_after();
           const float2 w2 = make_float2(wv, wv);
           const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + cs * kBN + cq * kEpiCols;
+          // 16 columns at a time (64 accumulator registers leave room for no
+          // more); the accumulator is released as soon as the last load has
+          // landed, before its columns are folded
 #pragma unroll
           for (int cc = 0; cc < kEpiCols / 16; ++cc) {
             uint32_t r[16];
             tmem_ld16(taddr + cc * 16, r);
             tmem_ld_wait();
+            if (cc == kEpiCols / 16 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_acc_empty + 8 * cs);
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float2 x =
@@ -704,14 +763,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               acc[cc * 8 + j] = __ffma2_rn(w2, x, acc[cc * 8 + j]);
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_acc_empty + 8 * cs);
           if (++cs == 2) {
             cs = 0;
             cph ^= 1;
           }
         }
+        cyc_fold.stop();
         DSA_STAMP(ts1);
         // the item's dependencies (met long ago, as a rule)
         if (ok) ok = mbar_wait(bar_deps + 8 * is, iph, a.limit_ns, abort_flag);
@@ -874,6 +931,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         is = 0;
         iph ^= 1;
       }
+    }
+    if (etid == 0) {
+      cycles_publish(a, kCycFoldWait, cyc_fw);
+      cycles_publish(a, kCycFold, cyc_fold);
+      cycles_publish(a, kCycFoldHeads, cyc_fheads);
     }
   }
 

@@ -8,15 +8,19 @@
 // key (score desc, index asc).  Keys are the order-preserving 32-bit images of
 // the fp32 scores (topk_row.cuh: score_key).
 //
-// select_value  the need-th largest of N keys given by a getter: a min/max
-//               pass, then rounds that histogram the remaining span into 256
-//               bins and keep the bin holding the need-th largest; a bin of
-//               at most 32 keys is ranked directly.
-// threshold     the rsel-th largest composite key among a row's sampled pools.
-// topk          the exact top-k of a candidate list (topk <= 512), sorted by
-//               pool index with a bitonic network held in registers.
-// Global loads go through L2 only (__ldcg): other CTAs wrote the data during
-// this kernel.
+// Selections run as passes over data that other CTAs wrote to global memory
+// (candidate lists, sampled scores), read through L2 with kU loads in flight
+// per lane.  A selection of the need-th largest key takes a min/max pass, then
+// rounds that histogram the remaining span into 256 bins and keep the bin
+// holding the need-th largest; a bin of at most 32 keys is ranked directly in
+// the next pass.  Two selections can share their passes (select2).
+//
+// threshold   the rsel-th largest composite key among a row's sampled pools;
+// topk        the exact top-k (topk <= 512) of a candidate list {key, pool}:
+//             T = the topk-th largest key, then one pass files the pools
+//             above T and the ties at T; the lowest-index ties complete the
+//             row (ranked in shared memory), which is sorted by pool index
+//             with a bitonic network held in registers.
 #pragma once
 
 #include "topk_row.cuh"
@@ -25,13 +29,18 @@ namespace dsa {
 namespace wsel {
 
 constexpr int kBins = 256;
-constexpr int kMaxK = 512;  // largest topk of the warp path
+constexpr int kMaxK = 512;     // largest topk of the warp path
 constexpr int kPer = kMaxK / 32;
+constexpr int kMaxTies = 2 * kBins;  // ties at the k-th key ranked in shared memory
+constexpr int kU = 16;         // loads in flight per lane in a pass (8 B or less each)
 
 struct alignas(16) Smem {
-  uint32_t hist[kBins];
-  uint32_t small[32];
+  union {
+    uint32_t hist[2][kBins];  // the selections' histograms
+    uint32_t ties[kMaxTies];  // then: the pools tied at the k-th key
+  } r1;
   uint32_t out[kMaxK];
+  uint32_t small[2][32];
 };
 
 __device__ __forceinline__ uint32_t warp_min(uint32_t v) {
@@ -59,47 +68,98 @@ __device__ __forceinline__ uint32_t warp_excl(uint32_t v, int lane) {
   }
   return x - v;
 }
+__device__ __forceinline__ uint32_t lanes_below(int lane) { return (1u << lane) - 1u; }
 
-// The need-th largest of the keys get(j, &k) yields for j < N (false: no key
-// at j).  Every key lies in [lo, hi] and at least `need` keys do.  Returns
-// it; *take_eq = how many keys equal to it are among the need largest.
-template <typename Get>
-__device__ __forceinline__ uint32_t select_value(Smem& sm, int lane, int N, uint32_t lo, uint32_t hi, uint32_t need,
-                                                 Get&& get, uint32_t* take_eq) {
-  while (true) {
-    if (lo == hi) {
-      *take_eq = need;
-      return lo;
-    }
-    const uint32_t span = hi - lo;
-    const int bits = 32 - __clz(span);
-    const int sh = bits > 8 ? bits - 8 : 0;
-    const uint32_t nb = (span >> sh) + 1u;
+// One pass over src[0 .. n): f(j, value, valid) for each element, called by
+// all lanes together (warp-uniform), U loads in flight per lane.
+template <int U = kU, typename T, typename F>
+__device__ __forceinline__ void scan(const T* src, int n, int lane, F&& f) {
+  for (int j0 = 0; j0 < n; j0 += 32 * U) {
+    T x[U];
 #pragma unroll
-    for (int q = 0; q < kBins / 32; ++q) sm.hist[lane + 32 * q] = 0u;
-    __syncwarp();
-    for (int j = lane; j < N; j += 32) {
-      uint32_t k;
-      if (get(j, k) && k >= lo && k <= hi) atomicAdd(&sm.hist[(k - lo) >> sh], 1u);
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u + lane;
+      x[u] = j < n ? __ldcg(src + j) : T{};
     }
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (j0 + 32 * u >= n) break;
+      const int j = j0 + 32 * u + lane;
+      f(j, x[u], j < n);
+    }
+  }
+}
+
+// A selection: the need-th largest key in [lo, hi] (at least need keys lie
+// there).  On completion val = that key and take = how many keys equal to it
+// are among the need largest.
+enum : int { kSelHist = 0, kSelSmall = 1, kSelDone = 2 };
+struct Sel {
+  uint32_t lo, hi, need;
+  uint32_t val, take;
+  uint32_t n;  // keys collected by a small pass
+  int sh;      // digit shift of a histogram pass
+  int st;
+};
+
+__device__ __forceinline__ Sel sel_make(uint32_t lo, uint32_t hi, uint32_t need) {
+  return Sel{lo, hi, need, 0u, 0u, 0u, 0, kSelHist};
+}
+__device__ __forceinline__ Sel sel_none(uint32_t val) { return Sel{0u, 0u, 0u, val, 0u, 0u, 0, kSelDone}; }
+
+__device__ __forceinline__ void sel_prepare(Sel& s, uint32_t* hist, int lane) {
+  if (s.st == kSelHist) {
+    if (s.lo == s.hi) {
+      s.val = s.lo;
+      s.take = s.need;
+      s.st = kSelDone;
+      return;
+    }
+    const int bits = 32 - __clz(s.hi - s.lo);
+    s.sh = bits > 8 ? bits - 8 : 0;
+#pragma unroll
+    for (int q = 0; q < kBins / 32; ++q) hist[lane + 32 * q] = 0u;
+  } else if (s.st == kSelSmall) {
+    s.n = 0u;
+  }
+}
+
+__device__ __forceinline__ void sel_feed(Sel& s, uint32_t* hist, uint32_t* small, int lane, uint32_t k, bool has) {
+  const bool in = has && k >= s.lo && k <= s.hi;
+  if (s.st == kSelHist) {
+    if (in) atomicAdd(&hist[(k - s.lo) >> s.sh], 1u);
+  } else if (s.st == kSelSmall) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, in);
+    const uint32_t pos = s.n + __popc(bal & lanes_below(lane));
+    if (in && pos < 32u) small[pos] = k;
+    s.n += __popc(bal);
+  }
+}
+
+// After a pass; false when the pass's counts contradict the selection (the
+// data changed), which the callers treat as a failed row.
+__device__ __forceinline__ bool sel_resolve(Sel& s, const uint32_t* hist, const uint32_t* small, int lane) {
+  if (s.st == kSelHist) {
+    const uint32_t nb = ((s.hi - s.lo) >> s.sh) + 1u;
     // lane L holds bins nb-1-8L .. nb-8-8L, in descending order
-    uint32_t c[8], s = 0;
+    uint32_t c[8], sum = 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int b = static_cast<int>(nb) - 1 - 8 * lane - q;
-      c[q] = b >= 0 ? sm.hist[b] : 0u;
-      s += c[q];
+      c[q] = b >= 0 ? hist[b] : 0u;
+      sum += c[q];
     }
-    const uint32_t excl = warp_excl(s, lane);
-    const bool mine = excl < need && excl + s >= need;
-    const int owner = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    const uint32_t excl = warp_excl(sum, lane);
+    const bool mine = excl < s.need && excl + sum >= s.need;
+    const uint32_t who = __ballot_sync(0xffffffffu, mine);
+    if (who == 0u) return false;
+    const int owner = __ffs(who) - 1;
     uint32_t b_sel = 0, above = 0, inbin = 0;
     if (mine) {
       uint32_t cum = excl;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        if (cum + c[q] >= need) {
+        if (cum + c[q] >= s.need) {
           b_sel = nb - 1 - 8 * lane - q;
           above = cum;
           inbin = c[q];
@@ -111,86 +171,103 @@ __device__ __forceinline__ uint32_t select_value(Smem& sm, int lane, int N, uint
     b_sel = __shfl_sync(0xffffffffu, b_sel, owner);
     above = __shfl_sync(0xffffffffu, above, owner);
     inbin = __shfl_sync(0xffffffffu, inbin, owner);
-    need -= above;
-    const uint32_t nlo = lo + (b_sel << sh);
-    const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << sh) - 1ull);
-    lo = nlo;
-    hi = nhi < hi ? static_cast<uint32_t>(nhi) : hi;
-    __syncwarp();
-    if (sh == 0) {
-      *take_eq = need;
-      return lo;
+    s.need -= above;
+    const uint32_t nlo = s.lo + (b_sel << s.sh);
+    const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << s.sh) - 1ull);
+    s.lo = nlo;
+    s.hi = nhi < s.hi ? static_cast<uint32_t>(nhi) : s.hi;
+    if (s.sh == 0) {
+      s.val = s.lo;
+      s.take = s.need;
+      s.st = kSelDone;
+    } else if (inbin <= 32u) {
+      s.st = kSelSmall;
     }
-    if (inbin > 32u) continue;
-    // at most 32 keys left in [lo, hi]: one per lane, ranked directly
-    uint32_t n = 0;
-    for (int j0 = 0; j0 < N; j0 += 32) {
-      const int j = j0 + lane;
-      uint32_t k = 0;
-      const bool in = j < N && get(j, k) && k >= lo && k <= hi;
-      const uint32_t bal = __ballot_sync(0xffffffffu, in);
-      if (in) sm.small[n + __popc(bal & ((1u << lane) - 1u))] = k;
-      n += __popc(bal);
-    }
-    __syncwarp();
-    const uint32_t kj = lane < static_cast<int>(n) ? sm.small[lane] : 0u;
+  } else if (s.st == kSelSmall) {
+    // at most 32 keys in [lo, hi]: one per lane, ranked directly
+    const uint32_t n = min(s.n, 32u);
+    const uint32_t kj = lane < static_cast<int>(n) ? small[lane] : 0u;
     uint32_t gt = 0, eq = 0;
     for (uint32_t q = 0; q < n; ++q) {
-      const uint32_t kq = sm.small[q];
+      const uint32_t kq = small[q];
       gt += kq > kj;
       eq += kq == kj;
     }
-    const bool hit = lane < static_cast<int>(n) && gt < need && need <= gt + eq;
-    const int who = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
-    const uint32_t T = __shfl_sync(0xffffffffu, kj, who);
-    *take_eq = need - __shfl_sync(0xffffffffu, gt, who);
-    __syncwarp();
-    return T;
+    const bool hit = lane < static_cast<int>(n) && gt < s.need && s.need <= gt + eq;
+    const uint32_t who = __ballot_sync(0xffffffffu, hit);
+    if (who == 0u || s.n > 32u) return false;
+    const int w = __ffs(who) - 1;
+    s.val = __shfl_sync(0xffffffffu, kj, w);
+    s.take = s.need - __shfl_sync(0xffffffffu, gt, w);
+    s.st = kSelDone;
   }
+  return true;
+}
+
+// Runs selections s0 and s1 to completion over shared passes: pass(f) makes
+// one pass calling f(k0, has0, k1, has1) warp-uniformly per element.
+template <typename Pass>
+__device__ __forceinline__ bool select2(Smem& sm, int lane, Sel& s0, Sel& s1, Pass&& pass) {
+  // each histogram pass narrows the span by 8 bits; a small pass ends it
+  for (int round = 0; round < 6; ++round) {
+    __syncwarp();
+    sel_prepare(s0, sm.r1.hist[0], lane);
+    sel_prepare(s1, sm.r1.hist[1], lane);
+    if (s0.st == kSelDone && s1.st == kSelDone) return true;
+    __syncwarp();
+    pass([&](uint32_t k0, bool h0, uint32_t k1, bool h1) {
+      sel_feed(s0, sm.r1.hist[0], sm.small[0], lane, k0, h0);
+      sel_feed(s1, sm.r1.hist[1], sm.small[1], lane, k1, h1);
+    });
+    __syncwarp();
+    if (!sel_resolve(s0, sm.r1.hist[0], sm.small[0], lane) || !sel_resolve(s1, sm.r1.hist[1], sm.small[1], lane))
+      return false;
+  }
+  return s0.st == kSelDone && s1.st == kSelDone;
 }
 
 // The rsel-th largest composite key (score key, -index) among the G sampled
 // scores samp[0 .. G) of one row, sample j being pool j * sigma: (t, p_t).
+// Should the passes disagree, the threshold lets every pool through, which
+// overflows the candidate list and sends the row to the fallback kernel.
 __device__ __noinline__ uint2 threshold(Smem& sm, int lane, const float* samp, int G, int rsel, int sigma) {
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-  for (int j = lane; j < G; j += 32) {
-    const uint32_t k = topk::score_key(__ldcg(samp + j));
-    lo = min(lo, k);
-    hi = max(hi, k);
-  }
+  scan(samp, G, lane, [&](int, float v, bool ok) {
+    if (ok) {
+      const uint32_t k = topk::score_key(v);
+      lo = min(lo, k);
+      hi = max(hi, k);
+    }
+  });
   lo = warp_min(lo);
   hi = warp_max(hi);
-  uint32_t take_eq;
-  const uint32_t T = select_value(sm, lane, G, lo, hi, static_cast<uint32_t>(min(rsel, G)),
-                                  [&](int j, uint32_t& k) {
-                                    k = topk::score_key(__ldcg(samp + j));
-                                    return true;
-                                  },
-                                  &take_eq);
-  // among the samples whose key is T, the take_eq-th smallest index: the
-  // take_eq-th largest of (G - 1 - j)
+  const uint2 all = make_uint2(0u, 0x7FFFFFFFu);
+  Sel s = sel_make(lo, hi, static_cast<uint32_t>(min(rsel, G))), none = sel_none(0u);
+  if (!select2(sm, lane, s, none, [&](auto&& f) {
+        scan(samp, G, lane, [&](int, float v, bool ok) { f(topk::score_key(v), ok, 0u, false); });
+      }))
+    return all;
+  const uint32_t T = s.val;
+  // among the samples whose key is T, the take-th smallest index: the take-th
+  // largest of (G - 1 - j)
   uint32_t vlo = 0xFFFFFFFFu, vhi = 0u;
-  for (int j = lane; j < G; j += 32)
-    if (topk::score_key(__ldcg(samp + j)) == T) {
+  scan(samp, G, lane, [&](int j, float v, bool ok) {
+    if (ok && topk::score_key(v) == T) {
       vlo = min(vlo, static_cast<uint32_t>(G - 1 - j));
       vhi = max(vhi, static_cast<uint32_t>(G - 1 - j));
     }
+  });
   vlo = warp_min(vlo);
   vhi = warp_max(vhi);
-  uint32_t dummy;
-  const uint32_t v = select_value(sm, lane, G, vlo, vhi, take_eq,
-                                  [&](int j, uint32_t& k) {
-                                    if (topk::score_key(__ldcg(samp + j)) != T) return false;
-                                    k = static_cast<uint32_t>(G - 1 - j);
-                                    return true;
-                                  },
-                                  &dummy);
-  return make_uint2(T, static_cast<uint32_t>(G - 1 - static_cast<int>(v)) * static_cast<uint32_t>(sigma));
-}
-
-__device__ __forceinline__ uint2 load_cand(const uint2* c, int j) {
-  const unsigned long long v = __ldcg(reinterpret_cast<const unsigned long long*>(c) + j);
-  return make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32));
+  Sel t = sel_make(vlo, vhi, s.take);
+  none = sel_none(0u);
+  if (!select2(sm, lane, t, none, [&](auto&& f) {
+        scan(samp, G, lane, [&](int j, float v, bool ok) {
+          f(static_cast<uint32_t>(G - 1 - j), ok && topk::score_key(v) == T, 0u, false);
+        });
+      }))
+    return all;
+  return make_uint2(T, static_cast<uint32_t>(G - 1 - static_cast<int>(t.val)) * static_cast<uint32_t>(sigma));
 }
 
 // Sorts the kMaxK values x (element r * 32 + lane in x[r]) ascending across
@@ -227,69 +304,78 @@ __device__ __forceinline__ void sort_warp(uint32_t (&x)[kPer], int lane) {
   }
 }
 
-// Exact top-k (topk <= kMaxK) of the candidate list c[0 .. count), count >=
-// topk, every pool of the row at or above the threshold being in it; writes
-// orow[0 .. topk) ascending.  Returns false (nothing written) if the kept
-// count does not come out at topk, which a complete list rules out.
+// Exact top-k (topk <= kMaxK) of the candidate list c[0 .. count) ({score
+// key, pool}), count >= topk, every pool of the row at or above the threshold
+// being in it; writes orow[0 .. topk) ascending.  Returns false (nothing
+// written) if the counts do not come out at topk, which a complete list rules
+// out.
 __device__ __noinline__ bool topk(Smem& sm, int lane, const uint2* c, int count, int topk, int32_t* orow) {
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-  for (int j = lane; j < count; j += 32) {
-    const uint32_t k = load_cand(c, j).x;
-    lo = min(lo, k);
-    hi = max(hi, k);
-  }
-  lo = warp_min(lo);
-  hi = warp_max(hi);
-  uint32_t take_eq;
-  const uint32_t T = select_value(sm, lane, count, lo, hi, static_cast<uint32_t>(topk),
-                                  [&](int j, uint32_t& k) {
-                                    k = load_cand(c, j).x;
-                                    return true;
-                                  },
-                                  &take_eq);
-  uint32_t eq = 0, ilo = 0xFFFFFFFFu, ihi = 0u;
-  for (int j = lane; j < count; j += 32) {
-    const uint2 x = load_cand(c, j);
-    if (x.x == T) {
-      ++eq;
-      ilo = min(ilo, x.y);
-      ihi = max(ihi, x.y);
+  scan(c, count, lane, [&](int, const uint2& x, bool v) {
+    if (v) {
+      lo = min(lo, x.x);
+      hi = max(hi, x.x);
     }
-  }
-  eq = warp_sum(eq);
-  uint32_t idx_cut = 0xFFFFFFFFu;
-  if (eq > take_eq) {
-    // keep the take_eq lowest indices among the ties: the take_eq-th largest of ~idx
-    ilo = warp_min(ilo);
-    ihi = warp_max(ihi);
-    uint32_t dummy;
-    idx_cut = ~select_value(sm, lane, count, ~ihi, ~ilo, take_eq,
-                            [&](int j, uint32_t& k) {
-                              const uint2 x = load_cand(c, j);
-                              if (x.x != T) return false;
-                              k = ~x.y;
-                              return true;
-                            },
-                            &dummy);
-  }
-  // compaction in list order (ballots), then a sort by pool index
-  uint32_t n = 0;
-  for (int j0 = 0; j0 < count; j0 += 32) {
-    const int j = j0 + lane;
-    bool keep = false;
-    uint32_t p = 0;
-    if (j < count) {
-      const uint2 x = load_cand(c, j);
-      keep = x.x > T || (x.x == T && x.y <= idx_cut);
-      p = x.y;
-    }
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    const uint32_t pos = n + __popc(bal & ((1u << lane) - 1u));
-    if (keep && pos < static_cast<uint32_t>(kMaxK)) sm.out[pos] = p;
-    n += __popc(bal);
-  }
+  });
+  Sel s = sel_make(warp_min(lo), warp_max(hi), static_cast<uint32_t>(topk)), none = sel_none(0u);
+  if (!select2(sm, lane, s, none, [&](auto&& f) {
+        scan(c, count, lane, [&](int, const uint2& x, bool v) { f(x.x, v, 0u, false); });
+      }))
+    return false;
+  const uint32_t T = s.val, take = s.take, n_gt = static_cast<uint32_t>(topk) - take;
+  // one pass: the pools above T, in list order, and the ties at T
   __syncwarp();
-  if (n != static_cast<uint32_t>(topk)) return false;
+  uint32_t ngt = 0, neq = 0;
+  scan(c, count, lane, [&](int, const uint2& x, bool v) {
+    const bool gt = v && x.x > T, eq = v && x.x == T;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t pg = ngt + __popc(bg & lanes_below(lane)), pe = neq + __popc(be & lanes_below(lane));
+    if (gt && pg < static_cast<uint32_t>(kMaxK)) sm.out[pg] = x.y;
+    if (eq && pe < static_cast<uint32_t>(kMaxTies)) sm.r1.ties[pe] = x.y;
+    ngt += __popc(bg);
+    neq += __popc(be);
+  });
+  if (ngt != n_gt || neq < take) return false;
+  __syncwarp();
+  uint32_t nk = 0;
+  if (neq <= static_cast<uint32_t>(kMaxTies)) {
+    // the take lowest pools among the ties (distinct pools: distinct ranks)
+    for (uint32_t e0 = 0; e0 < neq; e0 += 32) {
+      const uint32_t e = e0 + lane;
+      bool keep = false;
+      uint32_t p = 0;
+      if (e < neq) {
+        p = sm.r1.ties[e];
+        uint32_t rank = 0;
+        for (uint32_t f = 0; f < neq; ++f) rank += sm.r1.ties[f] < p;
+        keep = rank < take;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      const uint32_t pos = n_gt + nk + __popc(bal & lanes_below(lane));
+      if (keep && pos < static_cast<uint32_t>(kMaxK)) sm.out[pos] = p;
+      nk += __popc(bal);
+    }
+  } else {
+    // more ties than the list holds: the take-th smallest pool among them is
+    // the take-th largest of ~pool, then a pass keeps the ties up to it
+    Sel t = sel_make(0u, 0xFFFFFFFFu, take);
+    none = sel_none(0u);
+    if (!select2(sm, lane, t, none, [&](auto&& f) {
+          scan(c, count, lane, [&](int, const uint2& x, bool v) { f(~x.y, v && x.x == T, 0u, false); });
+        }))
+      return false;
+    const uint32_t cut = ~t.val;
+    __syncwarp();
+    scan(c, count, lane, [&](int, const uint2& x, bool v) {
+      const bool keep = v && x.x == T && x.y <= cut;
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      const uint32_t pos = n_gt + nk + __popc(bal & lanes_below(lane));
+      if (keep && pos < static_cast<uint32_t>(kMaxK)) sm.out[pos] = x.y;
+      nk += __popc(bal);
+    });
+  }
+  if (nk != take) return false;
+  __syncwarp();
   uint32_t x[kPer];
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
