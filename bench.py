@@ -313,11 +313,13 @@ def run_reference(args):
 
 def measure_l2_peaks(dsa, torch, dev):
     """L2 rates of the attention kernels' access shapes, on a 64 MiB buffer
-    (L2-resident): streaming reads, random 1 KB pool gathers, and 16-byte fp32
-    vector reductions four rows x 128 B per warp instruction."""
+    (L2-resident): streaming reads, random 1 KB pool gathers, 16-byte fp32
+    vector reductions four rows x 128 B per warp instruction, and bulk fp32
+    reductions from shared memory (2 KB and 512 B operations)."""
     buf = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
     out = {"buffer_mib": 64}
-    for kind, name in ((0, "stream_read_gbs"), (1, "gather_1kb_gbs"), (2, "red_v4_gbs")):
+    for kind, name in ((0, "stream_read_gbs"), (1, "gather_1kb_gbs"), (2, "red_v4_gbs"), (3, "bulk_red_2kb_gbs"),
+                       (4, "bulk_red_512b_gbs")):
         out[name] = max(dsa.measure_l2(kind, buf, iters=20) for _ in range(3))
     del buf
     return out

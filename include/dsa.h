@@ -13,8 +13,9 @@
  *              query chunk (peak scoring memory ~64 GiB -> ~2.3 GiB at 32k)
  *              and sharded by query, exchanging int32 selected-pool indices.
  *  [Anyscale]  "How Lila Sciences and Anyscale Scaled GLM-5.3-Flash
- *              Training", lessons "检查每一层是否运行您认为的内核" (a sparse
- *              kernel that silently fell back to dense attention) and the
+ *              Training", the lesson on checking that every layer runs the
+ *              kernel one expects (a sparse kernel had silently fallen back
+ *              to dense attention) and the
  *              second lesson, on the indexer: sparse attention moves its
  *              quadratic cost into the indexer rather than removing it, and
  *              scoring a few hundred queries at a time keeps the score
@@ -315,6 +316,24 @@ dsa_status_t dsa_sync_status(void* stream);
 /* Clears the device status word (synchronous). */
 dsa_status_t dsa_clear_status(void);
 
+/*
+ * What the last call on this host thread ran ([Anyscale, the lesson on
+ * checking that every layer runs the kernel one expects]).  Writes one JSON
+ * line describing the outermost dsa_* entry point
+ * this thread called last (an entry point that calls another reports as
+ * itself): {"entry": name, "variant": the path it took, "kernels": [[kernel,
+ * launches], ...] in launch order (consecutive launches of one kernel
+ * counted together; empty when the call failed before launching),
+ * "params": {the plan: sizes, query range, chunk slots, sample stride,
+ * threshold rank, candidate slots per row, spans, ...}}.  The fallback-row
+ * count of the indexer is on the device (dsa_index_topk_stats).  Writes at
+ * most len bytes including the terminating NUL (buf may be NULL with len 0)
+ * and returns the full length without the NUL, as snprintf does.
+ * Every entry point also opens an NVTX range named for it, visible to
+ * profilers that record NVTX (no cost otherwise).
+ */
+int dsa_last_kernel_config(char* buf, size_t len);
+
 /* Message describing the last non-OK status returned on this host thread. */
 const char* dsa_last_error(void);
 
@@ -347,7 +366,10 @@ const char* dsa_version(void);
  *   kind 2  red.global.add.v4.f32 on random 2 KB blocks, each warp
  *           instruction adding 128 bytes to each of a block's four 512-byte
  *           rows (the backward's dK/dV reductions); counts bytes added
- * Kind 2 adds into the buffer's contents.
+ *   kind 3  bulk reductions (cp.reduce.async.bulk .add.f32) from shared
+ *           memory, one 2 KB block per operation, random blocks
+ *   kind 4  the same with 512-byte operations (one row each)
+ * Kinds 2..4 add into the buffer's contents.
  */
 double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream);
 

@@ -30,7 +30,8 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_zigzag_ranges", "dsa_index_topk_varlen_workspace", "dsa_index_topk_varlen",
             "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen",
             "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic",
-            "dsa_index_topk_stats", "dsa_measure_l2", "dsa_index_topk_workspace_slots", "dsa_trace_configure")
+            "dsa_index_topk_stats", "dsa_measure_l2", "dsa_index_topk_workspace_slots", "dsa_trace_configure",
+            "dsa_last_kernel_config")
 
 _lock = threading.Lock()
 _lib = None
@@ -107,6 +108,8 @@ def load():
             lib.dsa_index_topk_stats.restype = ctypes.c_int
             lib.dsa_measure_l2.argtypes = [ctypes.c_int, vp, sz, ctypes.c_int, vp]
             lib.dsa_measure_l2.restype = ctypes.c_double
+            lib.dsa_last_kernel_config.argtypes = [ctypes.c_char_p, sz]
+            lib.dsa_last_kernel_config.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -417,8 +420,20 @@ def index_topk_stats(workspace: torch.Tensor, stream=None) -> dict:
     return {names[j]: int(out[j]) for j in range(min(n, len(names)))}
 
 
+def last_kernel_config() -> dict:
+    """What the last dsa_* call made on this host thread ran: its entry point,
+    variant, kernels (name, launches) in launch order and plan parameters."""
+    import json
+    lib = load()
+    n = lib.dsa_last_kernel_config(None, 0)
+    buf = ctypes.create_string_buffer(n + 1)
+    lib.dsa_last_kernel_config(buf, n + 1)
+    return json.loads(buf.value.decode())
+
+
 def measure_l2(kind: int, buf: torch.Tensor, iters: int = 20, stream=None) -> float:
-    """GB/s of an L2 probe kernel on `buf` (kind 0 stream read, 1 1-KB gather, 2 red.v4 reductions)."""
+    """GB/s of an L2 probe kernel on `buf` (kind 0 stream read, 1 1-KB gather, 2 red.v4 reductions,
+    3 / 4 bulk reductions of 2 KB / 512 B)."""
     lib = load()
     r = lib.dsa_measure_l2(kind, buf.data_ptr(), buf.numel() * buf.element_size(), iters, _stream_handle(stream))
     if r < 0:

@@ -5,9 +5,11 @@
 // scores one chunk of queries at a time, so its scratch is a ring of at most
 // eight chunks of scores (chunk x pools x 4 B each; two at the least) rather
 // than the whole S x S/4 matrix.
-// [Anyscale "检查每一层是否运行您认为的内核"] a shape the kernels do not
-// implement is an error, never a silent fallback.
+// [Anyscale, the lesson on checking that every layer runs the kernel one
+// expects] a shape the kernels do not implement is an error, never a silent
+// fallback; dsa_last_kernel_config reports what each call launched.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdarg>
@@ -36,6 +38,18 @@ namespace {
 __device__ unsigned int g_dsa_status;
 
 thread_local std::string g_last_error;
+
+// The record of the outermost entry point in progress (or last finished) on
+// this host thread: its name, the kernels it launched (consecutive launches of
+// one kernel counted together), its plan parameters and its variant.
+struct KernelRecord {
+  std::string entry;
+  std::string variant;
+  std::vector<std::pair<std::string, long long>> kernels;
+  std::vector<std::pair<std::string, long long>> params;
+};
+thread_local KernelRecord g_record;
+thread_local int g_call_depth = 0;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDi = 64;
@@ -173,7 +187,12 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch, int 
     cudaEventRecord(rec.start, stream);
   }
   cudaError_t e = launch();
-  if (e == cudaSuccess) g_launches.fetch_add(kernels, std::memory_order_relaxed);
+  if (e == cudaSuccess) {
+    g_launches.fetch_add(kernels, std::memory_order_relaxed);
+    auto& ks = g_record.kernels;
+    if (!ks.empty() && ks.back().first == name) ks.back().second += kernels;
+    else ks.emplace_back(name, kernels);
+  }
   if (prof) {
     cudaEventRecord(rec.stop, stream);
     std::lock_guard<std::mutex> lk(g_prof_mu);
@@ -274,6 +293,27 @@ size_t index_ws_bytes(int64_t S, int chunk, int topk, int nbuf) {
 namespace dsa {
 void set_last_error(const std::string& msg) { g_last_error = msg; }
 
+void call_begin(const char* fn) {
+  nvtxRangePushA(fn);
+  if (g_call_depth++ == 0) {
+    g_record = KernelRecord{};
+    g_record.entry = fn;
+  }
+}
+void call_end() {
+  --g_call_depth;
+  nvtxRangePop();
+}
+void call_param(const char* key, long long value) {
+  for (auto& kv : g_record.params)
+    if (kv.first == key) {
+      kv.second = value;
+      return;
+    }
+  g_record.params.emplace_back(key, value);
+}
+void call_variant(const char* variant) { g_record.variant = variant; }
+
 unsigned long long current_context_id() {
   using GetCurrent = CUresult (*)(CUcontext*);
   using GetId = CUresult (*)(CUcontext, unsigned long long*);
@@ -307,6 +347,22 @@ extern "C" {
 
 const char* dsa_last_error(void) { return g_last_error.c_str(); }
 
+int dsa_last_kernel_config(char* buf, size_t len) {
+  std::string s = "{\"entry\": \"" + g_record.entry + "\", \"variant\": \"" + g_record.variant + "\", \"kernels\": [";
+  for (size_t j = 0; j < g_record.kernels.size(); ++j)
+    s += (j ? ", [\"" : "[\"") + g_record.kernels[j].first + "\", " + std::to_string(g_record.kernels[j].second) + "]";
+  s += "], \"params\": {";
+  for (size_t j = 0; j < g_record.params.size(); ++j)
+    s += (j ? ", \"" : "\"") + g_record.params[j].first + "\": " + std::to_string(g_record.params[j].second);
+  s += "}}";
+  if (buf && len > 0) {
+    const size_t n = s.size() < len - 1 ? s.size() : len - 1;
+    std::memcpy(buf, s.data(), n);
+    buf[n] = '\0';
+  }
+  return static_cast<int>(s.size());
+}
+
 const char* dsa_version(void) { return "libdsa 0.1.0 (sm_103a)"; }
 
 size_t dsa_index_topk_workspace(int64_t S, int Hi, int Di, int chunk, int topk) {
@@ -322,6 +378,7 @@ size_t dsa_index_topk_workspace_slots(int64_t S, int Hi, int Di, int chunk, int 
 dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
                             int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
                             void* workspace, size_t ws_bytes, void* stream) {
+  const dsa::CallScope scope("dsa_index_topk");
   if (!q_idx || !k_idx || !w || !pool_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: null tensor pointer");
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(pool_idx))
     return fail(DSA_ERR_INVALID_ARG,
@@ -352,6 +409,17 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
   int nbuf = index_min_bufs(S, chunk);  // as many chunk slots as the workspace holds
   while (nbuf < index_max_bufs(S, chunk) && index_layout(S, pl, nbuf + 1).total <= ws_bytes) ++nbuf;
   const IndexLayout L = index_layout(S, pl, nbuf);
+  dsa::call_param("S", S);
+  dsa::call_param("q_begin", q_begin);
+  dsa::call_param("q_end", q_end);
+  dsa::call_param("Hi", Hi);
+  dsa::call_param("topk", topk);
+  dsa::call_param("chunk", chunk);
+  dsa::call_param("chunk_slots", nbuf);
+  dsa::call_param("sample_stride", pl.sigma);
+  dsa::call_param("threshold_rank", pl.rsel);
+  dsa::call_param("candidates_per_row", pl.cap);
+  dsa::call_variant("persistent indexer + top-k (bf16 hi/lo pooled keys), fallback rows recomputed");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   dsa::IndexBuffers b;
   b.sync = reinterpret_cast<unsigned long long*>(ws);
@@ -459,6 +527,7 @@ static dsa_status_t check_range(const char* fn, int64_t S, int64_t q_begin, int6
 dsa_status_t dsa_sparse_attn_fwd_range(const void* q, const void* k, const void* v, const int32_t* pool_idx,
                                        int64_t S, int64_t q_begin, int64_t q_end, int Hq, int D, int topk,
                                        float scale, void* o, float* lse, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_fwd_range");
   if (!q || !k || !v || !pool_idx || !o || !lse)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_fwd: null tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(pool_idx) || !aligned16(o) || !aligned4(lse))
@@ -472,6 +541,11 @@ dsa_status_t dsa_sparse_attn_fwd_range(const void* q, const void* k, const void*
   dsa::LaunchCtx ctx;
   st = make_ctx(stream, &ctx);
   if (st != DSA_OK) return st;
+  dsa::call_param("S", S);
+  dsa::call_param("q_begin", q_begin);
+  dsa::call_param("q_end", q_end);
+  dsa::call_param("topk", topk);
+  dsa::call_variant("gather-bound forward: one CTA per query, cp.async key-pool gather, mma.sync, online softmax");
   cudaError_t e = timed_launch("attn_fwd", ctx.stream, [&] {
     return dsa::launch_attn_fwd(q, k, v, pool_idx, q_begin, q_end, topk, scale, o, lse, ctx);
   });
@@ -481,6 +555,7 @@ dsa_status_t dsa_sparse_attn_fwd_range(const void* q, const void* k, const void*
 
 dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
                                  int Hq, int D, int topk, float scale, void* o, float* lse, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_fwd");
   return dsa_sparse_attn_fwd_range(q, k, v, pool_idx, S, 0, S, Hq, D, topk, scale, o, lse, stream);
 }
 
@@ -494,6 +569,7 @@ dsa_status_t dsa_sparse_attn_bwd_range(const void* dO, const void* q, const void
                                        const float* lse, const int32_t* pool_idx, int64_t S, int64_t q_begin,
                                        int64_t q_end, int Hq, int D, int topk, float scale, void* dq, void* dk,
                                        void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_bwd_range");
   if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_bwd: null tensor pointer");
   if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
@@ -520,6 +596,11 @@ dsa_status_t dsa_sparse_attn_bwd_range(const void* dO, const void* q, const void
   float* dv_acc = reinterpret_cast<float*>(ws + acc_bytes);
   float* delta = reinterpret_cast<float*>(ws + 2 * acc_bytes);
   const int64_t nq = q_end - q_begin;
+  dsa::call_param("S", S);
+  dsa::call_param("q_begin", q_begin);
+  dsa::call_param("q_end", q_end);
+  dsa::call_param("topk", topk);
+  dsa::call_variant("atomic: dq query-major, dK/dV fp32 red.v4 per (query, key), bf16 cast");
   // S * D floats is a multiple of 64, so acc_bytes == S * D * 4 and the accumulators are adjacent
   cudaError_t e = timed_launch("attn_bwd_pre", ctx.stream,
                                [&] { return dsa::launch_attn_bwd_pre(dO, o, nq, S, delta, dk_acc, dv_acc, ctx); });
@@ -539,6 +620,7 @@ dsa_status_t dsa_sparse_attn_bwd(const void* dO, const void* q, const void* k, c
                                  const float* lse, const int32_t* pool_idx, int64_t S, int Hq, int D, int topk,
                                  float scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                                  void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_bwd");
   return dsa_sparse_attn_bwd_range(dO, q, k, v, o, lse, pool_idx, S, 0, S, Hq, D, topk, scale, dq, dk, dv,
                                    workspace, ws_bytes, stream);
 }
@@ -585,6 +667,7 @@ dsa_status_t dsa_sparse_attn_bwd_deterministic(const void* dO, const void* q, co
                                                const void* o, const float* lse, const int32_t* pool_idx, int64_t S,
                                                int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
                                                void* workspace, size_t ws_bytes, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_bwd_deterministic");
   const char* fn = "dsa_sparse_attn_bwd_deterministic";
   if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
     return fail(DSA_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
@@ -609,6 +692,10 @@ dsa_status_t dsa_sparse_attn_bwd_deterministic(const void* dO, const void* q, co
   if (st != DSA_OK) return st;
   const dsa::DetPlan d = dsa::det_plan(S, topk);
   const DetLayout l = det_layout(S, Hq, topk, d);
+  dsa::call_param("S", S);
+  dsa::call_param("topk", topk);
+  dsa::call_param("spans", d.nspan);
+  dsa::call_variant("deterministic: dq query-major, dK/dV key-major in fixed order");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* delta = reinterpret_cast<float*>(ws + l.delta);
   dsa::DetBuffers b;
@@ -684,6 +771,7 @@ size_t dsa_index_topk_varlen_workspace(const int64_t* cu_seqlens, int nseq, int 
 dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const float* w, const int64_t* cu_seqlens,
                                    int nseq, int Hi, int Di, int chunk, int topk, int32_t* pool_idx, void* workspace,
                                    size_t ws_bytes, void* stream) {
+  const dsa::CallScope scope("dsa_index_topk_varlen");
   dsa_status_t st = check_cu_seqlens("dsa_index_topk_varlen", cu_seqlens, nseq);
   if (st != DSA_OK) return st;
   // checked up front, so that an error leaves every sequence untouched: the
@@ -707,6 +795,7 @@ dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const f
 dsa_status_t dsa_sparse_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* pool_idx,
                                         const int64_t* cu_seqlens, int nseq, int Hq, int D, int topk, float scale,
                                         void* o, float* lse, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_fwd_varlen");
   dsa_status_t st = check_cu_seqlens("dsa_sparse_attn_fwd_varlen", cu_seqlens, nseq);
   if (st != DSA_OK) return st;
   const int64_t qrow = static_cast<int64_t>(Hq) * D * 2, krow = static_cast<int64_t>(D) * 2;
@@ -732,6 +821,7 @@ dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const voi
                                         const float* lse, const int32_t* pool_idx, const int64_t* cu_seqlens,
                                         int nseq, int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
                                         void* workspace, size_t ws_bytes, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_bwd_varlen");
   dsa_status_t st = check_cu_seqlens("dsa_sparse_attn_bwd_varlen", cu_seqlens, nseq);
   if (st != DSA_OK) return st;
   const size_t need = dsa_sparse_attn_bwd_varlen_workspace(cu_seqlens, nseq, Hq, D);

@@ -26,6 +26,20 @@ inline cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<boo
   return e;
 }
 
+// Host side of every public entry point: an NVTX range named for it, and (for
+// the outermost entry a host thread is in) a fresh record of the kernels it
+// launches and the plan they ran with, read back by dsa_last_kernel_config.
+void call_begin(const char* fn);
+void call_end();
+void call_param(const char* key, long long value);
+void call_variant(const char* variant);
+struct CallScope {
+  explicit CallScope(const char* fn) { call_begin(fn); }
+  ~CallScope() { call_end(); }
+  CallScope(const CallScope&) = delete;
+  CallScope& operator=(const CallScope&) = delete;
+};
+
 struct LaunchCtx {
   cudaStream_t stream;
   unsigned* status;        // device status word (kStatus* bits)

@@ -35,6 +35,7 @@
 #include <string>
 
 #include "../../include/dsa.h"
+#include "dsa_kernels.h"
 
 namespace dsa {
 void set_last_error(const std::string& msg);  // dsa_api.cu: the message dsa_last_error() returns
@@ -68,6 +69,7 @@ extern "C" {
 dsa_status_t dsa_index_topk_noalloc(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
                                     int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
                                     void* stream) {
+  const dsa::CallScope scope("dsa_index_topk_noalloc");
   const size_t need = dsa_index_topk_workspace(S, Hi, Di, chunk, topk) == 0 ? 0 : dsa::index_topk_min_workspace(S, chunk, topk);
   if (need == 0) {
     // invalid sizes: let the regular entry point report the precise reason

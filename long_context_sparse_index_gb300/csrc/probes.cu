@@ -12,7 +12,11 @@
 //   kind 1  random 1 KB blocks, each read by one warp (two 16-byte loads a lane)
 //   kind 2  red.global.add.v4.f32 on random 2 KB blocks (4 rows x 512 B):
 //           each warp instruction adds 128 bytes to each of the 4 rows
-// All three report bytes moved (read, or added) per second.
+//   kind 3  bulk reductions (cp.reduce.async.bulk .add.f32) from shared
+//           memory: one 2 KB block per operation, random blocks, up to 8
+//           operations in flight per warp
+//   kind 4  the same with 512-byte operations (one row each)
+// All report bytes moved (read, or added) per second.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -79,13 +83,42 @@ __global__ void probe_red_kernel(float* __restrict__ buf, uint32_t nblocks, int 
   }
 }
 
+// Warp w's lane 0 adds its 2 KB shared-memory block of ones into random
+// 2 KB blocks of buf (op_bytes per bulk operation), keeping at most 8 bulk
+// groups in flight; all complete before the CTA exits.
+__global__ void probe_bulk_red_kernel(float* __restrict__ buf, uint32_t nblocks, int per_warp, int op_bytes) {
+  __shared__ __align__(128) float src[8][512];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = lane; e < 512; e += 32) src[wib][e] = 1.f;
+  __syncwarp();
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t s = dsa::smem_u32(src[wib]);
+    const int nops = 2048 / op_bytes;
+    for (int it = 0; it < per_warp; ++it) {
+      const uint32_t b = mix32(warp * 0x9E3779B9u + static_cast<uint32_t>(it)) % nblocks;
+      float* dst = buf + static_cast<int64_t>(b) * 512;
+      for (int o = 0; o < nops; ++o)
+        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                         dst + o * (op_bytes / 4)),
+                     "r"(s + o * op_bytes), "r"(op_bytes)
+                     : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 8;" ::: "memory");
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+}
+
 }  // namespace
 
 extern "C" {
 
 double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream) {
-  if (!buf || bytes < 4096 || iters < 1 || kind < 0 || kind > 2 || (reinterpret_cast<uintptr_t>(buf) & 15u)) {
-    dsa::set_last_error("dsa_measure_l2: kind must be 0..2, buf 16-byte aligned, bytes >= 4096, iters >= 1");
+  if (!buf || bytes < 4096 || iters < 1 || kind < 0 || kind > 4 || (reinterpret_cast<uintptr_t>(buf) & 15u)) {
+    dsa::set_last_error("dsa_measure_l2: kind must be 0..4, buf 16-byte aligned, bytes >= 4096, iters >= 1");
     return -1.0;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -110,11 +143,16 @@ double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream
       const int per_warp = 64 * reps;
       probe_gather_kernel<<<grid, block, 0, st>>>(static_cast<const uint4*>(buf), nb, per_warp, sink);
       moved = static_cast<double>(warps) * per_warp * 1024.0;
-    } else {
+    } else if (kind == 2) {
       const uint32_t nb = static_cast<uint32_t>(bytes / 2048);
       const int per_warp = 64 * reps;
       probe_red_kernel<<<grid, block, 0, st>>>(static_cast<float*>(buf), nb, per_warp);
       moved = static_cast<double>(warps) * per_warp * 512.0;
+    } else {
+      const uint32_t nb = static_cast<uint32_t>(bytes / 2048);
+      const int per_warp = 16 * reps;
+      probe_bulk_red_kernel<<<grid, block, 0, st>>>(static_cast<float*>(buf), nb, per_warp, kind == 3 ? 2048 : 512);
+      moved = static_cast<double>(warps) * per_warp * 2048.0;
     }
   };
   cudaEvent_t a, b;

@@ -155,6 +155,29 @@ def test_attention_ranges_are_checked(lib):
     assert b(*args) == dsa.DSA_ERR_INVALID_ARG
 
 
+def test_last_kernel_config_reports_the_outermost_call(lib):
+    """dsa_last_kernel_config describes the last entry point this thread
+    called: a call rejected before any launch lists no kernels; an entry point
+    that forwards to another (dsa_sparse_attn_fwd -> _range) reports as
+    itself; the output is truncated to the buffer with snprintf semantics."""
+    import json
+    import long_context_sparse_index_gb300 as dsa
+    assert _idx(lib, S=0) == dsa.DSA_ERR_INVALID_ARG
+    cfg = dsa.last_kernel_config()
+    assert cfg["entry"] == "dsa_index_topk" and cfg["kernels"] == []
+    f = lib.dsa_sparse_attn_fwd
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 16, 128, 8, 0.0, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG
+    cfg = dsa.last_kernel_config()
+    assert cfg["entry"] == "dsa_sparse_attn_fwd" and cfg["kernels"] == [] and cfg["params"] == {}
+    n = lib.dsa_last_kernel_config(None, 0)
+    full = ctypes.create_string_buffer(n + 1)
+    assert lib.dsa_last_kernel_config(full, n + 1) == n
+    assert json.loads(full.value.decode())["entry"] == "dsa_sparse_attn_fwd"
+    short = ctypes.create_string_buffer(8)
+    assert lib.dsa_last_kernel_config(short, 8) == n
+    assert short.value == full.value[:7]
+
+
 def test_deterministic_backward_workspace_and_checks(lib):
     """The deterministic backward's workspace holds at least its fp32 dK/dV
     accumulators, Delta and the per-pool query lists (S x topk int32), plus

@@ -472,3 +472,33 @@ def test_binding_refuses_bad_outputs_and_shapes():
         dsa.dsa_sparse_attn_bwd_deterministic(q, q, k, v, o, lse, st, dk=torch.empty((64, 64), dtype=torch.bfloat16,
                                                                                        device=DEV))
     dsa.dsa_sync_status()
+
+
+def test_last_kernel_config_names_the_kernels_that_ran():
+    """Each call's record names the kernels it launched, in order, and its plan."""
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q, k, w = _indexer_to_gpu(*synth.indexer_inputs(wl))
+    sel = dsa.dsa_index_topk(q, k, w, chunk=wl.chunk, topk=wl.topk)
+    cfg = dsa.last_kernel_config()
+    assert cfg["entry"] == "dsa_index_topk"
+    assert [name for name, _ in cfg["kernels"]] == ["pool_keys", "index_topk", "index_fallback"]
+    assert cfg["params"]["topk"] == wl.topk and cfg["params"]["chunk"] == wl.chunk
+    assert 1 <= cfg["params"]["chunk_slots"] <= 8
+    wa = synth.Workload("t", 4096, topk=256, seed=7)
+    qa, ka, va = synth.attention_inputs(wa)
+    qt, kt, vt, dOt = _attn_to_gpu(qa, ka, va, synth.grad_output(wa))
+    st = torch.from_numpy(synth.stand_in_selection(wa)).to(DEV)
+    o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, st)
+    cfg = dsa.last_kernel_config()
+    # the binding calls the range form, which the record names
+    assert cfg["entry"] in ("dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_range") and cfg["kernels"] == [["attn_fwd", 1]]
+    dsa.dsa_sparse_attn_bwd(dOt, qt, kt, vt, o, lse, st)
+    cfg = dsa.last_kernel_config()
+    assert cfg["variant"].startswith("atomic")
+    assert [name for name, _ in cfg["kernels"]] == ["attn_bwd_pre", "attn_bwd", "attn_bwd_cast"]
+    dsa.dsa_sparse_attn_bwd_deterministic(dOt, qt, kt, vt, o, lse, st)
+    cfg = dsa.last_kernel_config()
+    assert cfg["variant"].startswith("deterministic")
+    assert dict(cfg["kernels"])["det_span"] == cfg["params"]["spans"]
+    torch.cuda.synchronize()
+    assert sel.shape == (wl.S, wl.topk)
