@@ -247,11 +247,18 @@ dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges);
  * keys.  Tensors, scale and topk are as in the single-sequence calls, with
  * the packed length in place of S; dk/dv rows of a sequence hold that
  * sequence's gradient.  The workspace must hold the *_varlen_workspace()
- * bytes (the single-sequence workspace of the longest sequence); the
- * sequences run one after another on `stream`.  An invalid cu_seqlens or a
- * short workspace returns DSA_ERR_INVALID_ARG / DSA_ERR_WORKSPACE (and, for
- * the query functions, 0) before anything runs.  (The pages train single
- * sequences; packing is what a training data loader hands the layer.)
+ * bytes: for the indexer, the single-sequence workspace of the longest
+ * sequence; for the backward, the single-sequence workspace of the packed
+ * length (its fp32 dK/dV accumulators span the batch).  The attention calls
+ * cover the batch with one launch per kernel and per 256 sequences (a table
+ * of their starts rides in the launch parameters; each query finds its
+ * sequence by binary search).  The indexer fills the rows of every sequence
+ * of at most 4 * topk + 4 tokens (each row keeps all its pools) with one
+ * launch per 256 such sequences, and runs once per longer sequence, one after
+ * another on `stream`.  An invalid cu_seqlens or a short workspace returns
+ * DSA_ERR_INVALID_ARG / DSA_ERR_WORKSPACE (and, for the query functions, 0)
+ * before anything runs.  (The pages train single sequences; packing is what a
+ * training data loader hands the layer.)
  */
 size_t dsa_index_topk_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hi, int Di, int chunk, int topk);
 dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const float* w, const int64_t* cu_seqlens,

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const float* __restrict__ lse, const float* __restrict__ delta,
                     const int32_t* __restrict__ pool_idx, int64_t q0, int topk, float scale, float scale_log2,
                     __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
-                    unsigned* status) {
+                    unsigned* status, const __grid_constant__ SeqTable tab) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 127u) & ~127u;
@@ -102,7 +102,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int g = lane >> 2, t4 = lane & 3;
   // query i (global position) is local row r of q, dO, lse, Delta, pool_idx and dq
   const int64_t r = blockIdx.x;
-  const int64_t i = q0 + r;
+  int64_t i, kv0;
+  seq_locate(tab, q0, r, &i, &kv0);  // i: position in its sequence; its keys start at packed row kv0
+  k += kv0 * kD;
+  v += kv0 * kD;
+  if (dk_acc != nullptr) {
+    dk_acc += kv0 * kD;
+    dv_acc += kv0 * kD;
+  }
   const int64_t n_elig = i >> 2;
 
   if (tid == 0) s_nsel = topk;
@@ -420,15 +427,17 @@ cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64
 
 cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
                             const float* delta, const int32_t* pool_idx, int64_t q_begin, int64_t q_end, int topk,
-                            float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx) {
+                            float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx,
+                            const SeqTable* tab) {
   if (q_end <= q_begin) return cudaSuccess;
+  static const SeqTable kNoTable = {};
   static std::atomic<bool> attr_done[kAttrDevices];
   const cudaError_t e = set_smem_limit_once(attn_bwd_kernel, static_cast<int>(smem_bytes(kMaxTopk)), attr_done);
   if (e != cudaSuccess) return e;
   attn_bwd_kernel<<<static_cast<unsigned>(q_end - q_begin), kThreads, smem_bytes(topk), ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(q),
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), lse, delta, pool_idx, q_begin, topk,
-      scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc, ctx.status);
+      scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc, ctx.status, tab ? *tab : kNoTable);
   return cudaGetLastError();
 }
 

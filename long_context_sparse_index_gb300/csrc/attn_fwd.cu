@@ -80,7 +80,8 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
 __global__ void __launch_bounds__(kThreads, 3)
     attn_fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t q0, int topk,
-                    float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* status) {
+                    float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* status,
+                    const __grid_constant__ SeqTable tab) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 127u) & ~127u;
@@ -93,9 +94,13 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  // query i (global position) is local row r of q, pool_idx, o and lse
+  // query i (position in its sequence) is local row r of q, pool_idx, o and
+  // lse; its sequence's keys start at packed row kv0 of k and v
   const int64_t r = blockIdx.x;
-  const int64_t i = q0 + r;
+  int64_t i, kv0;
+  seq_locate(tab, q0, r, &i, &kv0);
+  k += kv0 * kD;
+  v += kv0 * kD;
   const int64_t n_elig = i >> 2;
 
   // ---- selected pools of this query (leading non-negative entries)
@@ -314,15 +319,17 @@ __global__ void __launch_bounds__(kThreads, 3)
 }  // namespace
 
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
-                            int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx) {
+                            int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx,
+                            const SeqTable* tab) {
   if (q_end <= q_begin) return cudaSuccess;
+  static const SeqTable kNoTable = {};
   static std::atomic<bool> attr_done[kAttrDevices];
   const cudaError_t e = set_smem_limit_once(attn_fwd_kernel, static_cast<int>(smem_bytes(kMaxTopk)), attr_done);
   if (e != cudaSuccess) return e;
   attn_fwd_kernel<<<static_cast<unsigned>(q_end - q_begin), kThreads, smem_bytes(topk), ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), pool_idx, q_begin, topk, scale * kLog2e, static_cast<__nv_bfloat16*>(o), lse,
-      ctx.status);
+      ctx.status, tab ? *tab : kNoTable);
   return cudaGetLastError();
 }
 

@@ -744,9 +744,12 @@ dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges) 
 }
 
 // ---------------------------------------------------------------- packed variable-length batches
-// Each sequence of the batch is its own causal layer: the calls below run the
-// single-sequence entry points on each sequence's rows in turn (one stream,
-// so one workspace serves them all).
+// Each sequence of the batch is its own causal layer.  The attention calls
+// cover the whole batch with one launch per kernel and per 256 sequences (a
+// table of sequence starts rides in the launch's parameters); the indexer
+// fills the rows of short sequences (every row keeps all its pools) in one
+// launch per 256 of them and runs the persistent indexer once per longer
+// sequence.
 
 static dsa_status_t check_cu_seqlens(const char* fn, const int64_t* cu, int nseq) {
   if (!cu || nseq < 1) return fail(DSA_ERR_INVALID_ARG, "%s: need cu_seqlens and nseq >= 1", fn);
@@ -754,6 +757,8 @@ static dsa_status_t check_cu_seqlens(const char* fn, const int64_t* cu, int nseq
   for (int s = 0; s < nseq; ++s)
     if (cu[s + 1] <= cu[s])
       return fail(DSA_ERR_INVALID_ARG, "%s: cu_seqlens must be strictly increasing (sequence %d is empty)", fn, s);
+  if (cu[nseq] > 0x7FFFFFFFLL)
+    return fail(DSA_ERR_INVALID_ARG, "%s: packed length %lld out of range", fn, (long long)cu[nseq]);
   return DSA_OK;
 }
 
@@ -761,6 +766,15 @@ static int64_t max_len(const int64_t* cu, int nseq) {
   int64_t m = 0;
   for (int s = 0; s < nseq; ++s) m = cu[s + 1] - cu[s] > m ? cu[s + 1] - cu[s] : m;
   return m;
+}
+
+// the table of sequences s0 .. s0+n-1
+static dsa::SeqTable seq_table(const int64_t* cu, int s0, int n) {
+  dsa::SeqTable t;
+  t.n = n;
+  t.row0 = cu[s0];
+  for (int j = 0; j <= n; ++j) t.cu[j] = cu[s0 + j];
+  return t;
 }
 
 size_t dsa_index_topk_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hi, int Di, int chunk, int topk) {
@@ -772,23 +786,63 @@ dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const f
                                    int nseq, int Hi, int Di, int chunk, int topk, int32_t* pool_idx, void* workspace,
                                    size_t ws_bytes, void* stream) {
   const dsa::CallScope scope("dsa_index_topk_varlen");
-  dsa_status_t st = check_cu_seqlens("dsa_index_topk_varlen", cu_seqlens, nseq);
+  const char* fn = "dsa_index_topk_varlen";
+  dsa_status_t st = check_cu_seqlens(fn, cu_seqlens, nseq);
   if (st != DSA_OK) return st;
-  // checked up front, so that an error leaves every sequence untouched: the
-  // other checks are the same for every sequence and fail on the first
+  // every check up front, so that an error leaves every sequence untouched
+  if (!q_idx || !k_idx || !w || !pool_idx) return fail(DSA_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(pool_idx))
+    return fail(DSA_ERR_INVALID_ARG, "%s: q_idx and k_idx must be 16-byte aligned, w and pool_idx 4-byte aligned", fn);
+  if (chunk < 1 || topk < 1 || Hi < 1)
+    return fail(DSA_ERR_INVALID_ARG, "%s: chunk=%d, topk=%d and Hi=%d must be >= 1", fn, chunk, topk, Hi);
+  if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "%s: Di=%d unsupported (kernels implement Di=64)", fn, Di);
+  if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "%s: Hi=%d unsupported (max %d)", fn, Hi, kMaxHi);
+  if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "%s: topk=%d unsupported (max %d)", fn, topk, kMaxTopk);
   const size_t need = dsa_index_topk_varlen_workspace(cu_seqlens, nseq, Hi, Di, chunk, topk);
   if (!workspace || ws_bytes < need)
-    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk_varlen: workspace of %zu bytes needed, %zu given", need,
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? ws_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  // a sequence of at most 4 * topk + 4 tokens: no row has more than topk pools
+  const int64_t short_max = 4 * static_cast<int64_t>(topk) + 4;
+  dsa::ShortSeqs sh;
+  sh.n = 0;
+  int n_short = 0, n_long = 0;
+  auto flush = [&]() -> dsa_status_t {
+    if (sh.n == 0) return DSA_OK;
+    const cudaError_t e = timed_launch("short_rows", ctx.stream, [&] {
+      return dsa::launch_short_rows(pool_idx, topk, sh, ctx);
+    });
+    sh.n = 0;
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "dsa_index_topk_varlen: short-row launch");
+  };
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t L = cu_seqlens[s + 1] - cu_seqlens[s];
+    if (L > short_max) continue;
+    sh.start[sh.n] = cu_seqlens[s];
+    sh.len[sh.n] = L;
+    ++n_short;
+    if (++sh.n == dsa::kSeqBatch && (st = flush()) != DSA_OK) return st;
+  }
+  if ((st = flush()) != DSA_OK) return st;
   const uint8_t* qb = static_cast<const uint8_t*>(q_idx);
   const uint8_t* kb = static_cast<const uint8_t*>(k_idx);
   for (int s = 0; s < nseq; ++s) {
     const int64_t o = cu_seqlens[s], L = cu_seqlens[s + 1] - o;
-    st = dsa_index_topk(qb ? qb + o * Hi * Di * 2 : nullptr, kb ? kb + o * Di * 2 : nullptr, w ? w + o * Hi : nullptr,
-                        L, Hi, Di, chunk, topk, 0, L, pool_idx ? pool_idx + o * topk : nullptr, workspace, ws_bytes,
-                        stream);
+    if (L <= short_max) continue;
+    ++n_long;
+    st = dsa_index_topk(qb + o * Hi * Di * 2, kb + o * Di * 2, w + o * Hi, L, Hi, Di, chunk, topk, 0, L,
+                        pool_idx + o * topk, workspace, ws_bytes, stream);
     if (st != DSA_OK) return st;
   }
+  dsa::call_param("sequences", nseq);
+  dsa::call_param("short_sequences", n_short);
+  dsa::call_param("indexed_sequences", n_long);
+  dsa::call_variant("short sequences filled in one launch per 256; the persistent indexer once per longer sequence");
   return DSA_OK;
 }
 
@@ -796,25 +850,40 @@ dsa_status_t dsa_sparse_attn_fwd_varlen(const void* q, const void* k, const void
                                         const int64_t* cu_seqlens, int nseq, int Hq, int D, int topk, float scale,
                                         void* o, float* lse, void* stream) {
   const dsa::CallScope scope("dsa_sparse_attn_fwd_varlen");
-  dsa_status_t st = check_cu_seqlens("dsa_sparse_attn_fwd_varlen", cu_seqlens, nseq);
+  const char* fn = "dsa_sparse_attn_fwd_varlen";
+  dsa_status_t st = check_cu_seqlens(fn, cu_seqlens, nseq);
   if (st != DSA_OK) return st;
-  const int64_t qrow = static_cast<int64_t>(Hq) * D * 2, krow = static_cast<int64_t>(D) * 2;
-  for (int s = 0; s < nseq; ++s) {
-    const int64_t off = cu_seqlens[s], L = cu_seqlens[s + 1] - off;
-    auto at = [&](const void* p, int64_t row_bytes) -> const uint8_t* {
-      return p ? static_cast<const uint8_t*>(p) + off * row_bytes : nullptr;
-    };
-    st = dsa_sparse_attn_fwd(at(q, qrow), at(k, krow), at(v, krow), pool_idx ? pool_idx + off * topk : nullptr, L,
-                             Hq, D, topk, scale, o ? static_cast<uint8_t*>(o) + off * qrow : nullptr,
-                             lse ? lse + off * Hq : nullptr, stream);
-    if (st != DSA_OK) return st;
+  if (!q || !k || !v || !pool_idx || !o || !lse) return fail(DSA_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(pool_idx) || !aligned16(o) || !aligned4(lse))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned, pool_idx and lse 4-byte aligned", fn);
+  const int64_t T = cu_seqlens[nseq];
+  st = check_attn_args(fn, T, Hq, D, topk);
+  if (st != DSA_OK) return st;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  const int64_t qrow = static_cast<int64_t>(Hq) * D * 2;
+  for (int s0 = 0; s0 < nseq; s0 += dsa::kSeqBatch) {
+    const int n = nseq - s0 < dsa::kSeqBatch ? nseq - s0 : dsa::kSeqBatch;
+    const dsa::SeqTable tab = seq_table(cu_seqlens, s0, n);
+    const int64_t r0 = tab.cu[0], rows = tab.cu[n] - r0;
+    const cudaError_t e = timed_launch("attn_fwd", ctx.stream, [&] {
+      return dsa::launch_attn_fwd(static_cast<const uint8_t*>(q) + r0 * qrow, k, v, pool_idx + r0 * topk, 0, rows,
+                                  topk, scale, static_cast<uint8_t*>(o) + r0 * qrow, lse + r0 * Hq, ctx, &tab);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_fwd_varlen: launch");
   }
+  dsa::call_param("sequences", nseq);
+  dsa::call_param("T", T);
+  dsa::call_param("topk", topk);
+  dsa::call_variant("gather-bound forward over the packed batch, one launch per 256 sequences");
   return DSA_OK;
 }
 
 size_t dsa_sparse_attn_bwd_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hq, int D) {
   if (check_cu_seqlens("dsa_sparse_attn_bwd_varlen_workspace", cu_seqlens, nseq) != DSA_OK) return 0;
-  return dsa_sparse_attn_bwd_workspace(max_len(cu_seqlens, nseq), Hq, D);
+  return dsa_sparse_attn_bwd_workspace(cu_seqlens[nseq], Hq, D);
 }
 
 dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const void* k, const void* v, const void* o,
@@ -822,26 +891,54 @@ dsa_status_t dsa_sparse_attn_bwd_varlen(const void* dO, const void* q, const voi
                                         int nseq, int Hq, int D, int topk, float scale, void* dq, void* dk, void* dv,
                                         void* workspace, size_t ws_bytes, void* stream) {
   const dsa::CallScope scope("dsa_sparse_attn_bwd_varlen");
-  dsa_status_t st = check_cu_seqlens("dsa_sparse_attn_bwd_varlen", cu_seqlens, nseq);
+  const char* fn = "dsa_sparse_attn_bwd_varlen";
+  dsa_status_t st = check_cu_seqlens(fn, cu_seqlens, nseq);
+  if (st != DSA_OK) return st;
+  if (!dO || !q || !k || !v || !o || !lse || !pool_idx || !dq || !dk || !dv)
+    return fail(DSA_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  if (!aligned16(dO) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+      !aligned4(pool_idx) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned, pool_idx and lse 4-byte aligned", fn);
+  const int64_t T = cu_seqlens[nseq];
+  st = check_attn_args(fn, T, Hq, D, topk);
   if (st != DSA_OK) return st;
   const size_t need = dsa_sparse_attn_bwd_varlen_workspace(cu_seqlens, nseq, Hq, D);
   if (!workspace || ws_bytes < need)
-    return fail(DSA_ERR_WORKSPACE, "dsa_sparse_attn_bwd_varlen: workspace of %zu bytes needed, %zu given", need,
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? ws_bytes : (size_t)0);
-  const int64_t qrow = static_cast<int64_t>(Hq) * D * 2, krow = static_cast<int64_t>(D) * 2;
-  for (int s = 0; s < nseq; ++s) {
-    const int64_t off = cu_seqlens[s], L = cu_seqlens[s + 1] - off;
-    auto at = [&](const void* p, int64_t row_bytes) -> const uint8_t* {
-      return p ? static_cast<const uint8_t*>(p) + off * row_bytes : nullptr;
-    };
-    auto atw = [&](void* p, int64_t row_bytes) -> uint8_t* {
-      return p ? static_cast<uint8_t*>(p) + off * row_bytes : nullptr;
-    };
-    st = dsa_sparse_attn_bwd(at(dO, qrow), at(q, qrow), at(k, krow), at(v, krow), at(o, qrow),
-                             lse ? lse + off * Hq : nullptr, pool_idx ? pool_idx + off * topk : nullptr, L, Hq, D,
-                             topk, scale, atw(dq, qrow), atw(dk, krow), atw(dv, krow), workspace, ws_bytes, stream);
-    if (st != DSA_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  // the packed batch's fp32 dK/dV accumulators (adjacent) and Delta
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t acc_bytes = round_up(static_cast<size_t>(T) * D * sizeof(float), 256);
+  float* dk_acc = reinterpret_cast<float*>(ws);
+  float* dv_acc = reinterpret_cast<float*>(ws + acc_bytes);
+  float* delta = reinterpret_cast<float*>(ws + 2 * acc_bytes);
+  cudaError_t e = timed_launch("attn_bwd_pre", ctx.stream,
+                               [&] { return dsa::launch_attn_bwd_pre(dO, o, T, T, delta, dk_acc, dv_acc, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_varlen: preprocess launch");
+  const int64_t qrow = static_cast<int64_t>(Hq) * D * 2;
+  for (int s0 = 0; s0 < nseq; s0 += dsa::kSeqBatch) {
+    const int n = nseq - s0 < dsa::kSeqBatch ? nseq - s0 : dsa::kSeqBatch;
+    const dsa::SeqTable tab = seq_table(cu_seqlens, s0, n);
+    const int64_t r0 = tab.cu[0], rows = tab.cu[n] - r0;
+    e = timed_launch("attn_bwd", ctx.stream, [&] {
+      return dsa::launch_attn_bwd(static_cast<const uint8_t*>(dO) + r0 * qrow, static_cast<const uint8_t*>(q) + r0 * qrow,
+                                  k, v, lse + r0 * Hq, delta + r0 * Hq, pool_idx + r0 * topk, 0, rows, topk, scale,
+                                  static_cast<uint8_t*>(dq) + r0 * qrow, dk_acc, dv_acc, ctx, &tab);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_varlen: launch");
   }
+  e = timed_launch("attn_bwd_cast", ctx.stream, [&] { return dsa::launch_cast_dkdv(dk_acc, dv_acc, T * D, dk, dv, ctx); });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_bwd_varlen: cast launch");
+  dsa::call_param("sequences", nseq);
+  dsa::call_param("T", T);
+  dsa::call_param("topk", topk);
+  dsa::call_variant("atomic backward over the packed batch, one launch per 256 sequences");
   return DSA_OK;
 }
 

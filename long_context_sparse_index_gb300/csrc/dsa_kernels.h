@@ -40,6 +40,10 @@ struct CallScope {
   CallScope& operator=(const CallScope&) = delete;
 };
 
+// sequences per launch of the varlen calls (their table rides in the kernel
+// parameters)
+constexpr int kSeqBatch = 256;
+
 struct LaunchCtx {
   cudaStream_t stream;
   unsigned* status;        // device status word (kStatus* bits)
@@ -133,18 +137,64 @@ cudaError_t launch_index_fallback(const void* q_idx, const IndexPlan& pl, const 
                                   int64_t q_begin, int Hi, int topk, int32_t* pool_idx, const LaunchCtx& ctx);
 size_t index_topk_smem_bytes();
 
+// Rows whose query keeps every eligible pool (n = floor(i/4) <= topk), for
+// whole short sequences of a packed batch: row i of sequence s (packed row
+// start[s] + i) gets pools 0 .. n-1, then -1.  One CTA per sequence.
+struct ShortSeqs {
+  int n;
+  int64_t start[kSeqBatch];
+  int64_t len[kSeqBatch];
+};
+cudaError_t launch_short_rows(int32_t* pool_idx, int topk, const ShortSeqs& seqs, const LaunchCtx& ctx);
+
+// Packed sequences of one attention launch (the varlen calls): the launch's
+// rows are packed rows row0 .. row0 + rows - 1, and sequence s of the table
+// holds packed rows cu[s] .. cu[s+1] - 1 (its keys and values are packed rows
+// too), s < n.  n == 0: one sequence, and the launch's row r is its query
+// q_begin + r.  Passed by value as a kernel parameter.
+struct SeqTable {
+  int n;
+  int64_t row0;
+  int64_t cu[kSeqBatch + 1];
+};
+
+// Query i and the packed row of its sequence's first key, for launch row r.
+__device__ __forceinline__ void seq_locate(const SeqTable& t, int64_t q0, int64_t r, int64_t* i, int64_t* kv0) {
+  if (t.n == 0) {
+    *i = q0 + r;
+    *kv0 = 0;
+    return;
+  }
+  const int64_t g = t.row0 + r;
+  int lo = 0, hi = t.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.cu[mid] <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  *kv0 = t.cu[lo];
+  *i = g - t.cu[lo];
+}
+
 // Queries [q_begin, q_end) (global positions); q, pool_idx, o and lse hold
-// their rows locally (row r = query q_begin + r); k and v are the whole sequence.
+// their rows locally (row r = query q_begin + r); k and v are the whole
+// sequence.  With a table (tab->n > 0), the launch covers its packed rows
+// instead (q_begin is unused, q_end - q_begin = rows) and k and v are the
+// whole packed batch.
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
-                            int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx);
+                            int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx,
+                            const SeqTable* tab = nullptr);
 
 // Delta for nq query rows, and zeroing of the two fp32 accumulators (skipped when dk_acc is null).
 cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx);
-// dq for queries [q_begin, q_end); dK/dV added into dk_acc/dv_acc unless they are null (dq only).
+// dq for queries [q_begin, q_end); dK/dV added into dk_acc/dv_acc unless they
+// are null (dq only).  A table works as for launch_attn_fwd (dk_acc and dv_acc
+// then span the packed batch).
 cudaError_t launch_attn_bwd(const void* dO, const void* q, const void* k, const void* v, const float* lse,
                             const float* delta, const int32_t* pool_idx, int64_t q_begin, int64_t q_end, int topk,
-                            float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx);
+                            float scale, void* dq, float* dk_acc, float* dv_acc, const LaunchCtx& ctx,
+                            const SeqTable* tab = nullptr);
 // Deterministic dK/dV (attn_bwd_det.cu): sizes of the pieces of its workspace.
 struct DetPlan {
   int64_t P;         // pools that can be selected: floor(S/4)

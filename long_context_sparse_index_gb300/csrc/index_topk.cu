@@ -1050,9 +1050,28 @@ __global__ void pool_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_
   d32[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
 }
 
+// A short sequence's rows all keep every eligible pool (see launch_short_rows).
+__global__ void __launch_bounds__(256) short_rows_kernel(int32_t* __restrict__ pool_idx, int topk,
+                                                         const __grid_constant__ ShortSeqs seqs) {
+  const int64_t start = seqs.start[blockIdx.x], len = seqs.len[blockIdx.x];
+  int32_t* out = pool_idx + start * topk;
+  const int64_t total = len * topk;
+  for (int64_t e = threadIdx.x; e < total; e += blockDim.x) {
+    const int64_t i = e / topk;
+    const int j = static_cast<int>(e - i * topk);
+    out[e] = j < (i >> 2) ? j : -1;
+  }
+}
+
 }  // namespace
 
 size_t index_topk_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_short_rows(int32_t* pool_idx, int topk, const ShortSeqs& seqs, const LaunchCtx& ctx) {
+  if (seqs.n < 1) return cudaSuccess;
+  short_rows_kernel<<<static_cast<unsigned>(seqs.n), 256, 0, ctx.stream>>>(pool_idx, topk, seqs);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pool_keys(const void* k_idx, int64_t P, void* khat2, float* khat32, unsigned long long* sync_words,
                              const LaunchCtx& ctx) {

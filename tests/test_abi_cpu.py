@@ -207,8 +207,9 @@ def test_deterministic_backward_workspace_and_checks(lib):
 
 def test_varlen_checks_cu_seqlens_and_workspace(lib):
     """Packed batches: cu_seqlens must start at 0 and increase strictly; the
-    workspace queries give the longest sequence's workspace; errors come back
-    before any sequence runs."""
+    indexer's workspace is the longest sequence's, the backward's that of the
+    packed length (its fp32 dK/dV accumulators span the batch); errors come
+    back before any sequence runs."""
     import ctypes
     import long_context_sparse_index_gb300 as dsa
     def cu(*v):
@@ -216,7 +217,7 @@ def test_varlen_checks_cu_seqlens_and_workspace(lib):
     good = cu(0, 5, 1029, 1030)
     assert lib.dsa_index_topk_varlen_workspace(good, 3, 8, 64, 256, 64) == lib.dsa_index_topk_workspace(1024, 8, 64,
                                                                                                          256, 64)
-    assert lib.dsa_sparse_attn_bwd_varlen_workspace(good, 3, 16, 128) == lib.dsa_sparse_attn_bwd_workspace(1024, 16,
+    assert lib.dsa_sparse_attn_bwd_varlen_workspace(good, 3, 16, 128) == lib.dsa_sparse_attn_bwd_workspace(1030, 16,
                                                                                                            128)
     for bad, n in ((cu(1, 5), 1), (cu(0, 5, 5), 2), (cu(0, 7, 3), 2), (cu(0), 0)):
         assert lib.dsa_index_topk_varlen_workspace(bad, n, 8, 64, 256, 64) == 0

@@ -267,6 +267,49 @@ def test_varlen_packed_batch_equals_each_sequence_alone():
         assert_close(gdv[a:b], rdv, "dv")
 
 
+def test_varlen_many_sequences_across_launch_batches():
+    """300 packed sequences (more than one 256-sequence launch table; most
+    short enough that every row keeps all its pools, some indexed): every
+    sequence matches the oracle run on it alone -- pool_idx bit for bit,
+    forward and backward within tolerance -- and the record shows the short
+    sequences filled without the persistent indexer."""
+    rng = np.random.default_rng(5)
+    lens = np.concatenate([rng.integers(1, 65, 280), rng.integers(265, 700, 20)])
+    rng.shuffle(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, Hi, topk, scale = int(cu[-1]), 8, 64, 0.05
+    q_idx = synth.int_bf16(T, 11, (T, Hi, 64), -3, 3)
+    k_idx = synth.int_bf16(T, 12, (T, 64), -3, 3)
+    w = synth.int_f32(T, 13, (T, Hi), 0, 3)
+    wl = synth.Workload("t", T, topk=topk, seed=19)
+    q, k, v = synth.attention_inputs(wl)
+    dO = synth.grad_output(wl)
+    qi, ki, wi = _indexer_to_gpu(q_idx, k_idx, w)
+    qt, kt, vt, dOt = _attn_to_gpu(q, k, v, dO)
+    sel = dsa.dsa_index_topk_varlen(qi, ki, wi, cu, chunk=256, topk=topk)
+    cfg = dsa.last_kernel_config()
+    assert cfg["params"]["short_sequences"] == int((lens <= 4 * topk + 4).sum()) == 280
+    assert dict(cfg["kernels"])["short_rows"] == 2 and cfg["params"]["indexed_sequences"] == 20
+    o, lse = dsa.dsa_sparse_attn_fwd_varlen(qt, kt, vt, sel, cu, scale=scale)
+    assert dsa.last_kernel_config()["kernels"] == [["attn_fwd", 2]]
+    dq, dk, dv = dsa.dsa_sparse_attn_bwd_varlen(dOt, qt, kt, vt, o, lse, sel, cu, scale=scale)
+    assert [n for n, _ in dsa.last_kernel_config()["kernels"]] == ["attn_bwd_pre", "attn_bwd", "attn_bwd_cast"]
+    dsa.dsa_sync_status()
+    sel, go, gl = sel.cpu().numpy(), torch_bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    gdq, gdk, gdv = torch_bf16_to_f64(dq), torch_bf16_to_f64(dk), torch_bf16_to_f64(dv)
+    for a, b in zip(cu[:-1], cu[1:]):
+        ref_sel, _ = oracle.index_topk(q_idx[a:b], k_idx[a:b], w[a:b], topk)
+        assert np.array_equal(sel[a:b], ref_sel), (a, b)
+        seq = (q[a:b], k[a:b], v[a:b])
+        ro, rl = oracle.attn_fwd(*seq, ref_sel, scale=scale)
+        assert_close(go[a:b], ro, "o")
+        assert_close(gl[a:b], rl, "lse", bf16_out=False)
+        assert_close(gdq[a:b], oracle.attn_bwd_dq(dO[a:b], *seq, ref_sel, scale=scale), "dq")
+        rdk, rdv = oracle.attn_bwd_dkdv(dO[a:b], *seq, ref_sel, scale=scale)
+        assert_close(gdk[a:b], rdk, "dk")
+        assert_close(gdv[a:b], rdv, "dv")
+
+
 # --------------------------------------------------------------------------- attention forward
 
 def _fwd_check(q, k, v, sel, rows=None, scale=0.0):
