@@ -129,8 +129,10 @@ def algorithmic_work(wl):
     }
 
 
-KERNEL_SOURCE = {"index_topk": ("index_topk.cu", "topk_row.cuh"), "attn_fwd": ("attn_fwd.cu",),
-                 "attn_bwd": ("attn_bwd.cu",), "det_span": ("attn_bwd_det.cu",)}
+# the files holding each kernel's device code (a capture goes stale when any changes)
+KERNEL_SOURCE = {"index_topk": ("index_topk.cu", "topk_row.cuh", "topk_warp.cuh", "topk_cand.cuh", "dsa_kernels.h"),
+                 "attn_fwd": ("attn_fwd.cu", "dsa_kernels.h"), "attn_bwd": ("attn_bwd.cu", "dsa_kernels.h"),
+                 "det_span": ("attn_bwd_det.cu",)}
 # profile summary file stem of a timed launcher whose kernel has another name
 PROFILE_STEM = {"det_span": "det_item"}
 
