@@ -814,6 +814,9 @@ def run_trace(args):
                               "mma_key_tile_wait_per_head": int(words[41]) / mheads,
                               "heads_issued": int(words[42]), "heads_folded_thread0": int(words[43]),
                               "fallback_rows": int(words[36])}
+    napp = max(int(words[47]), 1)
+    summary["append_cycles"] = {"compare_per_tile": int(words[44]) / napp, "atomic_per_tile": int(words[45]) / napp,
+                                "writes_per_tile": int(words[46]) / napp, "tiles_thread0": int(words[47])}
     summary.update({"workload": args.workload, "S": S, "call_ms": ev0.elapsed_time(ev1), "records_dropped": max(0, n - cap),
                     "note": "DSA_ITEM_TRACE build (measurement only): epilogue thread 0 stamps each work item; "
                             "fold = taking the item to the end of its fold over heads (waits on the MMAs included), "

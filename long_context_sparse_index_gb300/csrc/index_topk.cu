@@ -271,9 +271,13 @@ enum : int {
   kCycMmaAcc,                                 // ... for a free accumulator
   kCycMmaB,                                   // ... for a pooled-key tile
   kCycMmaHeads,                               // heads issued (a count)
-  kCycFoldHeads                               // heads folded by epilogue thread 0 (a count)
+  kCycFoldHeads,                              // heads folded by epilogue thread 0 (a count)
+  kCycAppendCmp,                              // epilogue thread 0: a tile's threshold compares
+  kCycAppendAtomic,                           // ... its row-count atomic (issue to result)
+  kCycAppendWrite,                            // ... its candidate writes
+  kCycAppends                                 // tiles appended by epilogue thread 0 (a count)
 };
-static_assert(kCycFoldHeads < kIndexSyncWords, "trace words");
+static_assert(kCycAppends < kIndexSyncWords, "trace words");
 
 struct CycleSum {
 #ifdef DSA_ITEM_TRACE
@@ -696,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const topk::Group grp{etid - gid * topk::kGT, 2 + gid};
     int cs = 0, is = 0;
     uint32_t cph = 0, iph = 0;
-    CycleSum cyc_fw, cyc_fold, cyc_fheads;
+    CycleSum cyc_fw, cyc_fold, cyc_fheads, cyc_cmp, cyc_atom, cyc_wr, cyc_app;
     while (true) {
       bool ok = mbar_wait(bar_item_full + 8 * is, iph, a.limit_ns, abort_flag);
       Item it{kItemEnd, 0, 0, 0};
@@ -815,25 +819,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int jt = static_cast<int>(
                 min(static_cast<int64_t>(th.y) - static_cast<int64_t>(pbase), static_cast<int64_t>(kEpiCols)));
             // bit j of `hit`: pool pbase + j is a candidate
+            cyc_app.add(1);
+            cyc_cmp.start();
             unsigned long long hit = 0ull;
 #pragma unroll
             for (int j = 0; j < kEpiCols; ++j) {
               const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
               if (j < jn && (v > tf || (v == tf && j <= jt))) hit |= 1ull << j;
             }
+            cyc_cmp.stop();
             if (hit != 0ull) {
+              cyc_atom.start();
               unsigned pos = atomicAdd(a.cnt + static_cast<int64_t>(bi) * a.thr_ld + rloc,
                                        static_cast<unsigned>(__popcll(hit)));
+#ifdef DSA_ITEM_TRACE
+              asm volatile("" ::"r"(pos));  // the timer below waits for the atomic's result
+#endif
+              cyc_atom.stop();
+              cyc_wr.start();
               uint2* dst = a.cands + static_cast<int64_t>(bi) * a.cand_slot + rloc * a.cap;
               const unsigned cap = static_cast<unsigned>(a.cap);
+              // each half of the thread's 64 scores goes through the warp's
+              // staging tile, so that every lane walks only its own hits
+              // (a register array cannot be indexed by a hit's position);
+              // the rows of a warp have different hits, and a loop over all
+              // 64 positions would issue a store step for each of them
+              float* stg = reinterpret_cast<float*>(gbase + kGrpOff + ew * kStgBytes) + lane * kStgLd;
 #pragma unroll
-              for (int j = 0; j < kEpiCols; ++j) {
-                if ((hit >> j) & 1ull) {
-                  const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
-                  if (pos < cap) dst[pos] = make_uint2(topk::score_key(v), pbase + j);
+              for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float2 u = acc[16 * half + 2 * q], w = acc[16 * half + 2 * q + 1];
+                  *reinterpret_cast<float4*>(stg + 4 * q) = make_float4(u.x, u.y, w.x, w.y);
+                }
+                // (a lane reads only its own staged row: no warp barrier, and
+                // lanes without hits never come here)
+                uint32_t h = static_cast<uint32_t>(hit >> (32 * half));
+                while (h != 0u) {
+                  const int j = __ffs(h) - 1;
+                  h &= h - 1u;
+                  if (pos < cap) dst[pos] = make_uint2(topk::score_key(stg[j]), pbase + 32 * half + j);
                   ++pos;
                 }
               }
+              cyc_wr.stop();
             }
           }
         }
@@ -936,6 +965,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       cycles_publish(a, kCycFoldWait, cyc_fw);
       cycles_publish(a, kCycFold, cyc_fold);
       cycles_publish(a, kCycFoldHeads, cyc_fheads);
+      cycles_publish(a, kCycAppendCmp, cyc_cmp);
+      cycles_publish(a, kCycAppendAtomic, cyc_atom);
+      cycles_publish(a, kCycAppendWrite, cyc_wr);
+      cycles_publish(a, kCycAppends, cyc_app);
     }
   }
 
