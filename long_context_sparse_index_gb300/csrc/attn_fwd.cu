@@ -233,12 +233,16 @@ __global__ void __launch_bounds__(kThreads, 3)
     l_run[1] = l_run[1] * al1 + (p[2] + p[3] + p[6] + p[7]);
     m_run[0] = mn0;
     m_run[1] = mn1;
+    // the accumulators are rescaled only when some row of the warp raised
+    // its maximum (a factor of exactly 1 leaves them unchanged)
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o_acc[j][0] *= al0;
-      o_acc[j][1] *= al0;
-      o_acc[j][2] *= al1;
-      o_acc[j][3] *= al1;
+      for (int j = 0; j < 16; ++j) {
+        o_acc[j][0] *= al0;
+        o_acc[j][1] *= al0;
+        o_acc[j][2] *= al1;
+        o_acc[j][3] *= al1;
+      }
     }
     uint32_t pa[4];
     pa[0] = pack_bf16(p[0], p[1]);
