@@ -70,6 +70,8 @@ def parse_args():
                     help="indexer item trace: one dsa_index_topk call through the DSA_ITEM_TRACE build, "
                          "time per work-item kind (fold, dependency wait, rest) and per-CTA idle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tc-alt", action="store_true",
+                    help="skip timing the tcgen05 forward alternative after the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time for the CPU baseline sample")
     return ap.parse_args()
 
@@ -327,6 +329,16 @@ def measure_l2_peaks(dsa, torch, dev):
     return out
 
 
+def measure_umma_costs(dsa):
+    """Cycles per tcgen05.mma (M 128, K 16, bf16) seen by the issuing thread:
+    N = 16 is the attention's product shape (one column per query head)."""
+    out = {}
+    for n, issuers in ((16, 1), (16, 3), (64, 1), (128, 1), (256, 1)):
+        out[f"n{n}_issuers{issuers}"] = round(dsa.measure_umma(n, issuers, groups=2000), 1)
+    out["nominal_cycles_n16"] = 128 * 16 * 16 / 4096  # dense bf16: 8192 flop per SM per clock
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -473,6 +485,28 @@ def run_ours(args):
                 roof[key] = kernels[dom][key]
     roof["l2_peaks_measured"] = l2
 
+    # ---- the tcgen05 forward (dsa_sparse_attn_fwd_tc) on the same selection,
+    # timed alone after the step (not part of it): the measured tensor-core
+    # alternative to attn_fwd, and the cost of one N = 16 tensor-core product
+    tc_alt = None
+    if not args.no_tc_alt:
+        o_tc, lse_tc = torch.empty_like(o), torch.empty_like(lse)
+        tms = []
+        for _ in range(3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dsa.dsa_sparse_attn_fwd_tc(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o_tc, lse=lse_tc)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tms.append(a.elapsed_time(b))
+        dsa.dsa_sparse_attn_fwd(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
+        dsa.dsa_sync_status()
+        tc_alt = {"ms": min(tms), "attn_fwd_ms": kernels.get("attn_fwd", {}).get("ms"),
+                  "max_abs_o_diff_vs_attn_fwd": (o_tc.float() - o.float()).abs().max().item(),
+                  "max_abs_lse_diff_vs_attn_fwd": (lse_tc - lse).abs().max().item(),
+                  "umma_cycles_per_instruction": measure_umma_costs(dsa)}
+
     # ---- end to end through the public API: pinned host -> device, the calls, device -> host
     e2e = None
     if not args.no_e2e:
@@ -585,7 +619,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{world} (one independent sequence per GPU)",
                 "clocks": clocks, "gpu_launches": gpu_launches, "e2e": e2e, "roofline": roof,
                 "kernels": kernels, "index_topk_stats": index_stats, "cpu_baseline": cpu,
-                "wall_s_timed_region": wall, "step_ms": step_ms}
+                "wall_s_timed_region": wall, "step_ms": step_ms, "attn_fwd_tcgen05": tc_alt}
         if backward:
             line["backward"] = "deterministic (key-major, fixed order)" if args.deterministic else "atomic dK/dV"
         print(json.dumps(line), flush=True)

@@ -143,6 +143,17 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
 dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
                                  int Hq, int D, int topk, float scale, void* o, float* lse, void* stream);
 
+/*
+ * The same forward with both contractions on the tcgen05 tensor cores
+ * (S^T = K.Q^T and O^T += V^T.P^T with fp32 accumulators in tensor memory),
+ * by one persistent warp-specialised CTA per SM.  Arguments, layouts, results
+ * (within rounding) and errors are those of dsa_sparse_attn_fwd.  It is the
+ * measured tensor-core alternative, not the faster path: with 16 heads every
+ * MMA has N = 16, and on GB300 it runs slower than dsa_sparse_attn_fwd.
+ */
+dsa_status_t dsa_sparse_attn_fwd_tc(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                                    int Hq, int D, int topk, float scale, void* o, float* lse, void* stream);
+
 /* Bytes of workspace dsa_sparse_attn_bwd needs: fp32 dK and dV accumulators
  * (2 x S x D x 4 B) plus the per-row softmax-gradient term (S x Hq x 4 B). */
 size_t dsa_sparse_attn_bwd_workspace(int64_t S, int Hq, int D);
@@ -379,6 +390,18 @@ const char* dsa_version(void);
  * Kinds 2..4 add into the buffer's contents.
  */
 double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream);
+
+/*
+ * Tensor-core issue probe (measurement helper).  On every SM, `issuers` CTAs
+ * (1..3) each have one thread issue `groups` groups of 8 back-to-back
+ * tcgen05.mma (kind::f16: bf16 operands from 128-byte swizzled shared
+ * memory, fp32 accumulator in tensor memory; M = 128, K = 16, N = n for n in
+ * {16, 32, 64, 128, 256}; issuers * max(n, 32) <= 512), then waits for them.
+ * Synchronises `stream` and returns the issuing thread's clock cycles per
+ * instruction, averaged over the CTAs, or -1.0 on error.  The sparse
+ * attention's products have N = 16 (one column per query head).
+ */
+double dsa_measure_umma(int n, int issuers, int groups, void* stream);
 
 /*
  * Item trace of the persistent indexer (measurement helper; only the trace

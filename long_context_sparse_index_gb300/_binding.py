@@ -31,7 +31,7 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen",
             "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic",
             "dsa_index_topk_stats", "dsa_measure_l2", "dsa_index_topk_workspace_slots", "dsa_trace_configure",
-            "dsa_last_kernel_config")
+            "dsa_last_kernel_config", "dsa_sparse_attn_fwd_tc", "dsa_measure_umma")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +58,7 @@ def load():
             lib.dsa_index_topk_workspace_slots.restype = sz
             lib.dsa_index_topk.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp, sz, vp]
             lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
+            lib.dsa_sparse_attn_fwd_tc.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
             lib.dsa_sparse_attn_bwd_workspace.argtypes = [i64, i32, i32]
             lib.dsa_sparse_attn_bwd_workspace.restype = sz
             lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp,
@@ -86,7 +87,8 @@ def load():
             lib.dsa_sparse_attn_bwd_deterministic.restype = ctypes.c_int
             lib.dsa_sync_status.argtypes = [vp]
             lib.dsa_clear_status.argtypes = []
-            for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_bwd, lib.dsa_sync_status,
+            for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_fwd_tc, lib.dsa_sparse_attn_bwd,
+                      lib.dsa_sync_status,
                       lib.dsa_clear_status):
                 f.restype = ctypes.c_int
             lib.dsa_last_error.argtypes = []
@@ -108,6 +110,8 @@ def load():
             lib.dsa_index_topk_stats.restype = ctypes.c_int
             lib.dsa_measure_l2.argtypes = [ctypes.c_int, vp, sz, ctypes.c_int, vp]
             lib.dsa_measure_l2.restype = ctypes.c_double
+            lib.dsa_measure_umma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+            lib.dsa_measure_umma.restype = ctypes.c_double
             lib.dsa_last_kernel_config.argtypes = [ctypes.c_char_p, sz]
             lib.dsa_last_kernel_config.restype = ctypes.c_int
             _lib = lib
@@ -246,6 +250,25 @@ def dsa_sparse_attn_fwd(q, k, v, pool_idx, scale: float = 0.0, o=None, lse=None,
     _check(load().dsa_sparse_attn_fwd_range(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S,
                                             q_begin, q_begin + nq, Hq, D, pool_idx.shape[1], float(scale),
                                             o.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
+    return o, lse
+
+
+def dsa_sparse_attn_fwd_tc(q, k, v, pool_idx, scale: float = 0.0, o=None, lse=None, stream=None):
+    """The whole-sequence forward on the tcgen05 tensor cores (the measured
+    tensor-core alternative to dsa_sparse_attn_fwd): (o [S, Hq, D] bf16,
+    lse [S, Hq] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 2)
+    _need(v, "v", torch.bfloat16, 2)
+    _need(pool_idx, "pool_idx", torch.int32, 2)
+    nq, Hq, D, S = _attn_shapes(q, k, v, pool_idx)
+    if nq != S:
+        raise ValueError("dsa_sparse_attn_fwd_tc: q must hold every query of the sequence")
+    o = _out(o, "o", q.shape, torch.bfloat16, q.device)
+    lse = _out(lse, "lse", (nq, Hq), torch.float32, q.device)
+    _check(load().dsa_sparse_attn_fwd_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S, Hq, D,
+                                         pool_idx.shape[1], float(scale), o.data_ptr(), lse.data_ptr(),
+                                         _stream_handle(stream)))
     return o, lse
 
 
@@ -436,6 +459,16 @@ def measure_l2(kind: int, buf: torch.Tensor, iters: int = 20, stream=None) -> fl
     3 / 4 bulk reductions of 2 KB / 512 B)."""
     lib = load()
     r = lib.dsa_measure_l2(kind, buf.data_ptr(), buf.numel() * buf.element_size(), iters, _stream_handle(stream))
+    if r < 0:
+        raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
+    return float(r)
+
+
+def measure_umma(n: int, issuers: int = 1, groups: int = 2000, stream=None) -> float:
+    """Clock cycles per tcgen05.mma (M 128, N n, K 16, bf16) as seen by its
+    issuing thread, with `issuers` issuing CTAs on every SM."""
+    lib = load()
+    r = lib.dsa_measure_umma(n, issuers, groups, _stream_handle(stream))
     if r < 0:
         raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
     return float(r)

@@ -559,6 +559,29 @@ dsa_status_t dsa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   return dsa_sparse_attn_fwd_range(q, k, v, pool_idx, S, 0, S, Hq, D, topk, scale, o, lse, stream);
 }
 
+dsa_status_t dsa_sparse_attn_fwd_tc(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t S,
+                                    int Hq, int D, int topk, float scale, void* o, float* lse, void* stream) {
+  const dsa::CallScope scope("dsa_sparse_attn_fwd_tc");
+  const char* fn = "dsa_sparse_attn_fwd_tc";
+  if (!q || !k || !v || !pool_idx || !o || !lse) return fail(DSA_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(pool_idx) || !aligned16(o) || !aligned4(lse))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned, pool_idx and lse 4-byte aligned", fn);
+  dsa_status_t st = check_attn_args(fn, S, Hq, D, topk);
+  if (st != DSA_OK) return st;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(D));
+  dsa::LaunchCtx ctx;
+  st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+  dsa::call_param("S", S);
+  dsa::call_param("topk", topk);
+  dsa::call_variant("tcgen05 forward: persistent CTA per SM; cp.async producers, one MMA issuer, softmax warps");
+  cudaError_t e = timed_launch("attn_fwd_tc", ctx.stream, [&] {
+    return dsa::launch_attn_fwd_tc(q, k, v, pool_idx, 0, S, topk, scale, o, lse, ctx);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_attn_fwd_tc: launch");
+  return DSA_OK;
+}
+
 size_t dsa_sparse_attn_bwd_workspace(int64_t S, int Hq, int D) {
   if (S < 1 || Hq < 1 || D < 1) return 0;
   return round_up(static_cast<size_t>(S) * D * sizeof(float), 256) * 2 +

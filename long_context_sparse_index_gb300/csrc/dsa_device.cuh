@@ -36,6 +36,23 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // kernel has issued this (or exited).
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ----------------------------------------------------------------- named barriers
+// Barrier `id` (1..15) over the first-arriving `n` threads (a multiple of 32):
+// every thread of the group must execute the same sequence of these.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// As named_bar_sync, and returns whether `v` is true in any thread of the group.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -146,6 +163,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 consecutive fp32 columns from registers: thread t writes row (lane base + t)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes (st.shared,
+// completed cp.async) before later async-proxy reads such as tcgen05.mma
+// operand fetches (after a barrier with the issuing thread).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // UMMA shared-memory descriptor for a K-major operand stored in the canonical
 // 128-byte-swizzle layout: rows of 64 bf16 (128 B), 8-row atoms of 1024 B.
@@ -160,6 +193,38 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// UMMA shared-memory descriptor for an MN-major operand in the 128-byte-swizzle
+// layout: each 1024-B atom holds 8 rows of K, each row 64 consecutive bf16 of
+// M (or N), 16-B chunks XOR-ed with the row's index mod 8.  `mn_stride` is the
+// byte distance between atoms that are 64 elements apart along M (N), and
+// `k_stride` between atoms that are 8 rows apart along K.  One K=16 step
+// spans two atoms along K, so it advances the start address by 2 * k_stride.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>((k_stride >> 4) & 0x3FFFu) << 32;   // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+// UMMA shared-memory descriptor for an MN-major operand without swizzle:
+// core matrices of 8 rows of K by 8 consecutive bf16 of M (or N), each row
+// 16 B and the 8 rows contiguous (128 B).  `k_stride` is the byte distance
+// between core matrices 8 rows apart along K, `mn_stride` between core
+// matrices 8 elements apart along M (N).
+__device__ __forceinline__ uint64_t umma_desc_mn_noswizzle(uint32_t saddr, uint32_t k_stride, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((k_stride >> 4) & 0x3FFFu) << 16;   // leading byte offset
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 32;  // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                           // swizzle mode 0: none
+  return d;
+}
+// Instruction-descriptor bits that make A (B) MN-major (transposed).
+constexpr uint32_t kUmmaAMnMajor = 1u << 15;
+constexpr uint32_t kUmmaBMnMajor = 1u << 16;
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32
@@ -173,6 +238,14 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;  // 0 bytes read -> 16 zero bytes written
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+// The mbarrier receives one arrival once every cp.async this thread issued
+// before has completed (its expected count must include that arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -198,6 +271,10 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

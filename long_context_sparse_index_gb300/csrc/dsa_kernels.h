@@ -185,6 +185,12 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, const i
                             int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx,
                             const SeqTable* tab = nullptr);
 
+// The same forward on tcgen05 (attn_fwd_tc.cu): one persistent CTA per SM
+// (at most ctx.num_sms CTAs), same arguments and results within rounding.
+cudaError_t launch_attn_fwd_tc(const void* q, const void* k, const void* v, const int32_t* pool_idx, int64_t q_begin,
+                               int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx,
+                               const SeqTable* tab = nullptr);
+
 // Delta for nq query rows, and zeroing of the two fp32 accumulators (skipped when dk_acc is null).
 cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx);

@@ -17,6 +17,13 @@
 //           operations in flight per warp
 //   kind 4  the same with 512-byte operations (one row each)
 // All report bytes moved (read, or added) per second.
+//
+// dsa_measure_umma times the tensor core on the attention's product shape:
+// one thread per CTA issues back-to-back groups of 8 chained tcgen05.mma
+// (kind::f16, bf16 operands from 128-byte swizzled shared memory, M = 128,
+// K = 16 each, N given) into a tensor-memory accumulator, and reports the
+// issuing thread's clock cycles per instruction, with `issuers` CTAs (each
+// its own issuer) resident on every SM.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -112,7 +119,66 @@ __global__ void probe_bulk_red_kernel(float* __restrict__ buf, uint32_t nblocks,
   }
 }
 
+// ---------------------------------------------------------------- tensor-core issue probe
+constexpr int kUmmaGroup = 8;  // chained MMAs per group (accumulate after the first)
+
+template <int N>
+__global__ void __launch_bounds__(128, 3) probe_umma_kernel(int groups, uint64_t limit_ns, unsigned long long* cycles,
+                                                          int* failed) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dsa::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* g = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + 16384;  // A: 128 rows x 128 B; B: N rows x 128 B
+  const uint32_t bar = sB + N * 128;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(g + 16384 + N * 128 + 64);
+  // small nonzero operands (bf16 1/64 .. 8/64, exact), in place before the first product
+  for (int i = threadIdx.x; i < (16384 + N * 128) / 4; i += blockDim.x) {
+    const uint32_t h = 0x3C80u + ((i * 7u) & 7u);
+    reinterpret_cast<uint32_t*>(g)[i] = h | (h << 16);
+  }
+  dsa::fence_proxy_async_smem();
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    dsa::mbar_init(bar, 1);
+    dsa::mbar_fence_init();
+  }
+  constexpr uint32_t kCols = N < 32 ? 32 : N;
+  if (warp == 0) dsa::tmem_alloc(dsa::smem_u32(slot), kCols);
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = dsa::umma_idesc_bf16_f32(128, N);
+    const uint64_t dA = dsa::umma_desc_sw128(sA), dB = dsa::umma_desc_sw128(sB);
+    const long long t0 = clock64();
+    for (int i = 0; i < groups; ++i) {
+#pragma unroll
+      for (int kk = 0; kk < kUmmaGroup; ++kk)
+        dsa::umma_bf16(tmem, dA + (((kk & 3) * 32) >> 4), dB + (((kk & 3) * 32) >> 4), idesc, kk > 0 ? 1u : 0u);
+    }
+    dsa::umma_commit(bar);
+    if (!dsa::mbar_wait(bar, 0, limit_ns, nullptr)) atomicExch(failed, 1);
+    atomicAdd(cycles, static_cast<unsigned long long>(clock64() - t0));
+  }
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  if (warp == 0) dsa::tmem_dealloc(tmem, kCols);
+}
+
+template <int N>
+static cudaError_t launch_probe_umma(int grid, int groups, unsigned long long* cycles, int* failed, cudaStream_t st) {
+  const int smem = 1024 + 16384 + N * 128 + 128;
+  cudaError_t e = cudaFuncSetAttribute(probe_umma_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  probe_umma_kernel<N><<<grid, 128, smem, st>>>(groups, 2000000000ull, cycles, failed);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
 
 extern "C" {
 
@@ -172,6 +238,53 @@ double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream
     return -1.0;
   }
   return moved / (ms * 1e-3) / 1e9;
+}
+
+double dsa_measure_umma(int n, int issuers, int groups, void* stream) {
+  if ((n != 16 && n != 32 && n != 64 && n != 128 && n != 256) || issuers < 1 || issuers > 3 || groups < 1 ||
+      issuers * (n < 32 ? 32 : n) > 512) {
+    dsa::set_last_error("dsa_measure_umma: n in {16, 32, 64, 128, 256}, issuers 1..3 with issuers * max(n, 32) <= "
+                        "512 tensor-memory columns, groups >= 1");
+    return -1.0;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    dsa::set_last_error("dsa_measure_umma: no device");
+    return -1.0;
+  }
+  unsigned long long* cycles = nullptr;
+  int* failed = nullptr;
+  cudaError_t e = cudaMalloc(&cycles, sizeof(unsigned long long) + sizeof(int));
+  if (e != cudaSuccess) {
+    dsa::set_last_error(std::string("dsa_measure_umma: ") + cudaGetErrorString(e));
+    return -1.0;
+  }
+  failed = reinterpret_cast<int*>(cycles + 1);
+  const int grid = sms * issuers;
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {  // the first pass warms up
+    e = cudaMemsetAsync(cycles, 0, sizeof(unsigned long long) + sizeof(int), st);
+    if (e != cudaSuccess) break;
+    switch (n) {
+      case 16: e = launch_probe_umma<16>(grid, groups, cycles, failed, st); break;
+      case 32: e = launch_probe_umma<32>(grid, groups, cycles, failed, st); break;
+      case 64: e = launch_probe_umma<64>(grid, groups, cycles, failed, st); break;
+      case 128: e = launch_probe_umma<128>(grid, groups, cycles, failed, st); break;
+      default: e = launch_probe_umma<256>(grid, groups, cycles, failed, st); break;
+    }
+  }
+  unsigned long long total = 0;
+  int bad = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&total, cycles, sizeof(total), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&bad, failed, sizeof(bad), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(cycles);
+  if (e != cudaSuccess || bad) {
+    dsa::set_last_error(std::string("dsa_measure_umma: ") + (bad ? "a completion wait ran out" : cudaGetErrorString(e)));
+    return -1.0;
+  }
+  return static_cast<double>(total) / grid / (static_cast<double>(groups) * kUmmaGroup);
 }
 
 }  // extern "C"

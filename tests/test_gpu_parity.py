@@ -312,9 +312,9 @@ def test_varlen_many_sequences_across_launch_batches():
 
 # --------------------------------------------------------------------------- attention forward
 
-def _fwd_check(q, k, v, sel, rows=None, scale=0.0):
+def _fwd_check(q, k, v, sel, rows=None, scale=0.0, fwd=None):
     qt, kt, vt = _attn_to_gpu(q, k, v)
-    o, lse = dsa.dsa_sparse_attn_fwd(qt, kt, vt, torch.from_numpy(sel).to(DEV), scale=scale)
+    o, lse = (fwd or dsa.dsa_sparse_attn_fwd)(qt, kt, vt, torch.from_numpy(sel).to(DEV), scale=scale)
     dsa.dsa_sync_status()
     ro, rl = oracle.attn_fwd(q, k, v, sel, scale=scale, rows=rows)
     go = torch_bf16_to_f64(o)
@@ -337,6 +337,45 @@ def test_attn_fwd_normal_edge_shapes(S, topk):
     q, k, v = synth.attention_inputs(wl)
     sel = synth.stand_in_selection(wl)
     _fwd_check(q, k, v, sel, scale=0.0 if S % 2 else 0.07)
+
+
+# The tcgen05 forward: one persistent CTA per SM walks many queries (S > 152
+# exercises the query-parity buffers and the producers' row prefetch), and
+# topk = 2048 takes its single row-buffer path.
+def test_attn_fwd_tc_tiny_int_with_oracle_selection():
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    sel, _ = oracle.index_topk(*synth.indexer_inputs(wl), wl.topk)
+    _fwd_check(*synth.attention_inputs(wl), sel, fwd=dsa.dsa_sparse_attn_fwd_tc)
+
+
+@pytest.mark.parametrize("S,topk", [(1, 1), (2, 4), (5, 1), (7, 3), (64, 16), (301, 8), (4096, 512), (4099, 100)])
+def test_attn_fwd_tc_normal_edge_shapes(S, topk):
+    wl = synth.Workload("t", S, topk=topk, seed=S)
+    q, k, v = synth.attention_inputs(wl)
+    sel = synth.stand_in_selection(wl)
+    _fwd_check(q, k, v, sel, scale=0.0 if S % 2 else 0.07, fwd=dsa.dsa_sparse_attn_fwd_tc)
+
+
+def test_attn_fwd_tc_topk_2048_sampled_rows():
+    wl = synth.Workload("t", 8300, topk=2048, seed=83)
+    q, k, v = synth.attention_inputs(wl)
+    sel = synth.stand_in_selection(wl)
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.random.RandomState(5).randint(0, wl.S, 160),
+                                     np.arange(wl.S - 8, wl.S)]))
+    _fwd_check(q, k, v, sel, rows=rows, fwd=dsa.dsa_sparse_attn_fwd_tc)
+
+
+def test_attn_fwd_tc_matches_default_forward():
+    """Both forwards on one input: the same softmax, so o agrees to bf16
+    rounding and lse to fp32 rounding."""
+    wl = synth.Workload("t", 20000, topk=512, seed=11)
+    q, k, v = _attn_to_gpu(*synth.attention_inputs(wl))
+    sel = torch.from_numpy(synth.stand_in_selection(wl)).to(DEV)
+    o1, l1 = dsa.dsa_sparse_attn_fwd(q, k, v, sel)
+    o2, l2 = dsa.dsa_sparse_attn_fwd_tc(q, k, v, sel)
+    dsa.dsa_sync_status()
+    assert (o1.float() - o2.float()).abs().max().item() <= 1.6e-2
+    assert (l1 - l2).abs().max().item() <= 1e-4
 
 
 # --------------------------------------------------------------------------- attention backward
