@@ -855,7 +855,52 @@ def run_trace(args):
                     "note": "DSA_ITEM_TRACE build (measurement only): epilogue thread 0 stamps each work item; "
                             "fold = taking the item to the end of its fold over heads (waits on the MMAs included), "
                             "wait = its dependency wait, rest = selection / append / store and publish"})
+    summary["attn_fwd_tc_profile"] = fwd_tc_profile(lib, wl, out, to, dev)
     print(json.dumps({"trace": summary}), flush=True)
+
+
+def fwd_tc_profile(lib, wl, pool_idx, to, dev):
+    """The tcgen05 forward (dsa_sparse_attn_fwd_tc) in the same measurement
+    build: each warp role's clock cycles per 128-key block and pipeline
+    segment, summed over the CTAs (DSA_FWD_PROFILE counters)."""
+    import torch
+    import synth
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    lib.dsa_sparse_attn_fwd_tc.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_float, vp, vp, vp]
+    lib.dsa_fwd_tc_profile.argtypes = [vp, i32]
+    qa, ka, va = synth.attention_inputs(wl)
+    q, k, v = to(qa), to(ka), to(va)
+    del qa, ka, va
+    S = wl.S
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((S, wl.Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for rep in range(2):  # the second call is the one read back
+        ev0.record()
+        rc = lib.dsa_sparse_attn_fwd_tc(q.data_ptr(), k.data_ptr(), v.data_ptr(), pool_idx.data_ptr(), S, wl.Hq, wl.D,
+                                        wl.topk, ctypes.c_float(wl.scale), o.data_ptr(), lse.data_ptr(), stream)
+        ev1.record()
+        if rc != 0:
+            raise RuntimeError(lib.dsa_last_error().decode())
+        torch.cuda.synchronize()
+    ctas = min(S, torch.cuda.get_device_properties(0).multi_processor_count)
+    cnt = np.zeros((ctas, 32), dtype=np.uint64)
+    if lib.dsa_fwd_tc_profile(cnt.ctypes.data, ctas) != 32 * ctas:
+        return {"error": lib.dsa_last_error().decode()}
+    c = cnt.astype(np.float64).sum(axis=0)
+    roles = {"producers": (0, ["row_buffer_wait", "selection_scan", "free_stage_wait", "block_record", "copy_issue",
+                               "drain"], 7),
+             "issuer": (8, ["full_stage_wait", "free_s_wait", "s_issue", "o_products_with_p_waits", "drain"], 15),
+             "softmax": (16, ["full_stage_wait", "s_wait_and_load", "max_check_and_rescale", "p_buffer_wait",
+                              "p_write", "epilogue"], 23)}
+    res = {"call_ms": ev0.elapsed_time(ev1), "ctas": ctas}
+    for role, (off, names, bw) in roles.items():
+        blocks = max(c[bw], 1.0)
+        res[role] = {n: round(c[off + j] / blocks, 1) for j, n in enumerate(names)}
+        res[role]["blocks"] = int(c[bw])
+    res["unit"] = "SM clock cycles per 128-key block, per role (one thread's view)"
+    return res
 
 
 def main():

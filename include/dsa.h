@@ -418,6 +418,23 @@ double dsa_measure_umma(int n, int issuers, int groups, void* stream);
  */
 int dsa_trace_configure(void* buf, size_t bytes);
 
+/*
+ * Role counters of the last dsa_sparse_attn_fwd_tc launch (measurement
+ * helper; only the trace build, compiled with DSA_FWD_PROFILE, has them --
+ * the default build returns -1).  Copies ctas x 32 uint64 words into
+ * `counters` (host memory), one row per CTA of the launch (the launch has
+ * min(S, number of SMs) CTAs): clock cycles each warp role spent per
+ * pipeline segment, summed over the blocks it handled --
+ *   words 0..5   producers: row-buffer wait, selection scan, free-stage wait,
+ *                block record, copy issue, drain; word 7 blocks
+ *   words 8..12  issuer: full-stage wait, free-S^T wait, S^T issue, O^T
+ *                products (their P^T waits included), final drain; word 15 blocks
+ *   words 16..21 softmax: full-stage wait, S^T wait and load, maximum check
+ *                (and rescale), P^T-buffer wait, P^T write, epilogue; word 23 blocks
+ * Returns the words copied, or -1.
+ */
+int dsa_fwd_tc_profile(uint64_t* counters, int ctas);
+
 void dsa_profile_enable(int on);
 int dsa_profile_read(char* names, int name_len, double* ms, int64_t* launches, int max_kernels);
 int64_t dsa_launch_count(void);

@@ -31,7 +31,8 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_sparse_attn_fwd_varlen", "dsa_sparse_attn_bwd_varlen_workspace", "dsa_sparse_attn_bwd_varlen",
             "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic",
             "dsa_index_topk_stats", "dsa_measure_l2", "dsa_index_topk_workspace_slots", "dsa_trace_configure",
-            "dsa_last_kernel_config", "dsa_sparse_attn_fwd_tc", "dsa_measure_umma")
+            "dsa_last_kernel_config", "dsa_sparse_attn_fwd_tc", "dsa_measure_umma",
+            "dsa_fwd_tc_profile")
 
 _lock = threading.Lock()
 _lib = None

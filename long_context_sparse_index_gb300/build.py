@@ -18,7 +18,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa.so")
 # measurement variant: the persistent indexer records one globaltimer trace
-# record per work item (DSA_ITEM_TRACE); nothing else differs
+# record per work item (DSA_ITEM_TRACE) and the tcgen05 forward sums each warp
+# role's cycles per pipeline segment (DSA_FWD_PROFILE); nothing else differs
 BUILD_TRACE = os.path.join(HERE, "_build_trace")
 LIB_TRACE = os.path.join(HERE, "libdsa_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -54,7 +55,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
         return lib
     os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + (["-DDSA_ITEM_TRACE=1"] if trace else [])
+    flags = NVCC_FLAGS + (["-DDSA_ITEM_TRACE=1", "-DDSA_FWD_PROFILE=1"] if trace else [])
 
     def compile_one(src: str) -> str:
         obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")

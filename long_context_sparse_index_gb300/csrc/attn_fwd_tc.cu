@@ -652,4 +652,17 @@ cudaError_t launch_attn_fwd_tc(const void* q, const void* k, const void* v, cons
   return cudaGetLastError();
 }
 
+// Role counters of the last profiled launch (profile build): ctas x 32
+// words, see g_fwd_prof.  Returns the words copied, or -1 without the build.
+int fwd_tc_profile_read(unsigned long long* out, int ctas) {
+#if DSA_FWD_PROFILE
+  if (ctas < 0 || ctas > 1024) return -1;
+  if (cudaMemcpyFromSymbol(out, g_fwd_prof, sizeof(unsigned long long) * 32 * ctas) != cudaSuccess) return -1;
+  return 32 * ctas;
+#else
+  (void)out, (void)ctas;
+  return -1;
+#endif
+}
+
 }  // namespace dsa

@@ -1014,6 +1014,16 @@ int dsa_trace_configure(void* buf, size_t bytes) {
 #endif
 }
 
+int dsa_fwd_tc_profile(uint64_t* counters, int ctas) {
+  if (!counters || ctas < 1) {
+    fail(DSA_ERR_INVALID_ARG, "dsa_fwd_tc_profile: counters must hold ctas x 32 words, ctas >= 1");
+    return -1;
+  }
+  const int n = dsa::fwd_tc_profile_read(reinterpret_cast<unsigned long long*>(counters), ctas);
+  if (n < 0) fail(DSA_ERR_UNSUPPORTED, "dsa_fwd_tc_profile: this library was built without DSA_FWD_PROFILE");
+  return n;
+}
+
 void dsa_profile_enable(int on) { g_profiling.store(on ? 1 : 0); }
 
 int dsa_profile_read(char* names, int name_len, double* ms, int64_t* launches, int max_kernels) {

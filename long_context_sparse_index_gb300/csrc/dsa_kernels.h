@@ -191,6 +191,9 @@ cudaError_t launch_attn_fwd_tc(const void* q, const void* k, const void* v, cons
                                int64_t q_end, int topk, float scale, void* o, float* lse, const LaunchCtx& ctx,
                                const SeqTable* tab = nullptr);
 
+// Its profile build's per-CTA role counters (-1 in the default build).
+int fwd_tc_profile_read(unsigned long long* out, int ctas);
+
 // Delta for nq query rows, and zeroing of the two fp32 accumulators (skipped when dk_acc is null).
 cudaError_t launch_attn_bwd_pre(const void* dO, const void* o, int64_t nq, int64_t S, float* delta, float* dk_acc,
                                 float* dv_acc, const LaunchCtx& ctx);
