@@ -530,6 +530,14 @@ def test_malformed_selection_is_reported_not_read():
         dsa.dsa_sync_status()
     assert ei.value.status == dsa.DSA_ERR_INTERNAL
     dsa.dsa_clear_status()
+    # the tcgen05 forward reports it the same way, and only that row changes
+    o_tc, _ = dsa.dsa_sparse_attn_fwd_tc(q, k, v, torch.from_numpy(sel).to(DEV))
+    with pytest.raises(dsa.DsaError) as ei:
+        dsa.dsa_sync_status()
+    assert ei.value.status == dsa.DSA_ERR_INTERNAL
+    dsa.dsa_clear_status()
+    keep = torch.arange(S, device=DEV) != 200
+    assert (o_tc[keep].float() - o[keep].float()).abs().max().item() <= 1.6e-2
 
 
 def test_binding_refuses_bad_outputs_and_shapes():
