@@ -54,7 +54,7 @@
 // clock64 cycles of its pipeline segments into per-thread counters, and one
 // thread of each role stores them per CTA in g_fwd_prof[cta][32] (producer
 // segments at 0.., issuer at 8.., softmax at 16..; the role's block count in
-// its last slot), for a harness to read back.
+// its last slot), read back by dsa_fwd_tc_profile.
 #if DSA_FWD_PROFILE
 __device__ unsigned long long g_fwd_prof[1024 * 32];
 #define FWD_PROF_BEGIN long long prof_[8] = {0, 0, 0, 0, 0, 0, 0, 0}, prof_t_ = clock64()
