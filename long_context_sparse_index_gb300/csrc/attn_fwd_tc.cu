@@ -136,7 +136,7 @@ constexpr uint32_t kBarQEmpty = 14;   // [2] last S^T product of the Q buffer's 
 constexpr uint32_t kBarOFull = 16;    // [2] O^T buffer complete for its query (commit)
 constexpr uint32_t kBarOEmpty = 18;   // [2] O^T buffer read (128 softmax arrivals)
 constexpr uint32_t kBarDrain = 20;    // every product issued has completed (commit)
-constexpr uint32_t kBarProw = 21;     // [2] a pool_idx row landed (128 copy-completion arrivals)
+constexpr uint32_t kBarProw = 21;     // [2] a pool_idx row landed (a copy-completion arrival per producer)
 constexpr int kNumBars = 23;
 static_assert(kNumBars * 8 <= 256, "barriers fit");
 static_assert(kProducerThreads % 16 == 0 && kKeysPerProducer * kProducerThreads == kBlkKeys * 16, "gather map");
@@ -183,9 +183,10 @@ __device__ __forceinline__ bool issue_pv(uint32_t bars, uint32_t tmem, uint64_t 
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                    const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t q0,
-                    int64_t rows, int topk, float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                    unsigned* status, uint64_t limit_ns, int prow_bufs, const __grid_constant__ SeqTable tab) {
+                       const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ pool_idx, int64_t q0,
+                       int64_t rows, int topk, float scale_log2, __nv_bfloat16* __restrict__ o,
+                       float* __restrict__ lse, unsigned* status, uint64_t limit_ns, int prow_bufs,
+                       const __grid_constant__ SeqTable tab) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-B swizzle atoms need 1024-B alignment
