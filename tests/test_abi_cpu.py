@@ -143,6 +143,32 @@ def test_attention_rejects_bad_arguments(lib):
     assert b(*args[:7], 64, 16, 128, 4096, 0.0, *args[12:], FAKE, 1 << 30, None) == dsa.DSA_ERR_UNSUPPORTED
 
 
+def test_tcgen05_forward_and_probes_reject_bad_arguments(lib):
+    """The tcgen05 forward takes the default forward's checks; the tensor-core
+    probe and the profile reader refuse bad arguments (and the profile reader
+    answers -1 in the default build, which has no counters) without touching
+    the device."""
+    import long_context_sparse_index_gb300 as dsa
+    f = lib.dsa_sparse_attn_fwd_tc
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 16, 128, 8, 0.0, FAKE, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 8, 128, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 16, 64, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 16, 128, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(FAKE + 8, FAKE, FAKE, FAKE, 64, 16, 128, 8, 0.0, FAKE, FAKE, None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"16-byte aligned" in lib.dsa_last_error()
+    m = lib.dsa_measure_umma
+    for n, issuers, groups in ((8, 1, 10), (48, 1, 10), (16, 0, 10), (16, 4, 10), (256, 3, 10), (16, 1, 0)):
+        assert m(n, issuers, groups, None) == -1.0
+    assert b"dsa_measure_umma" in lib.dsa_last_error()
+    p = lib.dsa_fwd_tc_profile
+    p.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    assert p(None, 4) == -1
+    buf = (ctypes.c_uint64 * (32 * 4))()
+    assert p(ctypes.addressof(buf), 0) == -1
+    assert p(ctypes.addressof(buf), 4) == -1
+    assert b"without DSA_FWD_PROFILE" in lib.dsa_last_error()
+
+
 def test_attention_ranges_are_checked(lib):
     """The range forms reject a query range outside [0, S) before any device access."""
     import long_context_sparse_index_gb300 as dsa
