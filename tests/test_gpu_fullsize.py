@@ -78,6 +78,14 @@ def test_s1m_cluster_index_topk_and_forward_sampled():
     ro, rl = oracle.attn_fwd(q, k, v, sel, scale=wl.scale, rows=rows)
     assert_close(torch_bf16_to_f64(o[torch.from_numpy(rows).to(DEV)]), ro, "o")
     assert_close(lse[torch.from_numpy(rows).to(DEV)].cpu().numpy().astype(np.float64), rl, "lse", bf16_out=False)
+    # the tcgen05 forward on the same launch size and rows
+    del o, lse
+    o, lse = dsa.dsa_sparse_attn_fwd_tc(bits_to_torch(q, DEV), bits_to_torch(k, DEV), bits_to_torch(v, DEV),
+                                        torch.from_numpy(sel).to(DEV), scale=wl.scale)
+    dsa.dsa_sync_status()
+    assert_close(torch_bf16_to_f64(o[torch.from_numpy(rows).to(DEV)]), ro, "o (tcgen05 forward)")
+    assert_close(lse[torch.from_numpy(rows).to(DEV)].cpu().numpy().astype(np.float64), rl, "lse (tcgen05 forward)",
+                 bf16_out=False)
 
 
 def _check_forward_on_oracle_selection(wl, n_rows, seed):
@@ -99,6 +107,12 @@ def _check_forward_on_oracle_selection(wl, n_rows, seed):
     ro, rl = oracle.attn_fwd(q, k, v, sel, scale=wl.scale, rows=rows)
     assert_close(torch_bf16_to_f64(o[ri]), ro, "o")
     assert_close(lse[ri].cpu().numpy().astype(np.float64), rl, "lse", bf16_out=False)
+    # the tcgen05 forward, same launch and rows
+    o, lse = dsa.dsa_sparse_attn_fwd_tc(bits_to_torch(q, DEV), bits_to_torch(k, DEV), bits_to_torch(v, DEV),
+                                        torch.from_numpy(sel).to(DEV), scale=wl.scale)
+    dsa.dsa_sync_status()
+    assert_close(torch_bf16_to_f64(o[ri]), ro, "o (tcgen05 forward)")
+    assert_close(lse[ri].cpu().numpy().astype(np.float64), rl, "lse (tcgen05 forward)", bf16_out=False)
 
 
 def test_s16k_forward_on_oracle_selection_sampled():
