@@ -464,6 +464,11 @@ def run_ours(args):
                 red = work["keys"] * 2 * wl.D * 4 / (ms * 1e-3) / 1e9
                 entry.update({"reduction_gbs": red, "frac_of_l2_red": red / l2["red_v4_gbs"]})
         kernels[name] = entry
+    if "index_topk" in kernels:
+        # the tile loop's handoff measured alone (same warp layout and register cap)
+        kernels["index_topk"]["fold_probe_cycles_per_head"] = {
+            "loads_and_fold": round(dsa.measure_fold(1), 1), "loads_only": round(dsa.measure_fold(0), 1),
+            "tmem_ld32": round(dsa.measure_fold(2), 1), "mma_chain_nominal": 1024}
     dom = max(prof.items(), key=lambda kv: kv[1][0])[0]
     dms, dl = prof[dom]
     if dom == "index_topk":

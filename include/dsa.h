@@ -404,6 +404,23 @@ double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream
 double dsa_measure_umma(int n, int issuers, int groups, void* stream);
 
 /*
+ * Accumulator-handoff probe of the indexer (measurement helper).  One CTA of
+ * the indexer's 19-warp layout: one thread issues, per head, 8 chained
+ * tcgen05.mma (M = 128, N = 256, K = 16, bf16) into one of two tensor-memory
+ * accumulators, and 16 epilogue warps each load their lane quarter's 64
+ * columns 16 at a time and release the accumulator after the last load.
+ *   mode 0  the loads alone
+ *   mode 1  the loads and the indexer's fold (ReLU, packed FMA into 64 fp32
+ *           sums a thread)
+ *   mode 2  one warp's 32-column tensor-memory load and its wait, alone
+ * Runs `heads` (>= 2) heads after one warm-up pass, synchronises `stream`
+ * and returns the issuing thread's clock cycles per head (mode 2: per load),
+ * or -1.0 on error.  The 8 products of one head take 1024 cycles at the
+ * dense bf16 rate.
+ */
+double dsa_measure_fold(int mode, int heads, void* stream);
+
+/*
  * Item trace of the persistent indexer (measurement helper; only the trace
  * build of the library, libdsa_trace.so, compiled with DSA_ITEM_TRACE, records
  * anything -- the default build returns -1).  `buf` is a device buffer of

@@ -32,7 +32,7 @@ EXPORTED = ("dsa_index_topk_workspace", "dsa_index_topk", "dsa_sparse_attn_fwd",
             "dsa_sparse_attn_bwd_deterministic_workspace", "dsa_sparse_attn_bwd_deterministic",
             "dsa_index_topk_stats", "dsa_measure_l2", "dsa_index_topk_workspace_slots", "dsa_trace_configure",
             "dsa_last_kernel_config", "dsa_sparse_attn_fwd_tc", "dsa_measure_umma",
-            "dsa_fwd_tc_profile")
+            "dsa_fwd_tc_profile", "dsa_measure_fold")
 
 _lock = threading.Lock()
 _lib = None
@@ -113,6 +113,8 @@ def load():
             lib.dsa_measure_l2.restype = ctypes.c_double
             lib.dsa_measure_umma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
             lib.dsa_measure_umma.restype = ctypes.c_double
+            lib.dsa_measure_fold.argtypes = [ctypes.c_int, ctypes.c_int, vp]
+            lib.dsa_measure_fold.restype = ctypes.c_double
             lib.dsa_last_kernel_config.argtypes = [ctypes.c_char_p, sz]
             lib.dsa_last_kernel_config.restype = ctypes.c_int
             _lib = lib
@@ -470,6 +472,17 @@ def measure_umma(n: int, issuers: int = 1, groups: int = 2000, stream=None) -> f
     issuing thread, with `issuers` issuing CTAs on every SM."""
     lib = load()
     r = lib.dsa_measure_umma(n, issuers, groups, _stream_handle(stream))
+    if r < 0:
+        raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
+    return float(r)
+
+
+def measure_fold(mode: int, heads: int = 2000, stream=None) -> float:
+    """Clock cycles per head of the indexer's accumulator handoff in isolation
+    (mode 0 loads only, 1 loads and fold), or per 32-column tensor-memory load
+    (mode 2)."""
+    lib = load()
+    r = lib.dsa_measure_fold(mode, heads, _stream_handle(stream))
     if r < 0:
         raise DsaError(DSA_ERR_CUDA, lib.dsa_last_error().decode())
     return float(r)

@@ -18,6 +18,14 @@
 //   kind 4  the same with 512-byte operations (one row each)
 // All report bytes moved (read, or added) per second.
 //
+// dsa_measure_fold times the indexer's accumulator handoff in isolation: the
+// same 19-warp layout (one MMA issuer, two idle control warps, 16 epilogue
+// warps, so the same 96-register cap), a chain of 8 tcgen05.mma (M 128,
+// N 256, K 16: one head of the hi/lo contraction) into one of two tensor-
+// memory accumulators per head, and each epilogue warp loading its lane
+// quarter's 64 columns 16 at a time and folding them (ReLU, then a packed
+// FMA into 64 fp32 sums) before the accumulator is released.
+//
 // dsa_measure_umma times the tensor core on the attention's product shape:
 // one thread per CTA issues back-to-back groups of 8 chained tcgen05.mma
 // (kind::f16, bf16 operands from 128-byte swizzled shared memory, M = 128,
@@ -177,6 +185,120 @@ static cudaError_t launch_probe_umma(int grid, int groups, unsigned long long* c
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------- accumulator handoff probe
+constexpr int kFoldThreads = 608;  // warp 0 issues, warps 1-2 idle, warps 3..18 fold
+constexpr int kFoldHeadMmas = 8;
+constexpr uint32_t kFoldA = 32768, kFoldB = 65536;  // [2][128 rows][128 B], [2][256 rows][128 B]
+
+template <int kMode>
+__global__ void __launch_bounds__(kFoldThreads, 1) probe_fold_kernel(int heads, uint64_t limit_ns,
+                                                                   unsigned long long* cycles, int* failed,
+                                                                   float* sink) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dsa::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* g = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + kFoldA;
+  const uint32_t full = sB + kFoldB, empty = full + 16;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(g + kFoldA + kFoldB + 64);
+  for (int i = threadIdx.x; i < static_cast<int>((kFoldA + kFoldB) / 4); i += blockDim.x) {
+    const uint32_t h = 0x3C80u + ((i * 7u) & 7u);  // small bf16 operands
+    reinterpret_cast<uint32_t*>(g)[i] = h | (h << 16);
+  }
+  dsa::fence_proxy_async_smem();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      dsa::mbar_init(full + 8 * x, 1);
+      dsa::mbar_init(empty + 8 * x, 16);
+    }
+    dsa::mbar_fence_init();
+  }
+  if (warp == 0) dsa::tmem_alloc(dsa::smem_u32(slot), 512);
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  const uint32_t tmem = *slot;
+  bool ok = true;
+  if (kMode == 2) {
+    // one warp: a 32-column load of its own lane quarter and its wait, back to back
+    if (warp == 3) {
+      uint32_t acc = 0;
+      const long long t0 = clock64();
+      for (int i = 0; i < heads; ++i) {
+        uint32_t r[32];
+        dsa::tmem_ld32(tmem + (static_cast<uint32_t>(3 * 32) << 16) + static_cast<uint32_t>(i & 7) * 32, r);
+        dsa::tmem_ld_wait();
+        acc += r[0] ^ r[31];
+      }
+      if (lane == 0) atomicAdd(cycles, static_cast<unsigned long long>((clock64() - t0) / heads));
+      if (acc == 0x9E3779B9u) sink[threadIdx.x] = 1.f;
+    }
+  } else if (warp == 0) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = dsa::umma_idesc_bf16_f32(128, 256);
+      const uint64_t dA = dsa::umma_desc_sw128(sA), dB = dsa::umma_desc_sw128(sB);
+      const long long t0 = clock64();
+      for (int h = 0; h < heads && ok; ++h) {
+        const int cs = h & 1;
+        if (h >= 2) ok = dsa::mbar_wait(empty + 8 * cs, ((h >> 1) - 1) & 1, limit_ns, nullptr);
+        dsa::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kFoldHeadMmas; ++kk)
+          dsa::umma_bf16(tmem + cs * 256, dA + (((kk >> 2) * (kFoldA / 2) + (kk & 3) * 32) >> 4),
+                         dB + (((kk >> 2) * (kFoldB / 2) + (kk & 3) * 32) >> 4), idesc, kk > 0 ? 1u : 0u);
+        dsa::umma_commit(full + 8 * cs);
+      }
+      if (ok) ok = dsa::mbar_wait(empty + 8 * ((heads - 1) & 1), ((heads - 1) >> 1) & 1, limit_ns, nullptr);
+      atomicAdd(cycles, static_cast<unsigned long long>((clock64() - t0) / heads));
+    }
+    __syncwarp();
+  } else if (warp >= 3) {
+    const int ew = warp - 3, lq = warp & 3, cq = ew >> 2;
+    float2 acc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
+    const float2 w2 = make_float2(0.5f, 0.5f);
+    for (int h = 0; h < heads && ok; ++h) {
+      const int cs = h & 1;
+      ok = dsa::mbar_wait(full + 8 * cs, (h >> 1) & 1, limit_ns, nullptr);
+      dsa::tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + cs * 256 + cq * 64;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[16];
+        dsa::tmem_ld16(taddr + cc * 16, r);
+        dsa::tmem_ld_wait();
+        if (cc == 3) {
+          dsa::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dsa::mbar_arrive(empty + 8 * cs);
+        }
+        if (kMode == 1) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 x =
+                make_float2(fmaxf(__uint_as_float(r[2 * j]), 0.f), fmaxf(__uint_as_float(r[2 * j + 1]), 0.f));
+            acc[cc * 8 + j] = __ffma2_rn(w2, x, acc[cc * 8 + j]);
+          }
+        } else {
+          acc[cc] = make_float2(acc[cc].x + __uint_as_float(r[0]), acc[cc].y);
+        }
+      }
+    }
+    float t = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) t += acc[j].x + acc[j].y;
+    if (t == 1.2345f) sink[threadIdx.x] = t;
+  }
+  if (!ok) atomicExch(failed, 1);
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  if (warp == 0) dsa::tmem_dealloc(tmem, 512);
+}
+
 }  // namespace
 
 
@@ -285,6 +407,46 @@ double dsa_measure_umma(int n, int issuers, int groups, void* stream) {
     return -1.0;
   }
   return static_cast<double>(total) / grid / (static_cast<double>(groups) * kUmmaGroup);
+}
+
+double dsa_measure_fold(int mode, int heads, void* stream) {
+  if (mode < 0 || mode > 2 || heads < 2) {
+    dsa::set_last_error("dsa_measure_fold: mode 0 (no arithmetic), 1 (the fold) or 2 (TMEM load), heads >= 2");
+    return -1.0;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned long long* cycles = nullptr;
+  cudaError_t e = cudaMalloc(&cycles, sizeof(unsigned long long) + sizeof(int) + kFoldThreads * sizeof(float));
+  if (e != cudaSuccess) {
+    dsa::set_last_error(std::string("dsa_measure_fold: ") + cudaGetErrorString(e));
+    return -1.0;
+  }
+  int* failed = reinterpret_cast<int*>(cycles + 1);
+  float* sink = reinterpret_cast<float*>(failed + 1);
+  const int smem = 1024 + static_cast<int>(kFoldA + kFoldB) + 128;
+  e = cudaFuncSetAttribute(probe_fold_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(probe_fold_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(probe_fold_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {  // the first pass warms up
+    e = cudaMemsetAsync(cycles, 0, sizeof(unsigned long long) + sizeof(int), st);
+    if (e == cudaSuccess) {
+      if (mode == 0) probe_fold_kernel<0><<<1, kFoldThreads, smem, st>>>(heads, 2000000000ull, cycles, failed, sink);
+      else if (mode == 1) probe_fold_kernel<1><<<1, kFoldThreads, smem, st>>>(heads, 2000000000ull, cycles, failed, sink);
+      else probe_fold_kernel<2><<<1, kFoldThreads, smem, st>>>(heads, 2000000000ull, cycles, failed, sink);
+      e = cudaGetLastError();
+    }
+  }
+  unsigned long long c = 0;
+  int bad = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&c, cycles, sizeof(c), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&bad, failed, sizeof(bad), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(cycles);
+  if (e != cudaSuccess || bad) {
+    dsa::set_last_error(std::string("dsa_measure_fold: ") + (bad ? "a completion wait ran out" : cudaGetErrorString(e)));
+    return -1.0;
+  }
+  return static_cast<double>(c);
 }
 
 }  // extern "C"

@@ -160,6 +160,10 @@ def test_tcgen05_forward_and_probes_reject_bad_arguments(lib):
     for n, issuers, groups in ((8, 1, 10), (48, 1, 10), (16, 0, 10), (16, 4, 10), (256, 3, 10), (16, 1, 0)):
         assert m(n, issuers, groups, None) == -1.0
     assert b"dsa_measure_umma" in lib.dsa_last_error()
+    fo = lib.dsa_measure_fold
+    for mode, heads in ((-1, 100), (3, 100), (1, 1)):
+        assert fo(mode, heads, None) == -1.0
+    assert b"dsa_measure_fold" in lib.dsa_last_error()
     p = lib.dsa_fwd_tc_profile
     p.argtypes = [ctypes.c_void_p, ctypes.c_int]
     assert p(None, 4) == -1
