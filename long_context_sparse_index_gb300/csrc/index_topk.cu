@@ -697,7 +697,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lq = warp & 3;
     const int cq = ew >> 2;
     const int gid = ew >> 2;
-    const topk::Group grp{etid - gid * topk::kGT, 2 + gid};
     int cs = 0, is = 0;
     uint32_t cph = 0, iph = 0;
     CycleSum cyc_fw, cyc_fold, cyc_fheads, cyc_cmp, cyc_atom, cyc_wr, cyc_app;
@@ -717,14 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_sync();
       if (!*group_ok || it.kind == kItemEnd) break;
 
-      const Chunk ch = chunk_of(a, it.chunk);
-      const int bi = it.chunk % a.nbuf;
+      Chunk ch = chunk_of(a, it.chunk);
+      int bi = it.chunk % a.nbuf;
       uint64_t ts0 = 0, ts1 = 0, ts2 = 0;
       DSA_STAMP(ts0);
       ts1 = ts0;
       if (it.kind == kItemTile || it.kind == kItemSample) {
-        const int qb = it.a;
-        const int64_t row = ch.row0 + static_cast<int64_t>(qb) * kBM + lq * 32 + lane;
+        int qb = it.a;
+        int64_t row = ch.row0 + static_cast<int64_t>(qb) * kBM + lq * 32 + lane;
         const bool valid = row < ch.row0 + ch.nrows;
         const float* wrow = a.w + (valid ? row : ch.row0) * a.Hi;
         float2 acc[kEpiCols / 2];
@@ -773,6 +772,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         cyc_fold.stop();
+        // the item, its chunk and this thread's row are read again here
+        // rather than held in registers through the fold (the item's ring
+        // slot stays as it is until every epilogue warp is done with it)
+        it.kind = items[is].kind;
+        it.chunk = items[is].chunk;
+        it.a = items[is].a;
+        it.b = items[is].b;
+        ch = chunk_of(a, it.chunk);
+        bi = it.chunk % a.nbuf;
+        qb = it.a;
+        row = ch.row0 + static_cast<int64_t>(qb) * kBM + lq * 32 + lane;
         DSA_STAMP(ts1);
         // the item's dependencies (met long ago, as a rule)
         if (ok) ok = mbar_wait(bar_deps + 8 * is, iph, a.limit_ns, abort_flag);
@@ -878,6 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!*wait_ok) break;
         DSA_STAMP(ts2);
         const int r0 = it.a, nr = it.b;
+        const topk::Group grp{etid - gid * topk::kGT, 2 + gid};
         if (a.rpi == kRowsPerWarpItem) {
           // one row per warp (topk <= 512)
           if (ew < nr) {
