@@ -44,6 +44,76 @@ class DsaError(RuntimeError):
         self.status = status
 
 
+def _configure(lib):
+    """Declares the argument and result types of every C ABI entry point."""
+    i64, i32, vp, sz, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+    lib.dsa_index_topk_workspace.argtypes = [i64, i32, i32, i32, i32]
+    lib.dsa_index_topk_workspace.restype = sz
+    lib.dsa_index_topk_workspace_slots.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.dsa_index_topk_workspace_slots.restype = sz
+    lib.dsa_index_topk.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp, sz, vp]
+    lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
+    lib.dsa_sparse_attn_fwd_tc.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
+    lib.dsa_sparse_attn_bwd_workspace.argtypes = [i64, i32, i32]
+    lib.dsa_sparse_attn_bwd_workspace.restype = sz
+    lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp,
+                                        sz, vp]
+    lib.dsa_sparse_attn_fwd_range.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, f32, vp, vp, vp]
+    lib.dsa_sparse_attn_bwd_range.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, f32,
+                                              vp, vp, vp, vp, sz, vp]
+    lib.dsa_zigzag_ranges.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+    for f in (lib.dsa_sparse_attn_fwd_range, lib.dsa_sparse_attn_bwd_range, lib.dsa_zigzag_ranges):
+        f.restype = ctypes.c_int
+    pi64 = ctypes.POINTER(ctypes.c_int64)
+    lib.dsa_index_topk_varlen_workspace.argtypes = [pi64, i32, i32, i32, i32, i32]
+    lib.dsa_index_topk_varlen_workspace.restype = sz
+    lib.dsa_index_topk_varlen.argtypes = [vp, vp, vp, pi64, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+    lib.dsa_sparse_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, pi64, i32, i32, i32, i32, f32, vp, vp, vp]
+    lib.dsa_sparse_attn_bwd_varlen_workspace.argtypes = [pi64, i32, i32, i32]
+    lib.dsa_sparse_attn_bwd_varlen_workspace.restype = sz
+    lib.dsa_sparse_attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, pi64, i32, i32, i32, i32, f32, vp,
+                                               vp, vp, vp, sz, vp]
+    for f in (lib.dsa_index_topk_varlen, lib.dsa_sparse_attn_fwd_varlen, lib.dsa_sparse_attn_bwd_varlen):
+        f.restype = ctypes.c_int
+    lib.dsa_sparse_attn_bwd_deterministic_workspace.argtypes = [i64, i32, i32, i32]
+    lib.dsa_sparse_attn_bwd_deterministic_workspace.restype = sz
+    lib.dsa_sparse_attn_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp,
+                                                      vp, vp, vp, sz, vp]
+    lib.dsa_sparse_attn_bwd_deterministic.restype = ctypes.c_int
+    lib.dsa_sync_status.argtypes = [vp]
+    lib.dsa_clear_status.argtypes = []
+    for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_fwd_tc, lib.dsa_sparse_attn_bwd,
+              lib.dsa_sync_status,
+              lib.dsa_clear_status):
+        f.restype = ctypes.c_int
+    lib.dsa_last_error.argtypes = []
+    lib.dsa_last_error.restype = ctypes.c_char_p
+    lib.dsa_version.argtypes = []
+    lib.dsa_version.restype = ctypes.c_char_p
+    lib.dsa_profile_enable.argtypes = [ctypes.c_int]
+    lib.dsa_profile_enable.restype = None
+    lib.dsa_profile_read.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
+    lib.dsa_profile_read.restype = ctypes.c_int
+    lib.dsa_launch_count.argtypes = []
+    lib.dsa_launch_count.restype = ctypes.c_int64
+    lib.dsa_index_topk_noalloc.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp]
+    lib.dsa_index_topk_noalloc.restype = ctypes.c_int
+    lib.dsa_launch_count_reset.argtypes = []
+    lib.dsa_launch_count_reset.restype = None
+    lib.dsa_index_topk_stats.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, vp]
+    lib.dsa_index_topk_stats.restype = ctypes.c_int
+    lib.dsa_measure_l2.argtypes = [ctypes.c_int, vp, sz, ctypes.c_int, vp]
+    lib.dsa_measure_l2.restype = ctypes.c_double
+    lib.dsa_measure_umma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    lib.dsa_measure_umma.restype = ctypes.c_double
+    lib.dsa_measure_fold.argtypes = [ctypes.c_int, ctypes.c_int, vp]
+    lib.dsa_measure_fold.restype = ctypes.c_double
+    lib.dsa_last_kernel_config.argtypes = [ctypes.c_char_p, sz]
+    lib.dsa_last_kernel_config.restype = ctypes.c_int
+    return lib
+
+
 def load():
     """Loads libdsa.so (built by __graft_entry__.build()); raises if it is missing."""
     global _lib
@@ -51,74 +121,15 @@ def load():
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise DsaError(DSA_ERR_CUDA, f"{LIB_PATH} is not built; run __graft_entry__.build()")
-            lib = ctypes.CDLL(LIB_PATH)
-            i64, i32, vp, sz, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
-            lib.dsa_index_topk_workspace.argtypes = [i64, i32, i32, i32, i32]
-            lib.dsa_index_topk_workspace.restype = sz
-            lib.dsa_index_topk_workspace_slots.argtypes = [i64, i32, i32, i32, i32, i32]
-            lib.dsa_index_topk_workspace_slots.restype = sz
-            lib.dsa_index_topk.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp, sz, vp]
-            lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
-            lib.dsa_sparse_attn_fwd_tc.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp]
-            lib.dsa_sparse_attn_bwd_workspace.argtypes = [i64, i32, i32]
-            lib.dsa_sparse_attn_bwd_workspace.restype = sz
-            lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp, vp, vp, vp,
-                                                sz, vp]
-            lib.dsa_sparse_attn_fwd_range.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, f32, vp, vp, vp]
-            lib.dsa_sparse_attn_bwd_range.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, f32,
-                                                      vp, vp, vp, vp, sz, vp]
-            lib.dsa_zigzag_ranges.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
-            for f in (lib.dsa_sparse_attn_fwd_range, lib.dsa_sparse_attn_bwd_range, lib.dsa_zigzag_ranges):
-                f.restype = ctypes.c_int
-            pi64 = ctypes.POINTER(ctypes.c_int64)
-            lib.dsa_index_topk_varlen_workspace.argtypes = [pi64, i32, i32, i32, i32, i32]
-            lib.dsa_index_topk_varlen_workspace.restype = sz
-            lib.dsa_index_topk_varlen.argtypes = [vp, vp, vp, pi64, i32, i32, i32, i32, i32, vp, vp, sz, vp]
-            lib.dsa_sparse_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, pi64, i32, i32, i32, i32, f32, vp, vp, vp]
-            lib.dsa_sparse_attn_bwd_varlen_workspace.argtypes = [pi64, i32, i32, i32]
-            lib.dsa_sparse_attn_bwd_varlen_workspace.restype = sz
-            lib.dsa_sparse_attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, pi64, i32, i32, i32, i32, f32, vp,
-                                                       vp, vp, vp, sz, vp]
-            for f in (lib.dsa_index_topk_varlen, lib.dsa_sparse_attn_fwd_varlen, lib.dsa_sparse_attn_bwd_varlen):
-                f.restype = ctypes.c_int
-            lib.dsa_sparse_attn_bwd_deterministic_workspace.argtypes = [i64, i32, i32, i32]
-            lib.dsa_sparse_attn_bwd_deterministic_workspace.restype = sz
-            lib.dsa_sparse_attn_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, vp,
-                                                              vp, vp, vp, sz, vp]
-            lib.dsa_sparse_attn_bwd_deterministic.restype = ctypes.c_int
-            lib.dsa_sync_status.argtypes = [vp]
-            lib.dsa_clear_status.argtypes = []
-            for f in (lib.dsa_index_topk, lib.dsa_sparse_attn_fwd, lib.dsa_sparse_attn_fwd_tc, lib.dsa_sparse_attn_bwd,
-                      lib.dsa_sync_status,
-                      lib.dsa_clear_status):
-                f.restype = ctypes.c_int
-            lib.dsa_last_error.argtypes = []
-            lib.dsa_last_error.restype = ctypes.c_char_p
-            lib.dsa_version.argtypes = []
-            lib.dsa_version.restype = ctypes.c_char_p
-            lib.dsa_profile_enable.argtypes = [ctypes.c_int]
-            lib.dsa_profile_enable.restype = None
-            lib.dsa_profile_read.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
-                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
-            lib.dsa_profile_read.restype = ctypes.c_int
-            lib.dsa_launch_count.argtypes = []
-            lib.dsa_launch_count.restype = ctypes.c_int64
-            lib.dsa_index_topk_noalloc.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp, vp]
-            lib.dsa_index_topk_noalloc.restype = ctypes.c_int
-            lib.dsa_launch_count_reset.argtypes = []
-            lib.dsa_launch_count_reset.restype = None
-            lib.dsa_index_topk_stats.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, vp]
-            lib.dsa_index_topk_stats.restype = ctypes.c_int
-            lib.dsa_measure_l2.argtypes = [ctypes.c_int, vp, sz, ctypes.c_int, vp]
-            lib.dsa_measure_l2.restype = ctypes.c_double
-            lib.dsa_measure_umma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
-            lib.dsa_measure_umma.restype = ctypes.c_double
-            lib.dsa_measure_fold.argtypes = [ctypes.c_int, ctypes.c_int, vp]
-            lib.dsa_measure_fold.restype = ctypes.c_double
-            lib.dsa_last_kernel_config.argtypes = [ctypes.c_char_p, sz]
-            lib.dsa_last_kernel_config.restype = ctypes.c_int
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(LIB_PATH))
     return _lib
+
+
+def load_library(path: str):
+    """A configured handle on another build of the library at `path` (the
+    debug build's range checks, the trace build's counters), for calling its
+    C ABI directly."""
+    return _configure(ctypes.CDLL(path))
 
 
 def _check(rc: int):

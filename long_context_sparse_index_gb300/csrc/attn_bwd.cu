@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t r = 4 * n_elig + (kr & 3);
       if (r <= i) row = static_cast<int32_t>(r);
     }
+    DSA_CHECK(status, row >= -1 && row <= i);
     rows[e] = row;
   }
   if (bad) record_status(status, kStatusInternal);

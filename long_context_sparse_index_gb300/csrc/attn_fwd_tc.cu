@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t p = bp[(kKeyStep / 4) * u];
           const int64_t row = 4 * static_cast<int64_t>(p) + jj;
           const bool ok = p >= 0 && row <= i;
+          DSA_CHECK(status, p <= n_elig && dst_off + u * (kKeyStep * 128) + 16 <= kTile);
           const int64_t src = (ok ? row : 0) * kD + cc * 8;
           if (ok) cp_async16(sb + u * (kKeyStep * 128), kq + src, true);
           cp_async16(sb + kTile + u * (kKeyStep * 128), vq + src, ok);
@@ -566,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_part[h + 1] += p1;
           pk[h / 2] = pack_bf16(p0, p1);
         }
+        DSA_CHECK(status, key >= 0 && key < kBlkKeys);
         const uint32_t pa = sP + static_cast<uint32_t>(b & 1) * kPBytes + key * 16;
         st_shared_v4(pa, pk[0], pk[1], pk[2], pk[3]);
         st_shared_v4(pa + kPHeads8, pk[4], pk[5], pk[6], pk[7]);

@@ -28,6 +28,20 @@ __device__ __forceinline__ void record_status(unsigned* status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Debug build (DSA_DEBUG=1): range checks on gathered rows and shared-memory
+// offsets that record kStatusInternal (read back as DSA_ERR_INTERNAL) instead
+// of trapping; the default build compiles them to nothing.
+#if DSA_DEBUG
+#define DSA_CHECK(status, cond)                                            \
+  do {                                                                     \
+    if (!(cond)) ::dsa::record_status((status), ::dsa::kStatusInternal);  \
+  } while (0)
+#else
+#define DSA_CHECK(status, cond) \
+  do {                          \
+  } while (0)
+#endif
+
 // ----------------------------------------------------------------- programmatic dependent launch
 // wait: blocks until the preceding kernel in the stream has completed and its
 // memory is visible (a no-op when the launch did not allow early start).

@@ -789,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) raise_abort(a, abort_flag);
         DSA_STAMP(ts2);
         const int64_t rloc = row - ch.row0;
+        DSA_CHECK(a.status, !valid || (rloc >= 0 && rloc < a.thr_ld));
         if (!ok) {
           // nothing is written; the publisher times out and the call reports it
         } else if (it.kind == kItemSample) {

@@ -433,6 +433,56 @@ def test_attn_bwd_repeatable_within_rounding():
         assert bool(((xf - yf).abs() <= bound).all())
 
 
+def test_debug_build_checks_pass_and_results_match():
+    """The DSA_DEBUG build (range checks on gathered rows and shared-memory
+    offsets that record DSA_ERR_INTERNAL) finds nothing on valid inputs, and
+    its results are the default build's: bit for bit, except dK/dV, whose
+    atomic sums agree to rounding."""
+    from long_context_sparse_index_gb300 import _binding
+    from long_context_sparse_index_gb300 import build as libbuild
+    dbg = _binding.load_library(libbuild.build(debug=True))
+    wl = synth.WORKLOADS["tiny_int_s2048"]
+    q_idx, k_idx, w = _indexer_to_gpu(*synth.indexer_inputs(wl))
+    q, k, v, dO = _attn_to_gpu(*synth.attention_inputs(wl), synth.grad_output(wl))
+    S, topk, chunk = wl.S, wl.topk, wl.chunk
+    Hi, Di = q_idx.shape[1], q_idx.shape[2]
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def ok(rc):
+        assert rc == 0, dbg.dsa_last_error()
+
+    ref_sel = dsa.dsa_index_topk(q_idx, k_idx, w, chunk=chunk, topk=topk)
+    ref_o, ref_lse = dsa.dsa_sparse_attn_fwd(q, k, v, ref_sel)
+    ref_otc, ref_lsetc = dsa.dsa_sparse_attn_fwd_tc(q, k, v, ref_sel)
+    ref_g = dsa.dsa_sparse_attn_bwd(dO, q, k, v, ref_o, ref_lse, ref_sel)
+    dsa.dsa_sync_status()
+
+    sel = torch.empty_like(ref_sel)
+    ws = torch.empty(dbg.dsa_index_topk_workspace(S, Hi, Di, chunk, topk), dtype=torch.uint8, device=DEV)
+    ok(dbg.dsa_index_topk(q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), S, Hi, Di, chunk, topk, 0, S,
+                          sel.data_ptr(), ws.data_ptr(), ws.numel(), stream))
+    o, lse = torch.empty_like(ref_o), torch.empty_like(ref_lse)
+    otc, lsetc = torch.empty_like(ref_o), torch.empty_like(ref_lse)
+    Hq, D = q.shape[1], q.shape[2]
+    for fn, oo, ll in ((dbg.dsa_sparse_attn_fwd, o, lse), (dbg.dsa_sparse_attn_fwd_tc, otc, lsetc)):
+        ok(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), sel.data_ptr(), S, Hq, D, topk, 0.0, oo.data_ptr(),
+              ll.data_ptr(), stream))
+    g = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    wsb = torch.empty(dbg.dsa_sparse_attn_bwd_workspace(S, Hq, D), dtype=torch.uint8, device=DEV)
+    ok(dbg.dsa_sparse_attn_bwd(dO.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               sel.data_ptr(), S, Hq, D, topk, 0.0, g[0].data_ptr(), g[1].data_ptr(), g[2].data_ptr(),
+                               wsb.data_ptr(), wsb.numel(), stream))
+    assert dbg.dsa_sync_status(None) == 0, dbg.dsa_last_error()
+    assert torch.equal(sel, ref_sel)
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    assert torch.equal(otc, ref_otc) and torch.equal(lsetc, ref_lsetc)
+    assert torch.equal(g[0], ref_g[0])
+    for x, y in zip(g[1:], ref_g[1:]):
+        xf, yf = x.float(), y.float()
+        bound = 2 ** -7 * torch.maximum(xf.abs(), yf.abs()) + 1e-6 * xf.abs().max()
+        assert bool(((xf - yf).abs() <= bound).all())
+
+
 # --------------------------------------------------------------------------- deterministic backward
 
 def test_attn_bwd_deterministic_tiny_int():
