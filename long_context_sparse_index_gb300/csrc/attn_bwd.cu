@@ -15,9 +15,12 @@
 // registers), dQ accumulated in registers, and the slice's dK/dV rows (16 keys x 128 dims, already summed
 // over the 16 heads by the MMA) added into fp32 accumulators with 16-byte
 // reductions.  The reductions are L2-bound, and L2 serves them best when one
-// warp instruction covers whole 128-byte lines: so each 32-dim block of the
-// slice's rows goes through a small shared tile, and each reduction
-// instruction then adds one pool's four key rows, 128 bytes of each.  A final
+// warp instruction covers whole 128-byte lines: each reduction instruction
+// adds one pool's four key rows, 128 bytes of each.  The dK/dV products read
+// Q and dO from copies whose dims are interleaved within each 16-dim group,
+// so that every lane's accumulator fragment holds four consecutive dims of a
+// key row; one lane exchange across the warp's halves then gives each
+// instruction its pool's four rows, with no shared-memory staging.  A final
 // kernel rounds the accumulators to bf16.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
@@ -36,10 +39,9 @@ constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kQBytes = kHq * kD * 2;
 constexpr uint32_t kTBytes = kHq * 16 * 2;  // per-warp [16 heads][16 keys] bf16 tile
-constexpr int kStgLd = 40;                   // staged rows: 32 dims + 8 pad floats (conflict-free float2 stores)
-constexpr uint32_t kStgBytes = 2 * 16 * kStgLd * 4;  // per warp: dV and dK blocks of 16 keys x 32 dims
 constexpr int kMaxTopk = 2048;
-constexpr size_t kSmemFixed = 128 + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes + kWarps * kStgBytes;
+// Q, dO, then their dim-interleaved copies, the gather ring, the P/dS tiles
+constexpr size_t kSmemFixed = 128 + 4 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes;
 // row table: one int32 per key of every block (topk pools + the own pool, in blocks of 16 slots)
 constexpr size_t smem_bytes(int topk) {
   return kSmemFixed + static_cast<size_t>((topk + 1 + kBlkPools - 1) / kBlkPools) * kBlkKeys * sizeof(int32_t);
@@ -75,8 +77,6 @@ __device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* _
   }
 }
 
-__device__ __forceinline__ int warp_of_thread() { return static_cast<int>(threadIdx.x) >> 5; }
-
 __global__ void __launch_bounds__(kThreads, 2)
     attn_bwd_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ q,
                     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
@@ -90,12 +90,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sdO = base + kQBytes;
-  const uint32_t sKV = base + 2 * kQBytes;
+  const uint32_t sQi = base + 2 * kQBytes;   // Q with dims interleaved (below)
+  const uint32_t sdOi = base + 3 * kQBytes;  // dO likewise
+  const uint32_t sKV = base + 4 * kQBytes;
   const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P hi, P lo, dS hi, dS lo tiles
-  float* stg = reinterpret_cast<float*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes) +
-               warp_of_thread() * (kStgBytes / 4);  // this warp's dV block, then its dK block
-  int32_t* rows = reinterpret_cast<int32_t*>(gbase + 2 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes +
-                                             kWarps * kStgBytes);
+  int32_t* rows = reinterpret_cast<int32_t*>(gbase + 4 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes);
   __shared__ int s_nsel;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,6 +180,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
         ldsm_x4(sdO + swz(r, c), dga[kk][0], dga[kk][1], dga[kk][2], dga[kk][3]);
       }
+      // Interleaved copies: in each 16-dim group (chunks 2j, 2j+1 of a head's
+      // row), chunk 2j holds dims {0,1,4,5,8,9,12,13} and chunk 2j+1 dims
+      // {2,3,6,7,10,11,14,15}.  Read as the B operand of an n8 product, the
+      // two chunks put dims 4t..4t+1 and 4t+2..4t+3 in the columns of lane
+      // group t, so each lane's dK/dV fragment holds four consecutive dims.
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int h = tid >> 3, j = tid & 7;
+        const uint32_t src = u == 0 ? sQ : sdO, dst = u == 0 ? sQi : sdOi;
+        const uint4 a = *reinterpret_cast<const uint4*>(gbase + (src - base) + swz(h, 2 * j));
+        const uint4 c = *reinterpret_cast<const uint4*>(gbase + (src - base) + swz(h, 2 * j + 1));
+        *reinterpret_cast<uint4*>(gbase + (dst - base) + swz(h, 2 * j)) = make_uint4(a.x, a.z, c.x, c.z);
+        *reinterpret_cast<uint4*>(gbase + (dst - base) + swz(h, 2 * j + 1)) = make_uint4(a.y, a.w, c.y, c.w);
+      }
+      __syncthreads();
     }
     {
       const int nb = b + kStages - 1;
@@ -280,63 +294,73 @@ __global__ void __launch_bounds__(kThreads, 2)
       ldsm_x4_t(sTw + 2 * kTBytes + off, dth[0], dth[1], dth[2], dth[3]);
       ldsm_x4_t(sTw + 3 * kTBytes + off, dtl[0], dtl[1], dtl[2], dtl[3]);
     }
-    // staged reductions: instruction k of a block adds slot (key0/4 + k)'s pool,
-    // key (lane >> 3) of it, dims 4 * (lane & 7) .. + 3 of the block
+    // Reductions: instruction kq adds slot (key0/4 + kq)'s pool: key
+    // (lane & 15) / 4 of it, dims 32 jj + 16 (lane / 16) + 4 (lane & 3) .. + 3.
+    const int kin = (lane & 15) >> 2;
+    const bool upper = lane >= 16;
+    const int dim0 = ((lane >> 4) << 4) + 4 * t4;
     int64_t rrow[4];
     bool rok[4];
 #pragma unroll
     for (int kq = 0; kq < 4; ++kq) {
-      const int32_t r = rows[b * kBlkKeys + row_slot(key0 + 4 * kq + (lane >> 3))];
+      const int32_t r = rows[b * kBlkKeys + row_slot(key0 + 4 * kq + kin)];
       rrow[kq] = r;
       rok[kq] = r >= 0;
     }
-    float* stg_v = stg;
-    float* stg_k = stg + 16 * kStgLd;
     // dV rows += P^T dO ; dK rows += (scale dS)^T Q   (16 keys x 128 dims, in 32-dim blocks)
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int j = 2 * jj + hh;
-        const int mat = lane >> 3;
-        const int r = (lane & 7) + ((mat & 1) << 3);
-        const int c = 2 * j + (mat >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sdO + swz(r, c), b0, b1, b2, b3);
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16_16816(c0, pth, b0, b1);
-        mma_bf16_16816(c0, ptl, b0, b1);
-        mma_bf16_16816(c1, pth, b2, b3);
-        mma_bf16_16816(c1, ptl, b2, b3);
-        const int col = hh * 16 + 2 * t4;
-        *reinterpret_cast<float2*>(stg_v + g * kStgLd + col) = make_float2(c0[0], c0[1]);
-        *reinterpret_cast<float2*>(stg_v + (g + 8) * kStgLd + col) = make_float2(c0[2], c0[3]);
-        *reinterpret_cast<float2*>(stg_v + g * kStgLd + col + 8) = make_float2(c1[0], c1[1]);
-        *reinterpret_cast<float2*>(stg_v + (g + 8) * kStgLd + col + 8) = make_float2(c1[2], c1[3]);
-        ldsm_x4_t(sQ + swz(r, c), b0, b1, b2, b3);
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16_16816(d0, dth, b0, b1);
-        mma_bf16_16816(d0, dtl, b0, b1);
-        mma_bf16_16816(d1, dth, b2, b3);
-        mma_bf16_16816(d1, dtl, b2, b3);
-        *reinterpret_cast<float2*>(stg_k + g * kStgLd + col) = make_float2(d0[0], d0[1]);
-        *reinterpret_cast<float2*>(stg_k + (g + 8) * kStgLd + col) = make_float2(d0[2], d0[3]);
-        *reinterpret_cast<float2*>(stg_k + g * kStgLd + col + 8) = make_float2(d1[0], d1[1]);
-        *reinterpret_cast<float2*>(stg_k + (g + 8) * kStgLd + col + 8) = make_float2(d1[2], d1[3]);
-      }
-      __syncwarp();
+      for (int m = 0; m < 2; ++m) {  // m = 0: dV from P and dO; m = 1: dK from scale dS and Q
+        const uint32_t(&th)[4] = m == 0 ? pth : dth;
+        const uint32_t(&tl)[4] = m == 0 ? ptl : dtl;
+        const uint32_t sB = m == 0 ? sdOi : sQi;
+        float* acc = m == 0 ? dv_acc : dk_acc;
+        // x[hh][e]: dims 16 (2 jj + hh) + 4 t4 + e of key g (lo) and of key g + 8 (hi)
+        float lo[2][4], hi[2][4];
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int row = 4 * kq + (lane >> 3);
-        const int cc = 4 * (lane & 7);
-        const float4 xv = *reinterpret_cast<const float4*>(stg_v + row * kStgLd + cc);
-        const float4 xk = *reinterpret_cast<const float4*>(stg_k + row * kStgLd + cc);
-        if (rok[kq]) {
-          red_add_v4(dv_acc + rrow[kq] * kD + 32 * jj + cc, xv.x, xv.y, xv.z, xv.w);
-          red_add_v4(dk_acc + rrow[kq] * kD + 32 * jj + cc, xk.x, xk.y, xk.z, xk.w);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int j = 2 * jj + hh;
+          const int mat = lane >> 3;
+          const int r = (lane & 7) + ((mat & 1) << 3);
+          const int c = 2 * j + (mat >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sB + swz(r, c), b0, b1, b2, b3);
+          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16_16816(c0, th, b0, b1);
+          mma_bf16_16816(c0, tl, b0, b1);
+          mma_bf16_16816(c1, th, b2, b3);
+          mma_bf16_16816(c1, tl, b2, b3);
+          lo[hh][0] = c0[0];
+          lo[hh][1] = c0[1];
+          lo[hh][2] = c1[0];
+          lo[hh][3] = c1[1];
+          hi[hh][0] = c0[2];
+          hi[hh][1] = c0[3];
+          hi[hh][2] = c1[2];
+          hi[hh][3] = c1[3];
+        }
+        // Lanes 0-15 hold keys 0-3 (lo) / 8-11 (hi) of the slice, lanes 16-31
+        // keys 4-7 / 12-15.  Each lane sends the 16-dim half its partner
+        // lane (lane ^ 16) needs: then lanes 0-15 carry the first half and
+        // lanes 16-31 the second half of the same four keys.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float(*x)[4] = half == 0 ? lo : hi;
+          float first[4], second[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float y = __shfl_xor_sync(0xffffffffu, upper ? x[0][e] : x[1][e], 16);
+            first[e] = upper ? y : x[0][e];
+            second[e] = upper ? x[1][e] : y;
+          }
+          const int kq0 = 2 * half;
+          if (rok[kq0])
+            red_add_v4(acc + rrow[kq0] * kD + 32 * jj + dim0, first[0], first[1], first[2], first[3]);
+          if (rok[kq0 + 1])
+            red_add_v4(acc + rrow[kq0 + 1] * kD + 32 * jj + dim0, second[0], second[1], second[2], second[3]);
         }
       }
-      __syncwarp();  // the staged block is rewritten by the next one
     }
     __syncwarp();  // the P / dS tiles are rewritten by the next slice
   }
@@ -346,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // ---- dq = scale * sum over the four warps' partial dq (rows padded to
   // 132 floats so the fragment stores spread over the banks)
   constexpr int kRedLd = kD + 4;
-  float* red = reinterpret_cast<float*>(gbase + 2 * kQBytes);  // reuses the gather ring
+  float* red = reinterpret_cast<float*>(gbase + 4 * kQBytes);  // reuses the gather ring
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = 8 * j + 2 * t4;
