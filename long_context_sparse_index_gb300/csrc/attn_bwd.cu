@@ -38,10 +38,9 @@ constexpr int kStages = 2;
 constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kQBytes = kHq * kD * 2;
-constexpr uint32_t kTBytes = kHq * 16 * 2;  // per-warp [16 heads][16 keys] bf16 tile
 constexpr int kMaxTopk = 2048;
-// Q, dO, then their dim-interleaved copies, the gather ring, the P/dS tiles
-constexpr size_t kSmemFixed = 128 + 4 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes;
+// Q, dO, then their dim-interleaved copies, the gather ring
+constexpr size_t kSmemFixed = 128 + 4 * kQBytes + kStages * kStageBytes;
 // row table: one int32 per key of every block (topk pools + the own pool, in blocks of 16 slots)
 constexpr size_t smem_bytes(int topk) {
   return kSmemFixed + static_cast<size_t>((topk + 1 + kBlkPools - 1) / kBlkPools) * kBlkKeys * sizeof(int32_t);
@@ -56,6 +55,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 256 + ((c ^ (r & 7)) << 4));
+}
+
+// Transposes an 8x8 bf16 matrix held one 32-bit word per lane in the mma
+// fragment order (lane 4r + c holds row r, columns 2c and 2c + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // Gathers the K and V rows of block `blk` into stage buffer `st` (rows as in
@@ -93,8 +100,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sQi = base + 2 * kQBytes;   // Q with dims interleaved (below)
   const uint32_t sdOi = base + 3 * kQBytes;  // dO likewise
   const uint32_t sKV = base + 4 * kQBytes;
-  const uint32_t sT = sKV + kStages * kStageBytes;  // per warp: P hi, P lo, dS hi, dS lo tiles
-  int32_t* rows = reinterpret_cast<int32_t*>(gbase + 4 * kQBytes + kStages * kStageBytes + 4 * kWarps * kTBytes);
+  int32_t* rows = reinterpret_cast<int32_t*>(gbase + 4 * kQBytes + kStages * kStageBytes);
   __shared__ int s_nsel;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -165,8 +171,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
   for (int j = 0; j < 16; ++j) dq_acc[j][0] = dq_acc[j][1] = dq_acc[j][2] = dq_acc[j][3] = 0.f;
   uint32_t qa[8][4], dga[8][4];  // Q and dO A fragments, read once per query
-  const uint32_t sTw = sT + warp * 4 * kTBytes;
-  uint8_t* gT = gbase + (sTw - base);
 
   for (int b = 0; b < nblk; ++b) {
     cp_async_wait<kStages - 2>();
@@ -262,37 +266,31 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (dk_acc == nullptr) continue;  // dq only: the deterministic backward adds dK/dV key by key
 
-    // P and dS as [16 heads][16 keys] bf16 tiles, each split into hi + lo
-    // (x = hi + lo to ~2^-17): the dK/dV sums run over thousands of queries
-    // for popular keys, where a single bf16 rounding of P or dS accumulates
-    // beyond the gradient tolerance.  Tiles: P hi, P lo, dS hi, dS lo.
+    // P^T and (scale dS)^T as A fragments [16 keys][16 heads], each split
+    // into bf16 hi + lo (x = hi + lo to ~2^-17): the dK/dV sums run over
+    // thousands of queries for popular keys, where a single bf16 rounding of
+    // P or dS accumulates beyond the gradient tolerance.  The S fragment's
+    // 8x8 quadrant (head block a, key block b) transposes in registers into
+    // the A fragment's quadrant (key block b, head block a).
+    uint32_t pth[4], ptl[4], dth[4], dtl[4];
     {
-      uint32_t* tw = reinterpret_cast<uint32_t*>(gT);
-      const int widx[4] = {g * 8 + t4, (g + 8) * 8 + t4, g * 8 + 4 + t4, (g + 8) * 8 + 4 + t4};
+      constexpr int kSrc[4] = {0, 2, 1, 3};  // A word w <- S quadrant pair kSrc[w] (x[2q], x[2q+1])
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const float* x = m == 0 ? P : dS;
-        const float mul = m == 0 ? 1.f : scale;  // the dK tiles carry scale * dS
+        const float mul = m == 0 ? 1.f : scale;  // the dK fragments carry scale * dS
+        uint32_t* th = m == 0 ? pth : dth;
+        uint32_t* tl = m == 0 ? ptl : dtl;
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-          const float x0 = mul * x[2 * qd], x1 = mul * x[2 * qd + 1];
+        for (int w = 0; w < 4; ++w) {
+          const int q = kSrc[w];
+          const float x0 = mul * x[2 * q], x1 = mul * x[2 * q + 1];
           const uint32_t hi = pack_bf16(x0, x1);
           const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
-          tw[(2 * m) * 128 + widx[qd]] = hi;
-          tw[(2 * m + 1) * 128 + widx[qd]] = pack_bf16(x0 - h0, x1 - h1);
+          th[w] = movmatrix_t(hi);
+          tl[w] = movmatrix_t(pack_bf16(x0 - h0, x1 - h1));
         }
       }
-    }
-    __syncwarp();
-    uint32_t pth[4], ptl[4], dth[4], dtl[4];
-    {
-      const int mat = lane >> 3;
-      const int h = (lane & 7) + ((mat >> 1) << 3);
-      const uint32_t off = static_cast<uint32_t>(h * 32 + (mat & 1) * 16);
-      ldsm_x4_t(sTw + 0 * kTBytes + off, pth[0], pth[1], pth[2], pth[3]);
-      ldsm_x4_t(sTw + 1 * kTBytes + off, ptl[0], ptl[1], ptl[2], ptl[3]);
-      ldsm_x4_t(sTw + 2 * kTBytes + off, dth[0], dth[1], dth[2], dth[3]);
-      ldsm_x4_t(sTw + 3 * kTBytes + off, dtl[0], dtl[1], dtl[2], dtl[3]);
     }
     // Reductions: instruction kq adds slot (key0/4 + kq)'s pool: key
     // (lane & 15) / 4 of it, dims 32 jj + 16 (lane / 16) + 4 (lane & 3) .. + 3.
@@ -362,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    __syncwarp();  // the P / dS tiles are rewritten by the next slice
   }
   cp_async_wait<0>();
   __syncthreads();
