@@ -15,8 +15,8 @@
 // registers, so a CTA takes 74 KB and three run per SM (12 warps), which
 // hides more of the MMA and gather latency than a deeper ring at two per SM.
 // Warp w owns keys 16w..16w+15 of every block: S = Q K^T and O += P V run on
-// bf16 mma.sync (m16n8k16, M = the 16 heads), with the running max, the
-// normaliser and O in fp32 registers.  The four warps' partial softmax
+// bf16 mma.sync (m16n8k16, M = the 16 heads), with a lagging per-row softmax
+// reference, the normaliser and O in fp32 registers.  The four warps' partial softmax
 // states are merged through shared memory at the end.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
@@ -51,6 +51,10 @@ __device__ __forceinline__ int row_slot(int kr) { return (kr & 7) * 8 + (kr >> 3
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// A row's softmax reference moves up only when a score exceeds it by more
+// than this (log2 units): P stays below 2^8, and the accumulators are
+// rescaled only then, not whenever the maximum rises a little.
+constexpr float kLag = 8.f;
 
 // byte offset of 16-B chunk c (0..15) of row r in a swizzled [rows][256 B] tile
 __device__ __forceinline__ uint32_t swz(int r, int c) {
@@ -218,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 3)
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+    // lagging reference: unchanged while the block's maximum stays within kLag of it
+    const float mn0 = mx0 > m_run[0] + kLag ? mx0 : m_run[0];
+    const float mn1 = mx1 > m_run[1] + kLag ? mx1 : m_run[1];
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
     const float al0 = exp2f(m_run[0] - mu0), al1 = exp2f(m_run[1] - mu1);
     float p[8];
@@ -234,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     l_run[1] = l_run[1] * al1 + (p[2] + p[3] + p[6] + p[7]);
     m_run[0] = mn0;
     m_run[1] = mn1;
-    // the accumulators are rescaled only when some row of the warp raised
-    // its maximum (a factor of exactly 1 leaves them unchanged)
+    // the accumulators are rescaled only when some row of the warp moved its
+    // reference (a factor of exactly 1 leaves them unchanged)
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
