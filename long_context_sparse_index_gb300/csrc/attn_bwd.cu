@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const bool hi = (e & 2) != 0;  // row g+8
-        P[e] = vm[e] ? exp2f(sc[e] * scale_log2 - (hi ? lse2_1 : lse2_0)) : 0.f;
+        P[e] = vm[e] ? ex2_ftz(fmaf(sc[e], scale_log2, -(hi ? lse2_1 : lse2_0))) : 0.f;
         dS[e] = P[e] * (dp[e] - (hi ? dl1 : dl0));
       }
     }

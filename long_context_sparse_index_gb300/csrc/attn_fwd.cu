@@ -198,21 +198,22 @@ __global__ void __launch_bounds__(kThreads, 3)
       mma_bf16_16816(s1, qa[kk], b2, b3);
     }
 
-    // mask: slot of each of this thread's 4 key columns
+    // mask: slot of each of this thread's 4 key columns (raw scores; the
+    // scale is positive, so the maxima can be taken before scaling)
     float x[8];
     {
       const int kc[4] = {key0 + 2 * t4, key0 + 2 * t4 + 1, key0 + 8 + 2 * t4, key0 + 9 + 2 * t4};
       bool valid[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) valid[e] = rows[b * kBlkKeys + row_slot(kc[e])] >= 0;
-      x[0] = valid[0] ? s0[0] * scale_log2 : -INFINITY;
-      x[1] = valid[1] ? s0[1] * scale_log2 : -INFINITY;
-      x[2] = valid[0] ? s0[2] * scale_log2 : -INFINITY;
-      x[3] = valid[1] ? s0[3] * scale_log2 : -INFINITY;
-      x[4] = valid[2] ? s1[0] * scale_log2 : -INFINITY;
-      x[5] = valid[3] ? s1[1] * scale_log2 : -INFINITY;
-      x[6] = valid[2] ? s1[2] * scale_log2 : -INFINITY;
-      x[7] = valid[3] ? s1[3] * scale_log2 : -INFINITY;
+      x[0] = valid[0] ? s0[0] : -INFINITY;
+      x[1] = valid[1] ? s0[1] : -INFINITY;
+      x[2] = valid[0] ? s0[2] : -INFINITY;
+      x[3] = valid[1] ? s0[3] : -INFINITY;
+      x[4] = valid[2] ? s1[0] : -INFINITY;
+      x[5] = valid[3] ? s1[1] : -INFINITY;
+      x[6] = valid[2] ? s1[2] : -INFINITY;
+      x[7] = valid[3] ? s1[3] : -INFINITY;
     }
     // online softmax: row g holds x[0,1,4,5]; row g+8 holds x[2,3,6,7]
     float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[4], x[5]));
@@ -222,20 +223,22 @@ __global__ void __launch_bounds__(kThreads, 3)
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
+    mx0 *= scale_log2;
+    mx1 *= scale_log2;
     // lagging reference: unchanged while the block's maximum stays within kLag of it
     const float mn0 = mx0 > m_run[0] + kLag ? mx0 : m_run[0];
     const float mn1 = mx1 > m_run[1] + kLag ? mx1 : m_run[1];
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(m_run[0] - mu0), al1 = exp2f(m_run[1] - mu1);
+    const float al0 = ex2_ftz(m_run[0] - mu0), al1 = ex2_ftz(m_run[1] - mu1);
     float p[8];
-    p[0] = exp2f(x[0] - mu0);
-    p[1] = exp2f(x[1] - mu0);
-    p[4] = exp2f(x[4] - mu0);
-    p[5] = exp2f(x[5] - mu0);
-    p[2] = exp2f(x[2] - mu1);
-    p[3] = exp2f(x[3] - mu1);
-    p[6] = exp2f(x[6] - mu1);
-    p[7] = exp2f(x[7] - mu1);
+    p[0] = ex2_ftz(fmaf(x[0], scale_log2, -mu0));
+    p[1] = ex2_ftz(fmaf(x[1], scale_log2, -mu0));
+    p[4] = ex2_ftz(fmaf(x[4], scale_log2, -mu0));
+    p[5] = ex2_ftz(fmaf(x[5], scale_log2, -mu0));
+    p[2] = ex2_ftz(fmaf(x[2], scale_log2, -mu1));
+    p[3] = ex2_ftz(fmaf(x[3], scale_log2, -mu1));
+    p[6] = ex2_ftz(fmaf(x[6], scale_log2, -mu1));
+    p[7] = ex2_ftz(fmaf(x[7], scale_log2, -mu1));
     l_run[0] = l_run[0] * al0 + (p[0] + p[1] + p[4] + p[5]);
     l_run[1] = l_run[1] * al1 + (p[2] + p[3] + p[6] + p[7]);
     m_run[0] = mn0;
