@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       cp_async16(sdO + swz(c >> 4, c & 15), drow + c * 8, true);
     }
   }
-  __syncthreads();
+  // the row table is visible to the gather; with no hole anywhere, only the
+  // last block (the own pool and the empty slots after it) needs a mask
+  const bool any_hole = __syncthreads_or(bad) != 0;
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
     if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, rows, s);
@@ -226,10 +228,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_bf16_16816(p1, dga[kk], b2, b3);
     }
 
-    // key validity and global rows of this thread's columns (2t, 2t+1, 8+2t, 9+2t)
-    // and of its dK/dV rows (keys g and g+8 of the slice)
-    bool valid[4];
-    {
+    // key validity of this thread's columns (2t, 2t+1, 8+2t, 9+2t)
+    bool valid[4] = {true, true, true, true};
+    if (b + 1 == nblk || any_hole) {
       const int kc[4] = {key0 + 2 * t4, key0 + 2 * t4 + 1, key0 + 8 + 2 * t4, key0 + 9 + 2 * t4};
 #pragma unroll
       for (int e = 0; e < 4; ++e) valid[e] = rows[b * kBlkKeys + row_slot(kc[e])] >= 0;

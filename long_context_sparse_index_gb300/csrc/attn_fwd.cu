@@ -150,7 +150,9 @@ __global__ void __launch_bounds__(kThreads, 3)
       cp_async16(sQ + swz(c >> 4, c & 15), qrow + c * 8, true);
     }
   }
-  __syncthreads();  // the row table is visible to the gather
+  // the row table is visible to the gather; with no hole anywhere, only the
+  // last block (the own pool and the empty slots after it) needs a mask
+  const bool any_hole = __syncthreads_or(bad) != 0;
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
     if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, rows, s);
@@ -200,20 +202,15 @@ __global__ void __launch_bounds__(kThreads, 3)
 
     // mask: slot of each of this thread's 4 key columns (raw scores; the
     // scale is positive, so the maxima can be taken before scaling)
-    float x[8];
-    {
+    float x[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
+    if (b + 1 == nblk || any_hole) {
       const int kc[4] = {key0 + 2 * t4, key0 + 2 * t4 + 1, key0 + 8 + 2 * t4, key0 + 9 + 2 * t4};
       bool valid[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) valid[e] = rows[b * kBlkKeys + row_slot(kc[e])] >= 0;
-      x[0] = valid[0] ? s0[0] : -INFINITY;
-      x[1] = valid[1] ? s0[1] : -INFINITY;
-      x[2] = valid[0] ? s0[2] : -INFINITY;
-      x[3] = valid[1] ? s0[3] : -INFINITY;
-      x[4] = valid[2] ? s1[0] : -INFINITY;
-      x[5] = valid[3] ? s1[1] : -INFINITY;
-      x[6] = valid[2] ? s1[2] : -INFINITY;
-      x[7] = valid[3] ? s1[3] : -INFINITY;
+      const bool vm[8] = {valid[0], valid[1], valid[0], valid[1], valid[2], valid[3], valid[2], valid[3]};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = vm[e] ? x[e] : -INFINITY;
     }
     // online softmax: row g holds x[0,1,4,5]; row g+8 holds x[2,3,6,7]
     float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[4], x[5]));
