@@ -515,35 +515,39 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host -> device, the calls, device -> host
     e2e = None
     if not args.no_e2e:
-        out_names = [("pool_idx", pool_idx), ("o", o), ("lse", lse)]
-        grad_names = [("dq", dq), ("dk", dk), ("dv", dv)] if backward else []
-        out_host = {name: torch.empty(t.shape, dtype=t.dtype).pin_memory() for name, t in out_names + grad_names}
+        # Two device sets of inputs and outputs, used by alternate steps, the
+        # way a training loop with prefetch runs: step s+1's inputs upload into
+        # the other set while step s computes (once step s-1 is done with that
+        # set), pool_idx, o and lse download during the backward, and dq, dk
+        # and dv during the next step (the last step's before the end event).
+        # Every copy is inside the timed region, on its own stream per
+        # direction; step 0's indexer inputs upload first, so its indexer
+        # starts while the rest of its inputs upload.
+        small_names = ("pool_idx", "o", "lse")
+        grad_names = ("dq", "dk", "dv") if backward else ()
+        outs0 = {"pool_idx": pool_idx, "o": o, "lse": lse}
+        if backward:
+            outs0.update({"dq": dq, "dk": dk, "dv": dv})
+        sets = [(d, outs0), ({n: torch.empty_like(t) for n, t in d.items()},
+                             {n: torch.empty_like(t) for n, t in outs0.items()})]
+        out_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs0.items()}
         bi = sum(t.numel() * t.element_size() for t in pin.values())
         bo = sum(t.numel() * t.element_size() for t in out_host.values())
-        # Pipelined the way a training loop with prefetch runs it, every copy
-        # inside the timed region: step s+1's indexer inputs upload while step s
-        # runs its attention (the indexer is done with their buffers); q, k, v
-        # (and dO) upload while the indexer runs, once the previous step's
-        # attention is done with them; pool_idx, o and lse come back while the
-        # backward (or the next step's indexer) runs; dq, dk and dv come back
-        # while the next step's indexer runs (the last step's before the end
-        # event).  Host-to-device and device-to-host copies run on their own
-        # streams.
         h2d = torch.cuda.Stream(device=dev)
         d2h = torch.cuda.Stream(device=dev)
         idx_in = ("q_idx", "k_idx", "w")
         attn_in = ("q", "k", "v", "dO") if backward else ("q", "k", "v")
 
-        def upload(names):
+        def upload(dst, names):
             with torch.cuda.stream(h2d):
                 for name in names:
-                    d[name].copy_(pin[name], non_blocking=True)
+                    dst[name].copy_(pin[name], non_blocking=True)
             return h2d.record_event()
 
-        def download(pairs):
+        def download(src, names):
             with torch.cuda.stream(d2h):
-                for name, src in pairs:
-                    out_host[name].copy_(src, non_blocking=True)
+                for name in names:
+                    out_host[name].copy_(src[name], non_blocking=True)
             return d2h.record_event()
 
         def e2e_run(nsteps, start=None, marks=None):
@@ -553,40 +557,37 @@ def run_ours(args):
                 start.record(stream)
             h2d.wait_stream(stream)
             d2h.wait_stream(stream)
-            ev_idx_in = upload(idx_in)
-            ev_attn_done = ev_small_out = ev_grads_out = None
+            ev_idx_in = upload(sets[0][0], idx_in)
+            ev_attn_in = upload(sets[0][0], attn_in)
+            ev_done, ev_out = [None] * nsteps, [None] * nsteps
             for s in range(nsteps):
+                t, out = sets[s % 2]
+                if s + 1 < nsteps:
+                    if s >= 1:
+                        h2d.wait_event(ev_done[s - 1])  # step s-1 is done with the other set
+                    ev_next_in = upload(sets[(s + 1) % 2][0], idx_in + attn_in)
                 flush.zero_()
                 stream.wait_event(ev_idx_in)
-                if ev_small_out is not None:
-                    stream.wait_event(ev_small_out)  # pool_idx, o, lse of the previous step are on the host
-                dsa.dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], chunk=wl.chunk, topk=topk, pool_idx=pool_idx,
-                                   workspace=ws_idx)
-                ev_idx_done = stream.record_event()
-                if ev_attn_done is not None:
-                    h2d.wait_event(ev_attn_done)  # the previous step's attention is done with q, k, v (, dO)
-                    if backward:
-                        d2h.wait_event(ev_attn_done)
-                        ev_grads_out = download(grad_names)
-                ev_attn_in = upload(attn_in)
+                if s >= 2:
+                    stream.wait_event(ev_out[s - 2])  # this set's outputs of step s-2 are on the host
+                dsa.dsa_index_topk(t["q_idx"], t["k_idx"], t["w"], chunk=wl.chunk, topk=topk,
+                                   pool_idx=out["pool_idx"], workspace=ws_idx)
                 stream.wait_event(ev_attn_in)
-                dsa.dsa_sparse_attn_fwd(d["q"], d["k"], d["v"], pool_idx, scale=wl.scale, o=o, lse=lse)
+                dsa.dsa_sparse_attn_fwd(t["q"], t["k"], t["v"], out["pool_idx"], scale=wl.scale, o=out["o"],
+                                        lse=out["lse"])
                 d2h.wait_stream(stream)
-                ev_small_out = download(out_names)
-                if s + 1 < nsteps:
-                    h2d.wait_event(ev_idx_done)
-                    ev_idx_in = upload(idx_in)
+                ev_out[s] = download(out, small_names)
                 if backward:
-                    if ev_grads_out is not None:
-                        stream.wait_event(ev_grads_out)  # dq, dk, dv of the previous step are on the host
-                    bwd(d["dO"], d["q"], d["k"], d["v"], o, lse, pool_idx, scale=wl.scale, dq=dq, dk=dk, dv=dv,
-                        workspace=ws_bwd)
-                ev_attn_done = stream.record_event()
+                    bwd(t["dO"], t["q"], t["k"], t["v"], out["o"], out["lse"], out["pool_idx"], scale=wl.scale,
+                        dq=out["dq"], dk=out["dk"], dv=out["dv"], workspace=ws_bwd)
+                ev_done[s] = stream.record_event()
+                if backward:
+                    d2h.wait_event(ev_done[s])
+                    ev_out[s] = download(out, grad_names)
                 if marks is not None:
                     marks[s].record(stream)
-            if backward:
-                d2h.wait_event(ev_attn_done)
-                download(grad_names)
+                if s + 1 < nsteps:
+                    ev_idx_in = ev_attn_in = ev_next_in
             stream.wait_stream(d2h)
             stream.wait_stream(h2d)
 
@@ -609,8 +610,9 @@ def run_ours(args):
                "d2h_bytes_per_step": bo, "ms_per_step": 1e3 * e2e_s / args.steps,
                "step_ms": [a.elapsed_time(b) for a, b in zip(bounds[:-1], bounds[1:])],
                "last_step_tail_ms": marks[-1].elapsed_time(e2e_end),
-               "pipelining": "next step's indexer inputs upload during this step's attention; this step's outputs "
-                             "download during the next step's work; all copies inside the timed region"}
+               "pipelining": "two device sets of inputs and outputs used by alternate steps: the next step's inputs "
+                             "upload while this step computes, pool_idx/o/lse download during the backward and "
+                             "dq/dk/dv during the next step; all copies inside the timed region"}
 
     if rank == 0:
         cpu = None
