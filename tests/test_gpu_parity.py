@@ -433,6 +433,26 @@ def test_attn_bwd_repeatable_within_rounding():
         assert bool(((xf - yf).abs() <= bound).all())
 
 
+def test_attention_late_large_scores_move_the_softmax_reference():
+    """Keys of the upper half of the sequence scaled by 8 (exact in bf16): a
+    query's later key blocks (pools ascend) score far above its earlier ones,
+    more than 2^8 in probability, so the forwards move their lagging softmax
+    reference and rescale the accumulators mid-row.  Both forwards still
+    match the oracle.  (The backward is left out: with one key holding ~99 %
+    of a row's softmax, Delta = dO . o cancels against dO . v, and the bf16
+    rounding of the forward's o, which the backward takes as its input, moves
+    dq by as much as dq itself, exactly as the fp64 computation from the
+    rounded o shows; the backward's own arithmetic is not involved.)"""
+    wl = synth.Workload("t", 2048, topk=128, seed=21)
+    q, k, v = synth.attention_inputs(wl)
+    f = (k.astype(np.uint32) << 16).view(np.float32).copy()
+    f[wl.S // 2:] *= 8.0
+    k = (f.view(np.uint32) >> 16).astype(np.uint16)
+    sel = synth.stand_in_selection(wl)
+    _fwd_check(q, k, v, sel)
+    _fwd_check(q, k, v, sel, fwd=dsa.dsa_sparse_attn_fwd_tc)
+
+
 def test_debug_build_checks_pass_and_results_match():
     """The DSA_DEBUG build (range checks on gathered rows and shared-memory
     offsets that record DSA_ERR_INTERNAL) finds nothing on valid inputs, and
