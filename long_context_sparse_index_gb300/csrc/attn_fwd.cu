@@ -8,9 +8,10 @@
 // of keys, which reproduces the one-shot softmax exactly in real arithmetic.
 //
 // Layout of the work: one CTA (4 warps) per query.  The key list is walked in
-// blocks of 16 pool slots (64 keys); 128 threads gather the K and V rows of a
-// block with 16-byte cp.async copies into a 2-stage ring in shared memory
-// (rows XOR-swizzled in 16-B chunks so ldmatrix reads are conflict-free).
+// blocks of 16 pool slots (64 keys); each warp gathers the K and V rows of its
+// own 16 keys of a block with 16-byte cp.async copies into its quarter of a
+// 2-stage ring in shared memory (rows XOR-swizzled in 16-B chunks so ldmatrix
+// reads are conflict-free), and waits only for its own copies.
 // The Q tile sits in the ring's second stage until it is read into
 // registers, so a CTA takes 74 KB and three run per SM (12 warps), which
 // hides more of the MMA and gather latency than a deeper ring at two per SM.
@@ -31,8 +32,10 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kBlkPools = 16;
 constexpr int kBlkKeys = 4 * kBlkPools;       // 64
 constexpr int kStages = 2;
-constexpr uint32_t kTileBytes = kBlkKeys * kD * 2;   // 16 KB (K or V of one block)
-constexpr uint32_t kStageBytes = 2 * kTileBytes;     // 32 KB
+constexpr int kWarpKeys = kBlkKeys / kWarps;           // 16 keys of each block per warp
+constexpr uint32_t kWarpTile = kWarpKeys * kD * 2;     // 4 KB: K (or V) rows of a warp's keys
+constexpr uint32_t kWarpStage = 2 * kWarpTile;         // K then V
+constexpr uint32_t kStageBytes = kWarps * kWarpStage;  // 32 KB: one block
 constexpr uint32_t kQBytes = kHq * kD * 2;           // 4 KB
 constexpr int kMaxTopk = 2048;
 // Q lives inside stage 1 of the ring until it is read into registers (before
@@ -44,10 +47,11 @@ constexpr size_t smem_bytes(int topk) {
   return kSmemFixed + static_cast<size_t>((topk + 1 + kBlkPools - 1) / kBlkPools) * kBlkKeys * sizeof(int32_t);
 }
 
-// Position in a block's row table of key kr (0..63): keys kr0, kr0 + 8, ...,
-// kr0 + 56 (kr0 = kr % 8) are adjacent, so the thread that gathers them
-// reads their rows with two 16-byte loads.
-__device__ __forceinline__ int row_slot(int kr) { return (kr & 7) * 8 + (kr >> 3); }
+// Position in a block's row table of key kr (0..63): warp w's keys 16w..16w+15
+// fill slots 16w..16w+15, its even keys first, so the lane that gathers keys
+// p, p + 2, ..., p + 14 of the warp (p = 0 or 1) reads their rows with two
+// 16-byte loads.
+__device__ __forceinline__ int row_slot(int kr) { return (kr & ~15) + (kr & 1) * 8 + ((kr & 15) >> 1); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -61,23 +65,26 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 256 + ((c ^ (r & 7)) << 4));
 }
 
-// Gathers the K and V rows of block `blk` into stage buffer `st`.  `rows`
-// holds the block's 64 key rows (-1: empty slot, hole or a row past the
-// query, zero-filled and masked by the caller).  Thread t copies 16-byte
-// chunk t % 16 of keys t / 16 + 8u, u = 0..7.
-__device__ __forceinline__ void gather_block(uint32_t st, const __nv_bfloat16* __restrict__ k,
-                                             const __nv_bfloat16* __restrict__ v, const int32_t* rows, int blk) {
-  const int kr0 = threadIdx.x >> 4, cc = threadIdx.x & 15;
-  const int4 ra = *reinterpret_cast<const int4*>(rows + blk * kBlkKeys + kr0 * 8);
-  const int4 rb = *reinterpret_cast<const int4*>(rows + blk * kBlkKeys + kr0 * 8 + 4);
+// Gathers the K and V rows of warp `w`'s 16 keys of block `blk` into the
+// warp's part `st` of a stage.  `rows` holds the block's 64 key rows (-1:
+// empty slot, hole or a row past the query, zero-filled and masked by the
+// caller).  Lane l copies 16-byte chunk l % 16 of the warp's keys l / 16 + 2u,
+// u = 0..7.  Only the warp reads them, so a warp-level wait and __syncwarp()
+// order them: the warps of a CTA do not wait for each other.
+__device__ __forceinline__ void gather_warp(uint32_t st, const __nv_bfloat16* __restrict__ k,
+                                            const __nv_bfloat16* __restrict__ v, const int32_t* rows, int blk,
+                                            int w, int lane) {
+  const int p = lane >> 4, cc = lane & 15;
+  const int4 ra = *reinterpret_cast<const int4*>(rows + blk * kBlkKeys + w * kWarpKeys + p * 8);
+  const int4 rb = *reinterpret_cast<const int4*>(rows + blk * kBlkKeys + w * kWarpKeys + p * 8 + 4);
   const int32_t r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int kr = kr0 + 8 * u;
+    const int kl = p + 2 * u;
     const bool ok = r8[u] >= 0;
     const int64_t src = static_cast<int64_t>(ok ? r8[u] : 0) * kD + cc * 8;
-    cp_async16(st + swz(kr, cc), k + src, ok);
-    cp_async16(st + kTileBytes + swz(kr, cc), v + src, ok);
+    cp_async16(st + swz(kl, cc), k + src, ok);
+    cp_async16(st + kWarpTile + swz(kl, cc), v + src, ok);
   }
 }
 
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   bool bad = false;
   for (int e = tid; e < nblk * kBlkKeys; e += kThreads) {
     const int blk = e / kBlkKeys, pos = e % kBlkKeys;
-    const int kr = (pos & 7) * 8 + (pos >> 3);  // inverse of row_slot
+    const int kr = (pos & ~15) + 2 * (pos & 7) + ((pos >> 3) & 1);  // inverse of row_slot
     const int slot = blk * kBlkPools + (kr >> 2);
     int32_t row = -1;
     if (slot < nsel) {
@@ -153,11 +160,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   // the row table is visible to the gather; with no hole anywhere, only the
   // last block (the own pool and the empty slots after it) needs a mask
   const bool any_hole = __syncthreads_or(bad) != 0;
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < nblk) gather_block(sKV + s * kStageBytes, k, v, rows, s);
-    cp_async_commit();
-  }
+  gather_warp(sKV + warp * kWarpStage, k, v, rows, 0, warp, lane);  // nblk >= 1
+  cp_async_commit();
 
   float o_acc[16][4];
 #pragma unroll
@@ -166,9 +170,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint32_t qa[8][4];
 
   for (int b = 0; b < nblk; ++b) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
+    cp_async_wait<0>();  // this lane's copies of block b (and, at b = 0, its part of Q)
     if (b == 0) {
+      __syncthreads();  // every thread's part of Q
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int mat = lane >> 3;
@@ -177,14 +181,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         ldsm_x4(sQ + swz(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
       __syncthreads();  // every warp has Q: block 1 may overwrite it
+    } else {
+      __syncwarp();  // the warp's copies of block b are visible to its lanes, and block b - 1 is read
     }
-    {
-      const int nb = b + kStages - 1;
-      if (nb < nblk) gather_block(sKV + (nb % kStages) * kStageBytes, k, v, rows, nb);
-      cp_async_commit();
-    }
-    const uint32_t sK = sKV + (b % kStages) * kStageBytes;
-    const uint32_t sV = sK + kTileBytes;
+    if (b + 1 < nblk) gather_warp(sKV + ((b + 1) & 1) * kStageBytes + warp * kWarpStage, k, v, rows, b + 1, warp, lane);
+    cp_async_commit();
+    const uint32_t sK = sKV + (b & 1) * kStageBytes + warp * kWarpStage;
+    const uint32_t sV = sK + kWarpTile;
     const int key0 = warp * 16;
 
     // S = Q K^T for this warp's 16 keys (two n-tiles of 8)
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int mat = lane >> 3;
-      const int r = key0 + ((mat >> 1) << 3) + (lane & 7);
+      const int r = ((mat >> 1) << 3) + (lane & 7);
       const int c = 2 * kk + (mat & 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(sK + swz(r, c), b0, b1, b2, b3);
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int mat = lane >> 3;
-      const int r = key0 + ((mat & 1) << 3) + (lane & 7);
+      const int r = ((mat & 1) << 3) + (lane & 7);
       const int c = 2 * j + (mat >> 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(sV + swz(r, c), b0, b1, b2, b3);
