@@ -833,10 +833,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             cyc_app.add(1);
             cyc_cmp.start();
             unsigned long long hit = 0ull;
+            if (jn == kEpiCols && (jt < 0 || jt >= kEpiCols - 1)) {
+              // every pool eligible, and the threshold's pool before (jt < 0)
+              // or at or after (jt >= 63) all of them: one compare per pool,
+              // v >= tf (ties count) or v > tf, the latter as v >= the next
+              // float above tf (+0 and -0 compare equal, so above both zeros
+              // comes the smallest positive subnormal)
+              float tq = tf;
+              if (jt < 0) {
+                const uint32_t b = __float_as_uint(tf);
+                tq = (b & 0x7FFFFFFFu) == 0u ? __uint_as_float(1u)
+                                             : __uint_as_float((b & 0x80000000u) ? b - 1u : b + 1u);
+              }
+              uint32_t lo = 0u, hi = 0u;
 #pragma unroll
-            for (int j = 0; j < kEpiCols; ++j) {
-              const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
-              if (j < jn && (v > tf || (v == tf && j <= jt))) hit |= 1ull << j;
+              for (int j = 0; j < kEpiCols; ++j) {
+                const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
+                if (v >= tq) {
+                  if (j < 32) lo |= 1u << j;
+                  else hi |= 1u << (j - 32);
+                }
+              }
+              hit = (static_cast<unsigned long long>(hi) << 32) | lo;
+            } else {
+#pragma unroll
+              for (int j = 0; j < kEpiCols; ++j) {
+                const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
+                if (j < jn && (v > tf || (v == tf && j <= jt))) hit |= 1ull << j;
+              }
             }
             cyc_cmp.stop();
             if (hit != 0ull) {
