@@ -156,6 +156,8 @@ WORKLOADS = {
     "s128k": Workload("s128k", 131072, values="normal", q_idx_scale=0.125, seed=2, backward=True),
     "s256k_cluster": Workload("s256k_cluster", 262144, chunk=512, values="cluster", seed=3),
     "s1m_cluster": Workload("s1m_cluster", 1048576, chunk=512, values="cluster", seed=3),
+    # the same inputs with the attention backward (the layer's whole step at 1M)
+    "s1m_cluster_bwd": Workload("s1m_cluster_bwd", 1048576, chunk=512, values="cluster", seed=3, backward=True),
     "s64k_zipf": Workload("s64k_zipf", 65536, values="zipf", seed=4, backward=True),
 }
 

@@ -5,7 +5,7 @@ benchmark times, on sampled outputs the oracle computes one by one.
                  forward and backward (the benchmark's step)
   s256k_cluster  S=262144, planted key clusters, chunk 512 (indexer + top-k)
   s1m_cluster    S=1048576, planted key clusters, chunk 512 (indexer + top-k,
-                 attention forward)
+                 attention forward; attention forward and backward)
   s16k, s256k_cluster   the forward configurations at S=16384 and S=262144:
                  the attention forward on the oracle's own selection of the
                  sampled rows
@@ -151,6 +151,18 @@ def test_s128k_attention_forward_backward_sampled():
     wl = synth.WORKLOADS["s128k"]
     sel = synth.stand_in_selection(wl)
     q_rows = _sample_rows(wl.S, 32, 5)
+    # keys of one late pool (few queries can see it, so the oracle stays quick) and the last rows
+    p = wl.S // 4 - 600
+    key_rows = np.array([4 * p, 4 * p + 3, wl.S - 3, wl.S - 1], np.int64)
+    _check_fwd_bwd(wl, sel, q_rows, key_rows)
+
+
+def test_s1m_cluster_attention_forward_backward_sampled():
+    """The layer's attention forward and backward at S=1048576 (planted key
+    clusters; selection: seeded stand-in), in one launch each."""
+    wl = synth.WORKLOADS["s1m_cluster_bwd"]
+    sel = synth.stand_in_selection(wl)
+    q_rows = _sample_rows(wl.S, 16, 9)
     # keys of one late pool (few queries can see it, so the oracle stays quick) and the last rows
     p = wl.S // 4 - 600
     key_rows = np.array([4 * p, 4 * p + 3, wl.S - 3, wl.S - 1], np.int64)
