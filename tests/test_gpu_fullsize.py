@@ -157,16 +157,19 @@ def test_s128k_attention_forward_backward_sampled():
     _check_fwd_bwd(wl, sel, q_rows, key_rows)
 
 
-def test_s1m_cluster_attention_forward_backward_sampled():
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_s1m_cluster_attention_forward_backward_sampled(deterministic):
     """The layer's attention forward and backward at S=1048576 (planted key
-    clusters; selection: seeded stand-in), in one launch each."""
+    clusters; selection: seeded stand-in), in one launch each; S = 2^20 is
+    also where the deterministic backward's counting moves to one block per
+    span."""
     wl = synth.WORKLOADS["s1m_cluster_bwd"]
     sel = synth.stand_in_selection(wl)
     q_rows = _sample_rows(wl.S, 16, 9)
     # keys of one late pool (few queries can see it, so the oracle stays quick) and the last rows
     p = wl.S // 4 - 600
     key_rows = np.array([4 * p, 4 * p + 3, wl.S - 3, wl.S - 1], np.int64)
-    _check_fwd_bwd(wl, sel, q_rows, key_rows)
+    _check_fwd_bwd(wl, sel, q_rows, key_rows, deterministic)
 
 
 @pytest.mark.parametrize("deterministic", [False, True])
