@@ -257,16 +257,23 @@ dsa_status_t dsa_zigzag_ranges(int64_t S, int world, int rank, int64_t* ranges);
  * entries count from its first token, and no query sees another sequence's
  * keys.  Tensors, scale and topk are as in the single-sequence calls, with
  * the packed length in place of S; dk/dv rows of a sequence hold that
- * sequence's gradient.  The workspace must hold the *_varlen_workspace()
- * bytes: for the indexer, the single-sequence workspace of the longest
- * sequence; for the backward, the single-sequence workspace of the packed
- * length (its fp32 dK/dV accumulators span the batch).  The attention calls
- * cover the batch with one launch per kernel and per 256 sequences (a table
- * of their starts rides in the launch parameters; each query finds its
- * sequence by binary search).  The indexer fills the rows of every sequence
- * of at most 4 * topk + 4 tokens (each row keeps all its pools) with one
- * launch per 256 such sequences, and runs once per longer sequence, one after
- * another on `stream`.  An invalid cu_seqlens or a short workspace returns
+ * sequence's gradient.  Workspaces: for the backward, the *_varlen_workspace()
+ * bytes, the single-sequence workspace of the packed length (its fp32 dK/dV
+ * accumulators span the batch).  For the indexer, at least one slice, the
+ * single-sequence recommended workspace of the longest sequence;
+ * dsa_index_topk_varlen_workspace() recommends one slice per long sequence
+ * indexed at once (up to 4).  The attention calls cover the batch with one
+ * launch per kernel and per 256 sequences (a table of their starts rides in
+ * the launch parameters; each query finds its sequence by binary search).
+ * The indexer fills the rows of every sequence of at most 4 * topk + 4
+ * tokens (each row keeps all its pools) with one launch per 256 such
+ * sequences, and runs once per longer sequence.  Sequences with fewer than
+ * 304 indexer tiles (128 queries x 256 pools; up to ~9000 tokens) leave most
+ * SMs idle in a launch of their own: when the workspace holds two or more
+ * slices they run that many at once, each on a helper stream of the library
+ * (forked from and joined back into `stream` by events) with a share of the
+ * SMs; the others run one after another on `stream` on every SM.  Results do
+ * not depend on the workspace size.  An invalid cu_seqlens or a short workspace returns
  * DSA_ERR_INVALID_ARG / DSA_ERR_WORKSPACE (and, for the query functions, 0)
  * before anything runs.  (The pages train single sequences; packing is what a
  * training data loader hands the layer.)

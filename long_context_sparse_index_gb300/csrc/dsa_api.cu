@@ -82,10 +82,16 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// packed batches: up to this many of the shorter long sequences are indexed
+// at once, each on a helper stream of its own
+constexpr int kVarlenStreams = 4;
+
 struct DeviceInfo {
   int num_sms = 0;
   unsigned* status = nullptr;
   unsigned long long ctx = 0;  // context the status address was looked up in
+  cudaStream_t helpers[kVarlenStreams] = {};
+  unsigned long long helpers_ctx = 0;  // context the helper streams were created in (0: none yet)
 };
 
 std::mutex g_dev_mu;
@@ -121,6 +127,28 @@ dsa_status_t device_info(DeviceInfo* out) {
   return DSA_OK;
 }
 
+// The current device's helper streams for packed batches, created on first
+// use in the current context (non-blocking: ordered only by the events the
+// caller records).
+static dsa_status_t varlen_streams(cudaStream_t (&out)[kVarlenStreams]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  const unsigned long long ctx = dsa::current_context_id();
+  if (d.helpers_ctx == 0 || ctx != d.helpers_ctx) {
+    for (int k = 0; k < kVarlenStreams; ++k) {
+      e = cudaStreamCreateWithFlags(&d.helpers[k], cudaStreamNonBlocking);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+    }
+    d.helpers_ctx = ctx;
+  }
+  for (int k = 0; k < kVarlenStreams; ++k) out[k] = d.helpers[k];
+  return DSA_OK;
+}
+
 dsa_status_t make_ctx(void* stream, dsa::LaunchCtx* ctx) {
   DeviceInfo d;
   dsa_status_t st = device_info(&d);
@@ -140,6 +168,7 @@ dsa_status_t make_ctx(void* stream, dsa::LaunchCtx* ctx) {
   }
   ctx->wait_limit_ns = static_cast<uint64_t>(ms * 1e6);
   ctx->pdl = 0;
+  ctx->persistent_ctas = 0;
   return DSA_OK;
 }
 
@@ -375,35 +404,12 @@ size_t dsa_index_topk_workspace_slots(int64_t S, int Hi, int Di, int chunk, int 
   return index_ws_bytes(S, chunk, topk, slots);
 }
 
-dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
-                            int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
-                            void* workspace, size_t ws_bytes, void* stream) {
-  const dsa::CallScope scope("dsa_index_topk");
-  if (!q_idx || !k_idx || !w || !pool_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: null tensor pointer");
-  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(pool_idx))
-    return fail(DSA_ERR_INVALID_ARG,
-                "dsa_index_topk: q_idx and k_idx must be 16-byte aligned, w and pool_idx 4-byte aligned");
-  if (S < 1 || S > 0x7FFFFFFFLL) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: S=%lld out of range", (long long)S);
-  if (chunk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: chunk=%d must be >= 1", chunk);
-  if (topk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: topk=%d must be >= 1", topk);
-  if (Hi < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: Hi=%d must be >= 1", Hi);
-  if (q_begin < 0 || q_end > S || q_begin >= q_end)
-    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: query range [%lld, %lld) not inside [0, %lld)",
-                (long long)q_begin, (long long)q_end, (long long)S);
-  if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Di=%d unsupported (kernels implement Di=64)", Di);
-  if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Hi=%d unsupported (max %d)", Hi, kMaxHi);
-  if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: topk=%d unsupported (max %d)", topk, kMaxTopk);
-  const size_t need = index_ws_bytes(S, chunk, topk, index_min_bufs(S, chunk));
-  if (!workspace || ws_bytes < need)
-    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk: workspace of at least %zu bytes needed (%zu recommended), %zu given",
-                need, dsa_index_topk_workspace(S, Hi, Di, chunk, topk), workspace ? ws_bytes : (size_t)0);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: workspace must be 256-byte aligned");
-
-  dsa::LaunchCtx ctx;
-  dsa_status_t st = make_ctx(stream, &ctx);
-  if (st != DSA_OK) return st;
-
+// The indexer call once its arguments are checked: plan, workspace carving,
+// tensor maps and the launches, on ctx.stream (the packed-batch path calls it
+// for each long sequence, on its own streams and grids).
+static dsa_status_t index_topk_run(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi,
+                                   int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
+                                   void* workspace, size_t ws_bytes, const dsa::LaunchCtx& ctx) {
   const dsa::IndexPlan pl = index_plan(S, chunk, topk);
   const int64_t P = pl.P;
   int nbuf = index_min_bufs(S, chunk);  // as many chunk slots as the workspace holds
@@ -506,6 +512,38 @@ dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w
     if (e != cudaSuccess) return cuda_fail(e, "dsa_index_topk: index_fallback launch");
   }
   return DSA_OK;
+}
+
+dsa_status_t dsa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t S, int Hi, int Di,
+                            int chunk, int topk, int64_t q_begin, int64_t q_end, int32_t* pool_idx,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  const dsa::CallScope scope("dsa_index_topk");
+  if (!q_idx || !k_idx || !w || !pool_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: null tensor pointer");
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(w) || !aligned4(pool_idx))
+    return fail(DSA_ERR_INVALID_ARG,
+                "dsa_index_topk: q_idx and k_idx must be 16-byte aligned, w and pool_idx 4-byte aligned");
+  if (S < 1 || S > 0x7FFFFFFFLL) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: S=%lld out of range", (long long)S);
+  if (chunk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: chunk=%d must be >= 1", chunk);
+  if (topk < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: topk=%d must be >= 1", topk);
+  if (Hi < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: Hi=%d must be >= 1", Hi);
+  if (q_begin < 0 || q_end > S || q_begin >= q_end)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: query range [%lld, %lld) not inside [0, %lld)",
+                (long long)q_begin, (long long)q_end, (long long)S);
+  if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Di=%d unsupported (kernels implement Di=64)", Di);
+  if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: Hi=%d unsupported (max %d)", Hi, kMaxHi);
+  if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "dsa_index_topk: topk=%d unsupported (max %d)", topk, kMaxTopk);
+  const size_t need = index_ws_bytes(S, chunk, topk, index_min_bufs(S, chunk));
+  if (!workspace || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "dsa_index_topk: workspace of at least %zu bytes needed (%zu recommended), %zu given",
+                need, dsa_index_topk_workspace(S, Hi, Di, chunk, topk), workspace ? ws_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_index_topk: workspace must be 256-byte aligned");
+
+  dsa::LaunchCtx ctx;
+  dsa_status_t st = make_ctx(stream, &ctx);
+  if (st != DSA_OK) return st;
+
+  return index_topk_run(q_idx, k_idx, w, S, Hi, chunk, topk, q_begin, q_end, pool_idx, workspace, ws_bytes, ctx);
 }
 
 static dsa_status_t check_attn_args(const char* fn, int64_t S, int Hq, int D, int topk) {
@@ -800,9 +838,38 @@ static dsa::SeqTable seq_table(const int64_t* cu, int s0, int n) {
   return t;
 }
 
+// The indexer tiles (128 queries x 256 pools) of one sequence of L tokens.
+static int64_t index_tiles(int64_t L) {
+  int64_t t = 0;
+  for (int64_t r0 = 0; r0 < L; r0 += 128) {
+    const int64_t last = r0 + 127 < L - 1 ? r0 + 127 : L - 1;
+    t += (last / 4 + 255) / 256;
+  }
+  return t;
+}
+// A long sequence with fewer tiles than this (two per SM of a GB300) leaves
+// most SMs idle in its own launch: such sequences are indexed several at once.
+constexpr int64_t kSmallSeqTiles = 304;
+
+// The long sequences (more than 4 * topk + 4 tokens, so the indexer runs)
+// with fewer than kSmallSeqTiles tiles.
+static int small_long_seqs(const int64_t* cu, int nseq, int topk) {
+  int n = 0;
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t L = cu[s + 1] - cu[s];
+    if (L > 4 * static_cast<int64_t>(topk) + 4 && index_tiles(L) < kSmallSeqTiles) ++n;
+  }
+  return n;
+}
+
 size_t dsa_index_topk_varlen_workspace(const int64_t* cu_seqlens, int nseq, int Hi, int Di, int chunk, int topk) {
   if (check_cu_seqlens("dsa_index_topk_varlen_workspace", cu_seqlens, nseq) != DSA_OK) return 0;
-  return dsa_index_topk_workspace(max_len(cu_seqlens, nseq), Hi, Di, chunk, topk);
+  const size_t one = dsa_index_topk_workspace(max_len(cu_seqlens, nseq), Hi, Di, chunk, topk);
+  if (one == 0) return 0;
+  // one slice per sequence indexed at once (the minimum accepted is one)
+  const int n = small_long_seqs(cu_seqlens, nseq, topk);
+  const int k = n < 2 ? 1 : (n < kVarlenStreams ? n : kVarlenStreams);
+  return one * static_cast<size_t>(k);
 }
 
 dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const float* w, const int64_t* cu_seqlens,
@@ -821,9 +888,13 @@ dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const f
   if (Di != kDi) return fail(DSA_ERR_UNSUPPORTED, "%s: Di=%d unsupported (kernels implement Di=64)", fn, Di);
   if (Hi > kMaxHi) return fail(DSA_ERR_UNSUPPORTED, "%s: Hi=%d unsupported (max %d)", fn, Hi, kMaxHi);
   if (topk > kMaxTopk) return fail(DSA_ERR_UNSUPPORTED, "%s: topk=%d unsupported (max %d)", fn, topk, kMaxTopk);
-  const size_t need = dsa_index_topk_varlen_workspace(cu_seqlens, nseq, Hi, Di, chunk, topk);
+  // one slice (the longest sequence's recommended indexer workspace) is the
+  // minimum; the recommended size holds one per sequence indexed at once
+  const size_t one = dsa_index_topk_workspace(max_len(cu_seqlens, nseq), Hi, Di, chunk, topk);
+  const size_t need = one;
   if (!workspace || ws_bytes < need)
-    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed (%zu recommended), %zu given", fn, need,
+                dsa_index_topk_varlen_workspace(cu_seqlens, nseq, Hi, Di, chunk, topk),
                 workspace ? ws_bytes : (size_t)0);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(DSA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
@@ -854,18 +925,75 @@ dsa_status_t dsa_index_topk_varlen(const void* q_idx, const void* k_idx, const f
   if ((st = flush()) != DSA_OK) return st;
   const uint8_t* qb = static_cast<const uint8_t*>(q_idx);
   const uint8_t* kb = static_cast<const uint8_t*>(k_idx);
-  for (int s = 0; s < nseq; ++s) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto run_seq = [&](int s, const dsa::LaunchCtx& c, uint8_t* slice) {
     const int64_t o = cu_seqlens[s], L = cu_seqlens[s + 1] - o;
+    return index_topk_run(qb + o * Hi * Di * 2, kb + o * Di * 2, w + o * Hi, L, Hi, chunk, topk, 0, L,
+                          pool_idx + o * topk, slice, one, c);
+  };
+  // the shorter long sequences, several at once when the workspace holds a
+  // slice for each: helper streams forked from and joined back into the
+  // caller's stream, each launch on a share of the SMs
+  const int n_small = small_long_seqs(cu_seqlens, nseq, topk);
+  int k_par = static_cast<int>(ws_bytes / one);
+  k_par = k_par < n_small ? k_par : n_small;
+  k_par = k_par < kVarlenStreams ? k_par : kVarlenStreams;
+  int n_par = 0;
+  if (k_par >= 2) {
+    cudaStream_t hs[kVarlenStreams];
+    if ((st = varlen_streams(hs)) != DSA_OK) return st;
+    cudaEvent_t fork = nullptr, join[kVarlenStreams] = {};
+    cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    for (int k = 0; k < k_par && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&join[k], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(fork, ctx.stream);
+    for (int k = 0; k < k_par && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(hs[k], fork, 0);
+    if (e != cudaSuccess) st = cuda_fail(e, "dsa_index_topk_varlen: stream fork");
+    // the next sequence goes to the stream with the fewest tiles so far
+    int64_t load[kVarlenStreams] = {};
+    for (int s = 0; s < nseq && st == DSA_OK; ++s) {
+      const int64_t L = cu_seqlens[s + 1] - cu_seqlens[s];
+      if (L <= short_max) continue;
+      const int64_t t = index_tiles(L);
+      if (t >= kSmallSeqTiles) continue;
+      int k = 0;
+      for (int j = 1; j < k_par; ++j) k = load[j] < load[k] ? j : k;
+      load[k] += t;
+      dsa::LaunchCtx c = ctx;
+      c.stream = hs[k];
+      const int share = ctx.num_sms / k_par;
+      c.persistent_ctas = static_cast<int>(t < 8 ? 8 : (t < share ? t : share));
+      st = run_seq(s, c, ws + static_cast<size_t>(k) * one);
+      ++n_long;
+      ++n_par;
+    }
+    // join even after an error, so that nothing on the helpers outlives the call's stream order
+    for (int k = 0; k < k_par; ++k) {
+      if (join[k] == nullptr) continue;
+      cudaError_t je = cudaEventRecord(join[k], hs[k]);
+      if (je == cudaSuccess) je = cudaStreamWaitEvent(ctx.stream, join[k], 0);
+      if (je != cudaSuccess && st == DSA_OK) st = cuda_fail(je, "dsa_index_topk_varlen: stream join");
+    }
+    if (fork != nullptr) cudaEventDestroy(fork);
+    for (int k = 0; k < k_par; ++k)
+      if (join[k] != nullptr) cudaEventDestroy(join[k]);
+    if (st != DSA_OK) return st;
+  }
+  // the rest one at a time on the caller's stream, each on every SM
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t L = cu_seqlens[s + 1] - cu_seqlens[s];
     if (L <= short_max) continue;
+    if (k_par >= 2 && index_tiles(L) < kSmallSeqTiles) continue;  // already indexed
     ++n_long;
-    st = dsa_index_topk(qb + o * Hi * Di * 2, kb + o * Di * 2, w + o * Hi, L, Hi, Di, chunk, topk, 0, L,
-                        pool_idx + o * topk, workspace, ws_bytes, stream);
+    st = run_seq(s, ctx, ws);
     if (st != DSA_OK) return st;
   }
   dsa::call_param("sequences", nseq);
   dsa::call_param("short_sequences", n_short);
   dsa::call_param("indexed_sequences", n_long);
-  dsa::call_variant("short sequences filled in one launch per 256; the persistent indexer once per longer sequence");
+  dsa::call_param("indexed_at_once", n_par);
+  dsa::call_param("helper_streams", k_par >= 2 ? k_par : 0);
+  dsa::call_variant("short sequences filled in one launch per 256; the persistent indexer once per longer sequence, "
+                    "the shorter of them several at once on helper streams");
   return DSA_OK;
 }
 

@@ -51,6 +51,7 @@ struct LaunchCtx {
   int inject_timeout;      // fault injection: producers issue no copies, so waits run out
   int num_sms;
   int pdl;                 // launch may start early (programmatic stream serialization)
+  int persistent_ctas;     // the persistent indexer's CTAs: 0 = one per SM, cooperative; else that many
 };
 
 // Launches `kernel` on ctx.stream, allowing early start when ctx.pdl is set.

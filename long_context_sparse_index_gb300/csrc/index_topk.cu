@@ -1191,8 +1191,15 @@ cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_
     const cudaError_t e = set_smem_limit_once(index_topk_kernel, static_cast<int>(kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
   }
+  // One CTA per SM, launched cooperatively so that all are resident at once.
+  // The items' waits do not depend on that: an item waits only for items of
+  // earlier tickets, and a CTA takes a ticket only while it runs, so the
+  // earliest unfinished item can always proceed.  A smaller grid
+  // (ctx.persistent_ctas) is therefore launched as a plain launch, which lets
+  // several short calls share the GPU from different streams.
+  const bool part = ctx.persistent_ctas > 0 && ctx.persistent_ctas < ctx.num_sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctx.num_sms);  // one CTA per SM, all resident: the items' waits need it
+  cfg.gridDim = dim3(part ? ctx.persistent_ctas : ctx.num_sms);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = ctx.stream;
@@ -1200,7 +1207,7 @@ cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = part ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, index_topk_kernel, q_map, khat_map, samp_map, a);
 }
 

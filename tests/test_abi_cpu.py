@@ -237,9 +237,11 @@ def test_deterministic_backward_workspace_and_checks(lib):
 
 def test_varlen_checks_cu_seqlens_and_workspace(lib):
     """Packed batches: cu_seqlens must start at 0 and increase strictly; the
-    indexer's workspace is the longest sequence's, the backward's that of the
-    packed length (its fp32 dK/dV accumulators span the batch); errors come
-    back before any sequence runs."""
+    indexer's workspace is one slice (the longest sequence's) per sequence
+    indexed at once -- the long sequences with fewer than 304 indexer tiles,
+    up to 4 of them -- the backward's that of the packed length (its fp32
+    dK/dV accumulators span the batch); errors come back before any sequence
+    runs."""
     import ctypes
     import long_context_sparse_index_gb300 as dsa
     def cu(*v):
@@ -249,6 +251,13 @@ def test_varlen_checks_cu_seqlens_and_workspace(lib):
                                                                                                          256, 64)
     assert lib.dsa_sparse_attn_bwd_varlen_workspace(good, 3, 16, 128) == lib.dsa_sparse_attn_bwd_workspace(1030, 16,
                                                                                                            128)
+    # topk 64: sequences of more than 260 tokens run the indexer; 1000 tokens
+    # make 8 tiles (each may run alongside others), 20000 tokens ~1500 (alone)
+    one = lib.dsa_index_topk_workspace(1000, 8, 64, 256, 64)
+    assert lib.dsa_index_topk_varlen_workspace(cu(0, 1000, 2000, 3000, 4000, 5000), 5, 8, 64, 256, 64) == 4 * one
+    assert lib.dsa_index_topk_varlen_workspace(cu(0, 1000, 1100, 2100), 3, 8, 64, 256, 64) == 2 * one
+    assert lib.dsa_index_topk_varlen_workspace(cu(0, 20000, 21000), 2, 8, 64, 256, 64) == \
+        lib.dsa_index_topk_workspace(20000, 8, 64, 256, 64)
     for bad, n in ((cu(1, 5), 1), (cu(0, 5, 5), 2), (cu(0, 7, 3), 2), (cu(0), 0)):
         assert lib.dsa_index_topk_varlen_workspace(bad, n, 8, 64, 256, 64) == 0
         assert lib.dsa_index_topk_varlen(FAKE, FAKE, FAKE, bad, n, 8, 64, 256, 64, FAKE, FAKE, 1 << 30,
