@@ -1,4 +1,5 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs."""
+import ctypes
 import os
 
 import numpy as np
@@ -308,6 +309,40 @@ def test_varlen_many_sequences_across_launch_batches():
         rdk, rdv = oracle.attn_bwd_dkdv(dO[a:b], *seq, ref_sel, scale=scale)
         assert_close(gdk[a:b], rdk, "dk")
         assert_close(gdv[a:b], rdv, "dv")
+
+
+def test_varlen_indexer_same_result_for_any_workspace():
+    """Long sequences with few indexer tiles run several at once when the
+    workspace holds a slice for each (helper streams, a share of the SMs
+    each), else one after another on the caller's stream: the pool indices
+    are bit-identical either way, and the oracle's for each sequence alone."""
+    rng = np.random.default_rng(9)
+    lens = rng.integers(300, 2500, 9)  # topk 64: every sequence runs the indexer, each under 304 tiles
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, Hi, topk = int(cu[-1]), 8, 64
+    q_idx = synth.int_bf16(T, 21, (T, Hi, 64), -3, 3)
+    k_idx = synth.int_bf16(T, 22, (T, 64), -3, 3)
+    w = synth.int_f32(T, 23, (T, Hi), 0, 3)
+    qi, ki, wi = _indexer_to_gpu(q_idx, k_idx, w)
+    one = dsa.index_topk_workspace_size(int(lens.max()), Hi, 64, 256, topk)
+    cu_c = (ctypes.c_int64 * len(cu))(*cu.tolist())
+    assert dsa.load().dsa_index_topk_varlen_workspace(cu_c, len(lens), Hi, 64, 256, topk) == 4 * one
+    ref = None
+    for slices in (1, 2, 3, 4):
+        ws = torch.empty(one * slices, dtype=torch.uint8, device=DEV)
+        sel = dsa.dsa_index_topk_varlen(qi, ki, wi, cu, chunk=256, topk=topk, workspace=ws)
+        params = dsa.last_kernel_config()["params"]
+        assert params["helper_streams"] == (slices if slices >= 2 else 0), params
+        assert params["indexed_at_once"] == (len(lens) if slices >= 2 else 0), params
+        dsa.dsa_sync_status()
+        if ref is None:
+            ref = sel.clone()
+        else:
+            assert torch.equal(sel, ref), slices
+    got = ref.cpu().numpy()
+    for a, b in zip(cu[:-1], cu[1:]):
+        ref_sel, _ = oracle.index_topk(q_idx[a:b], k_idx[a:b], w[a:b], topk)
+        assert np.array_equal(got[a:b], ref_sel), (a, b)
 
 
 # --------------------------------------------------------------------------- attention forward
