@@ -318,12 +318,15 @@ def run_reference(args):
 def measure_l2_peaks(dsa, torch, dev):
     """L2 rates of the attention kernels' access shapes, on a 64 MiB buffer
     (L2-resident): streaming reads, random 1 KB pool gathers, 16-byte fp32
-    vector reductions four rows x 128 B per warp instruction, and bulk fp32
-    reductions from shared memory (2 KB and 512 B operations)."""
+    vector reductions four rows x 128 B per warp instruction (the backward's
+    shape; also 2 x 256 B, 8 x 64 B and 16 x 32 B), bulk fp32 reductions from
+    shared memory (2 KB and 512 B operations), and vector and bulk
+    reductions issued together."""
     buf = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
     out = {"buffer_mib": 64}
     for kind, name in ((0, "stream_read_gbs"), (1, "gather_1kb_gbs"), (2, "red_v4_gbs"), (3, "bulk_red_2kb_gbs"),
-                       (4, "bulk_red_512b_gbs")):
+                       (4, "bulk_red_512b_gbs"), (5, "red_v4_2x256b_gbs"), (6, "red_v4_8x64b_gbs"),
+                       (7, "red_v4_16x32b_gbs"), (8, "red_v4_with_bulk_gbs")):
         out[name] = max(dsa.measure_l2(kind, buf, iters=20) for _ in range(3))
     del buf
     return out

@@ -394,7 +394,12 @@ const char* dsa_version(void);
  *   kind 3  bulk reductions (cp.reduce.async.bulk .add.f32) from shared
  *           memory, one 2 KB block per operation, random blocks
  *   kind 4  the same with 512-byte operations (one row each)
- * Kinds 2..4 add into the buffer's contents.
+ *   kind 5  red.v4 with 2 rows x 256 B per warp instruction
+ *   kind 6  red.v4 with 8 rows x 64 B per warp instruction
+ *   kind 7  red.v4 with 16 rows x 32 B per warp instruction (the shape of
+ *           reductions issued straight from mma.sync fragments)
+ *   kind 8  kind 2 and kind 3 at once, from the two halves of every CTA
+ * Kinds 2..8 add into the buffer's contents.
  */
 double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream);
 

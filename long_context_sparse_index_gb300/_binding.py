@@ -469,8 +469,9 @@ def last_kernel_config() -> dict:
 
 
 def measure_l2(kind: int, buf: torch.Tensor, iters: int = 20, stream=None) -> float:
-    """GB/s of an L2 probe kernel on `buf` (kind 0 stream read, 1 1-KB gather, 2 red.v4 reductions,
-    3 / 4 bulk reductions of 2 KB / 512 B)."""
+    """GB/s of an L2 probe kernel on `buf` (kind 0 stream read, 1 1-KB gather, 2 red.v4 reductions of
+    4 rows x 128 B, 3 / 4 bulk reductions of 2 KB / 512 B, 5 / 6 / 7 red.v4 of 2 x 256 B / 8 x 64 B /
+    16 x 32 B, 8 kinds 2 and 3 at once)."""
     lib = load()
     r = lib.dsa_measure_l2(kind, buf.data_ptr(), buf.numel() * buf.element_size(), iters, _stream_handle(stream))
     if r < 0:

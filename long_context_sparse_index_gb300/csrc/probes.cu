@@ -16,6 +16,12 @@
 //           memory: one 2 KB block per operation, random blocks, up to 8
 //           operations in flight per warp
 //   kind 4  the same with 512-byte operations (one row each)
+//   kind 5  red.v4 with 2 rows x 256 B per warp instruction (two rows of a block)
+//   kind 6  red.v4 with 8 rows x 64 B (four rows of each of two blocks)
+//   kind 7  red.v4 with 16 rows x 32 B (four blocks; the shape of reductions
+//           issued straight from mma.sync accumulator fragments)
+//   kind 8  kind 2 from half of each CTA's warps and kind 3 from the other
+//           half at the same time (do the two issue paths add up?)
 // All report bytes moved (read, or added) per second.
 //
 // dsa_measure_fold times the indexer's accumulator handoff in isolation: the
@@ -98,6 +104,33 @@ __global__ void probe_red_kernel(float* __restrict__ buf, uint32_t nblocks, int 
   }
 }
 
+// red.v4 with R rows per warp instruction, 512 / R bytes of each: the rows
+// are rows of R / 4 random 2 KB blocks (R >= 4), or R consecutive rows of one
+// random block (R = 2).
+template <int R>
+__global__ void probe_red_shape_kernel(float* __restrict__ buf, uint32_t nblocks, int per_warp) {
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kTpr = 32 / R;        // lanes per row
+  constexpr int kChunks = 128 / (4 * kTpr);  // chunks of 4 * kTpr floats in a 128-float row
+  const int row = lane / kTpr, c = lane % kTpr;
+  for (int it = 0; it < per_warp; ++it) {
+    const uint32_t h = mix32(warp * 0x9E3779B9u + static_cast<uint32_t>(it));
+    const int jj = static_cast<int>((h >> 24) % kChunks);
+    uint32_t b;
+    int r;
+    if (R >= 4) {
+      b = mix32(h + static_cast<uint32_t>(row >> 2) * 0x85EBCA6Bu) % nblocks;
+      r = row & 3;
+    } else {
+      b = h % nblocks;
+      r = static_cast<int>((h >> 20) & 2u) + row;  // rows 0-1 or 2-3
+    }
+    float* dst = buf + static_cast<int64_t>(b) * 512 + r * 128 + jj * 4 * kTpr + 4 * c;
+    dsa::red_add_v4(dst, 1.f, 1.f, 1.f, 1.f);
+  }
+}
+
 // Warp w's lane 0 adds its 2 KB shared-memory block of ones into random
 // 2 KB blocks of buf (op_bytes per bulk operation), keeping at most 8 bulk
 // groups in flight; all complete before the CTA exits.
@@ -125,6 +158,44 @@ __global__ void probe_bulk_red_kernel(float* __restrict__ buf, uint32_t nblocks,
     }
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
+}
+
+// Warps 0-3 of each 8-warp CTA issue kind 2's reductions (red_iters each),
+// warps 4-7 kind 3's bulk 2 KB reductions (bulk_iters each, lane 0, at most
+// 8 in flight), all at once.
+__global__ void probe_red_mix_kernel(float* __restrict__ buf, uint32_t nblocks, int red_iters, int bulk_iters) {
+  __shared__ __align__(128) float src[4][512];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (wib < 4) {
+    for (int it = 0; it < red_iters; ++it) {
+      const uint32_t h = mix32(warp * 0x9E3779B9u + static_cast<uint32_t>(it));
+      const uint32_t b = h % nblocks;
+      const int jj = static_cast<int>((h >> 28) & 3u);
+      float* dst = buf + static_cast<int64_t>(b) * 512 + (lane >> 3) * 128 + 32 * jj + 4 * (lane & 7);
+      dsa::red_add_v4(dst, 1.f, 1.f, 1.f, 1.f);
+    }
+    return;
+  }
+  float* mine = src[wib - 4];
+  for (int e = lane; e < 512; e += 32) mine[e] = 1.f;
+  __syncwarp();
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t s = dsa::smem_u32(mine);
+    for (int it = 0; it < bulk_iters; ++it) {
+      const uint32_t b = mix32(warp * 0x85EBCA6Bu + static_cast<uint32_t>(it)) % nblocks;
+      asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                       buf + static_cast<int64_t>(b) * 512),
+                   "r"(s), "r"(2048)
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 8;" ::: "memory");
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- tensor-core issue probe
@@ -305,8 +376,8 @@ __global__ void __launch_bounds__(kFoldThreads, 1) probe_fold_kernel(int heads, 
 extern "C" {
 
 double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream) {
-  if (!buf || bytes < 4096 || iters < 1 || kind < 0 || kind > 4 || (reinterpret_cast<uintptr_t>(buf) & 15u)) {
-    dsa::set_last_error("dsa_measure_l2: kind must be 0..4, buf 16-byte aligned, bytes >= 4096, iters >= 1");
+  if (!buf || bytes < 4096 || iters < 1 || kind < 0 || kind > 8 || (reinterpret_cast<uintptr_t>(buf) & 15u)) {
+    dsa::set_last_error("dsa_measure_l2: kind must be 0..8, buf 16-byte aligned, bytes >= 4096, iters >= 1");
     return -1.0;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -336,11 +407,25 @@ double dsa_measure_l2(int kind, void* buf, size_t bytes, int iters, void* stream
       const int per_warp = 64 * reps;
       probe_red_kernel<<<grid, block, 0, st>>>(static_cast<float*>(buf), nb, per_warp);
       moved = static_cast<double>(warps) * per_warp * 512.0;
-    } else {
+    } else if (kind == 3 || kind == 4) {
       const uint32_t nb = static_cast<uint32_t>(bytes / 2048);
       const int per_warp = 16 * reps;
       probe_bulk_red_kernel<<<grid, block, 0, st>>>(static_cast<float*>(buf), nb, per_warp, kind == 3 ? 2048 : 512);
       moved = static_cast<double>(warps) * per_warp * 2048.0;
+    } else if (kind <= 7) {
+      const uint32_t nb = static_cast<uint32_t>(bytes / 2048);
+      const int per_warp = 64 * reps;
+      float* fb = static_cast<float*>(buf);
+      if (kind == 5) probe_red_shape_kernel<2><<<grid, block, 0, st>>>(fb, nb, per_warp);
+      else if (kind == 6) probe_red_shape_kernel<8><<<grid, block, 0, st>>>(fb, nb, per_warp);
+      else probe_red_shape_kernel<16><<<grid, block, 0, st>>>(fb, nb, per_warp);
+      moved = static_cast<double>(warps) * per_warp * 512.0;
+    } else {
+      // equal bytes per warp on both paths: a red.v4 instruction adds 512 B, a bulk operation 2 KB
+      const uint32_t nb = static_cast<uint32_t>(bytes / 2048);
+      const int red_iters = 64 * reps, bulk_iters = 16 * reps;
+      probe_red_mix_kernel<<<grid, block, 0, st>>>(static_cast<float*>(buf), nb, red_iters, bulk_iters);
+      moved = static_cast<double>(grid) * 4.0 * (red_iters * 512.0 + bulk_iters * 2048.0);
     }
   };
   cudaEvent_t a, b;
