@@ -518,12 +518,12 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host -> device, the calls, device -> host
     e2e = None
     if not args.no_e2e:
-        # Two device sets of inputs and outputs, used by alternate steps, the
-        # way a training loop with prefetch runs: step s+1's inputs upload into
-        # the other set while step s computes (once step s-1 is done with that
-        # set), pool_idx, o and lse download during the backward, and dq, dk
-        # and dv during the next step (the last step's before the end event).
-        # Every copy is inside the timed region, on its own stream per
+        # Three device sets of inputs and outputs, used by steps in turn, the
+        # way a training loop with prefetch runs: step s+2's inputs upload into
+        # their set while steps s and s+1 compute (once step s-1 is done with
+        # that set), pool_idx, o and lse download during the backward, and dq,
+        # dk and dv during the next steps (the last step's before the end
+        # event).  Every copy is inside the timed region, on its own stream per
         # direction; step 0's indexer inputs upload first, so its indexer
         # starts while the rest of its inputs upload.
         small_names = ("pool_idx", "o", "lse")
@@ -531,8 +531,9 @@ def run_ours(args):
         outs0 = {"pool_idx": pool_idx, "o": o, "lse": lse}
         if backward:
             outs0.update({"dq": dq, "dk": dk, "dv": dv})
-        sets = [(d, outs0), ({n: torch.empty_like(t) for n, t in d.items()},
-                             {n: torch.empty_like(t) for n, t in outs0.items()})]
+        nsets = 3
+        sets = [(d, outs0)] + [({n: torch.empty_like(t) for n, t in d.items()},
+                                {n: torch.empty_like(t) for n, t in outs0.items()}) for _ in range(nsets - 1)]
         out_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs0.items()}
         bi = sum(t.numel() * t.element_size() for t in pin.values())
         bo = sum(t.numel() * t.element_size() for t in out_host.values())
@@ -560,22 +561,27 @@ def run_ours(args):
                 start.record(stream)
             h2d.wait_stream(stream)
             d2h.wait_stream(stream)
-            ev_idx_in = upload(sets[0][0], idx_in)
-            ev_attn_in = upload(sets[0][0], attn_in)
+            ev_idx_in = [None] * nsteps
+            ev_attn_in = [None] * nsteps
+            ev_idx_in[0] = upload(sets[0][0], idx_in)
+            ev_attn_in[0] = upload(sets[0][0], attn_in)
+            for j in range(1, min(nsets - 1, nsteps)):  # the next steps' sets are free from the start
+                ev_idx_in[j] = ev_attn_in[j] = upload(sets[j][0], idx_in + attn_in)
             ev_done, ev_out = [None] * nsteps, [None] * nsteps
             for s in range(nsteps):
-                t, out = sets[s % 2]
-                if s + 1 < nsteps:
+                t, out = sets[s % nsets]
+                nxt = s + nsets - 1
+                if nxt < nsteps:
                     if s >= 1:
-                        h2d.wait_event(ev_done[s - 1])  # step s-1 is done with the other set
-                    ev_next_in = upload(sets[(s + 1) % 2][0], idx_in + attn_in)
+                        h2d.wait_event(ev_done[s - 1])  # step s-1 is done with the set of step s+2
+                    ev_idx_in[nxt] = ev_attn_in[nxt] = upload(sets[nxt % nsets][0], idx_in + attn_in)
                 flush.zero_()
-                stream.wait_event(ev_idx_in)
-                if s >= 2:
-                    stream.wait_event(ev_out[s - 2])  # this set's outputs of step s-2 are on the host
+                stream.wait_event(ev_idx_in[s])
+                if s >= nsets:
+                    stream.wait_event(ev_out[s - nsets])  # this set's outputs of step s-3 are on the host
                 dsa.dsa_index_topk(t["q_idx"], t["k_idx"], t["w"], chunk=wl.chunk, topk=topk,
                                    pool_idx=out["pool_idx"], workspace=ws_idx)
-                stream.wait_event(ev_attn_in)
+                stream.wait_event(ev_attn_in[s])
                 dsa.dsa_sparse_attn_fwd(t["q"], t["k"], t["v"], out["pool_idx"], scale=wl.scale, o=out["o"],
                                         lse=out["lse"])
                 d2h.wait_stream(stream)
@@ -589,8 +595,6 @@ def run_ours(args):
                     ev_out[s] = download(out, grad_names)
                 if marks is not None:
                     marks[s].record(stream)
-                if s + 1 < nsteps:
-                    ev_idx_in = ev_attn_in = ev_next_in
             stream.wait_stream(d2h)
             stream.wait_stream(h2d)
 
@@ -613,9 +617,9 @@ def run_ours(args):
                "d2h_bytes_per_step": bo, "ms_per_step": 1e3 * e2e_s / args.steps,
                "step_ms": [a.elapsed_time(b) for a, b in zip(bounds[:-1], bounds[1:])],
                "last_step_tail_ms": marks[-1].elapsed_time(e2e_end),
-               "pipelining": "two device sets of inputs and outputs used by alternate steps: the next step's inputs "
-                             "upload while this step computes, pool_idx/o/lse download during the backward and "
-                             "dq/dk/dv during the next step; all copies inside the timed region"}
+               "pipelining": "three device sets of inputs and outputs used by steps in turn: inputs upload two steps "
+                             "ahead, pool_idx/o/lse download during the backward and dq/dk/dv during the next steps; "
+                             "all copies inside the timed region"}
 
     if rank == 0:
         cpu = None
