@@ -41,14 +41,17 @@
 // each (topk_cand.cuh).
 //
 // Items come from one global ticket counter, step by step; step s holds
-//     sample(s), thresh(s-1), tile(s-2), rows(s-2-lag)
-// and chunk c uses slot c % nbuf of a ring of per-chunk buffers (samples,
-// thresholds, candidate counts and lists).  Every wait is on an earlier
-// ticket: a sample item waits (before storing) for the thresh items of chunk
-// c-nbuf to be done reading the slot's samples; thresh(c) waits for the
-// samples of c and for the rows of c-nbuf (done with the slot's candidates,
-// step c-nbuf+2+lag <= c since lag <= nbuf-2); a tile waits (before
-// appending) for thresh(c); rows(c) wait for the tiles of c.  With one CTA
+//     sample(s), thresh(s-1-L), tile(s-2-L), rows(s-2-2L)
+// with L = min(3, (nbuf-1)/2), and chunk c uses slot c % nbuf of a ring of
+// per-chunk buffers (samples, thresholds, candidate counts and lists).  Every
+// wait is on an earlier step (L < nbuf-1), or on an earlier item of the same
+// step: a sample item (step c) waits, before storing, for the thresh items
+// of chunk c-nbuf (step c-nbuf+1+L) to be done reading the slot's samples;
+// thresh(c) (step c+1+L) waits for the samples of c and for the rows of
+// c-nbuf (step c-nbuf+2+2L), done with the slot's candidates; a tile waits,
+// before appending, for thresh(c); rows(c) wait for the tiles of c.  L steps
+// between samples and thresholds and between tiles and rows give the items
+// waited for time to finish when a step holds fewer items than CTAs.  With one CTA
 // per SM (cooperative launch: all resident), the lowest unfinished ticket can
 // always proceed.  There is no barrier per chunk, and the chunk size only
 // bounds the per-chunk buffers.
@@ -68,7 +71,7 @@ constexpr int kAStages = 4;
 constexpr int kItems = 2;          // work-item ring between the roles (the item in work + one prefetched)
 constexpr int kRowsPerGroupItem = 4;   // topk > 512: one row per 128-thread group
 constexpr int kRowsPerWarpItem = 16;   // topk <= 512: one row per epilogue warp
-constexpr int kMaxLag = 2;         // rows of chunk c come in step c + 2 + lag
+constexpr int kMaxLead = 3;        // thresholds of chunk c come in step c + 1 + lead, rows in c + 2 + 2 lead
 constexpr uint32_t kABytes = kBM * kDi * 2;        // 16 KB: q_idx tile of one head
 constexpr uint32_t kBHalf = kBN * kDi * 2;         // 32 KB: Khat hi (or lo) tile
 constexpr uint32_t kBBytes = 2 * kBHalf;           // 64 KB, one stage
@@ -139,7 +142,8 @@ struct Args {
   int rsel;             // the threshold is the rsel-th largest sample
   int rpi;              // rows per thresh / rows item: 16 (one per warp, topk <= 512) or 4 (one per group)
   int nbuf;             // slots, 1 .. kMaxBufs
-  int lag;              // min(kMaxLag, nbuf - 2), at least 0
+  int lead;             // min(kMaxLead, (nbuf - 1) / 2)
+  int lag;              // = lead
   int64_t q_begin, q_end;
   int chunk;
   int nchunks;
@@ -311,18 +315,18 @@ __device__ __forceinline__ unsigned long long rows_through(const Args& a, int c)
 }
 
 // The ticket taker's view of the sequence: step s holds the sample items of
-// chunk s, the thresh items of chunk s-1, the tiles of chunk s-2 and the row
-// items of chunk s-2-lag.
+// chunk s, the thresh items of chunk s-1-lead, the tiles of chunk s-2-lead
+// and the row items of chunk s-2-lead-lag.
 struct Cursor {
   int s;
   int64_t base;        // first ticket of step s
   int ns, nh, nt, nr;  // sample, thresh, tile and row items in step s
 };
 
-__device__ __forceinline__ int steps(const Args& a) { return a.nchunks + 2 + a.lag; }
+__device__ __forceinline__ int steps(const Args& a) { return a.nchunks + 2 + a.lead + a.lag; }
 
 __device__ __forceinline__ void cursor_load(const Args& a, Cursor& cur) {
-  const int cs = cur.s, ch_ = cur.s - 1, ct = cur.s - 2, cr = cur.s - 2 - a.lag;
+  const int cs = cur.s, ch_ = cur.s - 1 - a.lead, ct = ch_ - 1, cr = ct - a.lag;
   cur.ns = cs < a.nchunks ? sample_tiles(a, chunk_of(a, cs)) : 0;
   cur.nh = ch_ >= 0 && ch_ < a.nchunks ? (chunk_of(a, ch_).nrows + a.rpi - 1) / a.rpi : 0;
   cur.nt = ct >= 0 && ct < a.nchunks ? chunk_of(a, ct).ntiles : 0;
@@ -577,23 +581,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           off -= cur.ns;
           if (off < cur.nh) {
-            const Chunk ch = chunk_of(a, cur.s - 1);
+            const Chunk ch = chunk_of(a, cur.s - 1 - a.lead);
             const int r0 = off * a.rpi;
-            it = Item{kItemThresh, cur.s - 1, r0, min(a.rpi, ch.nrows - r0)};
+            it = Item{kItemThresh, cur.s - 1 - a.lead, r0, min(a.rpi, ch.nrows - r0)};
             break;
           }
           off -= cur.nh;
           if (off < cur.nt) {
-            const Chunk ch = chunk_of(a, cur.s - 2);
+            const Chunk ch = chunk_of(a, cur.s - 2 - a.lead);
             const int qb = off % ch.nqb, pb = off / ch.nqb;
             if (pb >= pool_tiles_of(ch, qb)) continue;  // past the causal edge: nothing to compute
-            it = Item{kItemTile, cur.s - 2, qb, pb};
+            it = Item{kItemTile, cur.s - 2 - a.lead, qb, pb};
             break;
           }
           off -= cur.nt;
-          const Chunk ch = chunk_of(a, cur.s - 2 - a.lag);
+          const Chunk ch = chunk_of(a, cur.s - 2 - a.lead - a.lag);
           const int r0 = off * a.rpi;
-          it = Item{kItemRows, cur.s - 2 - a.lag, r0, min(a.rpi, ch.nrows - r0)};
+          it = Item{kItemRows, cur.s - 2 - a.lead - a.lag, r0, min(a.rpi, ch.nrows - r0)};
           break;
         }
         items[is].kind = it.kind;
@@ -1170,7 +1174,11 @@ cudaError_t launch_index_topk(const CUtensorMap& q_map, const CUtensorMap& khat_
   a.rsel = pl.rsel;
   a.rpi = topk <= wsel::kMaxK ? kRowsPerWarpItem : kRowsPerGroupItem;
   a.nbuf = b.nbuf;
-  a.lag = b.nbuf - 2 < kMaxLag ? (b.nbuf - 2 > 0 ? b.nbuf - 2 : 0) : kMaxLag;
+  // lead = lag = (nbuf-1)/2 (at most kMaxLead) leaves each of the four
+  // distances between an item and what it waits for at least one step
+  const int half = (b.nbuf - 1) / 2;
+  a.lead = half < kMaxLead ? half : kMaxLead;
+  a.lag = a.lead;
   a.q_begin = q_begin;
   a.q_end = q_end;
   a.chunk = chunk;
