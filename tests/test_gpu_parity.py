@@ -89,9 +89,10 @@ def test_index_topk_result_does_not_depend_on_workspace_size():
 @pytest.mark.parametrize("chunk", [1, 37, 128])
 def test_index_topk_every_buffer_ring_size_bit_exact(nbuf, chunk):
     """The fused kernel's item dependencies for every slot-ring size the
-    workspace can give (2 to 8 chunk slots; rows handed out min(2, nbuf-2)
-    steps after their tiles): integer inputs give the oracle's pool indices
-    bit for bit."""
+    workspace can give (2 to 8 chunk slots; thresholds handed out
+    L = min(3, (nbuf-1)/2) steps after their samples and rows L steps after
+    their tiles, so L = 0, 1, 2 and 3 here): integer inputs give the oracle's
+    pool indices bit for bit."""
     wl = synth.WORKLOADS["tiny_int_s2048"]
     q_idx, k_idx, w = synth.indexer_inputs(wl)
     S = wl.S
