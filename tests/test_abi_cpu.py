@@ -286,3 +286,23 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(8, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         dsa.dsa_index_topk(q, torch.zeros(8, 64, dtype=torch.bfloat16), torch.zeros(8, 2), chunk=4, topk=1)
+
+
+def test_profile_summaries_match_the_kernel_sources():
+    """Each committed ncu summary under profiles/ names the hash of the
+    kernel sources it was captured on; the bench reports a kernel's DRAM
+    traffic only while that hash still matches.  A kernel edited without a new
+    capture fails here instead of dropping its traffic from the bench line."""
+    import importlib.util
+    import sys
+    spec = importlib.util.spec_from_file_location("bench_for_profiles", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    argv = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        spec.loader.exec_module(bench)
+    finally:
+        sys.argv = argv
+    for kernel in bench.KERNEL_SOURCE:
+        traffic, source = bench.profiled_traffic(kernel, 131072)
+        assert traffic is not None and traffic > 0, f"{kernel}: {source}"
