@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--trace", action="store_true",
                     help="indexer item trace: one dsa_index_topk call through the DSA_ITEM_TRACE build, "
                          "time per work-item kind (fold, dependency wait, rest) and per-CTA idle time")
+    ap.add_argument("--trace-stamps", action="store_true",
+                    help="the same item trace through the stamps-only build (no SM-cycle counters in the "
+                         "indexer's fold), whose per-item times are the default build's")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-tc-alt", action="store_true",
                     help="skip timing the tcgen05 forward alternative after the step")
@@ -799,14 +802,14 @@ def summarize_trace(rec, num_sms):
     return out
 
 
-def run_trace(args):
+def run_trace(args, stamps=False):
     import torch
     import synth
     from long_context_sparse_index_gb300 import build as libbuild
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
-    path = libbuild.build(trace=True)
+    path = libbuild.build(stamps=True) if stamps else libbuild.build(trace=True)
     lib = ctypes.CDLL(path)
     i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
     lib.dsa_index_topk_workspace.argtypes = [i64, i32, i32, i32, i32]
@@ -853,19 +856,21 @@ def run_trace(args):
     summary = summarize_trace(rec, torch.cuda.get_device_properties(0).multi_processor_count)
     # SM-cycle sums of the trace build (kernel words 37..43): epilogue thread 0 of
     # each CTA and the MMA issuer
-    words = ws[:64 * 8].cpu().numpy().view(np.uint64)
-    fheads, mheads = max(int(words[43]), 1), max(int(words[42]), 1)
-    summary["fold_cycles"] = {"per_head_folded": int(words[38]) / fheads,
-                              "acc_wait_per_head": int(words[37]) / fheads,
-                              "mma_q_tile_wait_per_head": int(words[39]) / mheads,
-                              "mma_acc_free_wait_per_head": int(words[40]) / mheads,
-                              "mma_key_tile_wait_per_head": int(words[41]) / mheads,
-                              "heads_issued": int(words[42]), "heads_folded_thread0": int(words[43]),
-                              "fallback_rows": int(words[36])}
-    napp = max(int(words[47]), 1)
-    summary["append_cycles"] = {"compare_per_tile": int(words[44]) / napp, "atomic_per_tile": int(words[45]) / napp,
-                                "writes_per_tile": int(words[46]) / napp, "tiles_thread0": int(words[47])}
+    if not stamps:
+        words = ws[:64 * 8].cpu().numpy().view(np.uint64)
+        fheads, mheads = max(int(words[43]), 1), max(int(words[42]), 1)
+        summary["fold_cycles"] = {"per_head_folded": int(words[38]) / fheads,
+                                  "acc_wait_per_head": int(words[37]) / fheads,
+                                  "mma_q_tile_wait_per_head": int(words[39]) / mheads,
+                                  "mma_acc_free_wait_per_head": int(words[40]) / mheads,
+                                  "mma_key_tile_wait_per_head": int(words[41]) / mheads,
+                                  "heads_issued": int(words[42]), "heads_folded_thread0": int(words[43]),
+                                  "fallback_rows": int(words[36])}
+        napp = max(int(words[47]), 1)
+        summary["append_cycles"] = {"compare_per_tile": int(words[44]) / napp, "atomic_per_tile": int(words[45]) / napp,
+                                    "writes_per_tile": int(words[46]) / napp, "tiles_thread0": int(words[47])}
     summary.update({"workload": args.workload, "S": S, "call_ms": ev0.elapsed_time(ev1), "records_dropped": max(0, n - cap),
+                    "build": "stamps only (DSA_TRACE_STAMPS_ONLY)" if stamps else "item stamps and SM-cycle counters",
                     "note": "DSA_ITEM_TRACE build (measurement only): epilogue thread 0 stamps each work item; "
                             "fold = taking the item to the end of its fold over heads (waits on the MMAs included), "
                             "wait = its dependency wait, rest = selection / append / store and publish"})
@@ -921,8 +926,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
-    elif args.trace:
-        run_trace(args)
+    elif args.trace or args.trace_stamps:
+        run_trace(args, stamps=args.trace_stamps)
     elif args.varlen or args.zigzag:
         run_layout(args)
     else:

@@ -22,6 +22,11 @@ LIB = os.path.join(HERE, "libdsa.so")
 # role's cycles per pipeline segment (DSA_FWD_PROFILE); nothing else differs
 BUILD_TRACE = os.path.join(HERE, "_build_trace")
 LIB_TRACE = os.path.join(HERE, "libdsa_trace.so")
+# the same item stamps without the indexer's SM-cycle counters, whose clock
+# reads in the fold loop make the trace build spill more and run slower: its
+# per-item times are the default build's
+BUILD_STAMPS = os.path.join(HERE, "_build_stamps")
+LIB_STAMPS = os.path.join(HERE, "libdsa_stamps.so")
 # checking variant: range checks on gathered rows and shared-memory offsets
 # that record a device status (DSA_ERR_INTERNAL) instead of trapping
 # (DSA_DEBUG); the arithmetic and results are the default build's
@@ -52,19 +57,22 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False, debug: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, trace: bool = False, debug: bool = False,
+          stamps: bool = False) -> str:
     """Compile and link libdsa.so (or, with trace=True, the measurement
-    variant libdsa_trace.so, or with debug=True the range-checking variant
+    variant libdsa_trace.so, with stamps=True its stamps-only form
+    libdsa_stamps.so, or with debug=True the range-checking variant
     libdsa_debug.so); returns its path."""
-    if trace and debug:
-        raise ValueError("build: the trace and debug variants are separate builds")
-    lib, bdir = (LIB_TRACE, BUILD_TRACE) if trace else (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if trace + debug + stamps > 1:
+        raise ValueError("build: the trace, stamps and debug variants are separate builds")
+    lib, bdir = (LIB_TRACE, BUILD_TRACE) if trace else (LIB_STAMPS, BUILD_STAMPS) if stamps else \
+        (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
     if not force and not _stale(lib):
         return lib
     os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + (["-DDSA_ITEM_TRACE=1", "-DDSA_FWD_PROFILE=1"] if trace else []) + \
-        (["-DDSA_DEBUG=1"] if debug else [])
+    flags = NVCC_FLAGS + (["-DDSA_ITEM_TRACE=1", "-DDSA_FWD_PROFILE=1"] if trace or stamps else []) + \
+        (["-DDSA_TRACE_STAMPS_ONLY=1"] if stamps else []) + (["-DDSA_DEBUG=1"] if debug else [])
 
     def compile_one(src: str) -> str:
         obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")

@@ -283,8 +283,10 @@ enum : int {
 };
 static_assert(kCycAppends < kIndexSyncWords, "trace words");
 
+// (not in the stamps-only trace build, DSA_TRACE_STAMPS_ONLY, whose clock
+// reads inside the fold would change the kernel it measures)
 struct CycleSum {
-#ifdef DSA_ITEM_TRACE
+#if defined(DSA_ITEM_TRACE) && !defined(DSA_TRACE_STAMPS_ONLY)
   long long sum = 0, t = 0;
   __device__ __forceinline__ void start() { t = clock64(); }
   __device__ __forceinline__ void stop() { sum += clock64() - t; }
@@ -297,7 +299,7 @@ struct CycleSum {
 };
 
 __device__ __forceinline__ void cycles_publish(const Args& a, int word, const CycleSum& c) {
-#ifdef DSA_ITEM_TRACE
+#if defined(DSA_ITEM_TRACE) && !defined(DSA_TRACE_STAMPS_ONLY)
   if (a.trace != nullptr && c.sum != 0) atomicAdd(a.sync + word, static_cast<unsigned long long>(c.sum));
 #else
   (void)a, (void)word, (void)c;
